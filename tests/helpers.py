@@ -1,0 +1,38 @@
+"""Shared test plumbing: turn generated torch tensors into oracle-ready numpy arrays."""
+import numpy as np
+import torch
+
+from decode_phase_gqa_gb300 import workloads as W
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> numpy uint16 bit patterns; other dtypes -> numpy as is."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def host_inputs(wl: W.Workload, layer: int = 0, tensors=None):
+    """Numpy copies (bf16 as uint16) of one layer's inputs plus the workload metadata."""
+    t = tensors if tensors is not None else W.make_tensors(wl, layer=layer, device="cpu")
+    h = {k: (None if v is None else bits(v)) for k, v in t.items()}
+    h["block_table"] = wl.block_table.copy()
+    h["seq_lens"] = wl.seq_lens.copy()
+    h["positions"] = wl.positions.copy()
+    return h
+
+
+def oracle_decode(wl: W.Workload, h, seq_mask=None, n_threads=0):
+    """Run the oracle's decode step on copies of the host inputs.
+
+    Returns (out float64, status, k_pages_after, v_pages_after, k_scales, v_scales).
+    """
+    import oracle
+    kp, vp = h["k_pages"].copy(), h["v_pages"].copy()
+    ks = None if h["k_scales"] is None else h["k_scales"].copy()
+    vs = None if h["v_scales"] is None else h["v_scales"].copy()
+    out, st = oracle.decode(h["q"], h["k_new"], h["v_new"], kp, vp, h["block_table"],
+                            h["seq_lens"], h["positions"], wl.rope_theta, wl.scale,
+                            ks, vs, seq_mask=seq_mask, n_threads=n_threads)
+    return out, st, kp, vp, ks, vs
