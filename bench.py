@@ -1,0 +1,549 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode step of GQA attention over a paged KV cache on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                    [--config NAME] [--no-extra-configs]
+
+A step is one pass of the whole hot path (RoPE + append + split-KV attention
++ merge: one kvattn_decode call per layer cache) over one batch.  The default
+workload is the SmolLM3-3B-shaped layer (16/4 heads, d 128, batch 8, cached
+lengths U[512, 4096], page 16).  Inputs are seeded synthetic N(0, 1) draws
+already resident in HBM; consecutive steps rotate over independent caches
+whose total size is far above the 129 MB L2, so every step reads its KV from
+HBM.  Steps are replayed from CUDA graphs (one graph per cache) and timed with
+CUDA events on the launching stream; rank 0 prints one JSON line.
+
+With N > 1 (torchrun) every rank decodes its own batch (weak scaling, no data
+exchange); the timing is the max over ranks.  ``--impl reference`` times the
+CPU oracle (the only reference this method has) on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from decode_phase_gqa_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-attn tokens/s and KV-read HBM GB/s (% of GB300 peak) per config"
+PRIMARY = "smollm3"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+SRC_FILES = ["decode_kernel.cuh", "kvattn_internal.cuh", "rope_append.cu", "kvattn_api.cu",
+             "decode_bf16.cu", "decode_int8.cu"]
+
+
+def workload_desc(wl: W.Workload) -> str:
+    return {
+        "tiny": "Tiny: 1 seq, 4/1 heads, d64, 256 cached + 1 new, page 16",
+        "smollm3": "SmolLM3-3B-shaped layer: 16/4 heads, d128, batch 8, L~U[512,4096], page 16",
+        "qwen3": "Qwen3-8B-shaped continuous batch: 32/8 heads, d128, batch 64, "
+                 "L log-uniform [128,8192], page 16, 36 layer caches per step",
+        "llama1b": "Llama-3.2-1B-shaped long context: 32/8 heads, d64, batch 32, "
+                   "half L=32768, half L~U[1,2048], page 16",
+        "int8": "Int8 KV cache, Qwen3-8B-shaped: 32/8 heads, d128, batch 128, "
+                "L~U[1024,4096], page 16, per-token-per-head fp32 scales",
+    }.get(wl.name, wl.name)
+
+
+# --------------------------------------------------------------- dist ---
+
+def dist_setup(use_gpu: bool = True):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (use_gpu and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (timing plumbing, not a data path)."""
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self, t_start: float, t_end: float):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if t_start <= r[0] <= t_end] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------- native ---
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in SRC_FILES:
+        with open(os.path.join(ROOT, "decode_phase_gqa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    """DRAM bytes per decode-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(config)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class NativeCase:
+    """Device-resident inputs of one config: `copies` independent caches (or the
+    36 layer caches of the Qwen config), one workspace, one output buffer."""
+
+    def __init__(self, name: str, seed: int, device, min_bytes: int = 4 * L2_BYTES):
+        from decode_phase_gqa_gb300 import kvattn as K
+        self.K = K
+        self.wl = W.make_workload(name, seed=seed)
+        wl = self.wl
+        self.device = device
+        self.calls_per_step = wl.layers
+        per_cache = wl.kv_bytes
+        if wl.layers > 1:
+            self.copies = wl.layers           # a step reads every layer cache once
+        else:
+            # enough independent caches that a rotation reads min_bytes of KV;
+            # capped for latency-bound toy shapes (their KV sits in L2 anyway)
+            self.copies = min(64, max(2, math.ceil(min_bytes / max(per_cache, 1))))
+        self.l2_resident = self.copies * per_cache * self.calls_per_step < 2 * L2_BYTES
+        self.caches = [W.make_tensors(wl, layer=i, device=device) for i in range(self.copies)]
+        self.bt = torch.from_numpy(wl.block_table).to(device)
+        self.sl = torch.from_numpy(wl.seq_lens).to(device)
+        self.pos = torch.from_numpy(wl.positions).to(device)
+        self.out = torch.empty((wl.n_seq, wl.n_qh, wl.head_dim), dtype=torch.bfloat16,
+                               device=device)
+        self.ws = K.alloc_workspace(wl.n_seq, wl.n_qh, wl.n_kvh, wl.head_dim, device=device)
+        self.graphs = []
+
+    def call(self, i, stream=None, out=None):
+        c = self.caches[i]
+        self.K.kvattn_decode(c["q"], c["k_new"], c["v_new"], c["k_pages"], c["v_pages"],
+                             self.bt, self.sl, self.pos, self.out if out is None else out,
+                             rope_theta=self.wl.rope_theta, scale=self.wl.scale,
+                             workspace=self.ws, k_scales=c["k_scales"], v_scales=c["v_scales"],
+                             stream=stream)
+
+    def step_groups(self):
+        """Cache indices of each distinct step (a step = calls_per_step calls)."""
+        if self.calls_per_step > 1:
+            return [list(range(self.copies))]
+        return [[i] for i in range(self.copies)]
+
+    def capture(self, stream):
+        for grp in self.step_groups():
+            for i in grp:          # warm the library's per-device set-up first
+                self.call(i, stream)
+        torch.cuda.synchronize()
+        for grp in self.step_groups():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in grp:
+                    self.call(i, stream)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def replay(self, step):
+        self.graphs[step % len(self.graphs)].replay()
+
+    def check_status(self):
+        return self.K.kvattn_read_device_status(self.ws)
+
+
+def time_steps(case: NativeCase, steps: int, warmup: int, world: int, stream):
+    with torch.cuda.stream(stream):
+        for s in range(warmup):
+            case.replay(s)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for s in range(steps):
+            case.replay(warmup + s)
+        end.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+    return start.elapsed_time(end), (t0, t1)
+
+
+def time_e2e(case: NativeCase, steps: int, warmup: int, world: int, stream):
+    """Same step through the public API with the step's inputs in pinned host
+    memory: H2D of q/k_new/v_new/block table/lengths/positions, the decode
+    call(s), D2H of the output, every step, inside the timed region."""
+    host = []
+    for c in case.caches[:case.calls_per_step if case.calls_per_step > 1 else 2]:
+        host.append({k: c[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")})
+    bt_h = case.bt.cpu().pin_memory()
+    sl_h = case.sl.cpu().pin_memory()
+    pos_h = case.pos.cpu().pin_memory()
+    out_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+    dev = {k: torch.empty_like(case.caches[0][k]) for k in ("q", "k_new", "v_new")}
+    bt_d, sl_d, pos_d = torch.empty_like(case.bt), torch.empty_like(case.sl), torch.empty_like(case.pos)
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values()) * case.calls_per_step
+    h2d += (bt_h.numel() + sl_h.numel() + pos_h.numel()) * 4
+    d2h = out_h.numel() * out_h.element_size() * case.calls_per_step
+
+    def one_step(s):
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        pos_d.copy_(pos_h, non_blocking=True)
+        idxs = case.step_groups()[s % len(case.step_groups())]
+        for n, i in enumerate(idxs):
+            hsrc = host[n % len(host)] if case.calls_per_step > 1 else host[s % len(host)]
+            for k in dev:
+                dev[k].copy_(hsrc[k], non_blocking=True)
+            c = case.caches[i]
+            case.K.kvattn_decode(dev["q"], dev["k_new"], dev["v_new"], c["k_pages"], c["v_pages"],
+                                 bt_d, sl_d, pos_d, case.out, rope_theta=case.wl.rope_theta,
+                                 scale=case.wl.scale, workspace=case.ws,
+                                 k_scales=c["k_scales"], v_scales=c["v_scales"], stream=stream)
+            out_h.copy_(case.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for s in range(warmup):
+            one_step(s)
+        torch.cuda.synchronize()
+        barrier(world)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for s in range(steps):
+            one_step(s)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    return start.elapsed_time(end), h2d, d2h
+
+
+def cpu_baseline(name: str, seed: int, budget_s: float = 10.0):
+    """The oracle, as it stands, on host copies of the same workload: whole
+    decode steps of one cache repeated until the time budget is used."""
+    import oracle
+    wl = W.make_workload(name, seed=seed)
+    t = W.make_tensors(wl, layer=0, device="cpu")
+    bits = lambda x: None if x is None else (
+        x.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+        if x.dtype == torch.bfloat16 else x.contiguous().numpy().copy())
+    h = {k: bits(v) for k, v in t.items()}
+    threads = oracle.max_threads()
+    seqs = 0
+    t0 = time.time()
+    n_steps = 0
+    # a sequence subset per step keeps one step well under the budget on big configs
+    order = np.arange(wl.n_seq)
+    chunk = wl.n_seq
+    while True:
+        mask = np.zeros(wl.n_seq, np.uint8)
+        sel = order[(n_steps * chunk) % wl.n_seq:][:chunk]
+        mask[sel] = 1
+        ts = time.time()
+        oracle.decode(h["q"], h["k_new"], h["v_new"], h["k_pages"], h["v_pages"],
+                      wl.block_table, wl.seq_lens, wl.positions, wl.rope_theta, wl.scale,
+                      h["k_scales"], h["v_scales"], seq_mask=mask, n_threads=threads)
+        dt = time.time() - ts
+        seqs += int(mask.sum())
+        n_steps += 1
+        if dt > budget_s / 4 and chunk > 1:
+            chunk = max(1, chunk // 2)
+        if time.time() - t0 >= budget_s:
+            break
+    elapsed = time.time() - t0
+    # one new token of a sequence needs one decode per layer cache
+    value = seqs / elapsed / wl.layers
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_steps} oracle steps over {seqs} sequences of one {wl.name} layer cache"
+                      f" ({elapsed:.1f} s, fp64, OpenMP over (sequence, KV head)); a step of "
+                      f"{wl.layers} layer(s) costs {wl.layers}x one layer"}
+
+
+def run_config(name, steps, warmup, rank, world, device, stream, with_e2e=True):
+    case = NativeCase(name, seed=1000 * rank, device=device)
+    case.capture(stream)
+    st = case.check_status()
+    if st:
+        raise RuntimeError(f"device status {st:#x} on {name}")
+    ms, window = time_steps(case, steps, warmup, world, stream)
+    ms = max_over_ranks(ms, world, device)
+    wl = case.wl
+    ms_step = ms / steps
+    kv_bytes_step = wl.kv_bytes * wl.layers
+    res = {
+        "name": name, "ms_per_step": ms_step,
+        "tokens_per_s": wl.n_seq * world * steps / (ms / 1e3),
+        "kv_gbs": kv_bytes_step * world / (ms_step / 1e3) / 1e9,
+        "kv_bytes_per_step": kv_bytes_step,
+        "calls_per_step": case.calls_per_step, "copies": case.copies,
+        "window": window, "case": case,
+    }
+    if with_e2e:
+        e2e_ms, h2d, d2h = time_e2e(case, steps, warmup, world, stream)
+        e2e_ms = max_over_ranks(e2e_ms, world, device)
+        res["e2e"] = {"value": wl.n_seq * world * steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    return res
+
+
+def native(args, rank, world, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from decode_phase_gqa_gb300 import build as B
+    B.build()
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind = measured_peak()
+    with ClockSampler(local) as clocks:
+        main = run_config(args.config, args.steps, args.warmup, rank, world, device, stream)
+    clk = clocks.summary(*main["window"])
+    wl = main["case"].wl
+    per_call_ms = main["ms_per_step"] / main["calls_per_step"]
+    achieved = wl.kv_bytes / (per_call_ms / 1e3) / 1e9   # GB/s over one call
+    line = {
+        "metric": METRIC,
+        "value": main["tokens_per_s"],
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": main["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.kv_dtype == "bf16" else "int8",
+        "data": "synthetic (seeded N(0,1) q/k/v and KV pages, no weights)",
+        "config": {
+            "workload": workload_desc(wl), "n_seq": wl.n_seq, "n_qh": wl.n_qh,
+            "n_kvh": wl.n_kvh, "head_dim": wl.head_dim, "page_size": wl.page_size,
+            "kv_dtype": wl.kv_dtype, "layer_caches_per_step": wl.layers,
+            "kv_bytes_per_step": main["kv_bytes_per_step"],
+            "kv_read_gbs": main["kv_gbs"],
+            "kv_read_frac_of_peak": main["kv_gbs"] / world / peak,
+            "l2": f"inputs larger than L2: {main['copies']} independent caches rotated, "
+                  f"{main['copies'] * wl.kv_bytes / 2**20:.0f} MiB of KV per rotation",
+            "timing": "CUDA events on the launching stream around K graph replays",
+            "parallelism": f"{world} independent replica(s), one batch per GPU",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": peak_kind,
+            "traffic": recorded_traffic(args.config),
+            "kernel": "kvattn decode call (RoPE/append + split-KV attention kernels, "
+                      "timed together): algorithmic K+V bytes per call / call time",
+        },
+        "e2e": main["e2e"],
+        "gpu_launches": 2 * main["calls_per_step"] * args.steps,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "impl": "native",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config, seed=0)
+    if not args.no_extra_configs:
+        extra = []
+        for name in W.CONFIG_ORDER:
+            if name == args.config:
+                continue
+            wl2 = W.make_workload(name)
+            call_ms_guess = max(wl2.kv_bytes * wl2.layers / (0.7 * peak * 1e9) * 1e3, 0.01)
+            k = max(10, min(2000, int(300.0 / call_ms_guess)))
+            r = run_config(name, k, max(3, k // 10), rank, world, device, stream, with_e2e=False)
+            extra.append({"config": name, "workload": workload_desc(r["case"].wl),
+                          "steps": k, "ms_per_step": r["ms_per_step"],
+                          "l2_resident": r["case"].l2_resident,
+                          "tokens_per_s": r["tokens_per_s"], "kv_read_gbs": r["kv_gbs"],
+                          "kv_read_frac_of_peak": r["kv_gbs"] / world / peak,
+                          "calls_per_step": r["calls_per_step"]})
+            del r
+            torch.cuda.empty_cache()
+        line["per_config"] = extra
+    return line
+
+
+# ---------------------------------------------------------- reference ---
+
+def reference(args, rank, world):
+    """The oracle as the reference arm: CPU fp64, host cores, bounded samples."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = W.make_workload(args.config, seed=0)
+    t = W.make_tensors(wl, layer=0, device="cpu")
+    bits = lambda x: None if x is None else (
+        x.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+        if x.dtype == torch.bfloat16 else x.contiguous().numpy().copy())
+    h = {k: bits(v) for k, v in t.items()}
+    threads = oracle.max_threads()
+
+    def step(mask):
+        oracle.decode(h["q"], h["k_new"], h["v_new"], h["k_pages"], h["v_pages"],
+                      wl.block_table, wl.seq_lens, wl.positions, wl.rope_theta, wl.scale,
+                      h["k_scales"], h["v_scales"], seq_mask=mask, n_threads=threads)
+
+    # calibrate a whole-batch step, then size the per-step sample (whole sequences)
+    full = np.ones(wl.n_seq, np.uint8)
+    ts = time.time()
+    step(full)
+    full_s = time.time() - ts
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    per_seq = full_s / wl.n_seq
+    n_sample = int(max(1, min(wl.n_seq, budget / max(per_seq, 1e-9))))
+    order = np.random.default_rng(0).permutation(wl.n_seq)
+
+    def mask_for(s):
+        m = np.zeros(wl.n_seq, np.uint8)
+        m[np.take(order, np.arange(s * n_sample, (s + 1) * n_sample), mode="wrap")] = 1
+        return m
+
+    for s in range(args.warmup):
+        step(mask_for(s))
+    seqs = 0
+    t0 = time.time()
+    for s in range(args.steps):
+        m = mask_for(args.warmup + s)
+        step(m)
+        seqs += int(m.sum())
+    elapsed = time.time() - t0
+    value = seqs / elapsed / wl.layers
+    sample = (f"{n_sample} of {wl.n_seq} sequences per step of one {wl.name} layer cache "
+              f"(fp64, OpenMP over (sequence, KV head)); steps of {wl.layers} layer(s) "
+              f"scaled as {wl.layers}x one layer")
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3 * wl.n_seq / n_sample * wl.layers,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), same recipe as the native arm)",
+        "config": {"workload": workload_desc(wl), "n_seq": wl.n_seq, "n_qh": wl.n_qh,
+                   "n_kvh": wl.n_kvh, "head_dim": wl.head_dim, "page_size": wl.page_size,
+                   "kv_dtype": wl.kv_dtype},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--config", choices=W.CONFIG_ORDER, default=PRIMARY)
+    ap.add_argument("--no-extra-configs", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_setup(use_gpu=args.impl == "native")
+    if args.impl == "reference":
+        line = reference(args, rank, world)
+    else:
+        line = native(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+// Host side of the C ABI declared in include/kvattn.h: argument checks (fail
+// closed, nothing is launched on an error), workspace layout, the RoPE
+// frequency table and the two launches of one decode step on the caller's
+// stream.  No host synchronisation except in kvattn_read_device_status.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kvattn_internal.cuh"
+
+using namespace kvattn;
+
+namespace {
+
+// Work units (16 tokens) a CTA is given at least when the step is small, so
+// tiny batches use few CTAs and merge few partial states.
+constexpr int kMinUnitsPerCta = 4;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_page(int page) {
+  return page == 16 || page == 32 || page == 64 || page == 128 || page == 256;
+}
+
+// SM count of the current device (cached per device).
+cudaError_t sm_count(int *out) {
+  static std::mutex mu;
+  static int cache[128] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (cache[dev] == 0) {
+    err = cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
+
+cudaError_t decode_launcher(const DecodeParams &p, int head_dim, int gs, bool int8, int grid,
+                            cudaStream_t stream, int *ctas_per_sm, bool launch) {
+  return int8 ? launch_decode_int8(p, head_dim, gs, grid, stream, ctas_per_sm, launch)
+              : launch_decode_bf16(p, head_dim, gs, grid, stream, ctas_per_sm, launch);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim) {
+  if (n_seq < 0 || n_seq > KVATTN_MAX_SEQS || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 ||
+      (head_dim != 64 && head_dim != 128))
+    return 0;
+  return workspace_layout(n_seq, n_qh, n_kvh, head_dim).total;
+}
+
+int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return KVATTN_EWORKSPACE;
+  if (cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVATTN_ECUDA;
+  return KVATTN_OK;
+}
+
+int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                         void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                         const int32_t *positions, void *out, int n_seq, int n_qh, int n_kvh,
+                         int head_dim, int page_size, float rope_theta, float scale,
+                         int kv_dtype, void *stream, int max_pages_per_seq, int num_pages,
+                         float *k_scales, float *v_scales, void *workspace,
+                         size_t workspace_bytes, int num_splits) {
+  // ---- shape checks ----
+  if (n_seq < 0 || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 || max_pages_per_seq < 1 ||
+      num_pages < 1 || num_splits < 0 || num_splits > KVATTN_MAX_SPLITS)
+    return KVATTN_EINVAL;
+  if (!std::isfinite(scale) || std::isnan(rope_theta) || std::isinf(rope_theta))
+    return KVATTN_EINVAL;
+  if (head_dim != 64 && head_dim != 128) return KVATTN_EUNSUPPORTED;
+  if (!supported_page(page_size)) return KVATTN_EUNSUPPORTED;
+  if (kv_dtype != KVATTN_KV_BF16 && kv_dtype != KVATTN_KV_INT8) return KVATTN_EUNSUPPORTED;
+  if (n_seq > KVATTN_MAX_SEQS || n_qh > 1024) return KVATTN_EUNSUPPORTED;
+  if ((long long)max_pages_per_seq * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
+  const bool int8 = kv_dtype == KVATTN_KV_INT8;
+  if (n_seq == 0) return KVATTN_OK;  // empty batch: nothing to read or write
+  // ---- pointer checks ----
+  if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_lens ||
+      !positions || !out)
+    return KVATTN_EINVAL;
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 2) || !aligned(k_new, 2) ||
+      !aligned(v_new, 2) || !aligned(out, 2) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4) || !aligned(positions, 4))
+    return KVATTN_EINVAL;
+  if (int8 && (!k_scales || !v_scales || !aligned(k_scales, 16) || !aligned(v_scales, 16)))
+    return KVATTN_EINVAL;
+  const WorkspaceLayout wl = workspace_layout(n_seq, n_qh, n_kvh, head_dim);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < wl.total)
+    return KVATTN_EWORKSPACE;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int g = n_qh / n_kvh;
+  const int gs = group_split(g);
+
+  // ---- launch 1: RoPE + append ----
+  RopeParams rp = {};
+  rp.q = static_cast<const __nv_bfloat16 *>(q);
+  rp.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  rp.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  rp.k_pages = k_pages;
+  rp.v_pages = v_pages;
+  rp.k_scales = k_scales;
+  rp.v_scales = v_scales;
+  rp.block_table = block_table;
+  rp.seq_lens = seq_lens;
+  rp.positions = positions;
+  rp.qhat = reinterpret_cast<float *>(ws + wl.qhat_off);
+  rp.counters = reinterpret_cast<uint32_t *>(ws + wl.counters_off);
+  rp.status = reinterpret_cast<uint32_t *>(ws + wl.status_off);
+  rp.n_seq = n_seq;
+  rp.n_qh = n_qh;
+  rp.n_kvh = n_kvh;
+  rp.head_dim = head_dim;
+  rp.page_size = page_size;
+  rp.max_pages = max_pages_per_seq;
+  rp.num_pages = num_pages;
+  rp.kv_int8 = int8 ? 1 : 0;
+  rp.streams_per_seq = n_kvh * (g / gs);
+  rp.use_rope = rope_theta > 0.0f ? 1 : 0;
+  // scores are formed in log2 units: fold scale * log2(e) into the query
+  rp.qscale = (float)((double)scale * 1.4426950408889634);
+  for (int i = 0; i < head_dim / 2; ++i)
+    rp.inv_freq[i] = rp.use_rope ? std::pow((double)rope_theta, -(2.0 * i) / head_dim) : 0.0;
+  if (launch_rope_append(rp, st) != cudaSuccess) return KVATTN_ECUDA;
+
+  // ---- launch 2: split-KV attention ----
+  DecodeParams dp = {};
+  dp.block_table = block_table;
+  dp.seq_lens = seq_lens;
+  dp.k_pages = k_pages;
+  dp.v_pages = v_pages;
+  dp.k_scales = k_scales;
+  dp.v_scales = v_scales;
+  dp.qhat = rp.qhat;
+  dp.out = static_cast<__nv_bfloat16 *>(out);
+  dp.records = reinterpret_cast<float *>(ws + wl.records_off);
+  dp.counters = rp.counters;
+  dp.status = rp.status;
+  dp.n_seq = n_seq;
+  dp.n_qh = n_qh;
+  dp.n_kvh = n_kvh;
+  dp.page_size = page_size;
+  dp.max_pages = max_pages_per_seq;
+  dp.num_pages = num_pages;
+  dp.n_sub = g / gs;
+  dp.min_units = kMinUnitsPerCta;
+  // the first call for a configuration on a device sets the kernel's shared
+  // memory limit and caches its occupancy; later calls only launch
+  int sms = 0, per_sm = 0;
+  if (sm_count(&sms) != cudaSuccess) return KVATTN_ECUDA;
+  if (decode_launcher(dp, head_dim, gs, int8, 0, st, &per_sm, false) != cudaSuccess)
+    return KVATTN_ECUDA;
+  int grid = num_splits;
+  if (grid == 0) {
+    grid = sms * (per_sm > 0 ? per_sm : 1);
+    if (grid > KVATTN_MAX_SPLITS) grid = KVATTN_MAX_SPLITS;
+  }
+  if (decode_launcher(dp, head_dim, gs, int8, grid, st, nullptr, true) != cudaSuccess)
+    return KVATTN_ECUDA;
+  return KVATTN_OK;
+}
+
+int kvattn_decode(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                  void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                  const int32_t *positions, void *out, int n_seq, int n_qh, int n_kvh,
+                  int head_dim, int page_size, float rope_theta, float scale, int kv_dtype,
+                  void *stream, int max_pages_per_seq, int num_pages, float *k_scales,
+                  float *v_scales, void *workspace, size_t workspace_bytes) {
+  return kvattn_decode_splits(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
+                              positions, out, n_seq, n_qh, n_kvh, head_dim, page_size,
+                              rope_theta, scale, kv_dtype, stream, max_pages_per_seq, num_pages,
+                              k_scales, v_scales, workspace, workspace_bytes, 0);
+}
+
+int kvattn_read_device_status(void *workspace, void *stream, uint32_t *bits) {
+  if (!bits) return KVATTN_EINVAL;
+  if (!workspace || !aligned(workspace, 256)) return KVATTN_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  if (cudaMemcpyAsync(&host, workspace, sizeof host, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return KVATTN_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KVATTN_ECUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof host, st) != cudaSuccess) return KVATTN_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KVATTN_ECUDA;
+  *bits = host;
+  return KVATTN_OK;
+}
+
+const char *kvattn_status_string(int status) {
+  switch (status) {
+    case KVATTN_OK: return "ok";
+    case KVATTN_EINVAL: return "invalid argument (null/misaligned pointer or inconsistent size)";
+    case KVATTN_EUNSUPPORTED: return "unsupported head_dim, page_size, kv_dtype or size";
+    case KVATTN_ECUDA: return "CUDA runtime error";
+    case KVATTN_EWORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int kvattn_version(void) { return 100; }
+
+}  // extern "C"

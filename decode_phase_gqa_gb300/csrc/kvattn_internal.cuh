@@ -1,0 +1,174 @@
+// Internal declarations of the decode-attention library: kernel parameter
+// blocks, workspace layout and small sm_100-family PTX wrappers (mbarrier,
+// bulk async copy, programmatic dependent launch).  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kvattn.h"
+
+namespace kvattn {
+
+// Tokens per work unit.  A page of page_size tokens (a multiple of 16) is
+// streamed as page_size / 16 units; each unit is one contiguous
+// [16][head_dim] block of the [page][kv_head][slot][d] pool.
+constexpr int kUnitRows = 16;
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeThreads = kDecodeWarps * 32;
+// A bounded wait gives up after this many SM clocks (about one second).
+constexpr long long kWaitCycles = 2000000000LL;
+
+// Query heads per CTA group: the largest of 4, 2, 1 dividing the GQA group.
+inline int group_split(int g) { return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1; }
+
+struct RopeParams {
+  const __nv_bfloat16 *q, *k_new, *v_new;
+  void *k_pages, *v_pages;
+  float *k_scales, *v_scales;
+  const int32_t *block_table, *seq_lens, *positions;
+  float *qhat;         // [n_seq][n_qh][d], rotated and multiplied by qscale
+  uint32_t *counters;  // [n_seq][streams_per_seq], zeroed here every call
+  uint32_t *status;
+  int n_seq, n_qh, n_kvh, head_dim, page_size, max_pages, num_pages, kv_int8;
+  int streams_per_seq, use_rope;
+  float qscale;               // scale * log2(e): scores come out in log2 units
+  double inv_freq[64];        // rope_theta^(-2i/d), i < d/2 (host-computed)
+};
+
+struct DecodeParams {
+  const int32_t *block_table, *seq_lens;
+  const void *k_pages, *v_pages;
+  const float *k_scales, *v_scales;
+  const float *qhat;
+  __nv_bfloat16 *out;
+  float *records;      // partial softmax states of split streams
+  uint32_t *counters;  // arrivals per stream
+  uint32_t *status;
+  int n_seq, n_qh, n_kvh, page_size, max_pages, num_pages;
+  int n_sub;           // query-head groups per KV head (G / GS)
+  int min_units;       // fewest units a CTA is given when work is scarce
+};
+
+// ---- workspace layout ----------------------------------------------------
+struct WorkspaceLayout {
+  size_t status_off, counters_off, qhat_off, records_off, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WorkspaceLayout workspace_layout(int n_seq, int n_qh, int n_kvh, int d) {
+  WorkspaceLayout w;
+  const int g = n_qh / n_kvh;
+  const int gs = group_split(g);
+  const size_t streams = (size_t)n_seq * n_kvh * (g / gs);
+  w.status_off = 0;
+  w.counters_off = 256;
+  w.qhat_off = align_up(w.counters_off + streams * sizeof(uint32_t), 256);
+  w.records_off = align_up(w.qhat_off + (size_t)n_seq * n_qh * d * sizeof(float), 256);
+  const size_t records = streams + KVATTN_MAX_SPLITS;
+  w.total = align_up(w.records_off + records * (size_t)gs * (d + 2) * sizeof(float), 256);
+  return w;
+}
+
+// ---- launchers (one per translation unit) ----------------------------------
+cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream);
+// Decode kernel of one (head_dim, group split) configuration: stores the
+// resident CTAs per SM in *ctas_per_sm (when non-NULL) and launches the kernel
+// with `grid` CTAs when `launch` is set.
+cudaError_t launch_decode_bf16(const DecodeParams &p, int head_dim, int gs, int grid,
+                               cudaStream_t stream, int *ctas_per_sm, bool launch);
+cudaError_t launch_decode_int8(const DecodeParams &p, int head_dim, int gs, int grid,
+                               cudaStream_t stream, int *ctas_per_sm, bool launch);
+
+#ifdef __CUDACC__
+// ---- device helpers ----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier; false if it did not complete within
+// kWaitCycles (the caller records KVATTN_DEV_TIMEOUT and stops using data).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+
+// One bulk (TMA) copy global -> shared, completing on `bar` with its byte count.
+// Both addresses 16-byte aligned, bytes a multiple of 16.  The data is read
+// once per step, so it is marked evict-first in L2.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Number of 16-token units a sequence with L cached tokens spans (the new
+// one included); 0 when the length is out of range.
+__device__ __forceinline__ int units_of(int L, long long cap_tokens) {
+  return (L >= 0 && (long long)L + 1 <= cap_tokens) ? (L + kUnitRows) / kUnitRows : 0;
+}
+#endif
+
+}  // namespace kvattn

@@ -1,0 +1,180 @@
+/*
+ * kvattn.h -- C ABI of the GB300 (sm_103a) decode-phase GQA attention library.
+ *
+ * One call performs one decode step of grouped-query attention for a batch of
+ * sequences, each contributing one new token, over a paged KV cache:
+ *
+ *   1. half-split RoPE on the new query and key ("C17 CPU-first LLM inference
+ *      engine", section 4.4 "Attention: GQA + RoPE"; "LLM inference from
+ *      smollm3.go", section "Positional encoding: why the model knows order");
+ *   2. append of the new key/value into slot seq_lens[b] of the sequence's
+ *      pages ("Qwen3-8B inference engine from scratch in C++/CUDA", section
+ *      4.3.1 "Paged KV cache"; smollm3.go page, section "KV cache");
+ *   3. scores scale * dot(q_h, k_t) for every cached position t = 0..seq_lens[b]
+ *      (the new token included) and their softmax (smollm3.go page, section
+ *      "Self-attention: how the current token looks back"; Qwen3-8B page,
+ *      section 4.4.2 "GQA grouped decode");
+ *   4. the softmax-weighted sum of the cached values.
+ * Query head h reads KV head h / (n_qh / n_kvh) (smollm3.go page, section
+ * "Multi-head attention").  The optional int8 cache stores per-(token, KV
+ * head) fp32 scales max|x| / 127 ("lightLLM, a pure-Python inference
+ * framework", section 1 "Overview", Int8KV; smollm3.go page, section "int8
+ * weight-only quantization").
+ *
+ * Conventions shared by every entry point
+ *  - Pointers marked "device" are CUDA device (or managed) memory owned by the
+ *    caller; the library allocates no memory and keeps no pointer after a call
+ *    returns, except that work already queued on `stream` uses them until it
+ *    completes.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - Arrays are dense, row-major, with the shapes given; bf16 is IEEE
+ *    bfloat16 stored in 2 bytes.
+ *  - Host-detectable errors return a non-zero status before anything is
+ *    launched.  Calls are asynchronous: no call except
+ *    kvattn_read_device_status synchronises.
+ *  - Errors found on the device (a sequence length or a block-table entry out
+ *    of range) never cause an out-of-bounds access: the offending sequence or
+ *    page is skipped and a bit is OR-ed into the device status word kept in the
+ *    workspace (KVATTN_DEV_* below).
+ */
+#ifndef KVATTN_H
+#define KVATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define KVATTN_OK 0
+#define KVATTN_EINVAL 1       /* a NULL/misaligned pointer, a negative or
+                                 inconsistent size, n_qh % n_kvh != 0 */
+#define KVATTN_EUNSUPPORTED 2 /* head_dim, page_size, kv_dtype or a size
+                                 outside what the library is built for */
+#define KVATTN_ECUDA 3        /* a CUDA runtime call or launch failed */
+#define KVATTN_EWORKSPACE 4   /* workspace NULL, misaligned or too small */
+
+/* ---- KV cache element types -------------------------------------------- */
+#define KVATTN_KV_BF16 0 /* K/V pages hold bf16 */
+#define KVATTN_KV_INT8 1 /* K/V pages hold int8 codes; scales hold fp32 */
+
+/* ---- device status bits (sticky, OR-ed into the workspace) ------------- */
+#define KVATTN_DEV_BAD_LEN 1u  /* seq_lens[b] < 0 or seq_lens[b] + 1 >
+                                  max_pages_per_seq * page_size: sequence
+                                  skipped, its output rows not written */
+#define KVATTN_DEV_BAD_PAGE 2u /* a block-table entry needed by the step is
+                                  outside [0, num_pages): that page's tokens
+                                  are left out (and no append lands there) */
+#define KVATTN_DEV_TIMEOUT 4u  /* a bounded wait for an on-chip copy gave up;
+                                  results of the call are not valid */
+
+/* ---- limits ------------------------------------------------------------ */
+#define KVATTN_MAX_SPLITS 4096 /* largest num_splits of kvattn_decode_splits */
+#define KVATTN_MAX_SEQS 8192   /* largest n_seq of one call */
+
+/*
+ * Bytes of device workspace one decode call needs for this shape.  The
+ * workspace holds the device status word, the rotated and pre-scaled
+ * queries, one completion counter per (sequence, query-head group) and the
+ * partial softmax states of split sequences.  0 when the shape is invalid.
+ */
+size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim);
+
+/*
+ * Zero the workspace's device status word (asynchronously on `stream`).
+ * Must be called once before the first kvattn_decode on a workspace; the
+ * other parts of the workspace need no initialisation.
+ * workspace: device, 256-byte aligned, at least 256 bytes.
+ */
+int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step (see the top of this file), queued on `stream`.
+ *
+ * q            device bf16 [n_seq, n_qh, head_dim]; query before RoPE.
+ * k_new, v_new device bf16 [n_seq, n_kvh, head_dim]; new key (before RoPE)
+ *              and value.
+ * k_pages,     device [num_pages, n_kvh, page_size, head_dim], bf16 or int8
+ * v_pages      per kv_dtype, 16-byte aligned; read, and written only in slot
+ *              seq_lens[b] % page_size of page block_table[b][seq_lens[b] /
+ *              page_size] for every valid sequence b.  Cached keys are stored
+ *              after RoPE.
+ * block_table  device int32 [n_seq, max_pages_per_seq]; physical page of each
+ *              logical page of a sequence.  The page of slot seq_lens[b] must
+ *              already be assigned (page allocation is the caller's policy).
+ * seq_lens     device int32 [n_seq]; tokens cached before this step, i.e. the
+ *              slot the new token goes to.  Attention covers seq_lens[b] + 1
+ *              tokens.
+ * positions    device int32 [n_seq]; RoPE position of the new token.
+ * out          device bf16 [n_seq, n_qh, head_dim]; attention output, fp32
+ *              accumulation rounded to nearest even.
+ * n_seq >= 0; with n_seq == 0 the call returns KVATTN_OK once the sizes pass
+ *              their checks, without looking at any pointer or launching.
+ * n_qh, n_kvh >= 1, n_qh % n_kvh == 0.
+ * head_dim     64 or 128.
+ * page_size    16, 32, 64, 128 or 256 tokens.
+ * rope_theta   RoPE base; <= 0 disables RoPE (a NoPE layer).  Frequency of
+ *              pair i is rope_theta^(-2i/head_dim); pairs are (i, i + head_dim/2).
+ * scale        score scale (usually 1/sqrt(head_dim)); finite.
+ * kv_dtype     KVATTN_KV_BF16 or KVATTN_KV_INT8.
+ * stream       cudaStream_t.
+ * max_pages_per_seq >= 1: row length of block_table.
+ * num_pages >= 1: pages in each of k_pages / v_pages (for bounds checks).
+ * k_scales,    device fp32 [num_pages, n_kvh, page_size], 16-byte aligned;
+ * v_scales     required for int8 (the scale of each cached row), NULL for bf16.
+ * workspace    device, 256-byte aligned, >= kvattn_workspace_size(...) bytes,
+ *              initialised once with kvattn_workspace_init.  Calls that share
+ *              a workspace must be ordered on one stream (or otherwise not
+ *              overlap on the GPU).
+ *
+ * The appended key is rotated with fp32 cos/sin (computed in double, then
+ * rounded), fp32 products and sums each rounded separately, then stored as
+ * bf16 (nearest even) or as int8 codes clamp(rint(x / s), -127, 127) with
+ * s = max|x| / 127 (s = 0 for an all-zero row); the value is stored as given
+ * (bf16) or quantised the same way.  The new token is attended through its
+ * stored value.
+ */
+int kvattn_decode(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                  void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                  const int32_t *positions, void *out, int n_seq, int n_qh, int n_kvh,
+                  int head_dim, int page_size, float rope_theta, float scale, int kv_dtype,
+                  void *stream, int max_pages_per_seq, int num_pages, float *k_scales,
+                  float *v_scales, void *workspace, size_t workspace_bytes);
+
+/*
+ * kvattn_decode with an explicit work split: the flattened list of 16-token
+ * units over all (sequence, KV head) pairs is cut into at most `num_splits`
+ * equal shares, one per CTA; a sequence cut across shares is finished by a
+ * log-sum-exp merge of the shares' partial softmax states.  num_splits = 0
+ * picks the default (a multiple of the GPU's SM count); otherwise
+ * 1 <= num_splits <= KVATTN_MAX_SPLITS.  Results for different splits agree
+ * to fp32 rounding.
+ */
+int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new,
+                         void *k_pages, void *v_pages, const int32_t *block_table,
+                         const int32_t *seq_lens, const int32_t *positions, void *out,
+                         int n_seq, int n_qh, int n_kvh, int head_dim, int page_size,
+                         float rope_theta, float scale, int kv_dtype, void *stream,
+                         int max_pages_per_seq, int num_pages, float *k_scales,
+                         float *v_scales, void *workspace, size_t workspace_bytes,
+                         int num_splits);
+
+/*
+ * Wait for `stream`, copy the device status word (KVATTN_DEV_* bits OR-ed by
+ * every call since the last read or init) into *bits, and clear it.
+ * Synchronises `stream`.
+ */
+int kvattn_read_device_status(void *workspace, void *stream, uint32_t *bits);
+
+/* Static English description of a return code (never NULL). */
+const char *kvattn_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int kvattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVATTN_H */

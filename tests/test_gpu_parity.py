@@ -1,0 +1,223 @@
+"""Parity of the CUDA decode path with the CPU oracle (needs a GB300).
+
+Every case runs the library through the C ABI and the oracle on the same
+seeded inputs, then checks: the whole K/V pool (and int8 scales) bit for bit
+after the append, the attention output within max-abs 2e-2 / mean-abs 2e-3,
+and a clean device status word.
+"""
+import numpy as np
+import pytest
+import torch
+
+from decode_phase_gqa_gb300 import kvattn as K
+from decode_phase_gqa_gb300 import workloads as W
+from tests import refmath as R
+from tests.gpu_helpers import (assert_close, check_against_oracle, out_f64, pool_bits,
+                               run_gpu, to_dev)
+from tests.helpers import host_inputs, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+
+def custom(n_qh, n_kvh, lens, d=128, page=16, kv="bf16", seed=0, theta=1e4, spare=0.1,
+           max_len=None):
+    wl = W.make_workload("custom", seed=seed, n_seq=len(lens), n_qh=n_qh, n_kvh=n_kvh,
+                         head_dim=d, page_size=page, rope_theta=theta, kv_dtype=kv,
+                         lengths=list(lens), spare=spare, max_len=max_len)
+    return wl, host_inputs(wl)
+
+
+def test_tiny_config():
+    wl = W.make_workload("tiny", seed=0)
+    check_against_oracle(wl, host_inputs(wl))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n_qh,n_kvh", [(4, 1), (16, 4), (8, 8), (4, 2), (12, 4), (24, 2), (6, 2)])
+def test_head_layouts(kv, d, n_qh, n_kvh):
+    # several 16-token tiles, ragged tails, the new token alone in a new page
+    lens = [0, 15, 16, 17, 100, 257, 511]
+    wl, h = custom(n_qh, n_kvh, lens, d=d, kv=kv, seed=n_qh * 7 + n_kvh)
+    check_against_oracle(wl, h)
+
+
+@pytest.mark.parametrize("page", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_page_sizes(page, kv):
+    lens = [1, page - 1, page, 3 * page + 5, 700]
+    wl, h = custom(8, 2, lens, d=64, page=page, kv=kv, seed=page)
+    check_against_oracle(wl, h)
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 5, 17, 64, 333, 4096])
+def test_split_counts_agree(num_splits):
+    wl, h = custom(16, 4, [3000, 1, 40, 777, 2048], d=128, seed=3)
+    out, ref, _ = check_against_oracle(wl, h, num_splits=num_splits)
+    # and against the single-share result: fp32 reordering only (1 bf16 ulp)
+    d = to_dev(host_inputs(wl))
+    one, _, _ = run_gpu(wl, d, num_splits=1)
+    a, b = out_f64(out), out_f64(one)
+    assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-6)
+
+
+def test_results_are_deterministic():
+    wl, h = custom(32, 8, [5000, 300, 12, 4096], d=128, seed=11)
+    outs = []
+    for _ in range(3):
+        d = to_dev(h)
+        o, st, _ = run_gpu(wl, d)
+        assert st == 0
+        outs.append(pool_bits(o))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+def test_page_permutation_is_bit_identical():
+    wl, h = custom(8, 2, [200, 64, 1000], d=128, seed=5, spare=0.0)
+    d1 = to_dev(h)
+    o1, _, _ = run_gpu(wl, d1)
+    perm = np.random.default_rng(1).permutation(wl.num_pages).astype(np.int32)
+    h2 = dict(h)
+    for k in ("k_pages", "v_pages"):
+        h2[k] = np.empty_like(h[k])
+        h2[k][perm] = h[k]
+    h2["block_table"] = np.where(wl.block_table >= 0, perm[np.maximum(wl.block_table, 0)],
+                                 -1).astype(np.int32)
+    o2, _, _ = run_gpu(wl, to_dev(h2))
+    assert np.array_equal(pool_bits(o1), pool_bits(o2))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_single_token_returns_value(kv):
+    wl, h = custom(8, 2, [0, 0, 0], d=128, kv=kv, seed=2)
+    d = to_dev(h)
+    out, st, _ = run_gpu(wl, d)
+    assert st == 0
+    ref, _, kp, vp, ks, vs = oracle_decode(wl, h)
+    if kv == "bf16":
+        # one weight of exactly 1: the stored value comes back bit for bit
+        want = np.repeat(h["v_new"], 4, axis=1)
+        assert np.array_equal(pool_bits(out), want)
+    else:
+        assert_close(out_f64(out), ref)
+
+
+def test_identical_keys_give_mean_of_values():
+    wl, h = custom(4, 1, [300], d=64, seed=4, theta=0.0)
+    # every cached key equals the new key (NoPE, so it is stored unchanged)
+    P = wl.page_size
+    for t in range(300):
+        h["k_pages"][wl.block_table[0, t // P], :, t % P] = h["k_new"][0]
+    out, st, _ = run_gpu(wl, to_dev(h))
+    vr = R.gather_rows(h["v_pages"], None, wl.block_table, 0, 299, P, False)[:, 0]
+    vmean = (vr.sum(axis=0) + R.bf16_bits_to_f64(h["v_new"][0, 0])) / 301
+    assert np.max(np.abs(out_f64(out)[0] - vmean)) < 2e-3
+
+
+def test_new_token_dominates_when_aligned():
+    wl, h = custom(1, 1, [900], d=128, seed=6, theta=0.0)
+    h["k_new"][0, 0] = h["q"][0, 0]
+    wl.scale = 30.0
+    out, st, _ = run_gpu(wl, to_dev(h))
+    assert np.max(np.abs(out_f64(out)[0, 0] - R.bf16_bits_to_f64(h["v_new"][0, 0]))) < 1e-2
+
+
+def test_relative_position_invariance_through_appends():
+    # fill two caches token by token through the library, positions t and t + s,
+    # then decode at m and m + s: scores depend on m - t only
+    d, n = 64, 40
+    rng = np.random.default_rng(0)
+    raw_k = R.f32_to_bf16_bits(rng.standard_normal((n + 1, 1, d)))
+    raw_v = R.f32_to_bf16_bits(rng.standard_normal((n + 1, 1, d)))
+    q = R.f32_to_bf16_bits(rng.standard_normal((1, 4, d)))
+    outs = []
+    for shift in (0, 1000):
+        wl, h = custom(4, 1, [n], d=d, seed=0, theta=1e4)
+        dev = to_dev(h)
+        ws = K.alloc_workspace(1, 4, 1, d)
+        out = torch.empty((1, 4, d), dtype=torch.bfloat16, device="cuda")
+        for t in range(n + 1):
+            dev["seq_lens"].fill_(t)
+            dev["positions"].fill_(t + shift)
+            dev["k_new"].copy_(torch.from_numpy(raw_k[t:t + 1].view(np.int16)).view(torch.bfloat16))
+            dev["v_new"].copy_(torch.from_numpy(raw_v[t:t + 1].view(np.int16)).view(torch.bfloat16))
+            if t == n:
+                dev["q"].copy_(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16))
+            K.kvattn_decode(dev["q"], dev["k_new"], dev["v_new"], dev["k_pages"], dev["v_pages"],
+                            dev["block_table"], dev["seq_lens"], dev["positions"], out,
+                            rope_theta=1e4, scale=wl.scale, workspace=ws)
+        assert K.kvattn_read_device_status(ws) == 0
+        outs.append(out_f64(out))
+    assert np.max(np.abs(outs[0] - outs[1])) < 2e-2
+
+
+def test_bad_length_and_bad_page_are_skipped_and_reported():
+    wl, h = custom(8, 2, [50, 60, 70], d=64, seed=8)
+    h["seq_lens"] = np.array([50, -3, 70], np.int32)
+    d = to_dev(h)
+    out, st, _ = run_gpu(wl, d)
+    assert st & K.KVATTN_DEV_BAD_LEN
+    o = out_f64(out)
+    assert np.all(np.isnan(o[1])) and np.all(np.isfinite(o[[0, 2]]))
+    ref, ost, *_ = oracle_decode(wl, h)
+    assert ost & 1
+    assert_close(o, ref, rows=[0, 2])
+    # an out-of-range page: its tokens are left out, everything else is exact
+    wl2, h2 = custom(8, 2, [50, 60, 70], d=64, seed=8)
+    bt = h2["block_table"].copy()
+    bt[1, 1] = 10 ** 6
+    bt[2, 0] = -7
+    h2["block_table"] = bt
+    wl2.block_table = bt
+    d2 = to_dev(h2)
+    out2, st2, _ = run_gpu(wl2, d2)
+    assert st2 & K.KVATTN_DEV_BAD_PAGE
+    ref2, ost2, kp, vp, _, _ = oracle_decode(wl2, h2)
+    assert ost2 & 2
+    assert_close(out_f64(out2), ref2)
+    assert np.array_equal(pool_bits(d2["k_pages"]), kp)
+
+
+def test_length_at_table_capacity():
+    # L + 1 == max_pages * page: the last slot of the last page
+    wl, h = custom(8, 2, [127, 63], d=128, seed=9, max_len=127)
+    assert wl.max_pages_per_seq == 8
+    check_against_oracle(wl, h)
+
+
+def test_many_short_sequences():
+    lens = list(np.random.default_rng(2).integers(0, 40, size=300))
+    wl, h = custom(8, 2, lens, d=64, seed=12)
+    check_against_oracle(wl, h)
+
+
+def test_empty_batch_is_a_no_op():
+    ws = K.alloc_workspace(0, 8, 2, 64)
+    z = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device="cuda")
+    K.kvattn_decode(z(0, 8, 64), z(0, 2, 64), z(0, 2, 64), z(4, 2, 16, 64), z(4, 2, 16, 64),
+                    z(0, 4, dt=torch.int32), z(0, dt=torch.int32), z(0, dt=torch.int32),
+                    z(0, 8, 64), rope_theta=1e4, scale=0.125, workspace=ws)
+    assert K.kvattn_read_device_status(ws) == 0
+
+
+def test_captured_in_cuda_graph():
+    wl, h = custom(16, 4, [1000, 20, 333], d=128, seed=13)
+    d = to_dev(h)
+    ws = K.alloc_workspace(3, 16, 4, 128)
+    out = torch.empty((3, 16, 128), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        K.kvattn_decode(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
+                        d["block_table"], d["seq_lens"], d["positions"], out,
+                        rope_theta=wl.rope_theta, scale=wl.scale, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        K.kvattn_decode(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
+                        d["block_table"], d["seq_lens"], d["positions"], out,
+                        rope_theta=wl.rope_theta, scale=wl.scale, workspace=ws, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    ref, *_ = oracle_decode(wl, h)
+    assert_close(out_f64(out), ref)
