@@ -33,6 +33,7 @@ KVATTN_DEV_TIMEOUT = 4
 
 KVATTN_MAX_SPLITS = 4096
 KVATTN_MAX_SEQS = 8192
+KVATTN_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 _lock = threading.Lock()
@@ -64,6 +65,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvattn_decode.restype = I
         L.kvattn_decode_splits.argtypes = dec + [I]
         L.kvattn_decode_splits.restype = I
+        L.kvattn_decode_noalloc.argtypes = dec[:-2] + [P]
+        L.kvattn_decode_noalloc.restype = I
         L.kvattn_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         L.kvattn_read_device_status.restype = I
         L.kvattn_status_string.argtypes = [I]

@@ -161,6 +161,42 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new,
                          int num_splits);
 
 /*
+ * kvattn_decode for callers that can neither pass a workspace nor let the
+ * library allocate one.  The source pages have no counterpart of this entry
+ * point.
+ *
+ * Such callers exist: an engine that reserved nearly all of HBM for its
+ * KV-page pool at start-up and keeps no allocator for anything else, or a
+ * plugin inside a host framework that owns every device allocation and does
+ * not allow plugins to call cudaMalloc.  The scratch that kvattn_decode keeps
+ * in the caller's workspace lives here in one fixed array inside the library,
+ * KVATTN_NOALLOC_SCRATCH_BYTES long; every GPU that loads the library holds it
+ * until the process exits.  No cudaMalloc/cudaFree or other allocation is
+ * made.
+ *
+ * Arguments: those of kvattn_decode without workspace/workspace_bytes, plus
+ * dev_status  device uint32, 4-byte aligned, that receives this call's
+ *             KVATTN_DEV_* bits; may be NULL.
+ * Returns KVATTN_EUNSUPPORTED, before anything is queued, when the shape needs
+ * more scratch than the array holds, i.e. when
+ * kvattn_workspace_size(n_seq, n_qh, n_kvh, head_dim) >
+ * KVATTN_NOALLOC_SCRATCH_BYTES.
+ * The first call on a device (with that device current) looks up the array's
+ * device address; make that first call before any stream capture.
+ * Every call uses the same array and finds the previous call's contents in it:
+ * calls that overlap on the GPU (other streams, other host threads) race and
+ * corrupt each other's results, so order them on one stream.
+ */
+#define KVATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+int kvattn_decode_noalloc(const void *q, const void *k_new, const void *v_new,
+                          void *k_pages, void *v_pages, const int32_t *block_table,
+                          const int32_t *seq_lens, const int32_t *positions, void *out,
+                          int n_seq, int n_qh, int n_kvh, int head_dim, int page_size,
+                          float rope_theta, float scale, int kv_dtype, void *stream,
+                          int max_pages_per_seq, int num_pages, float *k_scales,
+                          float *v_scales, uint32_t *dev_status);
+
+/*
  * Wait for `stream`, copy the device status word (KVATTN_DEV_* bits OR-ed by
  * every call since the last read or init) into *bits, and clear it.
  * Synchronises `stream`.

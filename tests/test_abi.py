@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
-        "kvattn_decode", "kvattn_decode_splits", "kvattn_read_device_status",
+        "kvattn_decode", "kvattn_decode_noalloc", "kvattn_decode_splits",
+        "kvattn_read_device_status",
         "kvattn_status_string", "kvattn_version", "kvattn_workspace_init",
         "kvattn_workspace_size"])
 
