@@ -1,4 +1,4 @@
-// Instantiations of the split-KV decode kernel for the int8 KV cache.
+// Instantiations of the CUDA-core split-KV decode kernel for the int8 KV cache.
 #include "decode_kernel.cuh"
 
 namespace kvattn {

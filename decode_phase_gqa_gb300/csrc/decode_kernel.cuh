@@ -1,4 +1,5 @@
-// Split-KV flash-decoding kernel over a paged KV cache (second launch of a step).
+// Split-KV flash-decoding kernel, CUDA-core inner loop (used for the int8 KV
+// cache; the bf16 cache uses the tensor-core kernel of decode_mma.cuh).
 //
 // Work decomposition.  Every (sequence b, KV head j, query-head group) is a
 // "stream" of ceil((L_b + 1) / 16) units of 16 cached tokens.  The streams are
@@ -34,7 +35,7 @@
 #include <set>
 #include <utility>
 
-#include "kvattn_internal.cuh"
+#include "decode_common.cuh"
 
 namespace kvattn {
 
@@ -50,15 +51,20 @@ struct DecodeCfg {
   static constexpr int kTile = kUnitRows * D * kESize;
   static constexpr int kScaleBytes = INT8 ? kUnitRows * 4 : 0;
   static constexpr int kStage = 2 * kTile + 2 * kScaleBytes;
-  static constexpr int kSW = (72 * 1024) / (kDecodeWarps * kStage) > 8
-                                 ? 8
-                                 : (72 * 1024) / (kDecodeWarps * kStage);
+  static constexpr int kScBytes = kDecodeWarps * kUnitRows * GS * 4;
+  static constexpr int kMergeBytes = kDecodeWarps * GS * (D + 3) * 4;  // acc, m, l, reduction
+  static constexpr int kMiscBytes = 64;
+  // stages per warp: as many as fit a 75 KB CTA (3 CTAs per SM) next to the
+  // other buffers and a 1 KB allowance for the per-sequence prefix sums
+  static constexpr int kOther = kDecodeWarps * 8 * 8 + kScBytes + kMergeBytes + kMiscBytes;
+  static constexpr int kSWFit = (kCtaSmemBudget - kOther - 1024) / (kDecodeWarps * kStage);
+  static constexpr int kSW = kSWFit > 8 ? 8 : kSWFit;
   static constexpr int kStagesBytes = kDecodeWarps * kSW * kStage;
   static constexpr int kBarBytes = kDecodeWarps * kSW * 8;
-  static constexpr int kScBytes = kDecodeWarps * kUnitRows * GS * 4;
-  static constexpr int kMergeBytes = kDecodeWarps * GS * (D + 2) * 4;
-  static constexpr int kMiscBytes = 64;
   static constexpr int kFixedSmem = kStagesBytes + kBarBytes + kScBytes + kMergeBytes + kMiscBytes;
+  // the rotated queries [GS][D] and cos/sin [D/2] of a stream's start share
+  // the merge area, which is only used at the stream's end
+  static_assert(GS * D * 4 + (D / 2) * 8 <= kDecodeWarps * GS * D * 4, "query buffers");
   static_assert(kStage % 128 == 0, "stage must keep 128-byte alignment");
   static_assert(kSW >= 2, "need at least double buffering");
 };
@@ -107,21 +113,6 @@ __device__ __forceinline__ void load_row8(const uint8_t *src, float (&f)[8]) {
   }
 }
 
-// a[i] for a lane-dependent i without dynamic register indexing
-template <int N>
-__device__ __forceinline__ float pick(const float (&a)[N], int i) {
-  float r = a[0];
-#pragma unroll
-  for (int k = 1; k < N; ++k) r = (i == k) ? a[k] : r;
-  return r;
-}
-
-// CTA that owns flattened unit t when T units are cut into n equal shares
-// (share c covers [floor(c T / n), floor((c + 1) T / n))).
-__device__ __forceinline__ long long owner_of(long long t, long long T, long long n) {
-  return ((t + 1) * n - 1) / T;
-}
-
 template <int D, int GS, bool INT8>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -133,82 +124,45 @@ __global__ void __launch_bounds__(kDecodeThreads)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStagesBytes);
   float *sc_all = reinterpret_cast<float *>(smem + C::kStagesBytes + C::kBarBytes);
   float *mg = sc_all + W * kUnitRows * GS;
-  int *misc = reinterpret_cast<int *>(mg + W * GS * (D + 2));
+  float *mg_m = mg + W * GS * D;
+  float *mg_l = mg_m + W * GS;
+  float *red = mg_l + W * GS;
+  int *misc = reinterpret_cast<int *>(red + W * GS);
   int *pref = misc + C::kMiscBytes / 4;
+  float *qs = mg;
+  float2 *cs = reinterpret_cast<float2 *>(qs + GS * D);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int B = p.n_seq;
   const int spu = p.n_kvh * p.n_sub;
-  const long long cap = (long long)p.max_pages * p.page_size;
-
-  // ---- units per sequence and their prefix sums (shared memory) ----------
-  {
-    const int chunk = (B + kDecodeThreads - 1) / kDecodeThreads;
-    const int b0 = min(B, tid * chunk), b1 = min(B, b0 + chunk);
-    int local = 0;
-    for (int b = b0; b < b1; ++b) local += units_of(p.seq_lens[b], cap);
-    int incl = local;
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, m);
-      if (lane >= m) incl += v;
-    }
-    if (lane == 31) misc[warp] = incl;
-    __syncthreads();
-    int run = incl - local, total = 0;
-    for (int w = 0; w < W; ++w) {
-      if (w < warp) run += misc[w];
-      total += misc[w];
-    }
-    for (int b = b0; b < b1; ++b) {
-      pref[b] = run;
-      run += units_of(p.seq_lens[b], cap);
-    }
-    if (tid == 0) pref[B] = total;
-    if (tid == 0) {
-      for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
-      fence_barrier_init();
-    }
-    __syncthreads();
+  Share sh;
+  if (!plan_share<kDecodeThreads>(p, pref, misc, sh)) return;
+  if (tid == 0) {
+    for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
   }
-  const long long T = (long long)spu * pref[B];
-  if (T == 0) return;
-  const long long n_active = min((long long)gridDim.x, max(1LL, (T + p.min_units - 1) / p.min_units));
-  const int c = blockIdx.x;
-  if (c >= n_active) return;
-  const long long t0 = (long long)c * T / n_active;
-  const long long t1 = (long long)(c + 1) * T / n_active;
-
-  // everything below reads what the RoPE/append grid wrote
-  pdl_wait_primary();
+  __syncthreads();
+  const long long t0 = sh.t0, t1 = sh.t1;
 
   const long long span = t1 - t0;
   const int count_w = span > warp ? (int)((span - warp - 1) / W + 1) : 0;
   const int cc = lane % C::kLPR, rg = lane / C::kLPR;
   const uint64_t pol = l2_evict_first_policy();
 
-  // sequence containing flattened unit t0 (binary search on the prefix sums)
-  int start_b;
-  {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((long long)spu * pref[mid] <= t0) lo = mid; else hi = mid - 1;
-    }
-    start_b = lo;
-  }
-
   // ---- producer side (lane 0 of each warp) --------------------------------
-  int ib = start_b;  // issue cursor
+  // Only the last unit of a stream holds the token the append grid writes in
+  // this step: wait for that grid before the first such unit.
+  int ib = sh.start_b;  // issue cursor
+  bool appended_visible = false;
   auto issue = [&](int i) {
     const long long t = t0 + warp + (long long)i * W;
-    while ((long long)spu * pref[ib + 1] <= t) ++ib;
-    const int units = pref[ib + 1] - pref[ib];
-    const long long r = t - (long long)spu * pref[ib];
-    const int si = (int)(r / units), u = (int)(r % units);
-    const int j = si / p.n_sub;
-    const int tok = u * kUnitRows;
-    const int page = p.block_table[(size_t)ib * p.max_pages + tok / p.page_size];
+    const UnitPos up = locate_unit(t, ib, pref, spu);
+    if (up.u == up.units - 1 && !appended_visible) {
+      pdl_wait_primary();
+      appended_visible = true;
+    }
+    const int j = up.si / p.n_sub;
+    const int tok = up.u * kUnitRows;
+    const int page = __ldg(p.block_table + (size_t)up.b * p.max_pages + tok / p.page_size);
     const int st = warp * C::kSW + i % C::kSW;
     uint8_t *dst = stages + (size_t)st * C::kStage;
     if (page >= 0 && page < p.num_pages) {
@@ -229,42 +183,34 @@ __global__ void __launch_bounds__(kDecodeThreads)
   };
   int issued = 0;
   if (lane == 0) {
-    const int n0 = min(C::kSW, count_w);
-    for (int i = 0; i < n0; ++i) issue(i);
-    issued = n0;
+    for (; issued < min(C::kSW, count_w); ++issued) issue(issued);
   }
 
   // ---- consumer side ---------------------------------------------------------
   float *sc = sc_all + warp * kUnitRows * GS;
-  float *mg_m = mg + W * GS * D;
-  float *mg_l = mg_m + W * GS;
-  volatile int *flag = misc + 8;
   bool aborted = false;
   int consumed = 0;
-  int cb = start_b;
+  int cb = sh.start_b;
   long long t = t0;
   while (t < t1) {
-    while ((long long)spu * pref[cb + 1] <= t) ++cb;
-    const int units = pref[cb + 1] - pref[cb];
-    const long long base = (long long)spu * pref[cb];
-    const int si = (int)((t - base) / units);
-    const long long F = base + (long long)si * units, E = F + units;
+    const UnitPos sp = locate_unit(t, cb, pref, spu);
+    const int si = sp.si;
+    const long long F = sp.first, E = F + sp.units;
     const long long e = min(t1, E);
-    const int L = p.seq_lens[cb];
+    const int L = __ldg(p.seq_lens + cb);
     const int j = si / p.n_sub, sub = si % p.n_sub;
     const int h0 = j * GS * p.n_sub + sub * GS;
 
+    stream_queries<D, GS, kDecodeThreads>(p, cb, h0, qs, cs);
     float q[GS][8];
-    {
-      const float *qp = p.qhat + ((size_t)cb * p.n_qh + h0) * D + cc * 8;
 #pragma unroll
-      for (int hh = 0; hh < GS; ++hh) {
-        const float4 x0 = *reinterpret_cast<const float4 *>(qp + hh * D);
-        const float4 x1 = *reinterpret_cast<const float4 *>(qp + hh * D + 4);
-        q[hh][0] = x0.x; q[hh][1] = x0.y; q[hh][2] = x0.z; q[hh][3] = x0.w;
-        q[hh][4] = x1.x; q[hh][5] = x1.y; q[hh][6] = x1.z; q[hh][7] = x1.w;
-      }
+    for (int hh = 0; hh < GS; ++hh) {
+      const float4 x0 = *reinterpret_cast<const float4 *>(qs + hh * D + cc * 8);
+      const float4 x1 = *reinterpret_cast<const float4 *>(qs + hh * D + cc * 8 + 4);
+      q[hh][0] = x0.x; q[hh][1] = x0.y; q[hh][2] = x0.z; q[hh][3] = x0.w;
+      q[hh][4] = x1.x; q[hh][5] = x1.y; q[hh][6] = x1.z; q[hh][7] = x1.w;
     }
+    named_barrier_sync(1, kDecodeThreads);  // queries read: the merge area is free again
     float m[GS], acc[GS][8], ls[C::kHPL];
 #pragma unroll
     for (int hh = 0; hh < GS; ++hh) {
@@ -425,68 +371,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     named_barrier_sync(1, kDecodeThreads);
 
-    const bool whole = (F >= t0) && (E <= t1);
-    const int sid = cb * spu + si;
-    __nv_bfloat16 *outp = p.out + ((size_t)cb * p.n_qh + h0) * D;
-    float *rec = p.records + (size_t)(sid + c) * (GS * (D + 2));
-    for (int idx = tid; idx < GS * D; idx += kDecodeThreads) {
-      const int hh = idx / D, dd = idx % D;
-      float M = kNegInf;
-#pragma unroll
-      for (int w = 0; w < W; ++w) M = fmaxf(M, mg_m[w * GS + hh]);
-      float o = 0.f, l = 0.f;
-      if (M != kNegInf) {
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-          const float f = exp2f(mg_m[w * GS + hh] - M);
-          o += f * mg[(w * GS + hh) * D + dd];
-          l += f * mg_l[w * GS + hh];
-        }
-      }
-      if (whole) {
-        outp[hh * D + dd] = __float2bfloat16_rn(l > 0.f ? o / l : 0.f);
-      } else {
-        rec[hh * D + dd] = o;
-        if (dd == 0) {
-          rec[GS * D + hh] = M;
-          rec[GS * D + GS + hh] = l;
-        }
-      }
-    }
-    if (!whole) {
-      __threadfence();
-      named_barrier_sync(1, kDecodeThreads);
-      if (tid == 0) {
-        const long long c0 = owner_of(F, T, n_active), c1 = owner_of(E - 1, T, n_active);
-        const unsigned nseg = (unsigned)(c1 - c0 + 1);
-        const unsigned old = atomicAdd(&p.counters[sid], 1u);
-        flag[0] = (old == nseg - 1) ? 1 : 0;
-        flag[1] = (int)c0;
-        flag[2] = (int)nseg;
-      }
-      named_barrier_sync(1, kDecodeThreads);
-      if (flag[0]) {
-        __threadfence();
-        const int c0 = flag[1], nseg = flag[2];
-        const float *r0 = p.records + (size_t)(sid + c0) * (GS * (D + 2));
-        for (int idx = tid; idx < GS * D; idx += kDecodeThreads) {
-          const int hh = idx / D, dd = idx % D;
-          float M = kNegInf;
-          for (int s = 0; s < nseg; ++s)
-            M = fmaxf(M, __ldcg(r0 + (size_t)s * GS * (D + 2) + GS * D + hh));
-          float o = 0.f, l = 0.f;
-          if (M != kNegInf) {
-            for (int s = 0; s < nseg; ++s) {
-              const float *rs = r0 + (size_t)s * GS * (D + 2);
-              const float f = exp2f(__ldcg(rs + GS * D + hh) - M);
-              o += f * __ldcg(rs + hh * D + dd);
-              l += f * __ldcg(rs + GS * D + GS + hh);
-            }
-          }
-          outp[hh * D + dd] = __float2bfloat16_rn(l > 0.f ? o / l : 0.f);
-        }
-      }
-    }
+    finish_stream<D, GS, W, kDecodeThreads>(p, sh, mg, mg_m, mg_l, misc + 8, red, F, E, cb,
+                                            cb * spu + si, h0);
     named_barrier_sync(1, kDecodeThreads);
     t = e;
   }

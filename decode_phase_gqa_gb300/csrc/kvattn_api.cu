@@ -1,7 +1,10 @@
 // Host side of the C ABI declared in include/kvattn.h: argument checks (fail
 // closed, nothing is launched on an error), workspace layout, the RoPE
-// frequency table and the two launches of one decode step on the caller's
-// stream.  No host synchronisation except in kvattn_read_device_status.
+// frequency table, the TMA descriptors of the pools and the two launches of
+// one decode step on the caller's stream (append, then split-KV attention as
+// its programmatic dependent).  No host synchronisation except in kvattn_read_device_status.
+#include <cudaTypedefs.h>
+
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -13,9 +16,9 @@ using namespace kvattn;
 
 namespace {
 
-// Work units (16 tokens) a CTA is given at least when the step is small, so
-// tiny batches use few CTAs and merge few partial states.
-constexpr int kMinUnitsPerCta = 4;
+// Work units (16 tokens) a share is given at least when the step is small, so
+// tiny batches use few shares and merge few partial states.
+constexpr int kMinUnitsPerShare = 4;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -40,6 +43,37 @@ cudaError_t sm_count(int *out) {
   return cudaSuccess;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D view [rows][head_dim] bf16 of a K or V pool, 16 x 64 boxes, 128-byte
+// swizzle (the box's 128-byte rows are written with their 16-byte chunks
+// permuted by row mod 8, which the kernel's ldmatrix addressing undoes)
+bool encode_pool_map(CUtensorMap *map, const void *base, long long rows, int head_dim) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estride[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+             box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t decode_launcher(const DecodeParams &p, int head_dim, int gs, bool int8, int grid,
                             cudaStream_t stream, int *ctas_per_sm, bool launch) {
   return int8 ? launch_decode_int8(p, head_dim, gs, grid, stream, ctas_per_sm, launch)
@@ -59,7 +93,8 @@ size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim) {
 
 int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return KVATTN_EWORKSPACE;
-  if (cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
     return KVATTN_ECUDA;
   return KVATTN_OK;
 }
@@ -82,13 +117,15 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   if (kv_dtype != KVATTN_KV_BF16 && kv_dtype != KVATTN_KV_INT8) return KVATTN_EUNSUPPORTED;
   if (n_seq > KVATTN_MAX_SEQS || n_qh > 1024) return KVATTN_EUNSUPPORTED;
   if ((long long)max_pages_per_seq * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
+  // pool rows are addressed with 32-bit TMA coordinates
+  if ((long long)num_pages * n_kvh * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
   const bool int8 = kv_dtype == KVATTN_KV_INT8;
   if (n_seq == 0) return KVATTN_OK;  // empty batch: nothing to read or write
   // ---- pointer checks ----
   if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_lens ||
       !positions || !out)
     return KVATTN_EINVAL;
-  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 2) || !aligned(k_new, 2) ||
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 16) || !aligned(k_new, 2) ||
       !aligned(v_new, 2) || !aligned(out, 2) || !aligned(block_table, 4) ||
       !aligned(seq_lens, 4) || !aligned(positions, 4))
     return KVATTN_EINVAL;
@@ -103,50 +140,50 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   const int g = n_qh / n_kvh;
   const int gs = group_split(g);
 
-  // ---- launch 1: RoPE + append ----
-  RopeParams rp = {};
-  rp.q = static_cast<const __nv_bfloat16 *>(q);
-  rp.k_new = static_cast<const __nv_bfloat16 *>(k_new);
-  rp.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-  rp.k_pages = k_pages;
-  rp.v_pages = v_pages;
-  rp.k_scales = k_scales;
-  rp.v_scales = v_scales;
-  rp.block_table = block_table;
-  rp.seq_lens = seq_lens;
-  rp.positions = positions;
-  rp.qhat = reinterpret_cast<float *>(ws + wl.qhat_off);
-  rp.counters = reinterpret_cast<uint32_t *>(ws + wl.counters_off);
-  rp.status = reinterpret_cast<uint32_t *>(ws + wl.status_off);
-  rp.n_seq = n_seq;
-  rp.n_qh = n_qh;
-  rp.n_kvh = n_kvh;
-  rp.head_dim = head_dim;
-  rp.page_size = page_size;
-  rp.max_pages = max_pages_per_seq;
-  rp.num_pages = num_pages;
-  rp.kv_int8 = int8 ? 1 : 0;
-  rp.streams_per_seq = n_kvh * (g / gs);
-  rp.use_rope = rope_theta > 0.0f ? 1 : 0;
-  // scores are formed in log2 units: fold scale * log2(e) into the query
-  rp.qscale = (float)((double)scale * 1.4426950408889634);
+  // ---- launch 1: RoPE on the new key, append of key and value ----
+  const bool use_rope = rope_theta > 0.0f;
+  AppendParams ap = {};
+  ap.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  ap.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  ap.k_pages = k_pages;
+  ap.v_pages = v_pages;
+  ap.k_scales = k_scales;
+  ap.v_scales = v_scales;
+  ap.block_table = block_table;
+  ap.seq_lens = seq_lens;
+  ap.positions = positions;
+  ap.status = reinterpret_cast<uint32_t *>(ws + wl.status_off);
+  ap.n_seq = n_seq;
+  ap.n_kvh = n_kvh;
+  ap.head_dim = head_dim;
+  ap.page_size = page_size;
+  ap.max_pages = max_pages_per_seq;
+  ap.num_pages = num_pages;
+  ap.kv_int8 = int8 ? 1 : 0;
+  ap.use_rope = use_rope ? 1 : 0;
+  // frequency of rotation pair i: rope_theta^(-2i/d), in double
   for (int i = 0; i < head_dim / 2; ++i)
-    rp.inv_freq[i] = rp.use_rope ? std::pow((double)rope_theta, -(2.0 * i) / head_dim) : 0.0;
-  if (launch_rope_append(rp, st) != cudaSuccess) return KVATTN_ECUDA;
+    ap.inv_freq[i] = use_rope ? std::pow((double)rope_theta, -(2.0 * i) / head_dim) : 0.0;
+  if (launch_append(ap, st) != cudaSuccess) return KVATTN_ECUDA;
 
   // ---- launch 2: split-KV attention ----
   DecodeParams dp = {};
   dp.block_table = block_table;
   dp.seq_lens = seq_lens;
+  dp.positions = positions;
+  dp.q = static_cast<const __nv_bfloat16 *>(q);
   dp.k_pages = k_pages;
   dp.v_pages = v_pages;
   dp.k_scales = k_scales;
   dp.v_scales = v_scales;
-  dp.qhat = rp.qhat;
   dp.out = static_cast<__nv_bfloat16 *>(out);
   dp.records = reinterpret_cast<float *>(ws + wl.records_off);
-  dp.counters = rp.counters;
-  dp.status = rp.status;
+  dp.counters = reinterpret_cast<uint32_t *>(ws + wl.counters_off);
+  dp.status = ap.status;
+  dp.use_rope = ap.use_rope;
+  // scores are formed in log2 units: fold scale * log2(e) into the query
+  dp.qscale = (float)((double)scale * 1.4426950408889634);
+  for (int i = 0; i < 64; ++i) dp.inv_freq[i] = ap.inv_freq[i];
   dp.n_seq = n_seq;
   dp.n_qh = n_qh;
   dp.n_kvh = n_kvh;
@@ -154,18 +191,27 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.max_pages = max_pages_per_seq;
   dp.num_pages = num_pages;
   dp.n_sub = g / gs;
-  dp.min_units = kMinUnitsPerCta;
+  dp.min_units = kMinUnitsPerShare;
+  if (!int8) {
+    const long long rows = (long long)num_pages * n_kvh * page_size;
+    if (!encode_pool_map(&dp.tmap_k, k_pages, rows, head_dim) ||
+        !encode_pool_map(&dp.tmap_v, v_pages, rows, head_dim))
+      return KVATTN_ECUDA;
+  }
   // the first call for a configuration on a device sets the kernel's shared
-  // memory limit and caches its occupancy; later calls only launch
+  // memory limit and caches its occupancy; later calls only launch.  A share
+  // of the unit list is one warp's work in the bf16 kernel and one CTA's in
+  // the int8 kernel.
   int sms = 0, per_sm = 0;
   if (sm_count(&sms) != cudaSuccess) return KVATTN_ECUDA;
   if (decode_launcher(dp, head_dim, gs, int8, 0, st, &per_sm, false) != cudaSuccess)
     return KVATTN_ECUDA;
-  int grid = num_splits;
-  if (grid == 0) {
-    grid = sms * (per_sm > 0 ? per_sm : 1);
-    if (grid > KVATTN_MAX_SPLITS) grid = KVATTN_MAX_SPLITS;
-  }
+  const int per_cta = int8 ? 1 : kDecodeWarps;
+  int shares = num_splits;
+  if (shares == 0) shares = sms * (per_sm > 0 ? per_sm : 1) * per_cta;
+  if (shares > KVATTN_MAX_SPLITS) shares = KVATTN_MAX_SPLITS;
+  dp.n_shares = shares;
+  const int grid = (shares + per_cta - 1) / per_cta;
   if (decode_launcher(dp, head_dim, gs, int8, grid, st, nullptr, true) != cudaSuccess)
     return KVATTN_ECUDA;
   return KVATTN_OK;

@@ -3,8 +3,9 @@
 // bulk async copy, programmatic dependent launch).  Not part of the ABI.
 #pragma once
 
-#include <cuda_runtime.h>
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/kvattn.h"
@@ -17,43 +18,55 @@ namespace kvattn {
 constexpr int kUnitRows = 16;
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeThreads = kDecodeWarps * 32;
+// shared memory a decode CTA may use so that 3 fit on one SM (228 KB, with
+// 1 KB reserved per CTA)
+constexpr int kCtaSmemBudget = 75 * 1024;
 // A bounded wait gives up after this many SM clocks (about one second).
 constexpr long long kWaitCycles = 2000000000LL;
 
 // Query heads per CTA group: the largest of 4, 2, 1 dividing the GQA group.
 inline int group_split(int g) { return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1; }
 
-struct RopeParams {
-  const __nv_bfloat16 *q, *k_new, *v_new;
+struct AppendParams {
+  const __nv_bfloat16 *k_new, *v_new;
   void *k_pages, *v_pages;
   float *k_scales, *v_scales;
   const int32_t *block_table, *seq_lens, *positions;
-  float *qhat;         // [n_seq][n_qh][d], rotated and multiplied by qscale
-  uint32_t *counters;  // [n_seq][streams_per_seq], zeroed here every call
   uint32_t *status;
-  int n_seq, n_qh, n_kvh, head_dim, page_size, max_pages, num_pages, kv_int8;
-  int streams_per_seq, use_rope;
-  float qscale;               // scale * log2(e): scores come out in log2 units
+  int n_seq, n_kvh, head_dim, page_size, max_pages, num_pages, kv_int8, use_rope;
   double inv_freq[64];        // rope_theta^(-2i/d), i < d/2 (host-computed)
 };
 
 struct DecodeParams {
-  const int32_t *block_table, *seq_lens;
+  // 2-D views [num_pages * n_kvh * page_size rows][head_dim] of the bf16
+  // K and V pools, boxes of 16 rows x 64 columns, 128-byte swizzle
+  CUtensorMap tmap_k, tmap_v;
+  const int32_t *block_table, *seq_lens, *positions;
+  const __nv_bfloat16 *q;
   const void *k_pages, *v_pages;
   const float *k_scales, *v_scales;
-  const float *qhat;
   __nv_bfloat16 *out;
   float *records;      // partial softmax states of split streams
-  uint32_t *counters;  // arrivals per stream
+  uint32_t *counters;  // arrivals per stream; the last arrival resets it to 0
   uint32_t *status;
   int n_seq, n_qh, n_kvh, page_size, max_pages, num_pages;
   int n_sub;           // query-head groups per KV head (G / GS)
-  int min_units;       // fewest units a CTA is given when work is scarce
+  int n_shares;        // the unit list is cut into at most this many shares
+  int min_units;       // fewest units a share is given when work is scarce
+  int use_rope;
+  float qscale;        // scale * log2(e): scores come out in log2 units
+  double inv_freq[64]; // rope_theta^(-2i/d), i < d/2 (host-computed)
 };
+
+// floats of one partial record (acc[gs][d], m[gs], l[gs]), padded so every
+// record starts on a 16-byte boundary
+__host__ __device__ inline constexpr int record_floats(int gs, int d) {
+  return (gs * (d + 2) + 3) & ~3;
+}
 
 // ---- workspace layout ----------------------------------------------------
 struct WorkspaceLayout {
-  size_t status_off, counters_off, qhat_off, records_off, total;
+  size_t status_off, counters_off, records_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -65,15 +78,14 @@ inline WorkspaceLayout workspace_layout(int n_seq, int n_qh, int n_kvh, int d) {
   const size_t streams = (size_t)n_seq * n_kvh * (g / gs);
   w.status_off = 0;
   w.counters_off = 256;
-  w.qhat_off = align_up(w.counters_off + streams * sizeof(uint32_t), 256);
-  w.records_off = align_up(w.qhat_off + (size_t)n_seq * n_qh * d * sizeof(float), 256);
+  w.records_off = align_up(w.counters_off + streams * sizeof(uint32_t), 256);
   const size_t records = streams + KVATTN_MAX_SPLITS;
-  w.total = align_up(w.records_off + records * (size_t)gs * (d + 2) * sizeof(float), 256);
+  w.total = align_up(w.records_off + records * (size_t)record_floats(gs, d) * sizeof(float), 256);
   return w;
 }
 
 // ---- launchers (one per translation unit) ----------------------------------
-cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 // Decode kernel of one (head_dim, group split) configuration: stores the
 // resident CTAs per SM in *ctas_per_sm (when non-NULL) and launches the kernel
 // with `grid` CTAs when `launch` is set.

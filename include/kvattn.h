@@ -75,16 +75,18 @@ extern "C" {
 
 /*
  * Bytes of device workspace one decode call needs for this shape.  The
- * workspace holds the device status word, the rotated and pre-scaled
- * queries, one completion counter per (sequence, query-head group) and the
- * partial softmax states of split sequences.  0 when the shape is invalid.
+ * workspace holds the device status word, one arrival counter per (sequence,
+ * KV head, query-head group) and the partial softmax states of sequences
+ * whose work is split across CTAs.  0 when the shape is invalid.
  */
 size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim);
 
 /*
- * Zero the workspace's device status word (asynchronously on `stream`).
- * Must be called once before the first kvattn_decode on a workspace; the
- * other parts of the workspace need no initialisation.
+ * Zero the workspace (all workspace_bytes, asynchronously on `stream`).  Must
+ * be called once before the first kvattn_decode on a workspace, and again
+ * after a call that reported KVATTN_DEV_TIMEOUT.  Every completed call leaves
+ * the arrival counters at zero, so a workspace can be reused for any shape it
+ * is large enough for.
  * workspace: device, 256-byte aligned, at least 256 bytes.
  */
 int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
@@ -92,7 +94,8 @@ int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
 /*
  * One decode step (see the top of this file), queued on `stream`.
  *
- * q            device bf16 [n_seq, n_qh, head_dim]; query before RoPE.
+ * q            device bf16 [n_seq, n_qh, head_dim], 16-byte aligned; query
+ *              before RoPE.
  * k_new, v_new device bf16 [n_seq, n_kvh, head_dim]; new key (before RoPE)
  *              and value.
  * k_pages,     device [num_pages, n_kvh, page_size, head_dim], bf16 or int8
