@@ -44,7 +44,8 @@ PRIMARY = "smollm3"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 SRC_FILES = ["decode_common.cuh", "decode_mma.cuh", "decode_kernel.cuh", "kvattn_internal.cuh",
-             "append.cu", "kvattn_api.cu", "decode_bf16.cu", "decode_int8.cu"]
+             "append.cu", "kvattn_api.cu", "decode_bf16.cu", "decode_int8.cu",
+             "combine.cu"]
 
 
 def workload_desc(wl: W.Workload) -> str:
@@ -228,6 +229,8 @@ class NativeCase:
         return [[i] for i in range(self.copies)]
 
     def capture(self, stream):
+        """One graph per step (a step's calls), plus one graph of a whole
+        rotation (every step once, in order) to cut graph-launch gaps."""
         for grp in self.step_groups():
             for i in grp:          # warm the library's per-device set-up first
                 self.call(i, stream)
@@ -238,10 +241,31 @@ class NativeCase:
                 for i in grp:
                     self.call(i, stream)
             self.graphs.append(g)
+        self.rotation = None
+        if len(self.graphs) > 1:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for grp in self.step_groups():
+                    for i in grp:
+                        self.call(i, stream)
+            self.rotation = g
         torch.cuda.synchronize()
 
     def replay(self, step):
         self.graphs[step % len(self.graphs)].replay()
+
+    def replay_steps(self, first, n):
+        """Replay steps first .. first + n - 1 (rotation order), whole
+        rotations from the rotation graph."""
+        s, end = first, first + n
+        r = len(self.graphs)
+        while s < end:
+            if self.rotation is not None and s % r == 0 and end - s >= r:
+                self.rotation.replay()
+                s += r
+            else:
+                self.graphs[s % r].replay()
+                s += 1
 
     def check_status(self):
         return self.K.kvattn_read_device_status(self.ws)
@@ -257,8 +281,7 @@ def time_steps(case: NativeCase, steps: int, warmup: int, world: int, stream):
         t0 = time.time()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for s in range(steps):
-            case.replay(warmup + s)
+        case.replay_steps(warmup, steps)
         end.record(stream)
         torch.cuda.synchronize()
         t1 = time.time()
@@ -417,7 +440,8 @@ def native(args, rank, world, local):
             "kv_read_frac_of_peak": main["kv_gbs"] / world / peak,
             "l2": f"inputs larger than L2: {main['copies']} independent caches rotated, "
                   f"{main['copies'] * wl.kv_bytes / 2**20:.0f} MiB of KV per rotation",
-            "timing": "CUDA events on the launching stream around K graph replays",
+            "timing": "CUDA events on the launching stream around K steps replayed from "
+                      "CUDA graphs (a graph per rotation of the caches, a graph per step)",
             "parallelism": f"{world} independent replica(s), one batch per GPU",
         },
         "roofline": {
@@ -428,7 +452,8 @@ def native(args, rank, world, local):
                       "timed together): algorithmic K+V bytes per call / call time",
         },
         "e2e": main["e2e"],
-        "gpu_launches": 2 * main["calls_per_step"] * args.steps,
+        # append + decode (+ combine for the bf16 cache) per call
+        "gpu_launches": (2 if wl.kv_dtype == "int8" else 3) * main["calls_per_step"] * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "impl": "native",
     }

@@ -117,13 +117,31 @@ __device__ __forceinline__ UnitPos locate_unit(long long t, int &b, const int *p
   return r;
 }
 
+// ---- RoPE angles of the query, fp32 only -----------------------------------------
+// Fractional part, in [-0.5, 0.5], of pos * g turns, g = g.x + g.y (fp32 head
+// and remainder).  The position is split into a multiple of 4096 and a
+// remainder (both exact in fp32), each product is split into its rounded value
+// and exact rounding error with an FMA, and the fractional part of every piece
+// is taken exactly (x - rint(x) is exact in binary floating point) before the
+// pieces are added: the result is accurate to about 1e-7 turns for positions
+// below 2^20, without any double-precision arithmetic.
+__device__ __forceinline__ float frac_turns(int pos, float2 g) {
+  const float ph = (float)(pos & ~0xfff), pl = (float)(pos & 0xfff);
+  const float a = ph * g.x, ae = fmaf(ph, g.x, -a);
+  const float b = pl * g.x, be = fmaf(pl, g.x, -b);
+  float t = (a - rintf(a)) + (ae - rintf(ae));
+  t += (b - rintf(b)) + (be - rintf(be));
+  t -= rintf(t);
+  const float c = (float)pos * g.y;
+  t += c - rintf(c);
+  return t - rintf(t);
+}
+
 // ---- queries ----------------------------------------------------------------------
 // Rotated queries of one stream's GS heads, multiplied by scale * log2(e), into
 // shared memory qs[GS][D] (fp32), using all kThreads threads of the CTA; cs
-// holds D/2 float2.  The angle position * theta^(-2i/d) is formed in double
-// and reduced modulo 2 pi in double (Cody-Waite reduction with 2 pi split into
-// a head and a tail), then cos/sin are taken in fp32: the query needs fp32
-// accuracy only, the bit-exact recipe applies to the stored key.
+// holds D/2 float2.  The angles come from frac_turns and sincospif: the query
+// needs fp32 accuracy only, the bit-exact recipe applies to the stored key.
 template <int D, int GS, int kThreads>
 __device__ __forceinline__ void stream_queries(const DecodeParams &p, int b, int h0, float *qs,
                                                float2 *cs) {
@@ -143,13 +161,7 @@ __device__ __forceinline__ void stream_queries(const DecodeParams &p, int b, int
   }
   if (tid < H) {
     float c = 1.f, sn = 0.f;
-    if (p.use_rope) {
-      const double phi = (double)__ldg(p.positions + b) * p.inv_freq[tid];
-      const double k = rint(phi * 0.15915494309189535);  // phi / (2 pi)
-      double r = fma(-k, 6.283185307179586, phi);          // head of 2 pi
-      r = fma(-k, 2.4492935982947064e-16, r);              // tail of 2 pi
-      sincosf((float)r, &sn, &c);
-    }
+    if (p.use_rope) sincospif(2.f * frac_turns(__ldg(p.positions + b), p.turns[tid]), &sn, &c);
     cs[tid] = make_float2(c, sn);
   }
   named_barrier_sync(1, kThreads);

@@ -8,8 +8,8 @@
 // tensor copies (cp.async.bulk.tensor.2d, [16 rows][64 columns] boxes, 128-byte
 // swizzle so the ldmatrix reads below hit all 32 banks), keeps its softmax
 // state in registers, and at each stream boundary either writes the output (a
-// stream inside its share) or a partial record; the last warp to finish a
-// split stream merges its records (atomic arrival counter, no waiting).
+// stream inside its share) or a partial record that the combine kernel
+// (combine.cu, launched as this grid's programmatic dependent) merges.
 //
 // Per unit the warp computes, with m16n8k16 bf16 MMAs (fp32 accumulate):
 //   S^T[16 tokens][8] = K[16][d] * Qc^T[d][8]
@@ -52,7 +52,7 @@ struct MmaCfg {
   static constexpr int kHL = GS == 1 ? 1 : 2;  // query heads per lane
   static constexpr int kStagesBytes = W * kSW * kStage;
   static constexpr int kBarOff = kStagesBytes;
-  static constexpr int kFreqOff = kBarOff + W * kSW * 8;  // rope frequencies, double[D/2]
+  static constexpr int kFreqOff = kBarOff + W * kSW * 8;  // rope turns per position, float2[D/2]
   static constexpr int kMiscOff = kFreqOff + 512;
   static constexpr int kQOff = kMiscOff + 64;             // [W][GS][D] bf16
   static constexpr int kValidOff = kQOff + W * kQBytes;   // [W][kSW] int
@@ -76,37 +76,36 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-// B fragments of the query columns for one stream, built by the warp from the
-// raw query rows q[GS][D] (bf16, shared memory): column c = lane / 4 of the MMA
-// is the bf16 head of query head c (c < GS), its bf16 remainder (GS <= c <
-// 2 GS), or zero.  RoPE: angle i of position `pos` is formed in double and
-// reduced modulo 2 pi in double (Cody-Waite, 2 pi split into head and tail),
-// then cos/sin are taken in fp32 (the query needs fp32 accuracy only).  Lane
-// l computes angles l + 32k; the others are shuffled in.
+// RoPE of the query, fp32 only (the query needs fp32 accuracy): lane l holds
+// cos/sin of angles l + 32k of position `pos`, from frac_turns and sincospif.
+// Then the B fragments of the query columns for one stream, built by the warp
+// from the raw query rows q[GS][D] (bf16, shared memory): column c = lane / 4
+// of the MMA is the bf16 head of query head c (c < GS), its bf16 remainder
+// (GS <= c < 2 GS), or zero; the angles each lane needs are shuffled in.
+template <int D>
+__device__ __forceinline__ void warp_query_angles(const DecodeParams &p, const float2 *turns,
+                                                  int pos, int lane, float (&cr)[D / 64],
+                                                  float (&sr)[D / 64]) {
+#pragma unroll
+  for (int k = 0; k < D / 64; ++k) {
+    cr[k] = 1.f;
+    sr[k] = 0.f;
+    if (p.use_rope) sincospif(2.f * frac_turns(pos, turns[lane + 32 * k]), &sr[k], &cr[k]);
+  }
+}
+
 template <int D, int GS>
-__device__ __forceinline__ void warp_query_fragments(const DecodeParams &p, const double *freq,
-                                                     const __nv_bfloat16 *qrows, int pos,
-                                                     int lane, uint32_t (&qb)[D / 16][2]) {
-  constexpr int H = D / 2, KS = D / 16, AP = H / 32;
+__device__ __forceinline__ void warp_query_fragments(const DecodeParams &p, const float (&cr)[D / 64],
+                                                     const float (&sr)[D / 64],
+                                                     const __nv_bfloat16 *qrows, int lane,
+                                                     uint32_t (&qb)[D / 16][2]) {
+  constexpr int H = D / 2, KS = D / 16;
   const int col = lane >> 2;
   const bool used = col < 2 * GS;
   const bool is_lo = col >= GS;
   const int head = used ? (is_lo ? col - GS : col) : 0;
   const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrows + head * D);
   const int d0 = 2 * (lane & 3);
-  float cr[AP], sr[AP];
-#pragma unroll
-  for (int k = 0; k < AP; ++k) {
-    cr[k] = 1.f;
-    sr[k] = 0.f;
-    if (p.use_rope) {
-      const double phi = (double)pos * freq[lane + 32 * k];
-      const double n = rint(phi * 0.15915494309189535);  // phi / (2 pi)
-      double r = fma(-n, 6.283185307179586, phi);          // head of 2 pi
-      r = fma(-n, 2.4492935982947064e-16, r);              // tail of 2 pi
-      sincosf((float)r, &sr[k], &cr[k]);
-    }
-  }
 #pragma unroll
   for (int kp = 0; kp < KS / 2; ++kp) {
     // elements 16 kp + d0 + {0, 1, 8, 9} (first half) and the same + H
@@ -145,88 +144,6 @@ __device__ __forceinline__ void warp_query_fragments(const DecodeParams &p, cons
   }
 }
 
-// Merge of the nseg partial records of one stream (first record r0) by one
-// warp: per-head maximum and normaliser, then the rescaled sum of the
-// accumulators, written to out (bf16).
-template <int D, int GS>
-__device__ __forceinline__ void warp_merge_records(const float *r0, int nseg,
-                                                   __nv_bfloat16 *outp, int lane) {
-  constexpr int RS = record_floats(GS, D);
-  const float kNegInf = -INFINITY;
-  float M[GS], L[GS];
-#pragma unroll
-  for (int hh = 0; hh < GS; ++hh) M[hh] = kNegInf;
-  for (int s = lane; s < nseg; s += 32)
-#pragma unroll
-    for (int hh = 0; hh < GS; ++hh) M[hh] = fmaxf(M[hh], __ldcg(r0 + (size_t)s * RS + GS * D + hh));
-#pragma unroll
-  for (int hh = 0; hh < GS; ++hh) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) M[hh] = fmaxf(M[hh], __shfl_xor_sync(0xffffffffu, M[hh], m));
-    L[hh] = 0.f;
-  }
-  for (int s = lane; s < nseg; s += 32)
-#pragma unroll
-    for (int hh = 0; hh < GS; ++hh)
-      if (M[hh] != kNegInf)
-        L[hh] += exp2f(__ldcg(r0 + (size_t)s * RS + GS * D + hh) - M[hh]) *
-                 __ldcg(r0 + (size_t)s * RS + GS * D + GS + hh);
-#pragma unroll
-  for (int hh = 0; hh < GS; ++hh)
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) L[hh] += __shfl_xor_sync(0xffffffffu, L[hh], m);
-  // each lane owns float4 columns q4 = lane + 32 k of the [GS][D] accumulator
-  constexpr int NQ = (GS * D / 4 + 31) / 32;
-  float4 o[NQ];
-  int hq[NQ];
-#pragma unroll
-  for (int k = 0; k < NQ; ++k) {
-    o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    hq[k] = ((lane + 32 * k) * 4) / D;
-  }
-  constexpr int U = 4;  // records in flight per lane
-  for (int s0 = 0; s0 < nseg; s0 += U) {
-    float4 a[U][NQ];
-    float f[U][NQ];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int s = s0 + u;
-#pragma unroll
-      for (int k = 0; k < NQ; ++k) {
-        const int q4 = lane + 32 * k;
-        if (s < nseg && q4 < GS * D / 4) {
-          const float *rs = r0 + (size_t)s * RS;
-          a[u][k] = __ldcg(reinterpret_cast<const float4 *>(rs) + q4);
-          f[u][k] = __ldcg(rs + GS * D + hq[k]);
-        } else {
-          a[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          f[u][k] = kNegInf;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-#pragma unroll
-      for (int k = 0; k < NQ; ++k) {
-        const float mh = pick(M, hq[k]);
-        const float e = (mh == kNegInf || f[u][k] == kNegInf) ? 0.f : exp2f(f[u][k] - mh);
-        o[k].x += e * a[u][k].x; o[k].y += e * a[u][k].y;
-        o[k].z += e * a[u][k].z; o[k].w += e * a[u][k].w;
-      }
-  }
-#pragma unroll
-  for (int k = 0; k < NQ; ++k) {
-    const int q4 = lane + 32 * k;
-    if (q4 < GS * D / 4) {
-      const float lh = pick(L, hq[k]);
-      const float inv = lh > 0.f ? 1.f / lh : 0.f;
-      __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(outp + q4 * 4);
-      dst[0] = __floats2bfloat162_rn(o[k].x * inv, o[k].y * inv);
-      dst[1] = __floats2bfloat162_rn(o[k].z * inv, o[k].w * inv);
-    }
-  }
-}
-
 template <int D, int GS>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
@@ -237,17 +154,27 @@ __global__ void __launch_bounds__(kDecodeThreads)
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t *stages = smem;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
-  double *freq = reinterpret_cast<double *>(smem + C::kFreqOff);
+  float2 *turns = reinterpret_cast<float2 *>(smem + C::kFreqOff);
   int *misc = reinterpret_cast<int *>(smem + C::kMiscOff);
   int *pref = reinterpret_cast<int *>(smem + C::kPrefOff);
   int *lens = pref + p.n_seq + 1;
   int *poss = lens + p.n_seq;
 
+  pdl_launch_dependents();  // the combine grid may start planning at once
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    // every CTA pulls its slice of the queries into L2 at once, so that the
+    // warps' query rows do not queue behind the flood of K/V requests
+    const size_t q_lines = ((size_t)p.n_seq * p.n_qh * D * 2 + 127) / 128;
+    const size_t per = (q_lines + gridDim.x - 1) / gridDim.x;
+    const char *qc = reinterpret_cast<const char *>(p.q);
+    for (size_t l = blockIdx.x * per + tid; l < min(q_lines, (blockIdx.x + 1) * per); l += kDecodeThreads)
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(qc + l * 128));
+  }
   __nv_bfloat16 *qbuf = reinterpret_cast<__nv_bfloat16 *>(smem + C::kQOff) + warp * GS * D;
   volatile int *svalid = reinterpret_cast<int *>(smem + C::kValidOff) + warp * C::kSW;
   const int spu = p.n_kvh * p.n_sub;
-  if (tid < D / 2) freq[tid] = p.inv_freq[tid];
+  if (tid < D / 2) turns[tid] = p.turns[tid];
   if (tid == 0) {
     for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -289,7 +216,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
   int pcur = start_b;  // per-lane cursor of the page windows
   int win_base = 0;
   int win_page = lane < count ? page_of_unit(p, pref, spu, wt0 + lane, pcur) : -1;
-  int nxt_page = 32 + lane < count ? page_of_unit(p, pref, spu, wt0 + 32 + lane, pcur) : -1;
+  int nxt_page = -1;  // loaded once the first units are requested
   int ib = start_b;
   bool appended_visible = false;
   auto issue = [&](int i) {  // called by the whole warp, in unit order
@@ -326,6 +253,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
   };
   int issued = 0;
   for (; issued < min(C::kSW, count); ++issued) issue(issued);
+  if (32 + lane < count) nxt_page = page_of_unit(p, pref, spu, wt0 + 32 + lane, pcur);
 
   // ---- consumer ---------------------------------------------------------------
   const int hb = (GS == 4) ? 2 * (lane & 1) : 0;  // first head of this lane's columns
@@ -343,9 +271,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int sid = sp.b * spu + sp.si;
 
     uint32_t qb[C::kKSteps][2];
+    float cr[D / 64], sr[D / 64];
+    warp_query_angles<D>(p, turns, poss[sp.b], lane, cr, sr);  // while the rows land
     cp_async_wait_all();
     __syncwarp();
-    warp_query_fragments<D, GS>(p, freq, qbuf, poss[sp.b], lane, qb);
+    warp_query_fragments<D, GS>(p, cr, sr, qbuf, lane, qb);
     __syncwarp();
     if (E < wt1) {  // the share continues: fetch the next stream's query rows
       int b = sp.b;
@@ -548,26 +478,6 @@ __global__ void __launch_bounds__(kDecodeThreads)
             rec[GS * D + GS + hb + h] = l[h];
           }
         }
-      }
-      __threadfence();
-      __syncwarp();
-      int last = 0, g0 = 0, nseg = 0;
-      if (lane == 0) {
-        const long long w0 = owner_of(F, T, nwa), w1 = owner_of(E - 1, T, nwa);
-        nseg = (int)(w1 - w0 + 1);
-        g0 = (int)w0;
-        const unsigned old = atomicAdd(&p.counters[sid], 1u);
-        last = old == (unsigned)(nseg - 1);
-        // every part of the stream has arrived: leave the counter at zero for
-        // the next call (the workspace starts zeroed)
-        if (last) p.counters[sid] = 0u;
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        g0 = __shfl_sync(0xffffffffu, g0, 0);
-        nseg = __shfl_sync(0xffffffffu, nseg, 0);
-        warp_merge_records<D, GS>(p.records + (size_t)(sid + g0) * C::RS, nseg, outp, lane);
       }
     }
     t = e;

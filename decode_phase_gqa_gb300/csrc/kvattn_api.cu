@@ -1,8 +1,8 @@
 // Host side of the C ABI declared in include/kvattn.h: argument checks (fail
 // closed, nothing is launched on an error), workspace layout, the RoPE
-// frequency table, the TMA descriptors of the pools and the two launches of
-// one decode step on the caller's stream (append, then split-KV attention as
-// its programmatic dependent).  No host synchronisation except in kvattn_read_device_status.
+// frequency table, the TMA descriptors of the pools and the launches of one
+// decode step on the caller's stream: append, split-KV attention as its
+// programmatic dependent, and (bf16 cache) the merge of split sequences.  No host synchronisation except in kvattn_read_device_status.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -183,7 +183,11 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.use_rope = ap.use_rope;
   // scores are formed in log2 units: fold scale * log2(e) into the query
   dp.qscale = (float)((double)scale * 1.4426950408889634);
-  for (int i = 0; i < 64; ++i) dp.inv_freq[i] = ap.inv_freq[i];
+  for (int i = 0; i < 64; ++i) {
+    const double g = ap.inv_freq[i] * 0.15915494309189535;  // / (2 pi)
+    const float hi = (float)g;
+    dp.turns[i] = make_float2(hi, (float)(g - (double)hi));
+  }
   dp.n_seq = n_seq;
   dp.n_qh = n_qh;
   dp.n_kvh = n_kvh;
@@ -214,6 +218,8 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   const int grid = (shares + per_cta - 1) / per_cta;
   if (decode_launcher(dp, head_dim, gs, int8, grid, st, nullptr, true) != cudaSuccess)
     return KVATTN_ECUDA;
+  // ---- launch 3 (bf16): merge of the streams the warp shares split ----
+  if (!int8 && launch_combine(dp, head_dim, gs, shares, st) != cudaSuccess) return KVATTN_ECUDA;
   return KVATTN_OK;
 }
 

@@ -55,7 +55,9 @@ struct DecodeParams {
   int min_units;       // fewest units a share is given when work is scarce
   int use_rope;
   float qscale;        // scale * log2(e): scores come out in log2 units
-  double inv_freq[64]; // rope_theta^(-2i/d), i < d/2 (host-computed)
+  // turns per position of rotation pair i, rope_theta^(-2i/d) / (2 pi), as an
+  // fp32 head and remainder (host-computed in double)
+  float2 turns[64];
 };
 
 // floats of one partial record (acc[gs][d], m[gs], l[gs]), padded so every
@@ -93,6 +95,10 @@ cudaError_t launch_decode_bf16(const DecodeParams &p, int head_dim, int gs, int 
                                cudaStream_t stream, int *ctas_per_sm, bool launch);
 cudaError_t launch_decode_int8(const DecodeParams &p, int head_dim, int gs, int grid,
                                cudaStream_t stream, int *ctas_per_sm, bool launch);
+// Merge of the partial records of split streams left by the bf16 decode
+// kernel (n_warps = number of warp shares it used).
+cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int n_warps,
+                           cudaStream_t stream);
 
 #ifdef __CUDACC__
 // ---- device helpers ----------------------------------------------------------
