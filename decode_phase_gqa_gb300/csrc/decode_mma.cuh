@@ -1,29 +1,49 @@
-// Split-KV flash-decoding kernel for the bf16 KV cache, tensor-core inner loop.
+// Split-KV flash-decoding kernel, tensor-core inner loop, for the bf16 and the
+// int8 KV cache.
 //
 // Work split.  Every (sequence, KV head, query-head group) is a stream of
 // 16-token units; the streams are laid end to end and the flattened unit list
 // is cut into equal contiguous shares, one per WARP of the grid.  Warps are
 // independent after the CTA's prologue (the per-sequence prefix sums): each
 // streams its share through its own ring of shared-memory stages filled by TMA
-// tensor copies (cp.async.bulk.tensor.2d, [16 rows][64 columns] boxes, 128-byte
-// swizzle so the ldmatrix reads below hit all 32 banks), keeps its softmax
-// state in registers, and at each stream boundary either writes the output (a
-// stream inside its share) or a partial record that the combine kernel
-// (combine.cu, launched as this grid's programmatic dependent) merges.
+// tensor copies (cp.async.bulk.tensor.2d, [16 rows][128 or 64 bytes] boxes,
+// 128- or 64-byte swizzle so the ldmatrix reads below hit all 32 banks; the
+// int8 cache's per-row scales come with the same barrier by cp.async.bulk),
+// keeps its softmax state in registers, and at each stream boundary either
+// writes the output (a stream inside its share) or a partial record that the
+// combine kernel (combine.cu, launched as this grid's programmatic dependent)
+// merges.
 //
-// Per unit the warp computes, with m16n8k16 bf16 MMAs (fp32 accumulate):
+// Per unit the warp computes, with m16n8k16 MMAs (fp32 accumulate):
 //   S^T[16 tokens][8] = K[16][d] * Qc^T[d][8]
 //   O^T[d][8]        += V^T[d][16] * P^T[16][8]
-// The 8 MMA columns carry, for the GS query heads of the group, the bf16 head
-// of each value and its bf16 remainder (x = hi + lo), so neither the query nor
-// the softmax weights lose precision to bf16 rounding: columns h and GS + h
-// are added back together.  K and V themselves are bf16 in the cache, exact.
+// The 8 MMA columns carry, for the GS query heads of the group, the head of
+// each value and its remainder (x = hi + lo) in the MMA's input type, so
+// neither the query nor the softmax weights lose precision to rounding:
+// columns h and GS + h are added back together.  K and V are exact in that
+// type: bf16 values of the bf16 cache, and int8 codes of the int8 cache
+// converted to f16 in registers (every integer below 2^11 is an f16).
 // Tokens are the MMA rows, so one K/V block serves every head of the group
 // ("Qwen3-8B inference engine from scratch in C++/CUDA", section 4.4.2:
 // read the group's KV once for all its query heads), and the online softmax
 // ("LLM inference from smollm3.go", section "Self-attention") runs on the
 // accumulator fragments in fp32, in log2 units.
+//
+// Int8 cache (per-row scales ks_t, vs_t, row = scale * codes: "lightLLM, a
+// pure-Python inference framework", section 1 "Overview", Int8KV; the dot
+// product of the codes times the row scale as in "LLM inference from
+// smollm3.go", section "int8 weight-only quantization"):
+//   * score_t = (q . codes_t) * ks_t: the query columns are f16 head and
+//     remainder of q * 2^kq, kq a power-of-two range scale per stream, and the
+//     raw dot product is multiplied by ks_t * 2^-kq;
+//   * the value weights p_t vs_t are formed as 2^(s_t + log2 vs_t - mo) with
+//     their own running maximum mo, so the largest weight of the stream so far
+//     is 1 (no f16 overflow or underflow whatever the scales); the normaliser
+//     l keeps the plain softmax maximum m, and the accumulator is brought
+//     from 2^mo to 2^m when the stream's part ends.
 #pragma once
+
+#include <cuda_fp16.h>
 
 #include <map>
 #include <mutex>
@@ -34,24 +54,31 @@
 
 namespace kvattn {
 
-template <int D, int GS>
+template <int D, int GS, bool INT8>
 struct MmaCfg {
   static constexpr int W = kDecodeWarps;
-  static constexpr int kRegions = D / 64;   // 64-column swizzled boxes per 16-row tile
-  static constexpr int kBox = 16 * 64 * 2;  // bytes of one box (2 KB)
+  static constexpr int kRowBytes = INT8 ? D : 2 * D;               // one cached row
+  static constexpr int kBoxW = kRowBytes < 128 ? kRowBytes : 128;  // bytes per box row
+  static constexpr int kChunks = kBoxW / 16;     // 16-byte chunks per box row
+  static constexpr int kRegions = kRowBytes / kBoxW;  // boxes per 16-row tile
+  static constexpr int kBox = kUnitRows * kBoxW;
   static constexpr int kTile = kRegions * kBox;
   static constexpr int kStage = 2 * kTile;  // K then V
+  static constexpr int kScales = INT8 ? 2 * kUnitRows * 4 : 0;  // K then V row scales
   static constexpr int kQBytes = GS * D * 2;  // one stream's raw query rows (bf16)
   // stages per warp: as many as fit a 75 KB CTA (3 CTAs per SM) next to the
-  // barriers, frequency table, per-warp query buffers and stage flags, the
+  // frequency table, per-warp query buffers, barriers and stage flags, the
   // 1 KB alignment slack and a 2 KB allowance for the per-sequence arrays
-  static constexpr int kOther = W * 8 * 8 + 512 + 64 + W * kQBytes + W * 8 * 4 + 1024;
-  static constexpr int kSWFit = (kCtaSmemBudget - kOther - 2048) / (W * kStage);
+  static constexpr int kOther = 512 + 64 + W * kQBytes + 1024;
+  static constexpr int kPerStage = kStage + kScales + 8 + 4;
+  static constexpr int kSWFit = (kCtaSmemBudget - kOther - 2048) / (W * kPerStage);
   static constexpr int kSW = kSWFit > 8 ? 8 : kSWFit;
-  static constexpr int kKSteps = D / 16;
+  static constexpr int kKSteps = D / 16;       // MMA k-steps (QK) and m-tiles (PV)
+  static constexpr int kLdm = kRowBytes / 32;  // ldmatrix.x4 per tile (2 chunks each)
   static constexpr int kHL = GS == 1 ? 1 : 2;  // query heads per lane
   static constexpr int kStagesBytes = W * kSW * kStage;
-  static constexpr int kBarOff = kStagesBytes;
+  static constexpr int kScaleOff = kStagesBytes;                  // [W][kSW][32] fp32
+  static constexpr int kBarOff = kScaleOff + W * kSW * kScales;
   static constexpr int kFreqOff = kBarOff + W * kSW * 8;  // rope turns per position, float2[D/2]
   static constexpr int kMiscOff = kFreqOff + 512;
   static constexpr int kQOff = kMiscOff + 64;             // [W][GS][D] bf16
@@ -64,24 +91,76 @@ struct MmaCfg {
   static_assert(kStage % 1024 == 0, "swizzled boxes need 1024-byte alignment");
   static_assert(kSW >= 2, "need at least double buffering");
   static_assert(kQBytes % 16 == 0, "query rows are copied in 16-byte chunks");
+  static_assert(kFreqOff % 16 == 0, "turns are read as float2");
 };
 
-// swizzled byte offset of 16-byte chunk `chunk` of tile row `row` (rows of
-// 128 bytes; chunk index XOR row mod 8, the TMA 128-byte swizzle)
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+// Byte offset of 16-byte chunk `ch` of row `row` in a [16][kRowBytes] tile
+// written by the TMA as kRegions boxes of [16][kBoxW] bytes: within a box the
+// chunk index is XORed with row mod 8 (128-byte swizzle: address bits 4-6
+// with bits 7-9) or with (row / 2) mod 4 (64-byte swizzle: bits 4-5 with
+// bits 7-8).
+template <class C>
+__device__ __forceinline__ uint32_t tile_off(int row, int ch) {
+  const int region = ch / C::kChunks, c = ch % C::kChunks;
+  if constexpr (C::kBoxW == 128)
+    return (uint32_t)(region * C::kBox + row * 128 + ((c ^ (row & 7)) << 4));
+  else
+    return (uint32_t)(region * C::kBox + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
 }
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float f16_round(float x) { return __half2float(__float2half_rn(x)); }
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Two int8 codes of `u` (bytes selected by `sel`, a prmt selector whose other
+// nibbles pick 0x64) as an f16 pair.  The codes arrive with their sign bit
+// flipped (x + 128, an unsigned byte b); 0x6400 | b is the f16 1024 + b, and
+// subtracting 1152 leaves x exactly (the magic-number integer conversion).
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u_flipped, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(u_flipped), "r"(0x64646464u), "r"(sel));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64806480u));
+  return r;
+}
+
+// D (16x8 fp32) += A (16x16 f16, row) * B (16x8 f16, col)
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 2^x and log2(x) from the special-function unit's approximations (relative
+// error near 2^-22; subnormal arguments and results flush to zero)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^k for an integer k in [-126, 127]
+__device__ __forceinline__ float pow2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
 // RoPE of the query, fp32 only (the query needs fp32 accuracy): lane l holds
 // cos/sin of angles l + 32k of position `pos`, from frac_turns and sincospif.
-// Then the B fragments of the query columns for one stream, built by the warp
-// from the raw query rows q[GS][D] (bf16, shared memory): column c = lane / 4
-// of the MMA is the bf16 head of query head c (c < GS), its bf16 remainder
-// (GS <= c < 2 GS), or zero; the angles each lane needs are shuffled in.
 template <int D>
 __device__ __forceinline__ void warp_query_angles(const DecodeParams &p, const float2 *turns,
                                                   int pos, int lane, float (&cr)[D / 64],
@@ -94,28 +173,61 @@ __device__ __forceinline__ void warp_query_angles(const DecodeParams &p, const f
   }
 }
 
-template <int D, int GS>
+// The B fragments of the query columns for one stream, built by the warp from
+// the raw query rows q[GS][D] (bf16, shared memory): column c = lane / 4 of
+// the MMA is the head of query head c (c < GS), its remainder (GS <= c <
+// 2 GS), or zero; the angles each lane needs are shuffled in.  Lane (c, j =
+// lane % 4) of k-step ks holds the elements d = 16 ks + {2j, 2j + 1, 2j + 8,
+// 2j + 9} (bf16 cache: the MMA's own k order) or d = 16 ks + 4j + {0..3}
+// (int8 cache: the k order of the K fragments the codes are unpacked into).
+// Int8: the values are scaled by 2^kq so that the largest lies in
+// [2^13, 2^14) (|q_rot| <= sqrt(2) max|q| bounds it: the rotation keeps each
+// pair's norm); *inv_sq returns 2^-kq.
+template <int D, int GS, bool INT8>
 __device__ __forceinline__ void warp_query_fragments(const DecodeParams &p, const float (&cr)[D / 64],
                                                      const float (&sr)[D / 64],
                                                      const __nv_bfloat16 *qrows, int lane,
-                                                     uint32_t (&qb)[D / 16][2]) {
+                                                     uint32_t (&qb)[D / 16][2], float &inv_sq) {
   constexpr int H = D / 2, KS = D / 16;
+  constexpr int e2 = INT8 ? 2 : 8;  // offset of the fragment's second element pair
   const int col = lane >> 2;
   const bool used = col < 2 * GS;
   const bool is_lo = col >= GS;
   const int head = used ? (is_lo ? col - GS : col) : 0;
   const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrows + head * D);
-  const int d0 = 2 * (lane & 3);
+  const int d0 = (INT8 ? 4 : 2) * (lane & 3);
+  uint32_t w[KS / 2][4];  // raw pairs: (d, d+1), (d+e2, d+e2+1) and the same + H
 #pragma unroll
   for (int kp = 0; kp < KS / 2; ++kp) {
-    // elements 16 kp + d0 + {0, 1, 8, 9} (first half) and the same + H
-    // (second half) of each rotation pair; their angles live in register
-    // (16 kp) / 32 of lanes (16 kp + d0 + e) % 32
     const int d = 16 * kp + d0;
-    const uint32_t l0 = used ? q32[d / 2] : 0u, l1 = used ? q32[(d + 8) / 2] : 0u;
-    const uint32_t h0 = used ? q32[(d + H) / 2] : 0u, h1 = used ? q32[(d + H + 8) / 2] : 0u;
+    w[kp][0] = used ? q32[d / 2] : 0u;
+    w[kp][1] = used ? q32[(d + e2) / 2] : 0u;
+    w[kp][2] = used ? q32[(d + H) / 2] : 0u;
+    w[kp][3] = used ? q32[(d + H + e2) / 2] : 0u;
+  }
+  float qs = p.qscale;
+  inv_sq = 1.f;
+  if constexpr (INT8) {
+    uint32_t mx = 0;  // largest |q| as bf16 magnitude bits
+#pragma unroll
+    for (int kp = 0; kp < KS / 2; ++kp)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx = max(mx, max(w[kp][k] & 0x7fffu, (w[kp][k] >> 16) & 0x7fffu));
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    const float bound = __uint_as_float(mx << 16) * fabsf(p.qscale) * 1.4143f;
+    const int eb = (int)((__float_as_uint(bound) >> 23) & 0xffu) - 127;
+    const int kq = max(-100, min(100, 13 - eb));
+    qs = p.qscale * pow2i(kq);
+    inv_sq = pow2i(-kq);
+  }
+#pragma unroll
+  for (int kp = 0; kp < KS / 2; ++kp) {
+    // elements d + {0, 1, e2, e2 + 1} of the first half and the same + H of
+    // the second half of each rotation pair; their angles live in register
+    // (16 kp) / 32 of lanes (d + e) % 32
+    const int d = 16 * kp + d0;
     const int reg = (16 * kp) / 32;
-    const int e[4] = {0, 1, 8, 9};
+    const int e[4] = {0, 1, e2, e2 + 1};
     float c[4], s[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -123,36 +235,48 @@ __device__ __forceinline__ void warp_query_fragments(const DecodeParams &p, cons
       c[k] = __shfl_sync(0xffffffffu, pick(cr, reg), src);
       s[k] = __shfl_sync(0xffffffffu, pick(sr, reg), src);
     }
-    const float2 a0 = bf16x2_to_float2(l0), a1 = bf16x2_to_float2(l1);
-    const float2 b0 = bf16x2_to_float2(h0), b1 = bf16x2_to_float2(h1);
+    const float2 a0 = bf16x2_to_float2(w[kp][0]), a1 = bf16x2_to_float2(w[kp][1]);
+    const float2 b0 = bf16x2_to_float2(w[kp][2]), b1 = bf16x2_to_float2(w[kp][3]);
     const float lo[4] = {a0.x, a0.y, a1.x, a1.y};
     const float hi[4] = {b0.x, b0.y, b1.x, b1.y};
     float vl[4], vh[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      vl[k] = (lo[k] * c[k] - hi[k] * s[k]) * p.qscale;
-      vh[k] = (hi[k] * c[k] + lo[k] * s[k]) * p.qscale;
-      const float tl = __bfloat162float(__float2bfloat16_rn(vl[k]));
-      const float th = __bfloat162float(__float2bfloat16_rn(vh[k]));
+      vl[k] = (lo[k] * c[k] - hi[k] * s[k]) * qs;
+      vh[k] = (hi[k] * c[k] + lo[k] * s[k]) * qs;
+      const float tl = INT8 ? f16_round(vl[k]) : bf16_round(vl[k]);
+      const float th = INT8 ? f16_round(vh[k]) : bf16_round(vh[k]);
       vl[k] = is_lo ? vl[k] - tl : tl;
       vh[k] = is_lo ? vh[k] - th : th;
     }
-    qb[kp][0] = pack_bf16(vl[0], vl[1]);
-    qb[kp][1] = pack_bf16(vl[2], vl[3]);
-    qb[kp + KS / 2][0] = pack_bf16(vh[0], vh[1]);
-    qb[kp + KS / 2][1] = pack_bf16(vh[2], vh[3]);
+    if constexpr (INT8) {
+      qb[kp][0] = pack_f16(vl[0], vl[1]);
+      qb[kp][1] = pack_f16(vl[2], vl[3]);
+      qb[kp + KS / 2][0] = pack_f16(vh[0], vh[1]);
+      qb[kp + KS / 2][1] = pack_f16(vh[2], vh[3]);
+    } else {
+      qb[kp][0] = pack_bf16(vl[0], vl[1]);
+      qb[kp][1] = pack_bf16(vl[2], vl[3]);
+      qb[kp + KS / 2][0] = pack_bf16(vh[0], vh[1]);
+      qb[kp + KS / 2][1] = pack_bf16(vh[2], vh[3]);
+    }
   }
 }
 
-template <int D, int GS>
-__global__ void __launch_bounds__(kDecodeThreads)
+template <int D, int GS, bool INT8>
+// at most 3 CTAs fit an SM's shared memory: let each thread have 1/384 of the
+// register file
+__global__ void __launch_bounds__(kDecodeThreads, 3)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
-  using C = MmaCfg<D, GS>;
+  using C = MmaCfg<D, GS, INT8>;
   constexpr int W = C::W;
   const float kNegInf = -INFINITY;
+  const float kFloor = -1e30f;  // initial reference maximum, below any score
+  const float kLazy = 8.f;      // log2 headroom of the lazy softmax references
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t *stages = smem;
+  float *scales = reinterpret_cast<float *>(smem + C::kScaleOff);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
   float2 *turns = reinterpret_cast<float2 *>(smem + C::kFreqOff);
   int *misc = reinterpret_cast<int *>(smem + C::kMiscOff);
@@ -201,11 +325,31 @@ __global__ void __launch_bounds__(kDecodeThreads)
       cp_async_16(reinterpret_cast<char *>(qbuf) + c * 16, src + c * 16);
     cp_async_commit();
   };
+  // position of the next unit to request: sequence, KV head, query-head group
+  // and unit of the stream, advanced one unit at a time by every lane alike
+  int cb_b, cb_j, cb_sub, cb_u, cb_units;
   {
     int b = start_b;
     const UnitPos up = locate_unit(wt0, b, pref, spu);
-    prefetch_queries(up.b, (up.si / p.n_sub) * GS * p.n_sub + (up.si % p.n_sub) * GS);
+    cb_b = up.b;
+    cb_j = up.si / p.n_sub;
+    cb_sub = up.si % p.n_sub;
+    cb_u = up.u;
+    cb_units = up.units;
+    prefetch_queries(up.b, cb_j * GS * p.n_sub + cb_sub * GS);
   }
+  auto advance = [&]() {  // only while units remain in the share
+    if (++cb_u < cb_units) return;
+    cb_u = 0;
+    if (++cb_sub < p.n_sub) return;
+    cb_sub = 0;
+    if (++cb_j < p.n_kvh) return;
+    cb_j = 0;
+    do {
+      ++cb_b;
+    } while (pref[cb_b + 1] == pref[cb_b]);
+    cb_units = pref[cb_b + 1] - pref[cb_b];
+  };
 
   // ---- producer ---------------------------------------------------------------
   // Physical pages are fetched 32 units ahead, one per lane, so the issuing
@@ -217,9 +361,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
   int win_base = 0;
   int win_page = lane < count ? page_of_unit(p, pref, spu, wt0 + lane, pcur) : -1;
   int nxt_page = -1;  // loaded once the first units are requested
-  int ib = start_b;
   bool appended_visible = false;
   auto issue = [&](int i) {  // called by the whole warp, in unit order
+    if (i > 0) advance();
     if (i - win_base >= 32) {
       win_base += 32;
       win_page = nxt_page;
@@ -228,22 +372,27 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     const int page = __shfl_sync(0xffffffffu, win_page, i - win_base);
     if (lane == 0) {
-      const UnitPos up = locate_unit(wt0 + i, ib, pref, spu);
-      if (up.u == up.units - 1 && !appended_visible) {
+      if (cb_u == cb_units - 1 && !appended_visible) {
         pdl_wait_primary();
         appended_visible = true;
       }
       const int st = warp * C::kSW + i % C::kSW;
       svalid[i % C::kSW] = page >= 0;
       if (page >= 0) {
-        const int row = (int)(((long long)page * p.n_kvh + up.si / p.n_sub) * p.page_size +
-                              (up.u * kUnitRows) % p.page_size);
+        const int row = (page * p.n_kvh + cb_j) * p.page_size +
+                        ((cb_u * kUnitRows) & (p.page_size - 1));
         uint8_t *dst = stages + (size_t)st * C::kStage;
-        mbar_arrive_expect_tx(&bars[st], C::kStage);
+        mbar_arrive_expect_tx(&bars[st], C::kStage + C::kScales);
 #pragma unroll
         for (int r = 0; r < C::kRegions; ++r) {
-          tma_load_2d(dst + r * C::kBox, &p.tmap_k, r * 64, row, &bars[st], pol);
-          tma_load_2d(dst + C::kTile + r * C::kBox, &p.tmap_v, r * 64, row, &bars[st], pol);
+          const int x = r * C::kBoxW / (INT8 ? 1 : 2);  // element column of box r
+          tma_load_2d(dst + r * C::kBox, &p.tmap_k, x, row, &bars[st], pol);
+          tma_load_2d(dst + C::kTile + r * C::kBox, &p.tmap_v, x, row, &bars[st], pol);
+        }
+        if constexpr (INT8) {
+          float *sd = scales + st * (2 * kUnitRows);
+          bulk_g2s(sd, p.k_scales + row, kUnitRows * 4, &bars[st], pol);
+          bulk_g2s(sd + kUnitRows, p.v_scales + row, kUnitRows * 4, &bars[st], pol);
         }
       } else {
         atomicOr(p.status, KVATTN_DEV_BAD_PAGE);
@@ -257,6 +406,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
   // ---- consumer ---------------------------------------------------------------
   const int hb = (GS == 4) ? 2 * (lane & 1) : 0;  // first head of this lane's columns
+  const int tokr = lane >> 2;                     // this lane's score rows: tokr, tokr + 8
+  // ldmatrix row addresses: K (and int8 V) read matrices (rows 0-7, chunk c),
+  // (rows 8-15, c), (rows 0-7, c + 1), (rows 8-15, c + 1); bf16 V, transposed,
+  // reads (rows 0-7, c), (rows 0-7, c + 1), (rows 8-15, c), (rows 8-15, c + 1)
+  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8, kcsel = lane >> 4;
+  const int vrow = INT8 ? krow : (lane & 7) + (lane >> 4) * 8;
+  const int vcsel = INT8 ? kcsel : (lane >> 3) & 1;
   bool aborted = false;
   int consumed = 0;
   int cb = start_b;
@@ -271,11 +427,12 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int sid = sp.b * spu + sp.si;
 
     uint32_t qb[C::kKSteps][2];
+    float inv_sq;
     float cr[D / 64], sr[D / 64];
     warp_query_angles<D>(p, turns, poss[sp.b], lane, cr, sr);  // while the rows land
     cp_async_wait_all();
     __syncwarp();
-    warp_query_fragments<D, GS>(p, cr, sr, qbuf, lane, qb);
+    warp_query_fragments<D, GS, INT8>(p, cr, sr, qbuf, lane, qb, inv_sq);
     __syncwarp();
     if (E < wt1) {  // the share continues: fetch the next stream's query rows
       int b = sp.b;
@@ -287,11 +444,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
     for (int dt = 0; dt < C::kKSteps; ++dt)
 #pragma unroll
       for (int k = 0; k < 4; ++k) o[dt][k] = 0.f;
-    float m[C::kHL], l[C::kHL];
+    // m, l: reference maximum and normaliser of the softmax; mo: reference
+    // maximum of the value weights (int8; the bf16 cache weighs the values by
+    // the softmax weights themselves).  The references start at a finite floor
+    // below every score, so no step needs a guard for an empty state.
+    float m[C::kHL], l[C::kHL], mo[C::kHL];
 #pragma unroll
     for (int h = 0; h < C::kHL; ++h) {
-      m[h] = kNegInf;
+      m[h] = kFloor;
       l[h] = 0.f;
+      mo[h] = kFloor;
     }
 
     for (long long tt = t; tt < e; ++tt) {
@@ -312,9 +474,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
         uint8_t *Ks = stages + (size_t)st * C::kStage;
         uint8_t *Vs = Ks + C::kTile;
         const uint32_t kb = smem_addr(Ks), vb = smem_addr(Vs);
-        if (nrows < kUnitRows) {
-          // rows past the sequence end hold stale data: zero them in V so that
-          // their zero weights cannot meet a NaN
+        if (!INT8 && nrows < kUnitRows) {
+          // bf16 rows past the sequence end hold stale data: zero them in V
+          // so that their zero weights cannot meet a NaN (int8 codes are
+          // always finite)
           const int n16 = (kUnitRows - nrows) * C::kRegions * 8;
           for (int idx = lane; idx < n16; idx += 32) {
             const int row = nrows + idx / (C::kRegions * 8);
@@ -324,17 +487,37 @@ __global__ void __launch_bounds__(kDecodeThreads)
           }
           __syncwarp();
         }
+        // int8: scale of this lane's score rows (with the query's 2^-kq) and
+        // log2 of the value scales
+        float ksr[2] = {1.f, 1.f}, lv[2] = {0.f, 0.f};
+        if constexpr (INT8) {
+          const float *sc = scales + st * (2 * kUnitRows);
+#pragma unroll
+          for (int t2 = 0; t2 < 2; ++t2) {
+            ksr[t2] = sc[tokr + 8 * t2] * inv_sq;
+            lv[t2] = lg2_approx(sc[kUnitRows + tokr + 8 * t2]);
+          }
+        }
 
         // S^T = K Qc^T
         float s[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int csel = lane >> 4;
 #pragma unroll
-          for (int ks = 0; ks < C::kKSteps; ++ks) {
-            uint32_t a[4];
-            ldmatrix_x4(a, kb + (ks >> 2) * C::kBox + swz(row, ((ks & 3) << 1) + csel));
-            mma_bf16_16816(s, a, qb[ks][0], qb[ks][1]);
+        for (int it = 0; it < C::kLdm; ++it) {
+          uint32_t a[4];
+          ldmatrix_x4(a, kb + tile_off<C>(krow, 2 * it + kcsel));
+          if constexpr (INT8) {
+            // codes of rows g, g + 8 at d = 4j..4j+3 of chunks 2 it, 2 it + 1:
+            // k-step 2 it + c takes (d 4j, 4j+1) as its columns 2j, 2j+1 and
+            // (4j+2, 4j+3) as 2j+8, 2j+9, matching the query fragments
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint32_t r0 = a[2 * c] ^ 0x80808080u, r1 = a[2 * c + 1] ^ 0x80808080u;
+              const uint32_t f[4] = {codes_to_f16x2(r0, 0x5140u), codes_to_f16x2(r1, 0x5140u),
+                                     codes_to_f16x2(r0, 0x5342u), codes_to_f16x2(r1, 0x5342u)};
+              mma_f16_16816(s, f, qb[2 * it + c][0], qb[2 * it + c][1]);
+            }
+          } else {
+            mma_bf16_16816(s, a, qb[it][0], qb[it][1]);
           }
         }
         // full scores sc[token half][head slot] = hi column + lo column
@@ -349,72 +532,120 @@ __global__ void __launch_bounds__(kDecodeThreads)
           sc[0][0] = s[0]; sc[0][1] = s[1]; sc[1][0] = s[2]; sc[1][1] = s[3];
         } else {
           sc[0][0] = s[0] + s[1]; sc[1][0] = s[2] + s[3];
-          sc[0][1] = sc[1][1] = kNegInf;
+          sc[0][1] = sc[1][1] = 0.f;  // no second head
         }
-        const int tokr = lane >> 2;
-        if (tokr >= nrows) sc[0][0] = sc[0][1] = kNegInf;
-        if (tokr + 8 >= nrows) sc[1][0] = sc[1][1] = kNegInf;
+        // value-weight exponents (int8): score + log2 vs
+        float xv[2][2];
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+          for (int h = 0; h < C::kHL; ++h) {
+            if constexpr (INT8) sc[t2][h] *= ksr[t2];
+            xv[t2][h] = sc[t2][h] + lv[t2];
+          }
+        if (nrows < kUnitRows) {  // a sequence's last unit: drop the rows past its end
+#pragma unroll
+          for (int t2 = 0; t2 < 2; ++t2)
+            if (tokr + 8 * t2 >= nrows)
+#pragma unroll
+              for (int h = 0; h < C::kHL; ++h) sc[t2][h] = xv[t2][h] = kNegInf;
+        }
 
-        // online softmax (log2 units)
-        float alpha[C::kHL], pw[2][C::kHL];
+        // online softmax (log2 units) with lazy references: a reference moves
+        // only when a score passes it by more than kLazy, so every weight stays
+        // below 2^kLazy and most units leave the accumulators as they are
+        float alpha[C::kHL], pw[2][C::kHL], pv[2][C::kHL];
+        bool moved = false;
 #pragma unroll
         for (int h = 0; h < C::kHL; ++h) {
           float mx = fmaxf(sc[0][h], sc[1][h]);
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(m[h], mx);
-          alpha[h] = (mn == kNegInf) ? 1.f : exp2f(m[h] - mn);
-          m[h] = mn;
-          pw[0][h] = (mn == kNegInf) ? 0.f : exp2f(sc[0][h] - mn);
-          pw[1][h] = (mn == kNegInf) ? 0.f : exp2f(sc[1][h] - mn);
-          l[h] = l[h] * alpha[h] + pw[0][h] + pw[1][h];
+          float a = 1.f;
+          if (mx > m[h] + kLazy) {
+            a = ex2_approx(m[h] - mx);
+            m[h] = mx;
+          }
+          pw[0][h] = ex2_approx(sc[0][h] - m[h]);
+          pw[1][h] = ex2_approx(sc[1][h] - m[h]);
+          l[h] = l[h] * a + pw[0][h] + pw[1][h];
+          if constexpr (INT8) {
+            float xo = fmaxf(xv[0][h], xv[1][h]);
+            xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 4));
+            xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 8));
+            xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 16));
+            a = 1.f;
+            if (xo > mo[h] + kLazy) {
+              a = ex2_approx(mo[h] - xo);
+              mo[h] = xo;
+            }
+            pv[0][h] = ex2_approx(xv[0][h] - mo[h]);
+            pv[1][h] = ex2_approx(xv[1][h] - mo[h]);
+          } else {
+            pv[0][h] = pw[0][h];
+            pv[1][h] = pw[1][h];
+          }
+          alpha[h] = a;
+          moved |= a != 1.f;
         }
-        // P^T fragments: this lane's two columns at tokens r and r + 8, bf16
-        // head or remainder of the weight, zero in padding columns
+        // P^T fragments: this lane's two columns at tokens r and r + 8, head
+        // or remainder of the value weight, zero in padding columns
         uint32_t pr[2];
 #pragma unroll
         for (int t2 = 0; t2 < 2; ++t2) {
           float x0, x1;
+          const auto rnd = [](float x) { return INT8 ? f16_round(x) : bf16_round(x); };
           if constexpr (GS == 4) {
-            x0 = pw[t2][0];
-            x1 = pw[t2][1];
+            x0 = pv[t2][0];
+            x1 = pv[t2][1];
             if (lane & 2) {
-              x0 -= __bfloat162float(__float2bfloat16_rn(x0));
-              x1 -= __bfloat162float(__float2bfloat16_rn(x1));
+              x0 -= rnd(x0);
+              x1 -= rnd(x1);
             }
           } else if constexpr (GS == 2) {
-            x0 = pw[t2][0];
-            x1 = pw[t2][1];
+            x0 = pv[t2][0];
+            x1 = pv[t2][1];
             if (lane & 1) {
-              x0 -= __bfloat162float(__float2bfloat16_rn(x0));
-              x1 -= __bfloat162float(__float2bfloat16_rn(x1));
+              x0 -= rnd(x0);
+              x1 -= rnd(x1);
             }
             if (lane & 2) x0 = x1 = 0.f;
           } else {
-            x0 = pw[t2][0];
-            x1 = x0 - __bfloat162float(__float2bfloat16_rn(x0));
+            x0 = pv[t2][0];
+            x1 = x0 - rnd(x0);
             if (lane & 3) x0 = x1 = 0.f;
           }
-          pr[t2] = pack_bf16(x0, x1);
+          pr[t2] = INT8 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
         }
         const uint32_t b0 = movmatrix_trans(pr[0]);
         const uint32_t b1 = movmatrix_trans(pr[1]);
-        // rescale the accumulators of this lane's columns
-        const float a0 = alpha[0], a1 = alpha[C::kHL - 1];
-#pragma unroll
-        for (int dt = 0; dt < C::kKSteps; ++dt) {
-          o[dt][0] *= a0; o[dt][1] *= a1; o[dt][2] *= a0; o[dt][3] *= a1;
-        }
-        // O^T += V^T P^T
-        {
-          const int row = (lane & 7) + (lane >> 4) * 8;
-          const int csel = (lane >> 3) & 1;
+        // rescale the accumulators of this lane's columns when a reference moved
+        if (__any_sync(0xffffffffu, moved)) {
+          const float a0 = alpha[0], a1 = alpha[C::kHL - 1];
 #pragma unroll
           for (int dt = 0; dt < C::kKSteps; ++dt) {
-            uint32_t a[4];
-            ldmatrix_x4_trans(a, vb + (dt >> 2) * C::kBox + swz(row, ((dt & 3) << 1) + csel));
-            mma_bf16_16816(o[dt], a, b0, b1);
+            o[dt][0] *= a0; o[dt][1] *= a1; o[dt][2] *= a0; o[dt][3] *= a1;
+          }
+        }
+        // O^T += V^T P^T
+#pragma unroll
+        for (int it = 0; it < C::kLdm; ++it) {
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, vb + tile_off<C>(vrow, 2 * it + vcsel));
+          if constexpr (INT8) {
+            // lane (g, j) holds codes of tokens 2j, 2j+1 (rows 0-7: a[2c],
+            // rows 8-15: a[2c+1]) at d = 2g, 2g+1 of chunk 2 it + c: m-tile
+            // row g takes d = 2g, row g + 8 takes d = 2g + 1
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint32_t r0 = a[2 * c] ^ 0x80808080u, r1 = a[2 * c + 1] ^ 0x80808080u;
+              const uint32_t f[4] = {codes_to_f16x2(r0, 0x5240u), codes_to_f16x2(r0, 0x5341u),
+                                     codes_to_f16x2(r1, 0x5240u), codes_to_f16x2(r1, 0x5341u)};
+              mma_f16_16816(o[2 * it + c], f, b0, b1);
+            }
+          } else {
+            mma_bf16_16816(o[it], a, b0, b1);
           }
         }
       }
@@ -439,26 +670,33 @@ __global__ void __launch_bounds__(kDecodeThreads)
           o[dt][k] += __shfl_xor_sync(0xffffffffu, o[dt][k], GS == 4 ? 2 : 1);
       }
     }
+    // accumulator scale to 2^m (int8: from 2^mo)
+    float to_m[C::kHL];
 #pragma unroll
     for (int h = 0; h < C::kHL; ++h) {
       l[h] += __shfl_xor_sync(0xffffffffu, l[h], 4);
       l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
       l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
+      to_m[h] = 1.f;
+      if constexpr (INT8) to_m[h] = ex2_approx(mo[h] - m[h]);
     }
     // lanes holding final values: GS 4 -> lane % 4 in {0, 1} (heads hb, hb + 1);
-    // GS 2 -> lane % 4 == 0 (heads 0, 1); GS 1 -> lane % 4 == 0 (head 0)
+    // GS 2 -> lane % 4 == 0 (heads 0, 1); GS 1 -> lane % 4 == 0 (head 0).
+    // Accumulator rows: o[dt][h] at d = dA, o[dt][2 + h] at d = dB.
     const bool writer = (GS == 4) ? (lane & 2) == 0 : (lane & 3) == 0;
     const int dr = lane >> 2;
+    const auto dA = [&](int dt) { return INT8 ? dt * 16 + 2 * dr : dt * 16 + dr; };
+    const auto dB = [&](int dt) { return INT8 ? dt * 16 + 2 * dr + 1 : dt * 16 + dr + 8; };
     __nv_bfloat16 *outp = p.out + ((size_t)sp.b * p.n_qh + h0) * D;
     if (F >= wt0 && E <= wt1) {
       if (writer) {
 #pragma unroll
         for (int h = 0; h < C::kHL; ++h) {
-          const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+          const float f = l[h] > 0.f ? to_m[h] / l[h] : 0.f;
 #pragma unroll
           for (int dt = 0; dt < C::kKSteps; ++dt) {
-            outp[(hb + h) * D + dt * 16 + dr] = __float2bfloat16_rn(o[dt][h] * inv);
-            outp[(hb + h) * D + dt * 16 + dr + 8] = __float2bfloat16_rn(o[dt][2 + h] * inv);
+            outp[(hb + h) * D + dA(dt)] = __float2bfloat16_rn(o[dt][h] * f);
+            outp[(hb + h) * D + dB(dt)] = __float2bfloat16_rn(o[dt][2 + h] * f);
           }
         }
       }
@@ -470,8 +708,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
         for (int h = 0; h < C::kHL; ++h) {
 #pragma unroll
           for (int dt = 0; dt < C::kKSteps; ++dt) {
-            rec[(hb + h) * D + dt * 16 + dr] = o[dt][h];
-            rec[(hb + h) * D + dt * 16 + dr + 8] = o[dt][2 + h];
+            rec[(hb + h) * D + dA(dt)] = o[dt][h] * to_m[h];
+            rec[(hb + h) * D + dB(dt)] = o[dt][2 + h] * to_m[h];
           }
           if (dr == 0) {
             rec[GS * D + hb + h] = m[h];
@@ -490,11 +728,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
   }
 }
 
-template <int D, int GS>
+template <int D, int GS, bool INT8>
 cudaError_t launch_decode_mma_t(const DecodeParams &p, int grid, cudaStream_t stream,
                                 int *ctas_per_sm, bool launch) {
-  using C = MmaCfg<D, GS>;
-  auto kern = decode_mma_kernel<D, GS>;
+  using C = MmaCfg<D, GS, INT8>;
+  auto kern = decode_mma_kernel<D, GS, INT8>;
   const int smem = C::kFixedSmem + (int)align_up((size_t)(3 * p.n_seq + 1) * 4, 16);
   static std::mutex mu;
   static std::map<std::pair<int, int>, int> occupancy;  // (device, smem) -> CTAs/SM

@@ -2,7 +2,9 @@
 // closed, nothing is launched on an error), workspace layout, the RoPE
 // frequency table, the TMA descriptors of the pools and the launches of one
 // decode step on the caller's stream: append, split-KV attention as its
-// programmatic dependent, and (bf16 cache) the merge of split sequences.  No host synchronisation except in kvattn_read_device_status.
+// programmatic dependent, and the merge of split streams as the attention's
+// programmatic dependent.  No host synchronisation except in
+// kvattn_read_device_status.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -59,18 +61,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D view [rows][head_dim] bf16 of a K or V pool, 16 x 64 boxes, 128-byte
-// swizzle (the box's 128-byte rows are written with their 16-byte chunks
-// permuted by row mod 8, which the kernel's ldmatrix addressing undoes)
-bool encode_pool_map(CUtensorMap *map, const void *base, long long rows, int head_dim) {
+// 2-D view [rows][head_dim] of a K or V pool in [16 rows][128 bytes] boxes
+// with 128-byte swizzle (bf16: 64 columns; int8, head_dim 128: 128 columns),
+// or [16][64 bytes] boxes with 64-byte swizzle (int8, head_dim 64): the box's
+// rows are written with their 16-byte chunks permuted, which the kernel's
+// ldmatrix addressing undoes
+bool encode_pool_map(CUtensorMap *map, const void *base, long long rows, int head_dim, bool int8) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
+  const int esize = int8 ? 1 : 2;
+  const int row_bytes = head_dim * esize;
+  const int box_bytes = row_bytes < 128 ? row_bytes : 128;
   cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(box_bytes / esize), 16};
   cuuint32_t estride[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-             box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return enc(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void *>(base), dims, strides, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -178,7 +187,6 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.v_scales = v_scales;
   dp.out = static_cast<__nv_bfloat16 *>(out);
   dp.records = reinterpret_cast<float *>(ws + wl.records_off);
-  dp.counters = reinterpret_cast<uint32_t *>(ws + wl.counters_off);
   dp.status = ap.status;
   dp.use_rope = ap.use_rope;
   // scores are formed in log2 units: fold scale * log2(e) into the query
@@ -196,30 +204,28 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.num_pages = num_pages;
   dp.n_sub = g / gs;
   dp.min_units = kMinUnitsPerShare;
-  if (!int8) {
+  {
     const long long rows = (long long)num_pages * n_kvh * page_size;
-    if (!encode_pool_map(&dp.tmap_k, k_pages, rows, head_dim) ||
-        !encode_pool_map(&dp.tmap_v, v_pages, rows, head_dim))
+    if (!encode_pool_map(&dp.tmap_k, k_pages, rows, head_dim, int8) ||
+        !encode_pool_map(&dp.tmap_v, v_pages, rows, head_dim, int8))
       return KVATTN_ECUDA;
   }
   // the first call for a configuration on a device sets the kernel's shared
   // memory limit and caches its occupancy; later calls only launch.  A share
-  // of the unit list is one warp's work in the bf16 kernel and one CTA's in
-  // the int8 kernel.
+  // of the unit list is one warp's work.
   int sms = 0, per_sm = 0;
   if (sm_count(&sms) != cudaSuccess) return KVATTN_ECUDA;
   if (decode_launcher(dp, head_dim, gs, int8, 0, st, &per_sm, false) != cudaSuccess)
     return KVATTN_ECUDA;
-  const int per_cta = int8 ? 1 : kDecodeWarps;
   int shares = num_splits;
-  if (shares == 0) shares = sms * (per_sm > 0 ? per_sm : 1) * per_cta;
+  if (shares == 0) shares = sms * (per_sm > 0 ? per_sm : 1) * kDecodeWarps;
   if (shares > KVATTN_MAX_SPLITS) shares = KVATTN_MAX_SPLITS;
   dp.n_shares = shares;
-  const int grid = (shares + per_cta - 1) / per_cta;
+  const int grid = (shares + kDecodeWarps - 1) / kDecodeWarps;
   if (decode_launcher(dp, head_dim, gs, int8, grid, st, nullptr, true) != cudaSuccess)
     return KVATTN_ECUDA;
-  // ---- launch 3 (bf16): merge of the streams the warp shares split ----
-  if (!int8 && launch_combine(dp, head_dim, gs, shares, st) != cudaSuccess) return KVATTN_ECUDA;
+  // ---- launch 3: merge of the streams the warp shares split ----
+  if (launch_combine(dp, head_dim, gs, shares, st) != cudaSuccess) return KVATTN_ECUDA;
   return KVATTN_OK;
 }
 

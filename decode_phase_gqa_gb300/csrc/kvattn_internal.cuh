@@ -47,7 +47,6 @@ struct DecodeParams {
   const float *k_scales, *v_scales;
   __nv_bfloat16 *out;
   float *records;      // partial softmax states of split streams
-  uint32_t *counters;  // arrivals per stream; the last arrival resets it to 0
   uint32_t *status;
   int n_seq, n_qh, n_kvh, page_size, max_pages, num_pages;
   int n_sub;           // query-head groups per KV head (G / GS)
@@ -68,7 +67,7 @@ __host__ __device__ inline constexpr int record_floats(int gs, int d) {
 
 // ---- workspace layout ----------------------------------------------------
 struct WorkspaceLayout {
-  size_t status_off, counters_off, records_off, total;
+  size_t status_off, records_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -79,8 +78,7 @@ inline WorkspaceLayout workspace_layout(int n_seq, int n_qh, int n_kvh, int d) {
   const int gs = group_split(g);
   const size_t streams = (size_t)n_seq * n_kvh * (g / gs);
   w.status_off = 0;
-  w.counters_off = 256;
-  w.records_off = align_up(w.counters_off + streams * sizeof(uint32_t), 256);
+  w.records_off = 256;
   const size_t records = streams + KVATTN_MAX_SPLITS;
   w.total = align_up(w.records_off + records * (size_t)record_floats(gs, d) * sizeof(float), 256);
   return w;

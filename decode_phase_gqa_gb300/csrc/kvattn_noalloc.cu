@@ -5,9 +5,9 @@
 // engine that reserved nearly all of HBM for its KV-page pool at start-up and
 // keeps no allocator for anything else, or a plugin inside a host framework
 // that owns every device allocation and does not allow plugins to call
-// cudaMalloc.  For them the step's scratch (status word, rotated queries,
-// arrival counters, partial softmax states) lives in one fixed array compiled
-// into this library instead of in a caller-owned workspace.
+// cudaMalloc.  For them the step's scratch (status word, partial softmax
+// states) lives in one fixed array compiled into this library instead of in a
+// caller-owned workspace.
 //
 // The array is a file-scope __device__ variable.  In host code its name only
 // stands in for the symbol, it is not a device address, so the address is
@@ -67,7 +67,7 @@ extern "C" int kvattn_decode_noalloc(const void *q, const void *k_new, const voi
   if (scratch_address(&scratch) != cudaSuccess) return KVATTN_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: the status word must start
-  // at zero (the arrival counters are reset by the step itself)
+  // at zero (every record the combine kernel reads is rewritten by the step)
   if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) return KVATTN_ECUDA;
   const int rc = kvattn_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
                                positions, out, n_seq, n_qh, n_kvh, head_dim, page_size,

@@ -75,18 +75,17 @@ extern "C" {
 
 /*
  * Bytes of device workspace one decode call needs for this shape.  The
- * workspace holds the device status word, one arrival counter per (sequence,
- * KV head, query-head group) and the partial softmax states of sequences
- * whose work is split across CTAs.  0 when the shape is invalid.
+ * workspace holds the device status word and the partial softmax states of
+ * the (sequence, KV head, query-head group) streams whose work is split
+ * across warps.  0 when the shape is invalid.
  */
 size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim);
 
 /*
  * Zero the workspace (all workspace_bytes, asynchronously on `stream`).  Must
  * be called once before the first kvattn_decode on a workspace, and again
- * after a call that reported KVATTN_DEV_TIMEOUT.  Every completed call leaves
- * the arrival counters at zero, so a workspace can be reused for any shape it
- * is large enough for.
+ * after a call that reported KVATTN_DEV_TIMEOUT.  A workspace can be reused
+ * for any shape it is large enough for.
  * workspace: device, 256-byte aligned, at least 256 bytes.
  */
 int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);

@@ -66,8 +66,8 @@ def test_workspace_size(lib):
     assert s(1, 4, 1, 64) % 256 == 0
     assert s(64, 32, 8, 128) > s(8, 32, 8, 128) > 0
     # a partial-state record (acc, m, l of a 4-head group) for every stream and
-    # split, plus one arrival counter per stream
-    assert s(64, 32, 8, 128) >= (64 * 8 + K.KVATTN_MAX_SPLITS) * 4 * 130 * 4 + 64 * 8 * 4
+    # split
+    assert s(64, 32, 8, 128) >= (64 * 8 + K.KVATTN_MAX_SPLITS) * 4 * 130 * 4
     for bad in ((-1, 4, 1, 64), (1, 0, 1, 64), (1, 4, 3, 64), (1, 4, 1, 96),
                 (K.KVATTN_MAX_SEQS + 1, 4, 1, 64)):
         assert s(*bad) == 0, bad

@@ -44,8 +44,8 @@ def _common_args(wl, d, out, stream):
 
 
 def _case(seed, kv, d):
-    # long and short sequences: the long ones are cut across CTAs, so the
-    # partial-state records and arrival counters of the scratch are exercised
+    # long and short sequences: the long ones are cut across warps, so the
+    # partial-state records of the scratch are exercised
     wl = W.make_workload("custom", seed=seed, n_seq=6, n_qh=16, n_kvh=4, head_dim=d,
                          page_size=16, rope_theta=1e6, kv_dtype=kv,
                          lengths=[3000, 17, 900, 0, 4095, 256], spare=0.1)
