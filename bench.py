@@ -190,11 +190,14 @@ class NativeCase:
     """Device-resident inputs of one config: `copies` independent caches (or the
     36 layer caches of the Qwen config), one workspace, one output buffer."""
 
-    def __init__(self, name: str, seed: int, device, min_bytes: int = 4 * L2_BYTES):
+    def __init__(self, name: str, seed: int, device, min_bytes: int = 4 * L2_BYTES,
+                 layers=None):
         from decode_phase_gqa_gb300 import kvattn as K
         self.K = K
         self.wl = W.make_workload(name, seed=seed)
         wl = self.wl
+        if layers is not None:   # fewer layer caches per step (profiling runs only)
+            wl.layers = max(1, min(wl.layers, layers))
         self.device = device
         self.calls_per_step = wl.layers
         per_cache = wl.kv_bytes
@@ -378,8 +381,8 @@ def cpu_baseline(name: str, seed: int, budget_s: float = 10.0):
                       f"{wl.layers} layer(s) costs {wl.layers}x one layer"}
 
 
-def run_config(name, steps, warmup, rank, world, device, stream, with_e2e=True):
-    case = NativeCase(name, seed=1000 * rank, device=device)
+def run_config(name, steps, warmup, rank, world, device, stream, with_e2e=True, layers=None):
+    case = NativeCase(name, seed=1000 * rank, device=device, layers=layers)
     case.capture(stream)
     st = case.check_status()
     if st:
@@ -413,7 +416,8 @@ def native(args, rank, world, local):
     stream = torch.cuda.Stream(device)
     peak, peak_kind = measured_peak()
     with ClockSampler(local) as clocks:
-        main = run_config(args.config, args.steps, args.warmup, rank, world, device, stream)
+        main = run_config(args.config, args.steps, args.warmup, rank, world, device, stream,
+                          layers=args.layers)
     clk = clocks.summary(*main["window"])
     wl = main["case"].wl
     per_call_ms = main["ms_per_step"] / main["calls_per_step"]
@@ -452,8 +456,8 @@ def native(args, rank, world, local):
                       "timed together): algorithmic K+V bytes per call / call time",
         },
         "e2e": main["e2e"],
-        # append + decode (+ combine for the bf16 cache) per call
-        "gpu_launches": (2 if wl.kv_dtype == "int8" else 3) * main["calls_per_step"] * args.steps,
+        # append, decode and combine kernels per call
+        "gpu_launches": 3 * main["calls_per_step"] * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "impl": "native",
     }
@@ -555,6 +559,9 @@ def main(argv=None):
     ap.add_argument("--config", choices=W.CONFIG_ORDER, default=PRIMARY)
     ap.add_argument("--no-extra-configs", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decode at most this many layer caches per step (a smaller case "
+                         "for profiling; the default is the workload's own count)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
