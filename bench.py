@@ -44,7 +44,7 @@ PRIMARY = "smollm3"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 SRC_FILES = ["decode_common.cuh", "decode_mma.cuh", "kvattn_internal.cuh",
-             "append.cu", "kvattn_api.cu", "decode_bf16.cu", "decode_int8.cu",
+             "storage.cuh", "kvattn_api.cu", "decode_bf16.cu", "decode_int8.cu",
              "combine.cu"]
 
 

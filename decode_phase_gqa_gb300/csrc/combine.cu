@@ -1,30 +1,30 @@
-// Combine kernel: log-sum-exp merge of the partial records of split streams
-// (third launch of a step for the bf16 cache).
+// Combine kernel: log-sum-exp merge of the streams the decode kernel's work
+// split cut across warp shares (second launch of a step).
 //
-// The decode kernel cuts the flattened unit list into equal per-warp shares; a
-// stream that crosses share boundaries leaves one record (acc[GS][d] relative
-// to 2^m, m[GS], l[GS]; log2 units) per share it touches.  One CTA per stream
-// recomputes the same split from the sequence lengths, and for a split stream
-// merges its records ("Qwen3-8B inference engine from scratch in C++/CUDA",
-// section 4.4.1: blockwise softmax never materialises the full score row; the
-// blocks are recombined by rescaling with the running maximum):
+// A split stream leaves one partial record (acc[GS][d] relative to 2^m,
+// m[GS], l[GS]; log2 units) per share it touches, in consecutive slots, and
+// its first share writes (first share, shares) into the stream's hand-off
+// entry ((0, 0) for a stream one share holds); this kernel merges the records
+// ("Qwen3-8B inference engine from scratch in C++/CUDA", section 4.4.1: the
+// blockwise softmax recombines its blocks by rescaling with the running
+// maximum):
 //   M = max_r m_r,  L = sum_r 2^(m_r - M) l_r,  out = sum_r 2^(m_r - M) acc_r / L.
-// Every thread merges a subset of the records of one float4 column online (a
-// running maximum, normaliser and sum, with all its loads issued at once),
-// then the record lanes of each column are merged in shared memory: one or
-// two L2 round trips per split stream.  The kernel is launched as a
-// programmatic dependent of the decode kernel: it plans while the decode grid
-// drains and waits for it only before reading records.
-#include <mutex>
-#include <set>
-
+// A stream cut into many shares has its columns split into up to four items,
+// so that one round of loads covers its records.  Two CTAs per SM at most;
+// CTA c looks at items c, c + gridDim.x, ...: its threads read those items'
+// hand-off entries at once and list the merges to do.  Every thread merges a
+// subset of the records of one float4 column online (running maximum,
+// normaliser and sum, with all its loads issued at once), then the record
+// lanes of each column are merged in shared memory.  The
+// kernel is launched as a programmatic dependent of the decode kernel and
+// waits for it before reading anything the decode grid writes.
 #include "decode_common.cuh"
 
 namespace kvattn {
 
 namespace {
 
-constexpr int kCombineThreads = 512;
+constexpr int kCombineThreads = 256;
 
 // running softmax state of one output column: max m, normaliser l (log2 units)
 // and the four accumulator values, all relative to 2^m
@@ -47,122 +47,127 @@ __device__ __forceinline__ void absorb(ColState &st, float m, float l, float4 a)
 }
 
 template <int D, int GS>
-__global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(const __grid_constant__ DecodeParams p, int n_warps) {
+__global__ void __launch_bounds__(kCombineThreads, 2)
+    combine_kernel(const __grid_constant__ DecodeParams p, int n_streams) {
   constexpr int RS = record_floats(GS, D);
-  constexpr int NC = GS * D / 4;             // float4 columns of a record's accumulator
-  constexpr int R = kCombineThreads / NC;    // record lanes per column
-  constexpr int U = 8;                       // records in flight per thread
+  constexpr int NC = GS * D / 4;  // float4 columns of a record's accumulator
+  // a long stream's columns may be split into up to kMaxChunks items (of at
+  // least 32 columns each) that different CTAs merge
+  constexpr int kMaxChunks = NC >= 128 ? 4 : NC >= 64 ? 2 : 1;
+  constexpr int U = 16;  // records in flight per thread
   static_assert(kCombineThreads % NC == 0, "columns must tile the CTA");
-  extern __shared__ int csmem[];
-  int *scratch = csmem;                                         // 32 ints
-  ColState *part = reinterpret_cast<ColState *>(csmem + 32);    // [R][NC]
-  int *pref = csmem + 32 + (int)(sizeof(ColState) / 4) * kCombineThreads;
+  __shared__ ColState part[kCombineThreads];  // [record lane][column]
+  __shared__ int4 list[kCombineThreads];      // (stream, chunk, chunks, first share)
+  __shared__ int lseg[kCombineThreads];
+  __shared__ int n_list;
 
   const int tid = threadIdx.x;
-  long long T = 0;
-  if (!plan_units<kCombineThreads>(p, pref, scratch, T)) return;
   const int spu = p.n_kvh * p.n_sub;
-  const int sid = blockIdx.x;
-  const int b = sid / spu, si = sid % spu;
-  const int units = pref[b + 1] - pref[b];
-  if (units == 0) return;
-  const long long nwa = min((long long)n_warps, max(1LL, (T + p.min_units - 1) / p.min_units));
-  const long long F = (long long)spu * pref[b] + (long long)si * units, E = F + units;
-  const long long w0 = owner_of(F, T, nwa), w1 = owner_of(E - 1, T, nwa);
-  const int nseg = (int)(w1 - w0 + 1);
-  if (nseg <= 1) return;  // written by the decode kernel directly
-  const int h0 = (si / p.n_sub) * GS * p.n_sub + (si % p.n_sub) * GS;
-  __nv_bfloat16 *outp = p.out + ((size_t)b * p.n_qh + h0) * D;
-  const float *r0 = p.records + (size_t)(sid + w0) * RS;
+  pdl_wait_primary();  // the decode grid's records and hand-off entries are visible
 
-  pdl_wait_primary();  // the decode grid's records are complete and visible
-
-  // thread (record lane rl, column c) merges records rl, rl + R, ... online
-  const int c = tid % NC, rl = tid / NC;
-  const int hc = (c * 4) / D;
-  ColState st = {-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
-  for (int s0 = rl; s0 < nseg; s0 += R * U) {
-    float mm[U], ll[U];
-    float4 a[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int s = s0 + u * R;
-      if (s < nseg) {
-        const float *rs = r0 + (size_t)s * RS;
-        a[u] = __ldcg(reinterpret_cast<const float4 *>(rs) + c);
-        mm[u] = __ldcg(rs + GS * D + hc);
-        ll[u] = __ldcg(rs + GS * D + GS + hc);
-      } else {
-        mm[u] = -INFINITY;
-        ll[u] = 0.f;
-        a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // item i: chunk i / n_streams of stream i % n_streams; CTA c takes items
+  // c, c + gridDim.x, ...
+  const long long n_items = (long long)n_streams * kMaxChunks;
+  const long long stride = (long long)gridDim.x * kCombineThreads;
+  for (long long base = blockIdx.x; base < n_items; base += stride) {
+    if (tid == 0) n_list = 0;
+    __syncthreads();
+    const long long it = base + (long long)tid * gridDim.x;
+    if (it < n_items) {
+      const int sid = (int)(it % n_streams), q = (int)(it / n_streams);
+      const int2 m = __ldcg(p.meta + sid);
+      const int nseg = m.y;
+      // fewest chunks whose record lanes cover the shares in one round
+      int nch = 1;
+      while (nch < kMaxChunks && nseg > (kCombineThreads * nch / NC) * U) nch *= 2;
+      if (nseg > 1 && q < nch) {
+        const int k = atomicAdd(&n_list, 1);
+        list[k] = make_int4(sid, q, nch, m.x);
+        lseg[k] = nseg;
       }
     }
+    __syncthreads();
+    for (int i = 0; i < n_list; ++i) {
+      const int4 w = list[i];
+      const int sid = w.x, q = w.y, nch = w.z, w0 = w.w, nseg = lseg[i];
+      const int b = sid / spu, si = sid % spu;
+      const int h0 = (si / p.n_sub) * GS * p.n_sub + (si % p.n_sub) * GS;
+      const float *r0 = p.records + (size_t)(sid + w0) * RS;
+      // thread (record lane rl, column cc of the chunk) merges records rl,
+      // rl + R, ... of column c online
+      const int ncq = NC / nch, R = kCombineThreads / ncq;
+      const int cc = tid % ncq, rl = tid / ncq;
+      const int c = q * ncq + cc;
+      const int hc = (c * 4) / D;
+      ColState st = {-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+      for (int s0 = rl; s0 < nseg; s0 += R * U) {
+        float mm[U], ll[U];
+        float4 a[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) absorb(st, mm[u], ll[u], a[u]);
-  }
-  part[rl * NC + c] = st;
-  __syncthreads();
-  if (rl == 0) {
-    for (int r = 1; r < R; ++r) {
-      const ColState q = part[r * NC + c];
-      absorb(st, q.m, q.l, q.o);
+        for (int u = 0; u < U; ++u) {
+          const int r = s0 + u * R;
+          if (r < nseg) {
+            const float *rs = r0 + (size_t)r * RS;
+            a[u] = __ldcg(reinterpret_cast<const float4 *>(rs) + c);
+            mm[u] = __ldcg(rs + GS * D + hc);
+            ll[u] = __ldcg(rs + GS * D + GS + hc);
+          } else {
+            mm[u] = -INFINITY;
+            ll[u] = 0.f;
+            a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) absorb(st, mm[u], ll[u], a[u]);
+      }
+      part[tid] = st;
+      __syncthreads();
+      if (rl == 0) {
+        for (int r = 1; r < R; ++r) {
+          const ColState o = part[r * ncq + cc];
+          absorb(st, o.m, o.l, o.o);
+        }
+        const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
+        __nv_bfloat162 *dst =
+            reinterpret_cast<__nv_bfloat162 *>(p.out + ((size_t)b * p.n_qh + h0) * D + c * 4);
+        dst[0] = __floats2bfloat162_rn(st.o.x * inv, st.o.y * inv);
+        dst[1] = __floats2bfloat162_rn(st.o.z * inv, st.o.w * inv);
+      }
+      __syncthreads();
     }
-    const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
-    __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(outp + c * 4);
-    dst[0] = __floats2bfloat162_rn(st.o.x * inv, st.o.y * inv);
-    dst[1] = __floats2bfloat162_rn(st.o.z * inv, st.o.w * inv);
   }
 }
 
 template <int D, int GS>
-cudaError_t launch_combine_t(const DecodeParams &p, int n_warps, cudaStream_t stream) {
-  const int grid = p.n_seq * p.n_kvh * p.n_sub;
-  const size_t fixed = 32 * sizeof(int) + sizeof(ColState) * kCombineThreads;
-  const size_t smem = fixed + (p.n_seq + 1) * sizeof(int);
-  auto kern = combine_kernel<D, GS>;
-  static std::mutex mu;
-  static std::set<int> configured;  // devices whose shared-memory limit is set
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!configured.count(dev)) {
-      err = cudaFuncSetAttribute(
-          kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-          (int)(fixed + (KVATTN_MAX_SEQS + 1) * sizeof(int)));
-      if (err != cudaSuccess) return err;
-      configured.insert(dev);
-    }
-  }
+cudaError_t launch_combine_t(const DecodeParams &p, int sms, cudaStream_t stream) {
+  const int n_streams = p.n_seq * p.n_kvh * p.n_sub;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  const long long items = (long long)n_streams * (GS * D / 4 >= 128 ? 4 : GS * D / 4 >= 64 ? 2 : 1);
+  cfg.gridDim = dim3((unsigned)(items < 2 * sms ? items : 2 * sms));
   cfg.blockDim = dim3(kCombineThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p, n_warps);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D, GS>, p, n_streams);
 }
 
 }  // namespace
 
-cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int n_warps,
+cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int sms,
                            cudaStream_t stream) {
   if (p.n_seq <= 0) return cudaSuccess;
   if (head_dim == 64) {
-    if (gs == 4) return launch_combine_t<64, 4>(p, n_warps, stream);
-    if (gs == 2) return launch_combine_t<64, 2>(p, n_warps, stream);
-    return launch_combine_t<64, 1>(p, n_warps, stream);
+    if (gs == 4) return launch_combine_t<64, 4>(p, sms, stream);
+    if (gs == 2) return launch_combine_t<64, 2>(p, sms, stream);
+    return launch_combine_t<64, 1>(p, sms, stream);
   }
-  if (gs == 4) return launch_combine_t<128, 4>(p, n_warps, stream);
-  if (gs == 2) return launch_combine_t<128, 2>(p, n_warps, stream);
-  return launch_combine_t<128, 1>(p, n_warps, stream);
+  if (gs == 4) return launch_combine_t<128, 4>(p, sms, stream);
+  if (gs == 2) return launch_combine_t<128, 2>(p, sms, stream);
+  return launch_combine_t<128, 1>(p, sms, stream);
 }
 
 }  // namespace kvattn

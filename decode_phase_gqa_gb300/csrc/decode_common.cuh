@@ -28,11 +28,13 @@ __device__ __forceinline__ float pick(const float (&a)[N], int i) {
 // ---- work split --------------------------------------------------------------
 // Units per sequence and their prefix sums into shared memory (pref[0..B]);
 // T = units over all streams.  Returns false when there is nothing to do.
-// `scratch` holds at least kThreads / 32 ints.  All threads of the CTA call it.
+// `scratch` holds at least kThreads / 32 ints.  All threads of the CTA call it;
+// with `report`, out-of-range lengths set KVATTN_DEV_BAD_LEN in the status word
+// and clear their streams' hand-off entries.
 template <int kThreads>
 __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int *scratch,
                                            long long &T, int *lens = nullptr,
-                                           int *poss = nullptr) {
+                                           int *poss = nullptr, bool report = false) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.n_seq;
   const int spu = p.n_kvh * p.n_sub;
@@ -40,7 +42,17 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
   const int chunk = (B + kThreads - 1) / kThreads;
   const int b0 = min(B, tid * chunk), b1 = min(B, b0 + chunk);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += units_of(__ldg(p.seq_lens + b), cap);
+  bool bad = false;
+  for (int b = b0; b < b1; ++b) {
+    const int n = units_of(__ldg(p.seq_lens + b), cap);
+    if (n == 0 && report) {  // only an out-of-range length spans no unit
+      bad = true;
+      for (int si = 0; si < p.n_kvh * p.n_sub; ++si)  // nothing for the combine kernel
+        p.meta[(size_t)b * p.n_kvh * p.n_sub + si] = make_int2(0, 0);
+    }
+    local += n;
+  }
+  if (bad) atomicOr(p.status, KVATTN_DEV_BAD_LEN);
   int incl = local;
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
@@ -116,20 +128,23 @@ __device__ __forceinline__ float frac_turns(int pos, float2 g) {
   return t - rintf(t);
 }
 
-// physical page of flattened unit t (cursor b advanced monotonically), or -1
-// when the block-table entry is out of range
-__device__ __forceinline__ int page_of_unit(const DecodeParams &p, const int *pref, int spu,
-                                            long long t, int &b) {
+// block-table entry (physical page, not yet range-checked) of flattened unit t
+// (cursor b advanced monotonically)
+__device__ __forceinline__ int page_raw_of_unit(const DecodeParams &p, const int *pref, int spu,
+                                                long long t, int &b) {
   const UnitPos up = locate_unit(t, b, pref, spu);
-  const int page =
-      __ldg(p.block_table + (size_t)up.b * p.max_pages + (up.u * kUnitRows) / p.page_size);
-  return (page >= 0 && page < p.num_pages) ? page : -1;
+  return __ldg(p.block_table + (size_t)up.b * p.max_pages + (up.u * kUnitRows) / p.page_size);
 }
 
 // 16-byte asynchronous global -> shared copy (no register staging)
 __device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
+}
+// make `bar` track this thread's earlier cp.async copies: its pending count
+// is raised now and lowered when they have landed
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");

@@ -51,6 +51,7 @@
 #include <utility>
 
 #include "decode_common.cuh"
+#include "storage.cuh"
 
 namespace kvattn {
 
@@ -66,12 +67,14 @@ struct MmaCfg {
   static constexpr int kStage = 2 * kTile;  // K then V
   static constexpr int kScales = INT8 ? 2 * kUnitRows * 4 : 0;  // K then V row scales
   static constexpr int kQBytes = GS * D * 2;  // one stream's raw query rows (bf16)
+  static constexpr int kNewBytes = new_row_bytes<D, INT8>();  // the new token's stored row
   // stages per warp: as many as fit a 75 KB CTA (3 CTAs per SM) next to the
-  // frequency table, per-warp query buffers, barriers and stage flags, the
-  // 1 KB alignment slack and a 2 KB allowance for the per-sequence arrays
-  static constexpr int kOther = 512 + 64 + W * kQBytes + 1024;
+  // frequency tables, per-warp query and new-row buffers, barriers and stage
+  // pages, the 1 KB alignment slack and 1600 bytes for the per-sequence
+  // arrays (batches of up to 132 sequences keep 3 CTAs per SM)
+  static constexpr int kOther = 1024 + 64 + W * (kQBytes + kNewBytes) + 1024;
   static constexpr int kPerStage = kStage + kScales + 8 + 4;
-  static constexpr int kSWFit = (kCtaSmemBudget - kOther - 2048) / (W * kPerStage);
+  static constexpr int kSWFit = (kCtaSmemBudget - kOther - 1600) / (W * kPerStage);
   static constexpr int kSW = kSWFit > 8 ? 8 : kSWFit;
   static constexpr int kKSteps = D / 16;       // MMA k-steps (QK) and m-tiles (PV)
   static constexpr int kLdm = kRowBytes / 32;  // ldmatrix.x4 per tile (2 chunks each)
@@ -80,9 +83,11 @@ struct MmaCfg {
   static constexpr int kScaleOff = kStagesBytes;                  // [W][kSW][32] fp32
   static constexpr int kBarOff = kScaleOff + W * kSW * kScales;
   static constexpr int kFreqOff = kBarOff + W * kSW * 8;  // rope turns per position, float2[D/2]
-  static constexpr int kMiscOff = kFreqOff + 512;
+  static constexpr int kInvOff = kFreqOff + 512;   // rope_theta^(-2i/d), double[D/2]
+  static constexpr int kMiscOff = kInvOff + 512;   // 4 ints of scratch
   static constexpr int kQOff = kMiscOff + 64;             // [W][GS][D] bf16
-  static constexpr int kValidOff = kQOff + W * kQBytes;   // [W][kSW] int
+  static constexpr int kNewOff = kQOff + W * kQBytes;     // [W][kNewBytes]
+  static constexpr int kValidOff = kNewOff + W * kNewBytes;  // [W][kSW] int: page of a stage
   static constexpr int kPrefOff = kValidOff + W * kSW * 4;
   // fixed part + alignment slack; the per-sequence arrays (prefix sums,
   // lengths, positions: 3 n_seq + 1 ints) follow
@@ -92,6 +97,7 @@ struct MmaCfg {
   static_assert(kSW >= 2, "need at least double buffering");
   static_assert(kQBytes % 16 == 0, "query rows are copied in 16-byte chunks");
   static_assert(kFreqOff % 16 == 0, "turns are read as float2");
+  static_assert(kNewOff % 16 == 0 && kNewBytes % 16 == 0, "new rows move in 16-byte chunks");
 };
 
 // Byte offset of 16-byte chunk `ch` of row `row` in a [16][kRowBytes] tile
@@ -130,6 +136,15 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u_flipped, uint32_t 
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(u_flipped), "r"(0x64646464u), "r"(sel));
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64806480u));
+  return r;
+}
+
+// Two int8 codes of `u` as the f16 pair 1152 + x (the conversion above without
+// its subtraction); the key's dot products start from -1152 * sum(q), so the
+// bias cancels inside the MMA accumulation.
+__device__ __forceinline__ uint32_t codes_to_f16x2_biased(uint32_t u_flipped, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(u_flipped), "r"(0x64646464u), "r"(sel));
   return r;
 }
 
@@ -279,6 +294,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   float *scales = reinterpret_cast<float *>(smem + C::kScaleOff);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
   float2 *turns = reinterpret_cast<float2 *>(smem + C::kFreqOff);
+  double *inv_freq = reinterpret_cast<double *>(smem + C::kInvOff);
   int *misc = reinterpret_cast<int *>(smem + C::kMiscOff);
   int *pref = reinterpret_cast<int *>(smem + C::kPrefOff);
   int *lens = pref + p.n_seq + 1;
@@ -294,11 +310,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const char *qc = reinterpret_cast<const char *>(p.q);
     for (size_t l = blockIdx.x * per + tid; l < min(q_lines, (blockIdx.x + 1) * per); l += kDecodeThreads)
       asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(qc + l * 128));
+    // and the new keys and values, which the warps appending them read
+    const size_t kv_lines = ((size_t)p.n_seq * p.n_kvh * D * 2 + 127) / 128;
+    const size_t kper = (kv_lines + gridDim.x - 1) / gridDim.x;
+    const char *kc = reinterpret_cast<const char *>(p.k_new);
+    const char *vc = reinterpret_cast<const char *>(p.v_new);
+    for (size_t l = blockIdx.x * kper + tid; l < min(kv_lines, (blockIdx.x + 1) * kper);
+         l += kDecodeThreads) {
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(kc + l * 128));
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(vc + l * 128));
+    }
   }
   __nv_bfloat16 *qbuf = reinterpret_cast<__nv_bfloat16 *>(smem + C::kQOff) + warp * GS * D;
-  volatile int *svalid = reinterpret_cast<int *>(smem + C::kValidOff) + warp * C::kSW;
+  // physical page of each stage's unit (-1: out of range, the unit is skipped)
+  volatile int *spage = reinterpret_cast<int *>(smem + C::kValidOff) + warp * C::kSW;
   const int spu = p.n_kvh * p.n_sub;
-  if (tid < D / 2) turns[tid] = p.turns[tid];
+  // the frequency tables go to shared memory: lanes index them by pair, and
+  // divergent reads of kernel parameters serialise
+  if (tid < D / 2) {
+    turns[tid] = p.turns[tid];
+    inv_freq[tid] = p.inv_freq[tid];
+  }
+  if (tid < (int)(sizeof(kSinCosStep) + 127) / 128)  // the sin/cos step table, into L1
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char *>(kSinCosStep) + 128 * tid));
   if (tid == 0) {
     for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -308,7 +342,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // prefix sums of units per sequence, lengths and positions (its barriers
   // also publish the above); shares are per warp here
   long long T = 0;
-  if (!plan_units<kDecodeThreads>(p, pref, misc, T, lens, poss)) return;
+  if (!plan_units<kDecodeThreads>(p, pref, misc, T, lens, poss, blockIdx.x == 0)) return;
   const long long n_warps = min((long long)gridDim.x * W, (long long)p.n_shares);
   const long long nwa = min(n_warps, max(1LL, (T + p.min_units - 1) / p.min_units));
   const long long g = (long long)blockIdx.x * W + warp;
@@ -318,11 +352,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   const int start_b = seq_of_unit(wt0, pref, p.n_seq, spu);
   const uint64_t pol = l2_evict_first_policy();
 
-  // raw query rows of a stream -> this warp's buffer (asynchronous copy)
+  // raw query rows of a stream -> this warp's buffer by 16-byte cp.async (an
+  // LSU copy from L2, where the prologue put the queries: a bulk copy would
+  // queue behind the SM's flood of tile copies).  With the int8 cache, lanes
+  // 0-7 issue the scale copies that the stage barriers track, so only lanes
+  // kQLane0.. copy (and wait for) query rows.
+  constexpr int kQLane0 = INT8 ? 8 : 0;
   auto prefetch_queries = [&](int b, int h0) {
+    __syncwarp();
     const char *src = reinterpret_cast<const char *>(p.q + ((size_t)b * p.n_qh + h0) * D);
-    for (int c = lane; c < C::kQBytes / 16; c += 32)
-      cp_async_16(reinterpret_cast<char *>(qbuf) + c * 16, src + c * 16);
+    if (lane >= kQLane0)
+      for (int c = lane - kQLane0; c < C::kQBytes / 16; c += 32 - kQLane0)
+        cp_async_16(reinterpret_cast<char *>(qbuf) + c * 16, src + c * 16);
+    cp_async_commit();
+  };
+  // raw new key and value rows of (sequence b, KV head j) -> the warp's
+  // new-row buffer, the same way (any plain load issued once the SM's inbound
+  // queue is full of tiles waits microseconds behind them)
+  uint8_t *nrow = smem + C::kNewOff + warp * C::kNewBytes;
+  auto prefetch_new_raw = [&](int b, int j) {
+    const size_t kv = ((size_t)b * p.n_kvh + j) * D;
+    const char *ks = reinterpret_cast<const char *>(p.k_new + kv);
+    const char *vs = reinterpret_cast<const char *>(p.v_new + kv);
+    if (lane >= kQLane0)
+      for (int c = lane - kQLane0; c < 4 * D / 16; c += 32 - kQLane0)
+        cp_async_16(nrow + c * 16, (c < 2 * D / 16 ? ks + c * 16 : vs + (c - 2 * D / 16) * 16));
     cp_async_commit();
   };
   // position of the next unit to request: sequence, KV head, query-head group
@@ -337,6 +391,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     cb_u = up.u;
     cb_units = up.units;
     prefetch_queries(up.b, cb_j * GS * p.n_sub + cb_sub * GS);
+    if (up.first + up.units <= wt1) prefetch_new_raw(up.b, cb_j);  // the first stream is appended here
   }
   auto advance = [&]() {  // only while units remain in the share
     if (++cb_u < cb_units) return;
@@ -353,46 +408,48 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
 
   // ---- producer ---------------------------------------------------------------
   // Physical pages are fetched 32 units ahead, one per lane, so the issuing
-  // lane never waits on the block table.  Only the last unit of a stream holds
-  // the token the append grid writes in this step: the issuing lane waits for
-  // that grid (programmatic dependent launch) before the first such unit and
-  // requests everything else at once.
+  // lane never waits on the block table.  The last unit of a stream holds the
+  // slot of the new token, which the warp consuming that unit fills in shared
+  // memory itself (below): nothing waits for the pool write.
+  // (raw block-table entries: the range check waits until a page is used, so
+  // that the second window's load does not stall the first requests)
   int pcur = start_b;  // per-lane cursor of the page windows
   int win_base = 0;
-  int win_page = lane < count ? page_of_unit(p, pref, spu, wt0 + lane, pcur) : -1;
-  int nxt_page = -1;  // loaded once the first units are requested
-  bool appended_visible = false;
+  int win_page = lane < count ? page_raw_of_unit(p, pref, spu, wt0 + lane, pcur) : -1;
+  int nxt_page = 32 + lane < count ? page_raw_of_unit(p, pref, spu, wt0 + 32 + lane, pcur) : -1;
   auto issue = [&](int i) {  // called by the whole warp, in unit order
     if (i > 0) advance();
     if (i - win_base >= 32) {
       win_base += 32;
       win_page = nxt_page;
       const int tn = win_base + 32 + lane;
-      nxt_page = tn < count ? page_of_unit(p, pref, spu, wt0 + tn, pcur) : -1;
+      nxt_page = tn < count ? page_raw_of_unit(p, pref, spu, wt0 + tn, pcur) : -1;
     }
-    const int page = __shfl_sync(0xffffffffu, win_page, i - win_base);
-    if (lane == 0) {
-      if (cb_u == cb_units - 1 && !appended_visible) {
-        pdl_wait_primary();
-        appended_visible = true;
+    int page = __shfl_sync(0xffffffffu, win_page, i - win_base);
+    page = (page >= 0 && page < p.num_pages) ? page : -1;
+    const int st = warp * C::kSW + i % C::kSW;
+    const int row = (page * p.n_kvh + cb_j) * p.page_size + ((cb_u * kUnitRows) & (p.page_size - 1));
+    if constexpr (INT8) {
+      // the unit's 2 x 64 bytes of row scales: one 16-byte cp.async per lane
+      // 0-7, which the stage's barrier tracks (each raises the barrier's
+      // pending count until its copy lands, before lane 0 arrives below)
+      if (page >= 0 && lane < 8) {
+        cp_async_16(scales + st * (2 * kUnitRows) + 4 * lane,
+                    (lane < 4 ? p.k_scales : p.v_scales) + row + 4 * (lane & 3));
+        cp_async_mbar_arrive(&bars[st]);
       }
-      const int st = warp * C::kSW + i % C::kSW;
-      svalid[i % C::kSW] = page >= 0;
+      __syncwarp();
+    }
+    if (lane == 0) {
+      spage[i % C::kSW] = page;
       if (page >= 0) {
-        const int row = (page * p.n_kvh + cb_j) * p.page_size +
-                        ((cb_u * kUnitRows) & (p.page_size - 1));
         uint8_t *dst = stages + (size_t)st * C::kStage;
-        mbar_arrive_expect_tx(&bars[st], C::kStage + C::kScales);
+        mbar_arrive_expect_tx(&bars[st], C::kStage);
 #pragma unroll
         for (int r = 0; r < C::kRegions; ++r) {
           const int x = r * C::kBoxW / (INT8 ? 1 : 2);  // element column of box r
           tma_load_2d(dst + r * C::kBox, &p.tmap_k, x, row, &bars[st], pol);
           tma_load_2d(dst + C::kTile + r * C::kBox, &p.tmap_v, x, row, &bars[st], pol);
-        }
-        if constexpr (INT8) {
-          float *sd = scales + st * (2 * kUnitRows);
-          bulk_g2s(sd, p.k_scales + row, kUnitRows * 4, &bars[st], pol);
-          bulk_g2s(sd + kUnitRows, p.v_scales + row, kUnitRows * 4, &bars[st], pol);
         }
       } else {
         atomicOr(p.status, KVATTN_DEV_BAD_PAGE);
@@ -402,7 +459,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   };
   int issued = 0;
   for (; issued < min(C::kSW, count); ++issued) issue(issued);
-  if (32 + lane < count) nxt_page = page_of_unit(p, pref, spu, wt0 + 32 + lane, pcur);
 
   // ---- consumer ---------------------------------------------------------------
   const int hb = (GS == 4) ? 2 * (lane & 1) : 0;  // first head of this lane's columns
@@ -426,19 +482,44 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int h0 = j * GS * p.n_sub + sub * GS;
     const int sid = sp.b * spu + sp.si;
 
+    // The warp that consumes the stream's last unit forms the stored key and
+    // value of the new token (the storage recipe, storage.cuh) once that
+    // unit's copy is in flight (kSW units ahead), while it waits for data
+    // anyway; when the tile has landed it puts them into the tile in place of
+    // whatever the pool held in the slot, and writes them to slot L of the
+    // pool (for the KV head's first query-head group only: one writer per
+    // slot).  So the step's attention never waits for its own append.
+    const bool own_last = E <= wt1;
+    const long long tab_at = max(t, E - C::kSW);
+
     uint32_t qb[C::kKSteps][2];
     float inv_sq;
     float cr[D / 64], sr[D / 64];
     warp_query_angles<D>(p, turns, poss[sp.b], lane, cr, sr);  // while the rows land
-    cp_async_wait_all();
+    if (lane >= kQLane0) cp_async_wait_all();
     __syncwarp();
     warp_query_fragments<D, GS, INT8>(p, cr, sr, qbuf, lane, qb, inv_sq);
     __syncwarp();
+    // int8: the key codes enter the MMA as 1152 + x; -1152 * (column sum of
+    // Qc), formed by the same MMA with a constant A of -1152, is where every
+    // unit's dot products start (this lane's columns 2 (lane % 4) + {0, 1})
+    float kbias[2] = {0.f, 0.f};
+    if constexpr (INT8) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t m1152[4] = {0xe480e480u, 0xe480e480u, 0xe480e480u, 0xe480e480u};
+#pragma unroll
+      for (int ks = 0; ks < C::kKSteps; ++ks) mma_f16_16816(acc, m1152, qb[ks][0], qb[ks][1]);
+      kbias[0] = acc[0];
+      kbias[1] = acc[1];
+    }
     if (E < wt1) {  // the share continues: fetch the next stream's query rows
       int b = sp.b;
       const UnitPos nx = locate_unit(E, b, pref, spu);
       prefetch_queries(nx.b, (nx.si / p.n_sub) * GS * p.n_sub + (nx.si % p.n_sub) * GS);
     }
+    // this stream's raw new rows (the first stream's came in the prologue),
+    // after the query wait above so that it does not wait for them
+    if (own_last && t > wt0) prefetch_new_raw(sp.b, j);
     float o[C::kKSteps][4];
 #pragma unroll
     for (int dt = 0; dt < C::kKSteps; ++dt)
@@ -457,6 +538,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
 
     for (long long tt = t; tt < e; ++tt) {
+      if (own_last && tt == tab_at) {
+        if (lane >= kQLane0) cp_async_wait_all();  // the raw rows
+        __syncwarp();
+        stage_new_row<D, INT8>(poss[sp.b], inv_freq, p.use_rope != 0, lane, nrow);
+      }
       const int i = (int)(tt - wt0);
       const int st = warp * C::kSW + i % C::kSW;
       bool ok = false;
@@ -469,11 +555,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       }
       consumed = i + 1;
       const int tok0 = (int)(tt - F) * kUnitRows;
-      if (ok && svalid[i % C::kSW]) {
+      const int upage = spage[i % C::kSW];
+      if (ok && upage >= 0) {
         const int nrows = min(kUnitRows, L + 1 - tok0);
         uint8_t *Ks = stages + (size_t)st * C::kStage;
         uint8_t *Vs = Ks + C::kTile;
         const uint32_t kb = smem_addr(Ks), vb = smem_addr(Vs);
+        if (own_last && tt == E - 1) {  // slot L is row L - tok0 of the last unit
+          const long long slot =
+              sub == 0 ? ((long long)upage * p.n_kvh + j) * p.page_size + L % p.page_size : -1;
+          put_new_row<D, INT8>(nrow, Ks, Vs, scales + st * (2 * kUnitRows), L - tok0, slot,
+                               p.k_pages, p.v_pages, p.k_scales, p.v_scales, lane,
+                               [](int r, int ch) { return tile_off<C>(r, ch); });
+          __syncwarp();
+        }
         if (!INT8 && nrows < kUnitRows) {
           // bf16 rows past the sequence end hold stale data: zero them in V
           // so that their zero weights cannot meet a NaN (int8 codes are
@@ -499,8 +594,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
           }
         }
 
-        // S^T = K Qc^T
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T = K Qc^T (int8: from -1152 * column sums of Qc, see kbias)
+        float s[4] = {kbias[0], kbias[1], kbias[0], kbias[1]};
 #pragma unroll
         for (int it = 0; it < C::kLdm; ++it) {
           uint32_t a[4];
@@ -512,8 +607,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               const uint32_t r0 = a[2 * c] ^ 0x80808080u, r1 = a[2 * c + 1] ^ 0x80808080u;
-              const uint32_t f[4] = {codes_to_f16x2(r0, 0x5140u), codes_to_f16x2(r1, 0x5140u),
-                                     codes_to_f16x2(r0, 0x5342u), codes_to_f16x2(r1, 0x5342u)};
+              const uint32_t f[4] = {codes_to_f16x2_biased(r0, 0x5140u),
+                                     codes_to_f16x2_biased(r1, 0x5140u),
+                                     codes_to_f16x2_biased(r0, 0x5342u),
+                                     codes_to_f16x2_biased(r1, 0x5342u)};
               mma_f16_16816(s, f, qb[2 * it + c][0], qb[2 * it + c][1]);
             }
           } else {
@@ -689,6 +786,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const auto dB = [&](int dt) { return INT8 ? dt * 16 + 2 * dr + 1 : dt * 16 + dr + 8; };
     __nv_bfloat16 *outp = p.out + ((size_t)sp.b * p.n_qh + h0) * D;
     if (F >= wt0 && E <= wt1) {
+      if (lane == 0) p.meta[sid] = make_int2(0, 0);  // nothing for the combine kernel
       if (writer) {
 #pragma unroll
         for (int h = 0; h < C::kHL; ++h) {
@@ -702,6 +800,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       }
     } else {
       // partial record of this warp's part: acc[GS][D] relative to 2^m, m, l
+      // (the records of a stream's parts are consecutive: one slot per share)
       float *rec = p.records + (size_t)(sid + g) * C::RS;
       if (writer) {
 #pragma unroll
@@ -717,11 +816,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
           }
         }
       }
+      // the stream's first share tells the combine kernel where its records are
+      if (F >= wt0 && lane == 0)
+        p.meta[sid] = make_int2((int)g, (int)(owner_of(E - 1, T, nwa) - g + 1));
     }
     t = e;
   }
 
-  cp_async_wait_all();  // no query prefetch may land after the warp has left
+  cp_async_wait_all();  // no copy may land after the warp has left
   if (aborted && lane == 0) {
     for (int i = consumed; i < issued; ++i)
       (void)mbar_wait_bounded(&bars[warp * C::kSW + i % C::kSW], (uint32_t)((i / C::kSW) & 1));
@@ -763,11 +865,8 @@ cudaError_t launch_decode_mma_t(const DecodeParams &p, int grid, cudaStream_t st
   cfg.blockDim = dim3(kDecodeThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // the first kernel of a call: an ordinary launch, ordered after all earlier
+  // work on the stream
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

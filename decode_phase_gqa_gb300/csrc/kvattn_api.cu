@@ -1,9 +1,9 @@
 // Host side of the C ABI declared in include/kvattn.h: argument checks (fail
 // closed, nothing is launched on an error), workspace layout, the RoPE
-// frequency table, the TMA descriptors of the pools and the launches of one
-// decode step on the caller's stream: append, split-KV attention as its
-// programmatic dependent, and the merge of split streams as the attention's
-// programmatic dependent.  No host synchronisation except in
+// frequency table, the TMA descriptors of the pools and the two launches of
+// one decode step on the caller's stream: the split-KV attention kernel (which
+// also appends the new token) and, as its programmatic dependent, the merge of
+// the streams its work split cut.  No host synchronisation except in
 // kvattn_read_device_status.
 #include <cudaTypedefs.h>
 
@@ -149,50 +149,31 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   const int g = n_qh / n_kvh;
   const int gs = group_split(g);
 
-  // ---- launch 1: RoPE on the new key, append of key and value ----
+  // ---- launch 1: append of the new token and split-KV attention ----
   const bool use_rope = rope_theta > 0.0f;
-  AppendParams ap = {};
-  ap.k_new = static_cast<const __nv_bfloat16 *>(k_new);
-  ap.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-  ap.k_pages = k_pages;
-  ap.v_pages = v_pages;
-  ap.k_scales = k_scales;
-  ap.v_scales = v_scales;
-  ap.block_table = block_table;
-  ap.seq_lens = seq_lens;
-  ap.positions = positions;
-  ap.status = reinterpret_cast<uint32_t *>(ws + wl.status_off);
-  ap.n_seq = n_seq;
-  ap.n_kvh = n_kvh;
-  ap.head_dim = head_dim;
-  ap.page_size = page_size;
-  ap.max_pages = max_pages_per_seq;
-  ap.num_pages = num_pages;
-  ap.kv_int8 = int8 ? 1 : 0;
-  ap.use_rope = use_rope ? 1 : 0;
-  // frequency of rotation pair i: rope_theta^(-2i/d), in double
-  for (int i = 0; i < head_dim / 2; ++i)
-    ap.inv_freq[i] = use_rope ? std::pow((double)rope_theta, -(2.0 * i) / head_dim) : 0.0;
-  if (launch_append(ap, st) != cudaSuccess) return KVATTN_ECUDA;
-
-  // ---- launch 2: split-KV attention ----
   DecodeParams dp = {};
   dp.block_table = block_table;
   dp.seq_lens = seq_lens;
   dp.positions = positions;
   dp.q = static_cast<const __nv_bfloat16 *>(q);
+  dp.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  dp.v_new = static_cast<const __nv_bfloat16 *>(v_new);
   dp.k_pages = k_pages;
   dp.v_pages = v_pages;
   dp.k_scales = k_scales;
   dp.v_scales = v_scales;
   dp.out = static_cast<__nv_bfloat16 *>(out);
   dp.records = reinterpret_cast<float *>(ws + wl.records_off);
-  dp.status = ap.status;
-  dp.use_rope = ap.use_rope;
+  dp.meta = reinterpret_cast<int2 *>(ws + wl.meta_off);
+  dp.status = reinterpret_cast<uint32_t *>(ws + wl.status_off);
+  dp.use_rope = use_rope ? 1 : 0;
   // scores are formed in log2 units: fold scale * log2(e) into the query
   dp.qscale = (float)((double)scale * 1.4426950408889634);
+  // frequency of rotation pair i: rope_theta^(-2i/d), in double
+  for (int i = 0; i < head_dim / 2; ++i)
+    dp.inv_freq[i] = use_rope ? std::pow((double)rope_theta, -(2.0 * i) / head_dim) : 0.0;
   for (int i = 0; i < 64; ++i) {
-    const double g = ap.inv_freq[i] * 0.15915494309189535;  // / (2 pi)
+    const double g = dp.inv_freq[i] * 0.15915494309189535;  // / (2 pi)
     const float hi = (float)g;
     dp.turns[i] = make_float2(hi, (float)(g - (double)hi));
   }
@@ -224,8 +205,8 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   const int grid = (shares + kDecodeWarps - 1) / kDecodeWarps;
   if (decode_launcher(dp, head_dim, gs, int8, grid, st, nullptr, true) != cudaSuccess)
     return KVATTN_ECUDA;
-  // ---- launch 3: merge of the streams the warp shares split ----
-  if (launch_combine(dp, head_dim, gs, shares, st) != cudaSuccess) return KVATTN_ECUDA;
+  // ---- launch 2: merge of the streams the warp shares split ----
+  if (launch_combine(dp, head_dim, gs, sms, st) != cudaSuccess) return KVATTN_ECUDA;
   return KVATTN_OK;
 }
 

@@ -27,26 +27,17 @@ constexpr long long kWaitCycles = 2000000000LL;
 // Query heads per CTA group: the largest of 4, 2, 1 dividing the GQA group.
 inline int group_split(int g) { return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1; }
 
-struct AppendParams {
-  const __nv_bfloat16 *k_new, *v_new;
-  void *k_pages, *v_pages;
-  float *k_scales, *v_scales;
-  const int32_t *block_table, *seq_lens, *positions;
-  uint32_t *status;
-  int n_seq, n_kvh, head_dim, page_size, max_pages, num_pages, kv_int8, use_rope;
-  double inv_freq[64];        // rope_theta^(-2i/d), i < d/2 (host-computed)
-};
-
 struct DecodeParams {
   // 2-D views [num_pages * n_kvh * page_size rows][head_dim] of the bf16
   // K and V pools, boxes of 16 rows x 64 columns, 128-byte swizzle
   CUtensorMap tmap_k, tmap_v;
   const int32_t *block_table, *seq_lens, *positions;
-  const __nv_bfloat16 *q;
-  const void *k_pages, *v_pages;
-  const float *k_scales, *v_scales;
+  const __nv_bfloat16 *q, *k_new, *v_new;
+  void *k_pages, *v_pages;      // written only in the new token's slot
+  float *k_scales, *v_scales;
   __nv_bfloat16 *out;
   float *records;      // partial softmax states of split streams
+  int2 *meta;          // per split stream: its first share and number of shares
   uint32_t *status;
   int n_seq, n_qh, n_kvh, page_size, max_pages, num_pages;
   int n_sub;           // query-head groups per KV head (G / GS)
@@ -57,6 +48,8 @@ struct DecodeParams {
   // turns per position of rotation pair i, rope_theta^(-2i/d) / (2 pi), as an
   // fp32 head and remainder (host-computed in double)
   float2 turns[64];
+  // rope_theta^(-2i/d) in double: the angles of the stored key
+  double inv_freq[64];
 };
 
 // floats of one partial record (acc[gs][d], m[gs], l[gs]), padded so every
@@ -67,7 +60,7 @@ __host__ __device__ inline constexpr int record_floats(int gs, int d) {
 
 // ---- workspace layout ----------------------------------------------------
 struct WorkspaceLayout {
-  size_t status_off, records_off, total;
+  size_t status_off, meta_off, records_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -78,14 +71,14 @@ inline WorkspaceLayout workspace_layout(int n_seq, int n_qh, int n_kvh, int d) {
   const int gs = group_split(g);
   const size_t streams = (size_t)n_seq * n_kvh * (g / gs);
   w.status_off = 0;
-  w.records_off = 256;
+  w.meta_off = 256;  // int2 per stream
+  w.records_off = align_up(w.meta_off + streams * 2 * sizeof(int), 256);
   const size_t records = streams + KVATTN_MAX_SPLITS;
   w.total = align_up(w.records_off + records * (size_t)record_floats(gs, d) * sizeof(float), 256);
   return w;
 }
 
 // ---- launchers (one per translation unit) ----------------------------------
-cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 // Decode kernel of one (head_dim, group split) configuration: stores the
 // resident CTAs per SM in *ctas_per_sm (when non-NULL) and launches the kernel
 // with `grid` CTAs when `launch` is set.
@@ -93,9 +86,9 @@ cudaError_t launch_decode_bf16(const DecodeParams &p, int head_dim, int gs, int 
                                cudaStream_t stream, int *ctas_per_sm, bool launch);
 cudaError_t launch_decode_int8(const DecodeParams &p, int head_dim, int gs, int grid,
                                cudaStream_t stream, int *ctas_per_sm, bool launch);
-// Merge of the partial records of split streams left by the bf16 decode
-// kernel (n_warps = number of warp shares it used).
-cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int n_warps,
+// Merge of the partial records of the streams the decode kernel's work split
+// cut (sms = the GPU's SM count).
+cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int sms,
                            cudaStream_t stream);
 
 #ifdef __CUDACC__
