@@ -43,7 +43,7 @@ METRIC = "decode-attn tokens/s and KV-read HBM GB/s (% of GB300 peak) per config
 PRIMARY = "smollm3"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
-SRC_FILES = ["decode_common.cuh", "decode_mma.cuh", "kvattn_internal.cuh",
+SRC_FILES = ["decode_common.cuh", "decode_mma.cuh", "kvattn_internal.cuh", "angle_table.inc",
              "storage.cuh", "kvattn_api.cu", "decode_bf16.cu", "decode_int8.cu",
              "combine.cu"]
 
@@ -452,12 +452,12 @@ def native(args, rank, world, local):
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_kind": peak_kind,
             "traffic": recorded_traffic(args.config),
-            "kernel": "kvattn decode call (RoPE/append + split-KV attention kernels, "
+            "kernel": "kvattn decode call (decode kernel with RoPE/append + combine kernel, "
                       "timed together): algorithmic K+V bytes per call / call time",
         },
         "e2e": main["e2e"],
-        # append, decode and combine kernels per call
-        "gpu_launches": 3 * main["calls_per_step"] * args.steps,
+        # decode (with the append) and combine kernels per call
+        "gpu_launches": 2 * main["calls_per_step"] * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "impl": "native",
     }

@@ -29,8 +29,7 @@ __device__ __forceinline__ float pick(const float (&a)[N], int i) {
 // Units per sequence and their prefix sums into shared memory (pref[0..B]);
 // T = units over all streams.  Returns false when there is nothing to do.
 // `scratch` holds at least kThreads / 32 ints.  All threads of the CTA call it;
-// with `report`, out-of-range lengths set KVATTN_DEV_BAD_LEN in the status word
-// and clear their streams' hand-off entries.
+// with `report`, out-of-range lengths set KVATTN_DEV_BAD_LEN in the status word.
 template <int kThreads>
 __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int *scratch,
                                            long long &T, int *lens = nullptr,
@@ -45,11 +44,7 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
   bool bad = false;
   for (int b = b0; b < b1; ++b) {
     const int n = units_of(__ldg(p.seq_lens + b), cap);
-    if (n == 0 && report) {  // only an out-of-range length spans no unit
-      bad = true;
-      for (int si = 0; si < p.n_kvh * p.n_sub; ++si)  // nothing for the combine kernel
-        p.meta[(size_t)b * p.n_kvh * p.n_sub + si] = make_int2(0, 0);
-    }
+    bad |= n == 0 && report;  // only an out-of-range length spans no unit
     local += n;
   }
   if (bad) atomicOr(p.status, KVATTN_DEV_BAD_LEN);

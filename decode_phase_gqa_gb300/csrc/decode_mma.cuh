@@ -84,7 +84,8 @@ struct MmaCfg {
   static constexpr int kBarOff = kScaleOff + W * kSW * kScales;
   static constexpr int kFreqOff = kBarOff + W * kSW * 8;  // rope turns per position, float2[D/2]
   static constexpr int kInvOff = kFreqOff + 512;   // rope_theta^(-2i/d), double[D/2]
-  static constexpr int kMiscOff = kInvOff + 512;   // 4 ints of scratch
+  // 4 ints of scratch; the warps' new-row barriers (uint64[W]) at +32
+  static constexpr int kMiscOff = kInvOff + 512;
   static constexpr int kQOff = kMiscOff + 64;             // [W][GS][D] bf16
   static constexpr int kNewOff = kQOff + W * kQBytes;     // [W][kNewBytes]
   static constexpr int kValidOff = kNewOff + W * kNewBytes;  // [W][kSW] int: page of a stage
@@ -97,6 +98,7 @@ struct MmaCfg {
   static_assert(kSW >= 2, "need at least double buffering");
   static_assert(kQBytes % 16 == 0, "query rows are copied in 16-byte chunks");
   static_assert(kFreqOff % 16 == 0, "turns are read as float2");
+  static_assert(32 + 8 * W <= 64, "the misc area holds the new-row barriers");
   static_assert(kNewOff % 16 == 0 && kNewBytes % 16 == 0, "new rows move in 16-byte chunks");
 };
 
@@ -335,6 +337,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char *>(kSinCosStep) + 128 * tid));
   if (tid == 0) {
     for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
+    for (int w = 0; w < W; ++w) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 32) + w, 1);
     fence_barrier_init();
     prefetch_tensormap(&p.tmap_k);
     prefetch_tensormap(&p.tmap_v);
@@ -345,8 +348,38 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   if (!plan_units<kDecodeThreads>(p, pref, misc, T, lens, poss, blockIdx.x == 0)) return;
   const long long n_warps = min((long long)gridDim.x * W, (long long)p.n_shares);
   const long long nwa = min(n_warps, max(1LL, (T + p.min_units - 1) / p.min_units));
-  const long long g = (long long)blockIdx.x * W + warp;
-  if (g >= nwa) return;
+  // A small batch leaves at least half of the warps idle: then the shares
+  // are spread over the CTAs (warp slots 0..A-1 of every CTA; A <= W/2) and
+  // idle warp A + a of a CTA forms the new token's stored row of active warp
+  // a's first stream, if a appends it, while a streams its units (a warp
+  // alone takes microseconds for the correctly rounded cos/sin).  Otherwise
+  // warp g of the grid takes share g.
+  const bool spread = 2 * nwa <= n_warps;
+  const int A = spread ? (int)((nwa + gridDim.x - 1) / gridDim.x) : W;
+  const long long g = spread ? (long long)warp * gridDim.x + blockIdx.x : (long long)blockIdx.x * W + warp;
+  uint64_t *row_ready = reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 32);  // [W]
+  if (g >= nwa) {
+    const int a = warp - A;
+    const long long ga = (long long)a * gridDim.x + blockIdx.x;
+    if (spread && a >= 0 && a < A && ga < nwa) {
+      const long long wa0 = ga * T / nwa, wa1 = (ga + 1) * T / nwa;
+      int b = seq_of_unit(wa0, pref, p.n_seq, spu);
+      const UnitPos up = locate_unit(wa0, b, pref, spu);
+      if (up.first + up.units <= wa1) {  // warp a appends its first stream's new token
+        uint8_t *arow = smem + C::kNewOff + a * C::kNewBytes;
+        const size_t kv = ((size_t)up.b * p.n_kvh + up.si / p.n_sub) * D;
+        const char *ks = reinterpret_cast<const char *>(p.k_new + kv);
+        const char *vs = reinterpret_cast<const char *>(p.v_new + kv);
+        for (int c = lane; c < 4 * D / 16; c += 32)
+          cp_async_16(arow + c * 16, (c < 2 * D / 16 ? ks + c * 16 : vs + (c - 2 * D / 16) * 16));
+        cp_async_wait_all();
+        __syncwarp();
+        stage_new_row<D, INT8>(poss[up.b], inv_freq, p.use_rope != 0, lane, arow);
+        if (lane == 0) mbar_arrive(&row_ready[a]);  // (release: the row is visible)
+      }
+    }
+    return;
+  }
   const long long wt0 = g * T / nwa, wt1 = (g + 1) * T / nwa;
   const int count = (int)(wt1 - wt0);
   const int start_b = seq_of_unit(wt0, pref, p.n_seq, spu);
@@ -391,7 +424,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     cb_u = up.u;
     cb_units = up.units;
     prefetch_queries(up.b, cb_j * GS * p.n_sub + cb_sub * GS);
-    if (up.first + up.units <= wt1) prefetch_new_raw(up.b, cb_j);  // the first stream is appended here
+    // the first stream's raw new rows, if this warp appends it and no idle
+    // warp does the work
+    if (up.first + up.units <= wt1 && !(spread && warp + A < W)) prefetch_new_raw(up.b, cb_j);
   }
   auto advance = [&]() {  // only while units remain in the share
     if (++cb_u < cb_units) return;
@@ -490,6 +525,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     // pool (for the KV head's first query-head group only: one writer per
     // slot).  So the step's attention never waits for its own append.
     const bool own_last = E <= wt1;
+    const bool helped = own_last && t == wt0 && spread && warp + A < W;  // row formed by a helper
     const long long tab_at = max(t, E - C::kSW);
 
     uint32_t qb[C::kKSteps][2];
@@ -538,7 +574,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
 
     for (long long tt = t; tt < e; ++tt) {
-      if (own_last && tt == tab_at) {
+      if (own_last && tt == tab_at && !helped) {
         if (lane >= kQLane0) cp_async_wait_all();  // the raw rows
         __syncwarp();
         stage_new_row<D, INT8>(poss[sp.b], inv_freq, p.use_rope != 0, lane, nrow);
@@ -562,6 +598,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
         uint8_t *Vs = Ks + C::kTile;
         const uint32_t kb = smem_addr(Ks), vb = smem_addr(Vs);
         if (own_last && tt == E - 1) {  // slot L is row L - tok0 of the last unit
+          if (helped && !__all_sync(0xffffffffu, mbar_wait_bounded(&row_ready[warp], 0))) {
+            aborted = true;
+            if (lane == 0) atomicOr(p.status, KVATTN_DEV_TIMEOUT);
+          }
           const long long slot =
               sub == 0 ? ((long long)upage * p.n_kvh + j) * p.page_size + L % p.page_size : -1;
           put_new_row<D, INT8>(nrow, Ks, Vs, scales + st * (2 * kUnitRows), L - tok0, slot,
@@ -786,7 +826,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const auto dB = [&](int dt) { return INT8 ? dt * 16 + 2 * dr + 1 : dt * 16 + dr + 8; };
     __nv_bfloat16 *outp = p.out + ((size_t)sp.b * p.n_qh + h0) * D;
     if (F >= wt0 && E <= wt1) {
-      if (lane == 0) p.meta[sid] = make_int2(0, 0);  // nothing for the combine kernel
       if (writer) {
 #pragma unroll
         for (int h = 0; h < C::kHL; ++h) {
@@ -816,9 +855,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
           }
         }
       }
-      // the stream's first share tells the combine kernel where its records are
-      if (F >= wt0 && lane == 0)
-        p.meta[sid] = make_int2((int)g, (int)(owner_of(E - 1, T, nwa) - g + 1));
     }
     t = e;
   }

@@ -164,7 +164,6 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.v_scales = v_scales;
   dp.out = static_cast<__nv_bfloat16 *>(out);
   dp.records = reinterpret_cast<float *>(ws + wl.records_off);
-  dp.meta = reinterpret_cast<int2 *>(ws + wl.meta_off);
   dp.status = reinterpret_cast<uint32_t *>(ws + wl.status_off);
   dp.use_rope = use_rope ? 1 : 0;
   // scores are formed in log2 units: fold scale * log2(e) into the query
@@ -206,7 +205,7 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   if (decode_launcher(dp, head_dim, gs, int8, grid, st, nullptr, true) != cudaSuccess)
     return KVATTN_ECUDA;
   // ---- launch 2: merge of the streams the warp shares split ----
-  if (launch_combine(dp, head_dim, gs, sms, st) != cudaSuccess) return KVATTN_ECUDA;
+  if (launch_combine(dp, head_dim, gs, shares, sms, st) != cudaSuccess) return KVATTN_ECUDA;
   return KVATTN_OK;
 }
 

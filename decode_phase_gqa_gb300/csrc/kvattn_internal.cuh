@@ -37,7 +37,6 @@ struct DecodeParams {
   float *k_scales, *v_scales;
   __nv_bfloat16 *out;
   float *records;      // partial softmax states of split streams
-  int2 *meta;          // per split stream: its first share and number of shares
   uint32_t *status;
   int n_seq, n_qh, n_kvh, page_size, max_pages, num_pages;
   int n_sub;           // query-head groups per KV head (G / GS)
@@ -60,7 +59,7 @@ __host__ __device__ inline constexpr int record_floats(int gs, int d) {
 
 // ---- workspace layout ----------------------------------------------------
 struct WorkspaceLayout {
-  size_t status_off, meta_off, records_off, total;
+  size_t status_off, records_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -71,8 +70,7 @@ inline WorkspaceLayout workspace_layout(int n_seq, int n_qh, int n_kvh, int d) {
   const int gs = group_split(g);
   const size_t streams = (size_t)n_seq * n_kvh * (g / gs);
   w.status_off = 0;
-  w.meta_off = 256;  // int2 per stream
-  w.records_off = align_up(w.meta_off + streams * 2 * sizeof(int), 256);
+  w.records_off = 256;
   const size_t records = streams + KVATTN_MAX_SPLITS;
   w.total = align_up(w.records_off + records * (size_t)record_floats(gs, d) * sizeof(float), 256);
   return w;
@@ -88,7 +86,7 @@ cudaError_t launch_decode_int8(const DecodeParams &p, int head_dim, int gs, int 
                                cudaStream_t stream, int *ctas_per_sm, bool launch);
 // Merge of the partial records of the streams the decode kernel's work split
 // cut (sms = the GPU's SM count).
-cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int sms,
+cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int n_warps, int sms,
                            cudaStream_t stream);
 
 #ifdef __CUDACC__
