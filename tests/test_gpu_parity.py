@@ -221,3 +221,19 @@ def test_captured_in_cuda_graph():
     torch.cuda.synchronize()
     ref, *_ = oracle_decode(wl, h)
     assert_close(out_f64(out), ref)
+
+
+@pytest.mark.parametrize("kv,d,theta", [("bf16", 128, 1e4), ("int8", 64, 5e5), ("bf16", 64, 1e6)])
+def test_appended_keys_over_many_positions(kv, d, theta):
+    # 384 short sequences whose RoPE positions spread over [0, 2^21): the stored
+    # key's cos/sin take the float-float path below angles of 2^18 and the
+    # double fallback above; every appended slot must equal the oracle's
+    # recipe bit for bit, and the outputs stay within tolerance
+    n = 384
+    lens = list(np.random.default_rng(d).integers(0, 20, size=n))
+    wl, h = custom(8, 2, lens, d=d, kv=kv, seed=d + 3, theta=theta)
+    pos = np.random.default_rng(7).integers(0, 1 << 21, size=n).astype(np.int32)
+    pos[:8] = [0, 1, 2, 3, 255, 256, 1 << 17, (1 << 18) + 1]
+    wl.positions = pos
+    h["positions"] = pos.copy()
+    check_against_oracle(wl, h)
