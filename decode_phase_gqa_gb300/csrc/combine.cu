@@ -107,6 +107,9 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   __shared__ int scratch[32];
   extern __shared__ int pref[];  // [n_seq + 1]
 
+  // the next call's decode grid may be placed now: it waits for this grid to
+  // end before it touches global memory
+  pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int spu = p.n_kvh * p.n_sub;
   // The decode kernel's split, recomputed from the lengths while it runs:

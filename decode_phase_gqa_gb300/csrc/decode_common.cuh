@@ -43,9 +43,12 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
   int local = 0;
   bool bad = false;
   for (int b = b0; b < b1; ++b) {
-    const int n = units_of(__ldg(p.seq_lens + b), cap);
+    const int L = __ldg(p.seq_lens + b);
+    if (poss) poss[b] = __ldg(p.positions + b);  // in flight with the length
+    const int n = units_of(L, cap);
     bad |= n == 0 && report;  // only an out-of-range length spans no unit
     local += n;
+    if (lens) lens[b] = L;
   }
   if (bad) atomicOr(p.status, KVATTN_DEV_BAD_LEN);
   int incl = local;
@@ -62,11 +65,8 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
     total += scratch[w];
   }
   for (int b = b0; b < b1; ++b) {
-    const int L = __ldg(p.seq_lens + b);
     pref[b] = run;
-    run += units_of(L, cap);
-    if (lens) lens[b] = L;
-    if (poss) poss[b] = __ldg(p.positions + b);
+    run += units_of(lens ? lens[b] : __ldg(p.seq_lens + b), cap);
   }
   if (tid == 0) pref[B] = total;
   __syncthreads();

@@ -302,8 +302,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   int *lens = pref + p.n_seq + 1;
   int *poss = lens + p.n_seq;
 
-  pdl_launch_dependents();  // the combine grid may start planning at once
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __nv_bfloat16 *qbuf = reinterpret_cast<__nv_bfloat16 *>(smem + C::kQOff) + warp * GS * D;
+  // physical page of each stage's unit (-1: out of range, the unit is skipped)
+  volatile int *spage = reinterpret_cast<int *>(smem + C::kValidOff) + warp * C::kSW;
+  const int spu = p.n_kvh * p.n_sub;
+  // set-up that reads nothing an earlier kernel writes (launched as a
+  // programmatic dependent, the grid may start before that kernel ends):
+  // the frequency tables go to shared memory (lanes index them by pair, and
+  // divergent reads of kernel parameters serialise), the sin/cos step table
+  // into L1, the stage barriers are initialised
+  if (tid < D / 2) {
+    turns[tid] = p.turns[tid];
+    inv_freq[tid] = p.inv_freq[tid];
+  }
+  if (tid < (int)(sizeof(kSinCosStep) + 127) / 128)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char *>(kSinCosStep) + 128 * tid));
+  if (tid == 0) {
+    for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
+    for (int w = 0; w < W; ++w) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 32) + w, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&p.tmap_k);
+    prefetch_tensormap(&p.tmap_v);
+  }
+  pdl_wait_primary();       // every earlier kernel of the stream is complete and visible
+  pdl_launch_dependents();  // the combine grid may start planning at once
   {
     // every CTA pulls its slice of the queries into L2 at once, so that the
     // warps' query rows do not queue behind the flood of K/V requests
@@ -322,28 +345,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(kc + l * 128));
       asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(vc + l * 128));
     }
-  }
-  __nv_bfloat16 *qbuf = reinterpret_cast<__nv_bfloat16 *>(smem + C::kQOff) + warp * GS * D;
-  // physical page of each stage's unit (-1: out of range, the unit is skipped)
-  volatile int *spage = reinterpret_cast<int *>(smem + C::kValidOff) + warp * C::kSW;
-  const int spu = p.n_kvh * p.n_sub;
-  // the frequency tables go to shared memory: lanes index them by pair, and
-  // divergent reads of kernel parameters serialise
-  if (tid < D / 2) {
-    turns[tid] = p.turns[tid];
-    inv_freq[tid] = p.inv_freq[tid];
-  }
-  if (tid < (int)(sizeof(kSinCosStep) + 127) / 128)  // the sin/cos step table, into L1
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char *>(kSinCosStep) + 128 * tid));
-  if (tid == 0) {
-    for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
-    for (int w = 0; w < W; ++w) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 32) + w, 1);
-    fence_barrier_init();
-    prefetch_tensormap(&p.tmap_k);
-    prefetch_tensormap(&p.tmap_v);
+    // and the block table when it is small, so that the page look-ups after
+    // the planning below find it in L2 instead of waiting on DRAM again
+    const size_t bt_lines = ((size_t)p.n_seq * p.max_pages * 4 + 127) / 128;
+    if (bt_lines <= kTablePrefetchLines) {
+      const size_t bper = (bt_lines + gridDim.x - 1) / gridDim.x;
+      const char *bc = reinterpret_cast<const char *>(p.block_table);
+      for (size_t l = blockIdx.x * bper + tid; l < min(bt_lines, (blockIdx.x + 1) * bper); l += kDecodeThreads)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(bc + l * 128));
+    }
   }
   // prefix sums of units per sequence, lengths and positions (its barriers
-  // also publish the above); shares are per warp here
+  // also publish the set-up above); shares are per warp here
   long long T = 0;
   if (!plan_units<kDecodeThreads>(p, pref, misc, T, lens, poss, blockIdx.x == 0)) return;
   const long long n_warps = min((long long)gridDim.x * W, (long long)p.n_shares);
@@ -901,8 +914,14 @@ cudaError_t launch_decode_mma_t(const DecodeParams &p, int grid, cudaStream_t st
   cfg.blockDim = dim3(kDecodeThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  // the first kernel of a call: an ordinary launch, ordered after all earlier
-  // work on the stream
+  // a programmatic dependent of the stream's previous kernel: the grid may be
+  // placed while that kernel finishes, and waits for it (griddepcontrol.wait)
+  // before it reads or writes anything in global memory
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -21,6 +21,9 @@ constexpr int kDecodeThreads = kDecodeWarps * 32;
 // shared memory a decode CTA may use so that 3 fit on one SM (228 KB, with
 // 1 KB reserved per CTA)
 constexpr int kCtaSmemBudget = 75 * 1024;
+// The decode grid pulls the whole block table into L2 at its start when the
+// table spans at most this many 128-byte lines (1 MB).
+constexpr long long kTablePrefetchLines = 8192;
 // A bounded wait gives up after this many SM clocks (about one second).
 constexpr long long kWaitCycles = 2000000000LL;
 
