@@ -69,10 +69,11 @@ struct MmaCfg {
   static constexpr int kQBytes = GS * D * 2;  // one stream's raw query rows (bf16)
   static constexpr int kNewBytes = new_row_bytes<D, INT8>();  // the new token's stored row
   // stages per warp: as many as fit a 75 KB CTA (3 CTAs per SM) next to the
-  // frequency tables, per-warp query and new-row buffers, barriers and stage
+  // frequency and angle tables, per-warp query and new-row buffers, barriers and stage
   // pages, the 1 KB alignment slack and 1600 bytes for the per-sequence
   // arrays (batches of up to 132 sequences keep 3 CTAs per SM)
-  static constexpr int kOther = 1024 + 64 + W * (kQBytes + kNewBytes) + 1024;
+  static constexpr int kTabBytes = (int)sizeof(kSinCosStep);  // sin/cos steps of the angle routine
+  static constexpr int kOther = 1024 + 64 + kTabBytes + W * (kQBytes + kNewBytes) + 1024;
   static constexpr int kPerStage = kStage + kScales + 8 + 4;
   static constexpr int kSWFit = (kCtaSmemBudget - kOther - 1600) / (W * kPerStage);
   static constexpr int kSW = kSWFit > 8 ? 8 : kSWFit;
@@ -89,7 +90,8 @@ struct MmaCfg {
   static constexpr int kQOff = kMiscOff + 64;             // [W][GS][D] bf16
   static constexpr int kNewOff = kQOff + W * kQBytes;     // [W][kNewBytes]
   static constexpr int kValidOff = kNewOff + W * kNewBytes;  // [W][kSW] int: page of a stage
-  static constexpr int kPrefOff = kValidOff + W * kSW * 4;
+  static constexpr int kTabOff = kValidOff + W * kSW * 4;  // copy of kSinCosStep (float4)
+  static constexpr int kPrefOff = kTabOff + kTabBytes;
   // fixed part + alignment slack; the per-sequence arrays (prefix sums,
   // lengths, positions: 3 n_seq + 1 ints) follow
   static constexpr int kFixedSmem = kPrefOff + 1024;
@@ -98,6 +100,7 @@ struct MmaCfg {
   static_assert(kSW >= 2, "need at least double buffering");
   static_assert(kQBytes % 16 == 0, "query rows are copied in 16-byte chunks");
   static_assert(kFreqOff % 16 == 0, "turns are read as float2");
+  static_assert(kTabOff % 16 == 0 && kTabBytes % 16 == 0, "the angle table is read as float4");
   static_assert(32 + 8 * W <= 64, "the misc area holds the new-row barriers");
   static_assert(kNewOff % 16 == 0 && kNewBytes % 16 == 0, "new rows move in 16-byte chunks");
 };
@@ -298,6 +301,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   float2 *turns = reinterpret_cast<float2 *>(smem + C::kFreqOff);
   double *inv_freq = reinterpret_cast<double *>(smem + C::kInvOff);
   int *misc = reinterpret_cast<int *>(smem + C::kMiscOff);
+  float4 *angle_tab = reinterpret_cast<float4 *>(smem + C::kTabOff);
   int *pref = reinterpret_cast<int *>(smem + C::kPrefOff);
   int *lens = pref + p.n_seq + 1;
   int *poss = lens + p.n_seq;
@@ -310,14 +314,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // set-up that reads nothing an earlier kernel writes (launched as a
   // programmatic dependent, the grid may start before that kernel ends):
   // the frequency tables go to shared memory (lanes index them by pair, and
-  // divergent reads of kernel parameters serialise), the sin/cos step table
-  // into L1, the stage barriers are initialised
+  // divergent reads of kernel parameters serialise), and so does the sin/cos
+  // step table; the stage barriers are initialised
   if (tid < D / 2) {
     turns[tid] = p.turns[tid];
     inv_freq[tid] = p.inv_freq[tid];
   }
-  if (tid < (int)(sizeof(kSinCosStep) + 127) / 128)
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char *>(kSinCosStep) + 128 * tid));
+  for (int i = tid; i < C::kTabBytes / 16; i += kDecodeThreads) angle_tab[i] = kSinCosStep[i];
   if (tid == 0) {
     for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
     for (int w = 0; w < W; ++w) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 32) + w, 1);
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
           cp_async_16(arow + c * 16, (c < 2 * D / 16 ? ks + c * 16 : vs + (c - 2 * D / 16) * 16));
         cp_async_wait_all();
         __syncwarp();
-        stage_new_row<D, INT8>(poss[up.b], inv_freq, p.use_rope != 0, lane, arow);
+        stage_new_row<D, INT8>(poss[up.b], inv_freq, angle_tab, p.use_rope != 0, lane, arow);
         if (lane == 0) mbar_arrive(&row_ready[a]);  // (release: the row is visible)
       }
     }
@@ -590,7 +593,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       if (own_last && tt == tab_at && !helped) {
         if (lane >= kQLane0) cp_async_wait_all();  // the raw rows
         __syncwarp();
-        stage_new_row<D, INT8>(poss[sp.b], inv_freq, p.use_rope != 0, lane, nrow);
+        stage_new_row<D, INT8>(poss[sp.b], inv_freq, angle_tab, p.use_rope != 0, lane, nrow);
       }
       const int i = (int)(tt - wt0);
       const int st = warp * C::kSW + i % C::kSW;

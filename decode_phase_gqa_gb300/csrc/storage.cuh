@@ -115,8 +115,11 @@ __device__ __forceinline__ bool near_midpoint(FF v) {
 }
 
 // fp32 cos/sin of the double angle pos * inv_freq, as (float)cos / (float)sin
-// of that double would round them.
-__device__ __forceinline__ void store_angle(int pos, double inv_freq, float &c, float &s) {
+// of that double would round them.  `table` is a copy of kSinCosStep (in
+// shared memory: a lane-divergent read of global memory would queue behind
+// the SM's tile copies).
+__device__ __forceinline__ void store_angle(int pos, double inv_freq, const float4 *table, float &c,
+                                            float &s) {
   const double phi = (double)pos * inv_freq;
   // the quadrant from an fp32 estimate of phi (its error and that of the
   // product with 2/pi stay below 5 * 2^-24 phi): while phi < 2^18 the
@@ -161,7 +164,7 @@ __device__ __forceinline__ void store_angle(int pos, double inv_freq, float &c, 
           ff_add(FF{-0.5f * t.hi, -0.5f * t.lo}, __fmul_rn(__fmul_rn(t.hi, t.hi), 1.f / 24.f));
       const float ds = __fmul_rn(__fmul_rn(rp.hi, t.hi), __fmaf_rn(t.hi, 1.f / 120.f, -1.f / 6.f));
       // 5. recombination with the table
-      const float4 tb = __ldg(&kSinCosStep[aj]);
+      const float4 tb = table[aj];
       const FF S = j < 0 ? FF{-tb.x, -tb.y} : FF{tb.x, tb.y};
       const FF C = {tb.z, tb.w};
       const FF s1 = ff_add(ff_add(S, ff_mul(S, dc)), ff_add(ff_mul(C, rp), __fmul_rn(C.hi, ds)));
@@ -222,8 +225,8 @@ __host__ __device__ constexpr int new_row_bytes() {
 // position pos, into `buf` (natural element order; int8: the two scales
 // follow the rows).  Ends with __syncwarp().
 template <int D, bool INT8>
-__device__ __forceinline__ void stage_new_row(int pos, const double *inv_freq, bool use_rope,
-                                              int lane, uint8_t *buf) {
+__device__ __forceinline__ void stage_new_row(int pos, const double *inv_freq, const float4 *table,
+                                              bool use_rope, int lane, uint8_t *buf) {
   constexpr int PPL = D / 64;
   static_assert(2 * D * (INT8 ? 1 : 2) + (INT8 ? 8 : 0) <= 4 * D, "the stored form fits");
   float xk[D / 32], xv[D / 32];
@@ -237,7 +240,7 @@ __device__ __forceinline__ void stage_new_row(int pos, const double *inv_freq, b
   if (use_rope) {
     float c[PPL], s[PPL];
 #pragma unroll
-    for (int k = 0; k < PPL; ++k) store_angle(pos, inv_freq[lane + 32 * k], c[k], s[k]);
+    for (int k = 0; k < PPL; ++k) store_angle(pos, inv_freq[lane + 32 * k], table, c[k], s[k]);
 #pragma unroll
     for (int k = 0; k < PPL; ++k) rot_store(xk[k], xk[PPL + k], c[k], s[k], xk[k], xk[PPL + k]);
   }
