@@ -79,7 +79,6 @@ struct MmaCfg {
   static constexpr int kSW = kSWFit > 8 ? 8 : kSWFit;
   static constexpr int kKSteps = D / 16;       // MMA k-steps (QK) and m-tiles (PV)
   static constexpr int kLdm = kRowBytes / 32;  // ldmatrix.x4 per tile (2 chunks each)
-  static constexpr int kHL = GS == 1 ? 1 : 2;  // query heads per lane
   static constexpr int kStagesBytes = W * kSW * kStage;
   static constexpr int kScaleOff = kStagesBytes;                  // [W][kSW][32] fp32
   static constexpr int kBarOff = kScaleOff + W * kSW * kScales;
@@ -195,8 +194,8 @@ __device__ __forceinline__ void warp_query_angles(const DecodeParams &p, const f
 
 // The B fragments of the query columns for one stream, built by the warp from
 // the raw query rows q[GS][D] (bf16, shared memory): column c = lane / 4 of
-// the MMA is the head of query head c (c < GS), its remainder (GS <= c <
-// 2 GS), or zero; the angles each lane needs are shuffled in.  Lane (c, j =
+// the MMA is the head (c even) or the remainder (c odd) of query head c / 2
+// (c < 2 GS), or zero; the angles each lane needs are shuffled in.  Lane (c, j =
 // lane % 4) of k-step ks holds the elements d = 16 ks + {2j, 2j + 1, 2j + 8,
 // 2j + 9} (bf16 cache: the MMA's own k order) or d = 16 ks + 4j + {0..3}
 // (int8 cache: the k order of the K fragments the codes are unpacked into).
@@ -212,8 +211,8 @@ __device__ __forceinline__ void warp_query_fragments(const DecodeParams &p, cons
   constexpr int e2 = INT8 ? 2 : 8;  // offset of the fragment's second element pair
   const int col = lane >> 2;
   const bool used = col < 2 * GS;
-  const bool is_lo = col >= GS;
-  const int head = used ? (is_lo ? col - GS : col) : 0;
+  const bool is_lo = (col & 1) != 0;
+  const int head = used ? col >> 1 : 0;
   const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrows + head * D);
   const int d0 = (INT8 ? 4 : 2) * (lane & 3);
   uint32_t w[KS / 2][4];  // raw pairs: (d, d+1), (d+e2, d+e2+1) and the same + H
@@ -512,7 +511,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   for (; issued < min(C::kSW, count); ++issued) issue(issued);
 
   // ---- consumer ---------------------------------------------------------------
-  const int hb = (GS == 4) ? 2 * (lane & 1) : 0;  // first head of this lane's columns
+  // this lane's score and output columns are 2 hl (head) and 2 hl + 1
+  // (remainder) of query head hl; lanes with hl >= GS hold padding columns
+  const int hl = lane & 3;
   const int tokr = lane >> 2;                     // this lane's score rows: tokr, tokr + 8
   // ldmatrix row addresses: K (and int8 V) read matrices (rows 0-7, chunk c),
   // (rows 8-15, c), (rows 0-7, c + 1), (rows 8-15, c + 1); bf16 V, transposed,
@@ -577,17 +578,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     for (int dt = 0; dt < C::kKSteps; ++dt)
 #pragma unroll
       for (int k = 0; k < 4; ++k) o[dt][k] = 0.f;
-    // m, l: reference maximum and normaliser of the softmax; mo: reference
-    // maximum of the value weights (int8; the bf16 cache weighs the values by
-    // the softmax weights themselves).  The references start at a finite floor
-    // below every score, so no step needs a guard for an empty state.
-    float m[C::kHL], l[C::kHL], mo[C::kHL];
-#pragma unroll
-    for (int h = 0; h < C::kHL; ++h) {
-      m[h] = kFloor;
-      l[h] = 0.f;
-      mo[h] = kFloor;
-    }
+    // m, l: reference maximum and normaliser of the softmax of head hl; mo:
+    // reference maximum of its value weights (int8; the bf16 cache weighs the
+    // values by the softmax weights themselves).  The references start at a
+    // finite floor below every score, so no step needs a guard for an empty
+    // state.
+    float m = kFloor, l = 0.f, mo = kFloor;
 
     for (long long tt = t; tt < e; ++tt) {
       if (own_last && tt == tab_at && !helped) {
@@ -673,113 +669,74 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
             mma_bf16_16816(s, a, qb[it][0], qb[it][1]);
           }
         }
-        // full scores sc[token half][head slot] = hi column + lo column
-        float sc[2][2];
-        if constexpr (GS == 4) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], 2);
-          sc[0][0] = s[0]; sc[0][1] = s[1]; sc[1][0] = s[2]; sc[1][1] = s[3];
-        } else if constexpr (GS == 2) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], 1);
-          sc[0][0] = s[0]; sc[0][1] = s[1]; sc[1][0] = s[2]; sc[1][1] = s[3];
-        } else {
-          sc[0][0] = s[0] + s[1]; sc[1][0] = s[2] + s[3];
-          sc[0][1] = sc[1][1] = 0.f;  // no second head
-        }
+        // full scores of head hl at tokens tokr, tokr + 8: head column plus
+        // remainder column
+        float sc[2] = {s[0] + s[1], s[2] + s[3]};
         // value-weight exponents (int8): score + log2 vs
-        float xv[2][2];
+        float xv[2];
 #pragma unroll
-        for (int t2 = 0; t2 < 2; ++t2)
-#pragma unroll
-          for (int h = 0; h < C::kHL; ++h) {
-            if constexpr (INT8) sc[t2][h] *= ksr[t2];
-            xv[t2][h] = sc[t2][h] + lv[t2];
-          }
+        for (int t2 = 0; t2 < 2; ++t2) {
+          if constexpr (INT8) sc[t2] *= ksr[t2];
+          xv[t2] = sc[t2] + lv[t2];
+        }
         if (nrows < kUnitRows) {  // a sequence's last unit: drop the rows past its end
 #pragma unroll
           for (int t2 = 0; t2 < 2; ++t2)
-            if (tokr + 8 * t2 >= nrows)
-#pragma unroll
-              for (int h = 0; h < C::kHL; ++h) sc[t2][h] = xv[t2][h] = kNegInf;
+            if (tokr + 8 * t2 >= nrows) sc[t2] = xv[t2] = kNegInf;
         }
 
         // online softmax (log2 units) with lazy references: a reference moves
         // only when a score passes it by more than kLazy, so every weight stays
         // below 2^kLazy and most units leave the accumulators as they are
-        float alpha[C::kHL], pw[2][C::kHL], pv[2][C::kHL];
-        bool moved = false;
-#pragma unroll
-        for (int h = 0; h < C::kHL; ++h) {
-          float mx = fmaxf(sc[0][h], sc[1][h]);
+        float pv[2];
+        float alpha = 1.f;
+        {
+          float mx = fmaxf(sc[0], sc[1]);
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           float a = 1.f;
-          if (mx > m[h] + kLazy) {
-            a = ex2_approx(m[h] - mx);
-            m[h] = mx;
+          if (mx > m + kLazy) {
+            a = ex2_approx(m - mx);
+            m = mx;
           }
-          pw[0][h] = ex2_approx(sc[0][h] - m[h]);
-          pw[1][h] = ex2_approx(sc[1][h] - m[h]);
-          l[h] = l[h] * a + pw[0][h] + pw[1][h];
+          const float pw0 = ex2_approx(sc[0] - m), pw1 = ex2_approx(sc[1] - m);
+          l = l * a + pw0 + pw1;
           if constexpr (INT8) {
-            float xo = fmaxf(xv[0][h], xv[1][h]);
+            float xo = fmaxf(xv[0], xv[1]);
             xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 4));
             xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 8));
             xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 16));
             a = 1.f;
-            if (xo > mo[h] + kLazy) {
-              a = ex2_approx(mo[h] - xo);
-              mo[h] = xo;
+            if (xo > mo + kLazy) {
+              a = ex2_approx(mo - xo);
+              mo = xo;
             }
-            pv[0][h] = ex2_approx(xv[0][h] - mo[h]);
-            pv[1][h] = ex2_approx(xv[1][h] - mo[h]);
+            pv[0] = ex2_approx(xv[0] - mo);
+            pv[1] = ex2_approx(xv[1] - mo);
           } else {
-            pv[0][h] = pw[0][h];
-            pv[1][h] = pw[1][h];
+            pv[0] = pw0;
+            pv[1] = pw1;
           }
-          alpha[h] = a;
-          moved |= a != 1.f;
+          alpha = a;
         }
-        // P^T fragments: this lane's two columns at tokens r and r + 8, head
-        // or remainder of the value weight, zero in padding columns
+        // P^T fragments: this lane's two columns at tokens tokr and tokr + 8:
+        // the value weight rounded to the MMA's type and what that rounding
+        // left out
         uint32_t pr[2];
 #pragma unroll
         for (int t2 = 0; t2 < 2; ++t2) {
-          float x0, x1;
-          const auto rnd = [](float x) { return INT8 ? f16_round(x) : bf16_round(x); };
-          if constexpr (GS == 4) {
-            x0 = pv[t2][0];
-            x1 = pv[t2][1];
-            if (lane & 2) {
-              x0 -= rnd(x0);
-              x1 -= rnd(x1);
-            }
-          } else if constexpr (GS == 2) {
-            x0 = pv[t2][0];
-            x1 = pv[t2][1];
-            if (lane & 1) {
-              x0 -= rnd(x0);
-              x1 -= rnd(x1);
-            }
-            if (lane & 2) x0 = x1 = 0.f;
-          } else {
-            x0 = pv[t2][0];
-            x1 = x0 - rnd(x0);
-            if (lane & 3) x0 = x1 = 0.f;
-          }
-          pr[t2] = INT8 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
+          const float hi = INT8 ? f16_round(pv[t2]) : bf16_round(pv[t2]);
+          pr[t2] = INT8 ? pack_f16(hi, pv[t2] - hi) : pack_bf16(hi, pv[t2] - hi);
         }
         const uint32_t b0 = movmatrix_trans(pr[0]);
         const uint32_t b1 = movmatrix_trans(pr[1]);
         // rescale the accumulators of this lane's columns when a reference moved
-        if (__any_sync(0xffffffffu, moved)) {
-          const float a0 = alpha[0], a1 = alpha[C::kHL - 1];
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int dt = 0; dt < C::kKSteps; ++dt) {
-            o[dt][0] *= a0; o[dt][1] *= a1; o[dt][2] *= a0; o[dt][3] *= a1;
-          }
+          for (int dt = 0; dt < C::kKSteps; ++dt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[dt][k] *= alpha;
         }
         // O^T += V^T P^T
 #pragma unroll
@@ -811,46 +768,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
 
     // ---- end of this warp's part of the stream ----------------------------------
-    // add the remainder columns to the head columns; sum l over the tokens
+    // head column plus remainder column; l summed over the tokens
+    float of[C::kKSteps][2];
 #pragma unroll
     for (int dt = 0; dt < C::kKSteps; ++dt) {
-      if constexpr (GS == 1) {
-        o[dt][0] += o[dt][1];
-        o[dt][2] += o[dt][3];
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          o[dt][k] += __shfl_xor_sync(0xffffffffu, o[dt][k], GS == 4 ? 2 : 1);
-      }
+      of[dt][0] = o[dt][0] + o[dt][1];
+      of[dt][1] = o[dt][2] + o[dt][3];
     }
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
     // accumulator scale to 2^m (int8: from 2^mo)
-    float to_m[C::kHL];
-#pragma unroll
-    for (int h = 0; h < C::kHL; ++h) {
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 4);
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
-      to_m[h] = 1.f;
-      if constexpr (INT8) to_m[h] = ex2_approx(mo[h] - m[h]);
-    }
-    // lanes holding final values: GS 4 -> lane % 4 in {0, 1} (heads hb, hb + 1);
-    // GS 2 -> lane % 4 == 0 (heads 0, 1); GS 1 -> lane % 4 == 0 (head 0).
-    // Accumulator rows: o[dt][h] at d = dA, o[dt][2 + h] at d = dB.
-    const bool writer = (GS == 4) ? (lane & 2) == 0 : (lane & 3) == 0;
+    const float to_m = INT8 ? ex2_approx(mo - m) : 1.f;
+    // lanes with hl < GS hold head hl's output rows d = dA(dt) (of[dt][0])
+    // and d = dB(dt) (of[dt][1])
+    const bool writer = hl < GS;
     const int dr = lane >> 2;
     const auto dA = [&](int dt) { return INT8 ? dt * 16 + 2 * dr : dt * 16 + dr; };
     const auto dB = [&](int dt) { return INT8 ? dt * 16 + 2 * dr + 1 : dt * 16 + dr + 8; };
-    __nv_bfloat16 *outp = p.out + ((size_t)sp.b * p.n_qh + h0) * D;
+    __nv_bfloat16 *outp = p.out + ((size_t)sp.b * p.n_qh + h0 + hl) * D;
     if (F >= wt0 && E <= wt1) {
       if (writer) {
+        const float f = l > 0.f ? to_m / l : 0.f;
 #pragma unroll
-        for (int h = 0; h < C::kHL; ++h) {
-          const float f = l[h] > 0.f ? to_m[h] / l[h] : 0.f;
-#pragma unroll
-          for (int dt = 0; dt < C::kKSteps; ++dt) {
-            outp[(hb + h) * D + dA(dt)] = __float2bfloat16_rn(o[dt][h] * f);
-            outp[(hb + h) * D + dB(dt)] = __float2bfloat16_rn(o[dt][2 + h] * f);
-          }
+        for (int dt = 0; dt < C::kKSteps; ++dt) {
+          outp[dA(dt)] = __float2bfloat16_rn(of[dt][0] * f);
+          outp[dB(dt)] = __float2bfloat16_rn(of[dt][1] * f);
         }
       }
     } else {
@@ -859,16 +802,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       float *rec = p.records + (size_t)(sid + g) * C::RS;
       if (writer) {
 #pragma unroll
-        for (int h = 0; h < C::kHL; ++h) {
-#pragma unroll
-          for (int dt = 0; dt < C::kKSteps; ++dt) {
-            rec[(hb + h) * D + dA(dt)] = o[dt][h] * to_m[h];
-            rec[(hb + h) * D + dB(dt)] = o[dt][2 + h] * to_m[h];
-          }
-          if (dr == 0) {
-            rec[GS * D + hb + h] = m[h];
-            rec[GS * D + GS + hb + h] = l[h];
-          }
+        for (int dt = 0; dt < C::kKSteps; ++dt) {
+          rec[hl * D + dA(dt)] = of[dt][0] * to_m;
+          rec[hl * D + dB(dt)] = of[dt][1] * to_m;
+        }
+        if (dr == 0) {
+          rec[GS * D + hl] = m;
+          rec[GS * D + GS + hl] = l;
         }
       }
     }
