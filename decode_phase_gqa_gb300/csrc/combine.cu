@@ -113,36 +113,37 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   const int tid = threadIdx.x;
   const int spu = p.n_kvh * p.n_sub;
   // The decode kernel's split, recomputed from the lengths while it runs:
-  // the unit list of T units is cut into nwa equal warp shares (share c
-  // covers [floor(c T / nwa), floor((c + 1) T / nwa))), and stream sid's
-  // records sit in slots sid + (its first share) onwards, one per share.
-  long long T = 0;
+  // the unit list of T units is cut into nwa equal warp shares (Split), and
+  // stream sid's records sit in slots sid + (its first share) onwards, one
+  // per share.
+  int T = 0;
   const bool any = plan_units<kCombineThreads>(p, pref, scratch, T);
-  const long long nwa = any ? min((long long)n_warps, max(1LL, (T + p.min_units - 1) / p.min_units)) : 1;
+  const int nwa = any ? min(n_warps, max(1, (T + kMinUnitsPerShare - 1) / kMinUnitsPerShare)) : 1;
+  const Split split(any ? T : 1, nwa);
   const int n_streams = p.n_seq * spu;
   // item it: chunk it / n_streams of stream it % n_streams; CTA c takes
   // items c, c + gridDim.x, ...
-  const long long n_items = any ? (long long)n_streams * kMaxChunks : 0;
-  const long long stride = (long long)gridDim.x * kCombineThreads;
+  const int n_items = any ? n_streams * kMaxChunks : 0;
+  const int stride = (int)gridDim.x * kCombineThreads;
   bool waited = false;
-  for (long long base = blockIdx.x; base < n_items; base += stride) {
+  for (int base = blockIdx.x; base < n_items; base += stride) {
     if (tid == 0) n_list = 0;
     __syncthreads();
-    const long long it = base + (long long)tid * gridDim.x;
+    const int it = base + tid * (int)gridDim.x;
     if (it < n_items) {
-      const int sid = (int)(it % n_streams), q = (int)(it / n_streams);
+      const int q = it / n_streams, sid = it - q * n_streams;
       const int b = sid / spu, si = sid % spu;
       const int units = pref[b + 1] - pref[b];
       if (units > 0) {
-        const long long F = (long long)spu * pref[b] + (long long)si * units;
-        const long long w0 = owner_of(F, T, nwa);
-        const int nseg = (int)(owner_of(F + units - 1, T, nwa) - w0 + 1);
+        const int F = spu * pref[b] + si * units;
+        const int w0 = split.owner(F);
+        const int nseg = split.owner(F + units - 1) - w0 + 1;
         int R = 1;
         while (R * 8 < nseg) R *= 2;
         const int nch = nseg <= kShort ? 1 : max(1, min(kMaxChunks, NC * R / kCombineThreads));
         if (nseg > 1 && q < nch) {
           const int k = atomicAdd(&n_list, 1);
-          list[k] = make_int4(sid, q, nch, (int)w0);
+          list[k] = make_int4(sid, q, nch, w0);
           lseg[k] = nseg;
         }
       }

@@ -10,11 +10,23 @@
 
 namespace kvattn {
 
-// CTA that owns flattened unit t when T units are cut into n equal shares
-// (share c covers [floor(c T / n), floor((c + 1) T / n))).
-__device__ __forceinline__ long long owner_of(long long t, long long T, long long n) {
-  return ((t + 1) * n - 1) / T;
-}
+// T units cut into n equal shares: share c covers [begin(c), begin(c + 1)),
+// begin(c) = floor(c T / n) = c q + floor(c r / n) with T = q n + r.  All in
+// 32-bit integers (the host keeps T below 2^31 and n <= 4096, so c r < 2^24):
+// a 64-bit division is a long software routine on this GPU.
+struct Split {
+  int T, n, q, r;
+  __device__ __forceinline__ Split(int T_, int n_) : T(T_), n(n_), q(T_ / n_), r(T_ - (T_ / n_) * n_) {}
+  __device__ __forceinline__ int begin(int c) const { return c * q + (c * r) / n; }
+  // share holding unit t (0 <= t < T): an fp32 estimate of t n / T, off by
+  // at most one, corrected against the exact boundaries
+  __device__ __forceinline__ int owner(int t) const {
+    int c = min(n - 1, (int)((float)t * ((float)n / (float)T)));
+    while (c > 0 && begin(c) > t) --c;
+    while (c + 1 < n && begin(c + 1) <= t) ++c;
+    return c;
+  }
+};
 
 // a[i] for a lane-dependent i without dynamic register indexing
 template <int N>
@@ -27,12 +39,13 @@ __device__ __forceinline__ float pick(const float (&a)[N], int i) {
 
 // ---- work split --------------------------------------------------------------
 // Units per sequence and their prefix sums into shared memory (pref[0..B]);
-// T = units over all streams.  Returns false when there is nothing to do.
+// T = units over all streams (below 2^31: the host bounds it by the block
+// table's capacity).  Returns false when there is nothing to do.
 // `scratch` holds at least kThreads / 32 ints.  All threads of the CTA call it;
 // with `report`, out-of-range lengths set KVATTN_DEV_BAD_LEN in the status word.
 template <int kThreads>
 __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int *scratch,
-                                           long long &T, int *lens = nullptr,
+                                           int &T, int *lens = nullptr,
                                            int *poss = nullptr, bool report = false) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.n_seq;
@@ -70,16 +83,16 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
   }
   if (tid == 0) pref[B] = total;
   __syncthreads();
-  T = (long long)spu * pref[B];
+  T = spu * pref[B];
   return T > 0;
 }
 
 // Sequence holding flattened unit t (binary search on the prefix sums).
-__device__ __forceinline__ int seq_of_unit(long long t, const int *pref, int B, int spu) {
+__device__ __forceinline__ int seq_of_unit(int t, const int *pref, int B, int spu) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if ((long long)spu * pref[mid] <= t) lo = mid; else hi = mid - 1;
+    if (spu * pref[mid] <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -88,18 +101,18 @@ __device__ __forceinline__ int seq_of_unit(long long t, const int *pref, int B, 
 // stream within the sequence and unit within the stream.
 struct UnitPos {
   int b, si, u, units;
-  long long first;  // flattened index of the stream's first unit
+  int first;  // flattened index of the stream's first unit
 };
 
-__device__ __forceinline__ UnitPos locate_unit(long long t, int &b, const int *pref, int spu) {
-  while ((long long)spu * pref[b + 1] <= t) ++b;
+__device__ __forceinline__ UnitPos locate_unit(int t, int &b, const int *pref, int spu) {
+  while (spu * pref[b + 1] <= t) ++b;
   UnitPos r;
   r.b = b;
   r.units = pref[b + 1] - pref[b];
-  const long long base = (long long)spu * pref[b];
-  r.si = (int)((t - base) / r.units);
-  r.u = (int)((t - base) % r.units);
-  r.first = base + (long long)r.si * r.units;
+  const int off = t - spu * pref[b];
+  r.si = off / r.units;
+  r.u = off - r.si * r.units;
+  r.first = t - r.u;
   return r;
 }
 
@@ -126,9 +139,9 @@ __device__ __forceinline__ float frac_turns(int pos, float2 g) {
 // block-table entry (physical page, not yet range-checked) of flattened unit t
 // (cursor b advanced monotonically)
 __device__ __forceinline__ int page_raw_of_unit(const DecodeParams &p, const int *pref, int spu,
-                                                long long t, int &b) {
+                                                int t, int &b) {
   const UnitPos up = locate_unit(t, b, pref, spu);
-  return __ldg(p.block_table + (size_t)up.b * p.max_pages + (up.u * kUnitRows) / p.page_size);
+  return __ldg(p.block_table + (size_t)up.b * p.max_pages + (up.u >> p.unit_shift));
 }
 
 // 16-byte asynchronous global -> shared copy (no register staging)

@@ -359,10 +359,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   }
   // prefix sums of units per sequence, lengths and positions (its barriers
   // also publish the set-up above); shares are per warp here
-  long long T = 0;
+  int T = 0;
   if (!plan_units<kDecodeThreads>(p, pref, misc, T, lens, poss, blockIdx.x == 0)) return;
-  const long long n_warps = min((long long)gridDim.x * W, (long long)p.n_shares);
-  const long long nwa = min(n_warps, max(1LL, (T + p.min_units - 1) / p.min_units));
+  const int n_warps = min((int)gridDim.x * W, p.n_shares);
+  const int nwa = min(n_warps, max(1, (T + kMinUnitsPerShare - 1) / kMinUnitsPerShare));
+  const Split split(T, nwa);
   // A small batch leaves at least half of the warps idle: then the shares
   // are spread over the CTAs (warp slots 0..A-1 of every CTA; A <= W/2) and
   // idle warp A + a of a CTA forms the new token's stored row of active warp
@@ -370,14 +371,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // alone takes microseconds for the correctly rounded cos/sin).  Otherwise
   // warp g of the grid takes share g.
   const bool spread = 2 * nwa <= n_warps;
-  const int A = spread ? (int)((nwa + gridDim.x - 1) / gridDim.x) : W;
-  const long long g = spread ? (long long)warp * gridDim.x + blockIdx.x : (long long)blockIdx.x * W + warp;
+  const int A = spread ? (nwa + (int)gridDim.x - 1) / (int)gridDim.x : W;
+  const int g = spread ? warp * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.x * W + warp;
   uint64_t *row_ready = reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 32);  // [W]
   if (g >= nwa) {
     const int a = warp - A;
-    const long long ga = (long long)a * gridDim.x + blockIdx.x;
+    const int ga = a * (int)gridDim.x + (int)blockIdx.x;
     if (spread && a >= 0 && a < A && ga < nwa) {
-      const long long wa0 = ga * T / nwa, wa1 = (ga + 1) * T / nwa;
+      const int wa0 = split.begin(ga), wa1 = split.begin(ga + 1);
       int b = seq_of_unit(wa0, pref, p.n_seq, spu);
       const UnitPos up = locate_unit(wa0, b, pref, spu);
       if (up.first + up.units <= wa1) {  // warp a appends its first stream's new token
@@ -395,8 +396,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     return;
   }
-  const long long wt0 = g * T / nwa, wt1 = (g + 1) * T / nwa;
-  const int count = (int)(wt1 - wt0);
+  const int wt0 = split.begin(g), wt1 = split.begin(g + 1);
+  const int count = wt1 - wt0;
   const int start_b = seq_of_unit(wt0, pref, p.n_seq, spu);
   const uint64_t pol = l2_evict_first_policy();
 
@@ -524,11 +525,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   bool aborted = false;
   int consumed = 0;
   int cb = start_b;
-  long long t = wt0;
+  int t = wt0;
   while (t < wt1) {
     const UnitPos sp = locate_unit(t, cb, pref, spu);
-    const long long F = sp.first, E = F + sp.units;
-    const long long e = min(wt1, E);
+    const int F = sp.first, E = F + sp.units;
+    const int e = min(wt1, E);
     const int L = lens[sp.b];
     const int j = sp.si / p.n_sub, sub = sp.si % p.n_sub;
     const int h0 = j * GS * p.n_sub + sub * GS;
@@ -543,7 +544,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     // slot).  So the step's attention never waits for its own append.
     const bool own_last = E <= wt1;
     const bool helped = own_last && t == wt0 && spread && warp + A < W;  // row formed by a helper
-    const long long tab_at = max(t, E - C::kSW);
+    const int tab_at = max(t, E - C::kSW);
 
     uint32_t qb[C::kKSteps][2];
     float inv_sq;
@@ -585,7 +586,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     // state.
     float m = kFloor, l = 0.f, mo = kFloor;
 
-    for (long long tt = t; tt < e; ++tt) {
+    for (int tt = t; tt < e; ++tt) {
       if (own_last && tt == tab_at && !helped) {
         if (lane >= kQLane0) cp_async_wait_all();  // the raw rows
         __syncwarp();
@@ -615,7 +616,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
             if (lane == 0) atomicOr(p.status, KVATTN_DEV_TIMEOUT);
           }
           const long long slot =
-              sub == 0 ? ((long long)upage * p.n_kvh + j) * p.page_size + L % p.page_size : -1;
+              sub == 0 ? ((long long)upage * p.n_kvh + j) * p.page_size + (L & (p.page_size - 1)) : -1;
           put_new_row<D, INT8>(nrow, Ks, Vs, scales + st * (2 * kUnitRows), L - tok0, slot,
                                p.k_pages, p.v_pages, p.k_scales, p.v_scales, lane,
                                [](int r, int ch) { return tile_off<C>(r, ch); });

@@ -18,10 +18,6 @@ using namespace kvattn;
 
 namespace {
 
-// Work units (16 tokens) a share is given at least when the step is small, so
-// tiny batches use few shares and merge few partial states.
-constexpr int kMinUnitsPerShare = 4;
-
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool supported_page(int page) {
@@ -128,6 +124,10 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   if ((long long)max_pages_per_seq * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
   // pool rows are addressed with 32-bit TMA coordinates
   if ((long long)num_pages * n_kvh * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
+  // the work split counts 16-token units of all streams in 32-bit integers
+  if ((long long)n_seq * n_kvh * (n_qh / n_kvh / group_split(n_qh / n_kvh)) *
+          ((long long)max_pages_per_seq * page_size / kUnitRows) > (long long)INT_MAX)
+    return KVATTN_EUNSUPPORTED;
   const bool int8 = kv_dtype == KVATTN_KV_INT8;
   if (n_seq == 0) return KVATTN_OK;  // empty batch: nothing to read or write
   // ---- pointer checks ----
@@ -183,7 +183,7 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.max_pages = max_pages_per_seq;
   dp.num_pages = num_pages;
   dp.n_sub = g / gs;
-  dp.min_units = kMinUnitsPerShare;
+  for (int u = page_size / kUnitRows; u > 1; u >>= 1) ++dp.unit_shift;
   {
     const long long rows = (long long)num_pages * n_kvh * page_size;
     if (!encode_pool_map(&dp.tmap_k, k_pages, rows, head_dim, int8) ||

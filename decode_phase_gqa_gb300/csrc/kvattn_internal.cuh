@@ -18,6 +18,9 @@ namespace kvattn {
 constexpr int kUnitRows = 16;
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeThreads = kDecodeWarps * 32;
+// Work units a share is given at least when the step is small, so tiny
+// batches use few shares and merge few partial states.
+constexpr int kMinUnitsPerShare = 4;
 // shared memory a decode CTA may use so that 3 fit on one SM (228 KB, with
 // 1 KB reserved per CTA)
 constexpr int kCtaSmemBudget = 75 * 1024;
@@ -44,7 +47,7 @@ struct DecodeParams {
   int n_seq, n_qh, n_kvh, page_size, max_pages, num_pages;
   int n_sub;           // query-head groups per KV head (G / GS)
   int n_shares;        // the unit list is cut into at most this many shares
-  int min_units;       // fewest units a share is given when work is scarce
+  int unit_shift;      // log2(page_size / 16): units per page
   int use_rope;
   float qscale;        // scale * log2(e): scores come out in log2 units
   // turns per position of rotation pair i, rope_theta^(-2i/d) / (2 pi), as an

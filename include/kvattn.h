@@ -51,7 +51,12 @@ extern "C" {
 #define KVATTN_EINVAL 1       /* a NULL/misaligned pointer, a negative or
                                  inconsistent size, n_qh % n_kvh != 0 */
 #define KVATTN_EUNSUPPORTED 2 /* head_dim, page_size, kv_dtype or a size
-                                 outside what the library is built for */
+                                 outside what the library is built for (among
+                                 them: n_seq * n_kvh * (G / gs) *
+                                 max_pages_per_seq * page_size / 16 above
+                                 2^31 - 1, the most 16-token work units a step
+                                 can hold; G = n_qh / n_kvh, gs = the largest of
+                                 4, 2, 1 dividing G) */
 #define KVATTN_ECUDA 3        /* a CUDA runtime call or launch failed */
 #define KVATTN_EWORKSPACE 4   /* workspace NULL, misaligned or too small */
 

@@ -111,6 +111,9 @@ def call(lib, **kw):
     (dict(kv_dtype=2), K.KVATTN_EUNSUPPORTED),
     (dict(n_seq=K.KVATTN_MAX_SEQS + 1), K.KVATTN_EUNSUPPORTED),
     (dict(max_pages_per_seq=1 << 27, page_size=64), K.KVATTN_EUNSUPPORTED),
+    # 4096 sequences x 64 KV heads x 131072 units: the unit count passes 2^31
+    (dict(n_seq=4096, n_qh=64, n_kvh=64, max_pages_per_seq=8192, page_size=256),
+     K.KVATTN_EUNSUPPORTED),
     (dict(q=None), K.KVATTN_EINVAL),
     (dict(out=None), K.KVATTN_EINVAL),
     (dict(block_table=None), K.KVATTN_EINVAL),
