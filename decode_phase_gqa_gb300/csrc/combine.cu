@@ -113,13 +113,13 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   const int tid = threadIdx.x;
   const int spu = p.n_kvh * p.n_sub;
   // The decode kernel's split, recomputed from the lengths while it runs:
-  // the unit list of T units is cut into nwa equal warp shares (Split), and
+  // the unit list of T units is cut into nwa warp shares (WeightedSplit), and
   // stream sid's records sit in slots sid + (its first share) onwards, one
   // per share.
   int T = 0;
   const bool any = plan_units<kCombineThreads>(p, pref, scratch, T);
   const int nwa = any ? min(n_warps, max(1, (T + kMinUnitsPerShare - 1) / kMinUnitsPerShare)) : 1;
-  const Split split(any ? T : 1, nwa);
+  const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, any ? T : 1, nwa);
   const int n_streams = p.n_seq * spu;
   // item it: chunk it / n_streams of stream it % n_streams; CTA c takes
   // items c, c + gridDim.x, ...
@@ -136,8 +136,8 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
       const int units = pref[b + 1] - pref[b];
       if (units > 0) {
         const int F = spu * pref[b] + si * units;
-        const int w0 = split.owner(F);
-        const int nseg = split.owner(F + units - 1) - w0 + 1;
+        const int w0 = split.owner(F, sid);
+        const int nseg = split.owner(F + units - 1, sid) - w0 + 1;
         int R = 1;
         while (R * 8 < nseg) R *= 2;
         const int nch = nseg <= kShort ? 1 : max(1, min(kMaxChunks, NC * R / kCombineThreads));

@@ -87,15 +87,59 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
   return T > 0;
 }
 
-// Sequence holding flattened unit t (binary search on the prefix sums).
-__device__ __forceinline__ int seq_of_unit(int t, const int *pref, int B, int spu) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (spu * pref[mid] <= t) lo = mid; else hi = mid - 1;
+// The split actually used: a warp share is an equal part of a weighted unit
+// list, in which every unit weighs 4 and every stream weighs `sc` more (its
+// fixed costs: the query set-up at its start, the new token's row at its end),
+// placed after its last unit.  Unit t of stream s (s = b spu + si) sits at
+// weighted position 4 t + sc s; the list is X = 4 T + sc B spu long (the host
+// keeps X below 2^31).  Share c holds the units whose positions fall in
+// [split.begin(c), split.begin(c + 1)); its unit range is
+// [first_unit(split.begin(c)), first_unit(split.begin(c + 1))).
+struct WeightedSplit {
+  const int *pref;  // units per stream, prefix over sequences
+  int B, spu, sc, T;
+  Split split;
+  __device__ __forceinline__ WeightedSplit(const int *pref_, int B_, int spu_, int sc_, int T_, int n)
+      : pref(pref_), B(B_), spu(spu_), sc(sc_), T(T_), split(4 * T_ + sc_ * B_ * spu_, n) {}
+  // weighted position of sequence b's first stream
+  __device__ __forceinline__ int seq_pos(int b) const { return 4 * spu * pref[b] + sc * spu * b; }
+  // First unit whose weighted position is >= y (T when there is none) and its
+  // sequence *b (the sequence of the unit; B - 1 when there is none).  Called
+  // by a whole warp with the same y: the last sequence starting at or before
+  // y is found by a 32-way search (one shared-memory read per lane and level,
+  // two levels up to 1024 sequences).
+  __device__ __forceinline__ int first_unit(int y, int lane, int *b) const {
+    if (y >= split.T) {
+      *b = B - 1;
+      return T;
+    }
+    int lo = 0, n = B;  // seq_pos(lo) <= y; the answer lies in [lo, lo + n)
+    while (n > 1) {
+      const int step = (n + 31) >> 5;
+      const int c = lo + lane * step;
+      const unsigned m = __ballot_sync(0xffffffffu, c < lo + n && seq_pos(c) <= y);
+      const int k = 31 - __clz(m);  // lane 0 always qualifies
+      const int nlo = lo + k * step;
+      n = min(step, lo + n - nlo);
+      lo = nlo;
+    }
+    const int u = pref[lo + 1] - pref[lo];
+    const int ws = 4 * u + sc;  // > 0: y lies inside sequence lo's streams
+    const int off = y - seq_pos(lo);
+    const int si = off / ws, rem = off - si * ws;
+    const int t = spu * pref[lo] + si * u + min(u, (rem + 3) >> 2);
+    // past the sequence's last unit: the next sequence with units holds t
+    int bb = lo;
+    while (bb + 1 < B && spu * pref[bb + 1] <= t) ++bb;
+    *b = bb;
+    return t;
   }
-  return lo;
-}
+  __device__ __forceinline__ int begin_unit(int c, int lane, int *b) const {
+    return first_unit(split.begin(c), lane, b);
+  }
+  // share holding unit t of stream sid
+  __device__ __forceinline__ int owner(int t, int sid) const { return split.owner(4 * t + sc * sid); }
+};
 
 // Position of flattened unit t: sequence (cursor b, advanced monotonically),
 // stream within the sequence and unit within the stream.

@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   if (!plan_units<kDecodeThreads>(p, pref, misc, T, lens, poss, blockIdx.x == 0)) return;
   const int n_warps = min((int)gridDim.x * W, p.n_shares);
   const int nwa = min(n_warps, max(1, (T + kMinUnitsPerShare - 1) / kMinUnitsPerShare));
-  const Split split(T, nwa);
+  const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, T, nwa);
   // A small batch leaves at least half of the warps idle: then the shares
   // are spread over the CTAs (warp slots 0..A-1 of every CTA; A <= W/2) and
   // idle warp A + a of a CTA forms the new token's stored row of active warp
@@ -378,10 +378,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int a = warp - A;
     const int ga = a * (int)gridDim.x + (int)blockIdx.x;
     if (spread && a >= 0 && a < A && ga < nwa) {
-      const int wa0 = split.begin(ga), wa1 = split.begin(ga + 1);
-      int b = seq_of_unit(wa0, pref, p.n_seq, spu);
-      const UnitPos up = locate_unit(wa0, b, pref, spu);
-      if (up.first + up.units <= wa1) {  // warp a appends its first stream's new token
+      int b = 0, b1 = 0;
+      const int wa0 = split.begin_unit(ga, lane, &b), wa1 = split.begin_unit(ga + 1, lane, &b1);
+      if (wa0 >= wa1) b = 0;
+      const UnitPos up = locate_unit(wa0 < wa1 ? wa0 : 0, b, pref, spu);
+      if (wa0 < wa1 && up.first + up.units <= wa1) {  // warp a appends its first stream's new token
         uint8_t *arow = smem + C::kNewOff + a * C::kNewBytes;
         const size_t kv = ((size_t)up.b * p.n_kvh + up.si / p.n_sub) * D;
         const char *ks = reinterpret_cast<const char *>(p.k_new + kv);
@@ -396,9 +397,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     return;
   }
-  const int wt0 = split.begin(g), wt1 = split.begin(g + 1);
+  int start_b = 0, end_b = 0;
+  const int wt0 = split.begin_unit(g, lane, &start_b), wt1 = split.begin_unit(g + 1, lane, &end_b);
   const int count = wt1 - wt0;
-  const int start_b = seq_of_unit(wt0, pref, p.n_seq, spu);
+  if (count == 0) return;  // a share of stream costs only
   const uint64_t pol = l2_evict_first_policy();
 
   // raw query rows of a stream -> this warp's buffer by 16-byte cp.async (an

@@ -7,6 +7,7 @@
 // kvattn_read_device_status.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -17,6 +18,14 @@
 using namespace kvattn;
 
 namespace {
+
+// Weight of a stream's fixed costs in the work split, in quarters of a
+// 16-token unit: the query set-up at the stream's start and the new token's
+// stored row at its end (the correctly rounded cos/sin and, int8, the
+// quantisation) take about as long as streaming this many units when every
+// warp of the GPU streams.
+constexpr int kStreamCostBf16 = 4;
+constexpr int kStreamCostInt8 = 12;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -124,10 +133,14 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   if ((long long)max_pages_per_seq * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
   // pool rows are addressed with 32-bit TMA coordinates
   if ((long long)num_pages * n_kvh * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
-  // the work split counts 16-token units of all streams in 32-bit integers
-  if ((long long)n_seq * n_kvh * (n_qh / n_kvh / group_split(n_qh / n_kvh)) *
-          ((long long)max_pages_per_seq * page_size / kUnitRows) > (long long)INT_MAX)
-    return KVATTN_EUNSUPPORTED;
+  // the work split weighs the 16-token units of all streams in 32-bit integers
+  {
+    const long long streams = (long long)n_seq * n_kvh * (n_qh / n_kvh / group_split(n_qh / n_kvh));
+    const long long units = streams * ((long long)max_pages_per_seq * page_size / kUnitRows);
+    if (units > kMaxStepUnits ||
+        4 * units + streams * std::max(kStreamCostBf16, kStreamCostInt8) > (long long)INT_MAX)
+      return KVATTN_EUNSUPPORTED;
+  }
   const bool int8 = kv_dtype == KVATTN_KV_INT8;
   if (n_seq == 0) return KVATTN_OK;  // empty batch: nothing to read or write
   // ---- pointer checks ----
@@ -184,6 +197,7 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.num_pages = num_pages;
   dp.n_sub = g / gs;
   for (int u = page_size / kUnitRows; u > 1; u >>= 1) ++dp.unit_shift;
+  dp.stream_cost = int8 ? kStreamCostInt8 : kStreamCostBf16;
   {
     const long long rows = (long long)num_pages * n_kvh * page_size;
     if (!encode_pool_map(&dp.tmap_k, k_pages, rows, head_dim, int8) ||

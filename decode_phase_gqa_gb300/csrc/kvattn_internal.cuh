@@ -21,6 +21,8 @@ constexpr int kDecodeThreads = kDecodeWarps * 32;
 // Work units a share is given at least when the step is small, so tiny
 // batches use few shares and merge few partial states.
 constexpr int kMinUnitsPerShare = 4;
+// Most 16-token units (over all streams) a step's block tables may hold.
+constexpr long long kMaxStepUnits = (1LL << 28) - 1;
 // shared memory a decode CTA may use so that 3 fit on one SM (228 KB, with
 // 1 KB reserved per CTA)
 constexpr int kCtaSmemBudget = 75 * 1024;
@@ -48,6 +50,8 @@ struct DecodeParams {
   int n_sub;           // query-head groups per KV head (G / GS)
   int n_shares;        // the unit list is cut into at most this many shares
   int unit_shift;      // log2(page_size / 16): units per page
+  int stream_cost;     // weight of a stream's fixed costs in the work split
+                       // (quarters of a unit's weight)
   int use_rope;
   float qscale;        // scale * log2(e): scores come out in log2 units
   // turns per position of rotation pair i, rope_theta^(-2i/d) / (2 pi), as an

@@ -54,7 +54,7 @@ extern "C" {
                                  outside what the library is built for (among
                                  them: n_seq * n_kvh * (G / gs) *
                                  max_pages_per_seq * page_size / 16 above
-                                 2^31 - 1, the most 16-token work units a step
+                                 2^28 - 1, the most 16-token work units a step
                                  can hold; G = n_qh / n_kvh, gs = the largest of
                                  4, 2, 1 dividing G) */
 #define KVATTN_ECUDA 3        /* a CUDA runtime call or launch failed */
