@@ -55,6 +55,7 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
   const int b0 = min(B, tid * chunk), b1 = min(B, b0 + chunk);
   int local = 0;
   bool bad = false;
+#pragma unroll 1
   for (int b = b0; b < b1; ++b) {
     const int L = __ldg(p.seq_lens + b);
     if (poss) poss[b] = __ldg(p.positions + b);  // in flight with the length
@@ -77,6 +78,7 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
     if (w < warp) run += scratch[w];
     total += scratch[w];
   }
+#pragma unroll 1
   for (int b = b0; b < b1; ++b) {
     pref[b] = run;
     run += units_of(lens ? lens[b] : __ldg(p.seq_lens + b), cap);
@@ -181,11 +183,19 @@ __device__ __forceinline__ float frac_turns(int pos, float2 g) {
 }
 
 // block-table entry (physical page, not yet range-checked) of flattened unit t
-// (cursor b advanced monotonically)
+// (cursor b advanced monotonically); *jrow = the unit's first pool row within
+// its page's rows: KV head j's slot block, (j page_size + first slot)
 __device__ __forceinline__ int page_raw_of_unit(const DecodeParams &p, const int *pref, int spu,
-                                                int t, int &b) {
+                                                int t, int &b, int *jrow) {
   const UnitPos up = locate_unit(t, b, pref, spu);
+  *jrow = (up.si / p.n_sub) * p.page_size + ((up.u * kUnitRows) & (p.page_size - 1));
   return __ldg(p.block_table + (size_t)up.b * p.max_pages + (up.u >> p.unit_shift));
+}
+
+// L2 prefetch of `bytes` contiguous bytes (16-byte aligned, a multiple of 16)
+// by the bulk-copy engine
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // 16-byte asynchronous global -> shared copy (no register staging)

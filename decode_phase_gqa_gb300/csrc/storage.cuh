@@ -114,11 +114,20 @@ __device__ __forceinline__ bool near_midpoint(FF v) {
   return fabsf(half_gap - fabsf(v.lo)) <= kAngleEps;
 }
 
+// The rare slow path of store_angle below: cos/sin in double, then rounded.
+// Kept out of line, so that the kernels carry one copy of it.
+static __device__ __noinline__ void angle_slow(double phi, float &c, float &s) {
+  double sd, cd;
+  sincos(phi, &sd, &cd);
+  c = (float)cd;
+  s = (float)sd;
+}
+
 // fp32 cos/sin of the double angle pos * inv_freq, as (float)cos / (float)sin
 // of that double would round them.  `table` is a copy of kSinCosStep (in
 // shared memory: a lane-divergent read of global memory would queue behind
 // the SM's tile copies).
-__device__ __forceinline__ void store_angle(int pos, double inv_freq, const float4 *table, float &c,
+static __device__ __noinline__ void store_angle(int pos, double inv_freq, const float4 *table, float &c,
                                             float &s) {
   const double phi = (double)pos * inv_freq;
   // the quadrant from an fp32 estimate of phi (its error and that of the
@@ -179,12 +188,7 @@ __device__ __forceinline__ void store_angle(int pos, double inv_freq, const floa
       slow = true;
     }
   }
-  if (slow) {
-    double sd, cd;
-    sincos(phi, &sd, &cd);
-    c = (float)cd;
-    s = (float)sd;
-  }
+  if (slow) angle_slow(phi, c, s);
 }
 
 // Quantise one warp-held row of d fp32 values: int8 codes (lane's slots, in
