@@ -183,19 +183,11 @@ __device__ __forceinline__ float frac_turns(int pos, float2 g) {
 }
 
 // block-table entry (physical page, not yet range-checked) of flattened unit t
-// (cursor b advanced monotonically); *jrow = the unit's first pool row within
-// its page's rows: KV head j's slot block, (j page_size + first slot)
+// (cursor b advanced monotonically)
 __device__ __forceinline__ int page_raw_of_unit(const DecodeParams &p, const int *pref, int spu,
-                                                int t, int &b, int *jrow) {
+                                                int t, int &b) {
   const UnitPos up = locate_unit(t, b, pref, spu);
-  *jrow = (up.si / p.n_sub) * p.page_size + ((up.u * kUnitRows) & (p.page_size - 1));
   return __ldg(p.block_table + (size_t)up.b * p.max_pages + (up.u >> p.unit_shift));
-}
-
-// L2 prefetch of `bytes` contiguous bytes (16-byte aligned, a multiple of 16)
-// by the bulk-copy engine
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // 16-byte asynchronous global -> shared copy (no register staging)

@@ -77,7 +77,6 @@ struct MmaCfg {
   static constexpr int kPerStage = kStage + kScales + 8 + 4;
   static constexpr int kSWFit = (kCtaSmemBudget - kOther - 1600) / (W * kPerStage);
   static constexpr int kSW = kSWFit > 8 ? 8 : kSWFit;
-  static constexpr int kL2Ahead = 0;  // units between a tile's L2 prefetch and its copy
   static constexpr int kKSteps = D / 16;       // MMA k-steps (QK) and m-tiles (PV)
   static constexpr int kLdm = kRowBytes / 32;  // ldmatrix.x4 per tile (2 chunks each)
   static constexpr int kStagesBytes = W * kSW * kStage;
@@ -471,33 +470,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // (raw block-table entries: the range check waits until a page is used, so
   // that the second window's load does not stall the first requests)
   int pcur = start_b;  // per-lane cursor of the page windows
-  int win_base = 0, win_jr = 0, nxt_jr = 0;
-  int win_page = lane < count ? page_raw_of_unit(p, pref, spu, wt0 + lane, pcur, &win_jr) : -1;
-  int nxt_page = 32 + lane < count ? page_raw_of_unit(p, pref, spu, wt0 + 32 + lane, pcur, &nxt_jr) : -1;
+  int win_base = 0;
+  int win_page = lane < count ? page_raw_of_unit(p, pref, spu, wt0 + lane, pcur) : -1;
+  int nxt_page = 32 + lane < count ? page_raw_of_unit(p, pref, spu, wt0 + 32 + lane, pcur) : -1;
   auto issue = [&](int i) {  // called by the whole warp, in unit order
     if (i > 0) advance();
     if (i - win_base >= 32) {
       win_base += 32;
       win_page = nxt_page;
-      win_jr = nxt_jr;
       const int tn = win_base + 32 + lane;
-      nxt_page = tn < count ? page_raw_of_unit(p, pref, spu, wt0 + tn, pcur, &nxt_jr) : -1;
-    }
-    if constexpr (C::kL2Ahead > 0) {
-      // pull unit i + kL2Ahead into L2 now, so that its tile copies, issued
-      // kL2Ahead units later, wait for L2 instead of DRAM: more bytes in flight
-      // per SM than its stage ring holds
-      const int k = i + C::kL2Ahead, kl = k - win_base;  // kl < 64
-      const int pg_w = __shfl_sync(0xffffffffu, win_page, kl & 31);
-      const int pg_n = __shfl_sync(0xffffffffu, nxt_page, kl & 31);
-      const int jr_w = __shfl_sync(0xffffffffu, win_jr, kl & 31);
-      const int jr_n = __shfl_sync(0xffffffffu, nxt_jr, kl & 31);
-      const int pg = kl < 32 ? pg_w : pg_n, jr = kl < 32 ? jr_w : jr_n;
-      if (lane == 0 && k < count && pg >= 0 && pg < p.num_pages) {
-        const size_t off = ((size_t)pg * p.n_kvh * p.page_size + jr) * C::kRowBytes;
-        bulk_prefetch_l2(static_cast<const uint8_t *>(p.k_pages) + off, C::kTile);
-        bulk_prefetch_l2(static_cast<const uint8_t *>(p.v_pages) + off, C::kTile);
-      }
+      nxt_page = tn < count ? page_raw_of_unit(p, pref, spu, wt0 + tn, pcur) : -1;
     }
     int page = __shfl_sync(0xffffffffu, win_page, i - win_base);
     page = (page >= 0 && page < p.num_pages) ? page : -1;
