@@ -237,3 +237,52 @@ def test_appended_keys_over_many_positions(kv, d, theta):
     wl.positions = pos
     h["positions"] = pos.copy()
     check_against_oracle(wl, h)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_back_to_back_steps_see_the_previous_append(kv):
+    # two decode steps queued on one stream with no other kernel between them:
+    # the second step attends over the token the first one appended (lengths
+    # at and across unit and page boundaries)
+    lens = [14, 15, 16, 31, 100, 255, 0, 47]
+    wl, h1 = custom(8, 2, lens, d=128, kv=kv, seed=21, spare=0.5, max_len=300)
+    bt = h1["block_table"]
+    used = set(int(x) for x in bt.ravel() if x >= 0)
+    free = [p for p in range(wl.num_pages) if p not in used]
+    for b, L in enumerate(lens):  # the second step's slot L + 1 may start a new page
+        n = L // wl.page_size + 1
+        if (L + 1) // wl.page_size + 1 > n:
+            bt[b, n] = free.pop()
+    rng = np.random.default_rng(5)
+    h2 = dict(h1)
+    for k in ("q", "k_new", "v_new"):
+        h2[k] = R.f32_to_bf16_bits(rng.standard_normal(h1[k].shape))
+    h2["seq_lens"] = h1["seq_lens"] + 1
+    h2["positions"] = h1["positions"] + 1
+
+    d1 = to_dev(h1)
+    d2 = dict(d1)
+    for k in ("q", "k_new", "v_new", "seq_lens", "positions"):
+        d2[k] = to_dev(h2)[k]
+    ws = K.alloc_workspace(len(lens), 8, 2, 128)
+    outs = []
+    for d in (d1, d2):
+        out = torch.full((len(lens), 8, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        K.kvattn_decode(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
+                        d["block_table"], d["seq_lens"], d["positions"], out,
+                        rope_theta=wl.rope_theta, scale=wl.scale, workspace=ws,
+                        k_scales=d["k_scales"], v_scales=d["v_scales"])
+        outs.append(out)
+    assert K.kvattn_read_device_status(ws) == 0
+
+    ref1, st1, kp, vp, ks, vs = oracle_decode(wl, h1)
+    h2.update(k_pages=kp, v_pages=vp, k_scales=ks, v_scales=vs)
+    ref2, st2, kp, vp, ks, vs = oracle_decode(wl, h2)
+    assert st1 == st2 == 0
+    assert np.array_equal(pool_bits(d1["k_pages"]), kp)
+    assert np.array_equal(pool_bits(d1["v_pages"]), vp)
+    if ks is not None:
+        assert np.array_equal(d1["k_scales"].cpu().numpy().view(np.uint32), ks.view(np.uint32))
+        assert np.array_equal(d1["v_scales"].cpu().numpy().view(np.uint32), vs.view(np.uint32))
+    assert_close(out_f64(outs[0]), ref1)
+    assert_close(out_f64(outs[1]), ref2)
