@@ -294,36 +294,66 @@ def time_steps(case: NativeCase, steps: int, warmup: int, world: int, stream):
 
 def time_e2e(case: NativeCase, steps: int, warmup: int, world: int, stream):
     """Same step through the public API with the step's inputs in pinned host
-    memory: H2D of q/k_new/v_new/block table/lengths/positions, the decode
-    call(s), D2H of the output, every step, inside the timed region."""
-    host = []
-    for c in case.caches[:case.calls_per_step if case.calls_per_step > 1 else 2]:
-        host.append({k: c[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")})
-    bt_h = case.bt.cpu().pin_memory()
-    sl_h = case.sl.cpu().pin_memory()
-    pos_h = case.pos.cpu().pin_memory()
-    out_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
-    dev = {k: torch.empty_like(case.caches[0][k]) for k in ("q", "k_new", "v_new")}
-    bt_d, sl_d, pos_d = torch.empty_like(case.bt), torch.empty_like(case.sl), torch.empty_like(case.pos)
-    h2d = sum(t.numel() * t.element_size() for t in host[0].values()) * case.calls_per_step
-    h2d += (bt_h.numel() + sl_h.numel() + pos_h.numel()) * 4
-    d2h = out_h.numel() * out_h.element_size() * case.calls_per_step
+    memory: the step's q/k_new/v_new (every call's) and block table, lengths
+    and positions are laid out in one pinned staging buffer and copied to the
+    device in one transfer, the decode call(s) run on views of the device copy,
+    and the outputs of all calls are read back in one transfer, every step,
+    inside the timed region."""
+    n_calls = case.calls_per_step
+    n_sets = 1 if n_calls > 1 else 2  # packed input sets alternated over steps
+
+    def layout():
+        segs, off = [], 0
+        for n in range(n_calls):
+            for k in ("q", "k_new", "v_new"):
+                t = case.caches[0][k]
+                segs.append((("in", n, k), off, t.shape, t.dtype))
+                off += -(-t.numel() * t.element_size() // 256) * 256
+        for name, t in (("bt", case.bt), ("sl", case.sl), ("pos", case.pos)):
+            segs.append(((name,), off, t.shape, t.dtype))
+            off += -(-t.numel() * t.element_size() // 256) * 256
+        return segs, off
+
+    segs, total = layout()
+
+    def views(buf):
+        out = {}
+        for key, off, shape, dtype in segs:
+            nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            out[key] = buf[off:off + nbytes].view(dtype).view(shape)
+        return out
+
+    host_packs = []
+    for s in range(n_sets):
+        hp = torch.empty(total, dtype=torch.uint8).pin_memory()
+        v = views(hp)
+        for n in range(n_calls):
+            src = case.caches[(s * n_calls + n) % len(case.caches)]
+            for k in ("q", "k_new", "v_new"):
+                v[("in", n, k)].copy_(src[k].cpu())
+        v[("bt",)].copy_(case.bt.cpu())
+        v[("sl",)].copy_(case.sl.cpu())
+        v[("pos",)].copy_(case.pos.cpu())
+        host_packs.append(hp)
+    dev_pack = torch.empty(total, dtype=torch.uint8, device=case.out.device)
+    dv = views(dev_pack)
+    out_d = torch.empty((n_calls,) + tuple(case.out.shape), dtype=case.out.dtype, device=case.out.device)
+    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+    h2d = sum(int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+              for _, _, shape, dtype in segs)
+    d2h = out_h.numel() * out_h.element_size()
 
     def one_step(s):
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        pos_d.copy_(pos_h, non_blocking=True)
+        dev_pack.copy_(host_packs[s % n_sets], non_blocking=True)
         idxs = case.step_groups()[s % len(case.step_groups())]
         for n, i in enumerate(idxs):
-            hsrc = host[n % len(host)] if case.calls_per_step > 1 else host[s % len(host)]
-            for k in dev:
-                dev[k].copy_(hsrc[k], non_blocking=True)
             c = case.caches[i]
-            case.K.kvattn_decode(dev["q"], dev["k_new"], dev["v_new"], c["k_pages"], c["v_pages"],
-                                 bt_d, sl_d, pos_d, case.out, rope_theta=case.wl.rope_theta,
-                                 scale=case.wl.scale, workspace=case.ws,
-                                 k_scales=c["k_scales"], v_scales=c["v_scales"], stream=stream)
-            out_h.copy_(case.out, non_blocking=True)
+            case.K.kvattn_decode(dv[("in", n, "q")], dv[("in", n, "k_new")], dv[("in", n, "v_new")],
+                                 c["k_pages"], c["v_pages"], dv[("bt",)], dv[("sl",)], dv[("pos",)],
+                                 out_d[n], rope_theta=case.wl.rope_theta, scale=case.wl.scale,
+                                 workspace=case.ws, k_scales=c["k_scales"], v_scales=c["v_scales"],
+                                 stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for s in range(warmup):

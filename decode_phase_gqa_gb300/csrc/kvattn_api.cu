@@ -11,6 +11,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "kvattn_internal.cuh"
@@ -86,6 +87,81 @@ bool encode_pool_map(CUtensorMap *map, const void *base, long long rows, int hea
              CU_TENSOR_MAP_INTERLEAVE_NONE,
              box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Small caches of per-call host work that only depends on a few arguments:
+// the RoPE frequency tables (64 pow calls) per (rope_theta, head_dim) and the
+// pools' tensor maps per (base, rows, head_dim, element type).  A call takes
+// its entries by copy under the lock; misses replace entries round robin.
+struct FreqEntry {
+  uint32_t theta_bits;
+  int head_dim;
+  double inv_freq[64];
+  float2 turns[64];
+};
+struct MapEntry {
+  const void *base;
+  long long rows;
+  int head_dim;
+  bool int8;
+  CUtensorMap map;
+};
+std::mutex g_cache_mu;
+FreqEntry g_freq[8];
+int g_freq_n = 0, g_freq_next = 0;
+MapEntry g_maps[16];
+int g_maps_n = 0, g_maps_next = 0;
+
+// frequency of rotation pair i: rope_theta^(-2i/d) in double, and the same in
+// turns (/ 2 pi) as an fp32 head and remainder; zero without RoPE
+void freq_tables(float rope_theta, int head_dim, double *inv_freq, float2 *turns) {
+  uint32_t bits;
+  std::memcpy(&bits, &rope_theta, 4);
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  for (int e = 0; e < g_freq_n; ++e)
+    if (g_freq[e].theta_bits == bits && g_freq[e].head_dim == head_dim) {
+      std::memcpy(inv_freq, g_freq[e].inv_freq, sizeof(g_freq[e].inv_freq));
+      std::memcpy(turns, g_freq[e].turns, sizeof(g_freq[e].turns));
+      return;
+    }
+  FreqEntry &f = g_freq[g_freq_next];
+  g_freq_next = (g_freq_next + 1) % 8;
+  if (g_freq_n < 8) ++g_freq_n;
+  f.theta_bits = bits;
+  f.head_dim = head_dim;
+  const bool use_rope = rope_theta > 0.0f;
+  for (int i = 0; i < 64; ++i)
+    f.inv_freq[i] = (use_rope && i < head_dim / 2) ? std::pow((double)rope_theta, -(2.0 * i) / head_dim) : 0.0;
+  for (int i = 0; i < 64; ++i) {
+    const double g = f.inv_freq[i] * 0.15915494309189535;  // / (2 pi)
+    const float hi = (float)g;
+    f.turns[i] = make_float2(hi, (float)(g - (double)hi));
+  }
+  std::memcpy(inv_freq, f.inv_freq, sizeof(f.inv_freq));
+  std::memcpy(turns, f.turns, sizeof(f.turns));
+}
+
+bool cached_pool_map(CUtensorMap *map, const void *base, long long rows, int head_dim, bool int8) {
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    for (int e = 0; e < g_maps_n; ++e)
+      if (g_maps[e].base == base && g_maps[e].rows == rows && g_maps[e].head_dim == head_dim &&
+          g_maps[e].int8 == int8) {
+        *map = g_maps[e].map;
+        return true;
+      }
+  }
+  if (!encode_pool_map(map, base, rows, head_dim, int8)) return false;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  MapEntry &m = g_maps[g_maps_next];
+  g_maps_next = (g_maps_next + 1) % 16;
+  if (g_maps_n < 16) ++g_maps_n;
+  m.base = base;
+  m.rows = rows;
+  m.head_dim = head_dim;
+  m.int8 = int8;
+  m.map = *map;
+  return true;
 }
 
 cudaError_t decode_launcher(const DecodeParams &p, int head_dim, int gs, bool int8, int grid,
@@ -181,14 +257,7 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.use_rope = use_rope ? 1 : 0;
   // scores are formed in log2 units: fold scale * log2(e) into the query
   dp.qscale = (float)((double)scale * 1.4426950408889634);
-  // frequency of rotation pair i: rope_theta^(-2i/d), in double
-  for (int i = 0; i < head_dim / 2; ++i)
-    dp.inv_freq[i] = use_rope ? std::pow((double)rope_theta, -(2.0 * i) / head_dim) : 0.0;
-  for (int i = 0; i < 64; ++i) {
-    const double g = dp.inv_freq[i] * 0.15915494309189535;  // / (2 pi)
-    const float hi = (float)g;
-    dp.turns[i] = make_float2(hi, (float)(g - (double)hi));
-  }
+  freq_tables(rope_theta, head_dim, dp.inv_freq, dp.turns);
   dp.n_seq = n_seq;
   dp.n_qh = n_qh;
   dp.n_kvh = n_kvh;
@@ -200,8 +269,8 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.stream_cost = int8 ? kStreamCostInt8 : kStreamCostBf16;
   {
     const long long rows = (long long)num_pages * n_kvh * page_size;
-    if (!encode_pool_map(&dp.tmap_k, k_pages, rows, head_dim, int8) ||
-        !encode_pool_map(&dp.tmap_v, v_pages, rows, head_dim, int8))
+    if (!cached_pool_map(&dp.tmap_k, k_pages, rows, head_dim, int8) ||
+        !cached_pool_map(&dp.tmap_v, v_pages, rows, head_dim, int8))
       return KVATTN_ECUDA;
   }
   // the first call for a configuration on a device sets the kernel's shared
