@@ -106,38 +106,50 @@ struct WeightedSplit {
   // weighted position of sequence b's first stream
   __device__ __forceinline__ int seq_pos(int b) const { return 4 * spu * pref[b] + sc * spu * b; }
   // First unit whose weighted position is >= y (T when there is none) and its
-  // sequence *b (the sequence of the unit; B - 1 when there is none).  Called
-  // by a whole warp with the same y: the last sequence starting at or before
-  // y is found by a 32-way search (one shared-memory read per lane and level,
-  // two levels up to 1024 sequences).
-  __device__ __forceinline__ int first_unit(int y, int lane, int *b) const {
+  // sequence *b (the sequence of the unit; B - 1 when there is none), found by
+  // one lane: a binary search for the last sequence starting at or before y,
+  // the stream and unit inside it, and a second binary search that moves past
+  // sequences without units (the unit then belongs to the next sequence that
+  // has some).
+  __device__ __forceinline__ int first_unit(int y, int *b) const {
     if (y >= split.T) {
       *b = B - 1;
       return T;
     }
-    int lo = 0, n = B;  // seq_pos(lo) <= y; the answer lies in [lo, lo + n)
-    while (n > 1) {
-      const int step = (n + 31) >> 5;
-      const int c = lo + lane * step;
-      const unsigned m = __ballot_sync(0xffffffffu, c < lo + n && seq_pos(c) <= y);
-      const int k = 31 - __clz(m);  // lane 0 always qualifies
-      const int nlo = lo + k * step;
-      n = min(step, lo + n - nlo);
-      lo = nlo;
+    int lo = 0, hi = B;  // seq_pos(lo) <= y; every sequence from hi on starts after y
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (seq_pos(mid) <= y)
+        lo = mid;
+      else
+        hi = mid;
     }
     const int u = pref[lo + 1] - pref[lo];
     const int ws = 4 * u + sc;  // > 0: y lies inside sequence lo's streams
     const int off = y - seq_pos(lo);
     const int si = off / ws, rem = off - si * ws;
     const int t = spu * pref[lo] + si * u + min(u, (rem + 3) >> 2);
-    // past the sequence's last unit: the next sequence with units holds t
-    int bb = lo;
-    while (bb + 1 < B && spu * pref[bb + 1] <= t) ++bb;
-    *b = bb;
+    int bl = lo, bh = B;  // the last sequence whose first unit is at or before t
+    while (bh - bl > 1) {
+      const int mid = (bl + bh) >> 1;
+      if (spu * pref[mid] <= t)
+        bl = mid;
+      else
+        bh = mid;
+    }
+    *b = bl;
     return t;
   }
-  __device__ __forceinline__ int begin_unit(int c, int lane, int *b) const {
-    return first_unit(split.begin(c), lane, b);
+  // Unit range [*t0, *t1) of share c and the sequences of its ends, for the
+  // whole warp: even lanes search the start, odd lanes the end, at once.
+  __device__ __forceinline__ void share_bounds(int c, int lane, int *t0, int *b0, int *t1,
+                                               int *b1) const {
+    int b = 0;
+    const int t = first_unit(split.begin(c + (lane & 1)), &b);
+    *t0 = __shfl_sync(0xffffffffu, t, 0);
+    *b0 = __shfl_sync(0xffffffffu, b, 0);
+    *t1 = __shfl_sync(0xffffffffu, t, 1);
+    *b1 = __shfl_sync(0xffffffffu, b, 1);
   }
   // share holding unit t of stream sid
   __device__ __forceinline__ int owner(int t, int sid) const { return split.owner(4 * t + sc * sid); }

@@ -327,11 +327,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     prefetch_tensormap(&p.tmap_k);
     prefetch_tensormap(&p.tmap_v);
   }
-  pdl_wait_primary();       // every earlier kernel of the stream is complete and visible
-  pdl_launch_dependents();  // the combine grid may start planning at once
   {
-    // every CTA pulls its slice of the queries into L2 at once, so that the
-    // warps' query rows do not queue behind the flood of K/V requests
+    // L2 prefetches of the step's small inputs, issued before the wait on the
+    // previous kernel so that their address translations and DRAM reads
+    // overlap its end.  A prefetch consumes nothing: L2 is the GPU's point of
+    // coherence, so a line the previous kernel writes afterwards is updated
+    // there, and every read of these inputs comes after the wait.
+    // The lengths and positions, which every CTA reads first:
+    const int n_len_lines = (p.n_seq * 4 + 127) / 128;
+    for (int l = tid; l < n_len_lines; l += kDecodeThreads) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(p.seq_lens) + l * 128));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(p.positions) + l * 128));
+    }
+    // every CTA pulls its slice of the queries into L2, so that the warps'
+    // query rows do not queue behind the flood of K/V requests
     const size_t q_lines = ((size_t)p.n_seq * p.n_qh * D * 2 + 127) / 128;
     const size_t per = (q_lines + gridDim.x - 1) / gridDim.x;
     const char *qc = reinterpret_cast<const char *>(p.q);
@@ -360,6 +369,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(bc + l * 128));
     }
   }
+  pdl_wait_primary();       // every earlier kernel of the stream is complete and visible
+  pdl_launch_dependents();  // the combine grid may start planning at once
   // prefix sums of units per sequence, lengths and positions (its barriers
   // also publish the set-up above); shares are per warp here
   int T = 0;
@@ -381,8 +392,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int a = warp - A;
     const int ga = a * (int)gridDim.x + (int)blockIdx.x;
     if (spread && a >= 0 && a < A && ga < nwa) {
-      int b = 0, b1 = 0;
-      const int wa0 = split.begin_unit(ga, lane, &b), wa1 = split.begin_unit(ga + 1, lane, &b1);
+      int b = 0, b1 = 0, wa0 = 0, wa1 = 0;
+      split.share_bounds(ga, lane, &wa0, &b, &wa1, &b1);
       if (wa0 >= wa1) b = 0;
       const UnitPos up = locate_unit(wa0 < wa1 ? wa0 : 0, b, pref, spu);
       if (wa0 < wa1 && up.first + up.units <= wa1) {  // warp a appends its first stream's new token
@@ -400,8 +411,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     return;
   }
-  int start_b = 0, end_b = 0;
-  const int wt0 = split.begin_unit(g, lane, &start_b), wt1 = split.begin_unit(g + 1, lane, &end_b);
+  int start_b = 0, end_b = 0, wt0 = 0, wt1 = 0;
+  split.share_bounds(g, lane, &wt0, &start_b, &wt1, &end_b);
   const int count = wt1 - wt0;
   if (count == 0) return;  // a share of stream costs only
   const uint64_t pol = l2_evict_first_policy();
