@@ -11,7 +11,8 @@
 // Two CTAs per SM at most; CTA c takes items c, c + gridDim.x, ... and lists
 // the merges to do while the decode grid still runs, so that only the record
 // loads remain after the wait.  A thread merges the records of one float4
-// column online (running maximum, normaliser and sum, eight loads in flight);
+// column eight at a time (their largest maximum first, then the eight weights
+// at once, so no exponential waits on another);
 // a stream cut into many shares gives each column several record lanes,
 // merged in shared memory, and spreads its columns over several CTAs.
 // The kernel is launched as a programmatic dependent of the decode kernel and
@@ -31,20 +32,34 @@ struct ColState {
   float4 o;
 };
 
-__device__ __forceinline__ void absorb(ColState &st, float m, float l, float4 a) {
-  if (m == -INFINITY) return;
-  const float mn = fmaxf(st.m, m);
-  const float so = (st.m == -INFINITY) ? 0.f : exp2f(st.m - mn);
-  const float sa = exp2f(m - mn);
-  st.l = st.l * so + l * sa;
-  st.o.x = st.o.x * so + a.x * sa;
-  st.o.y = st.o.y * so + a.y * sa;
-  st.o.z = st.o.z * so + a.z * sa;
-  st.o.w = st.o.w * so + a.w * sa;
-  st.m = mn;
+// Fold U states (m, l, a) into st at once: the batch's largest maximum first,
+// then each weight 2^(m_u - M) on its own, so the exponentials do not wait on
+// one another.  Empty slots carry m = -inf (weight 0, l = 0, a = 0).
+template <int U>
+__device__ __forceinline__ void absorb_batch(ColState &st, const float (&m)[U], const float (&l)[U],
+                                             const float4 (&a)[U]) {
+  float mb = st.m;
+#pragma unroll
+  for (int u = 0; u < U; ++u) mb = fmaxf(mb, m[u]);
+  if (mb == -INFINITY) return;  // nothing but empty slots so far
+  const float so = ex2_approx(st.m - mb);
+  float ls = st.l * so;
+  float4 o = make_float4(st.o.x * so, st.o.y * so, st.o.z * so, st.o.w * so);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const float w = ex2_approx(m[u] - mb);
+    ls = fmaf(l[u], w, ls);
+    o.x = fmaf(a[u].x, w, o.x);
+    o.y = fmaf(a[u].y, w, o.y);
+    o.z = fmaf(a[u].z, w, o.z);
+    o.w = fmaf(a[u].w, w, o.w);
+  }
+  st.m = mb;
+  st.l = ls;
+  st.o = o;
 }
 
-// Online merge, by one thread, of column c of records r0 + r * RS for
+// Merge, by one thread, of column c of records r0 + r * RS for
 // r = first, first + step, ... < nseg, eight loads in flight at a time.
 template <int D, int GS>
 __device__ __forceinline__ ColState merge_column(const float *r0, int first, int step, int nseg,
@@ -70,9 +85,7 @@ __device__ __forceinline__ ColState merge_column(const float *r0, int first, int
         a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (s0 + u * step < nseg) absorb(st, mm[u], ll[u], a[u]);
+    absorb_batch<U>(st, mm, ll, a);
   }
   return st;
 }
@@ -93,10 +106,10 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   constexpr int kGroups = kCombineThreads / NC;  // concurrent short merges per CTA
   // A stream of at most kShort shares is merged by a group of NC threads,
   // one column each, kGroups at a time and without CTA barriers.  A longer
-  // one takes R record lanes per column, R = its shares / 8 rounded up to a
-  // power of two, so that one round of eight loads per thread covers its
-  // records; its columns are then split into nch = NC R / (CTA threads)
-  // items (each of at least kMinCols columns) that different CTAs merge.
+  // one takes R record lanes per column, R = its shares / 4 rounded up to a
+  // power of two, so that a thread merges at most four of its records; its
+  // columns are then split into nch = NC R / (CTA threads) items (each of at
+  // least kMinCols columns, which caps R at 16) that different CTAs merge.
   constexpr int kShort = 8;
   constexpr int kMinCols = 16 < NC ? 16 : NC;
   constexpr int kMaxChunks = NC / kMinCols;
@@ -139,7 +152,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
         const int w0 = split.owner(F, sid);
         const int nseg = split.owner(F + units - 1, sid) - w0 + 1;
         int R = 1;
-        while (R * 8 < nseg) R *= 2;
+        while (R * 4 < nseg) R *= 2;
         const int nch = nseg <= kShort ? 1 : max(1, min(kMaxChunks, NC * R / kCombineThreads));
         if (nseg > 1 && q < nch) {
           const int k = atomicAdd(&n_list, 1);
@@ -182,9 +195,18 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
       part[tid] = st;
       __syncthreads();
       if (rl == 0) {
-        for (int r = 1; r < R; ++r) {
-          const ColState o = part[r * ncq + cc];
-          absorb(st, o.m, o.l, o.o);
+        for (int r0 = 1; r0 < R; r0 += 8) {  // the other record lanes' states, eight at a time
+          float mm[8], ll[8];
+          float4 a[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const bool in = r0 + k < R;
+            const ColState o = part[(in ? r0 + k : 0) * ncq + cc];
+            mm[k] = in ? o.m : -INFINITY;
+            ll[k] = in ? o.l : 0.f;
+            a[k] = in ? o.o : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          absorb_batch<8>(st, mm, ll, a);
         }
         store_column(p.out + ((size_t)b * p.n_qh + h0) * D + c * 4, st);
       }

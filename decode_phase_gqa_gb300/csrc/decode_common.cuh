@@ -28,6 +28,19 @@ struct Split {
   }
 };
 
+// 2^x and log2(x) from the special-function unit's approximations (relative
+// error near 2^-22; subnormal arguments and results flush to zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // a[i] for a lane-dependent i without dynamic register indexing
 template <int N>
 __device__ __forceinline__ float pick(const float (&a)[N], int i) {
