@@ -106,10 +106,12 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   constexpr int kGroups = kCombineThreads / NC;  // concurrent short merges per CTA
   // A stream of at most kShort shares is merged by a group of NC threads,
   // one column each, kGroups at a time and without CTA barriers.  A longer
-  // one takes R record lanes per column, R = its shares / 4 rounded up to a
-  // power of two, so that a thread merges at most four of its records; its
-  // columns are then split into nch = NC R / (CTA threads) items (each of at
-  // least kMinCols columns, which caps R at 16) that different CTAs merge.
+  // one takes R record lanes per column, R = its shares / 8 rounded up to a
+  // power of two, so that one batch of eight records per thread covers them;
+  // its columns are then split into nch = NC R / (CTA threads) items (each of
+  // at least kMinCols columns, which caps R at 16) that different CTAs merge.
+  // (Four records a lane, twice the items, was slower on the Qwen3-shaped
+  // batch: a CTA merges its long items one after another.)
   constexpr int kShort = 8;
   constexpr int kMinCols = 16 < NC ? 16 : NC;
   constexpr int kMaxChunks = NC / kMinCols;
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   // per share.
   int T = 0;
   const bool any = plan_units<kCombineThreads>(p, pref, scratch, T);
-  const int nwa = any ? min(n_warps, max(1, (T + kMinUnitsPerShare - 1) / kMinUnitsPerShare)) : 1;
+  const int nwa = any ? warp_shares(4 * T + p.stream_cost * p.n_seq * spu, n_warps) : 1;
   const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, any ? T : 1, nwa);
   const int n_streams = p.n_seq * spu;
   // item it: chunk it / n_streams of stream it % n_streams; CTA c takes
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
         const int w0 = split.owner(F, sid);
         const int nseg = split.owner(F + units - 1, sid) - w0 + 1;
         int R = 1;
-        while (R * 4 < nseg) R *= 2;
+        while (R * 8 < nseg) R *= 2;
         const int nch = nseg <= kShort ? 1 : max(1, min(kMaxChunks, NC * R / kCombineThreads));
         if (nseg > 1 && q < nch) {
           const int k = atomicAdd(&n_list, 1);

@@ -168,6 +168,20 @@ struct WeightedSplit {
   __device__ __forceinline__ int owner(int t, int sid) const { return split.owner(4 * t + sc * sid); }
 };
 
+// Number of warp shares a step's weighted unit list (X = 4 per unit plus the
+// stream costs) is cut into, for a grid of n_warps warps.  A share's time is
+// set by the units it streams one after another, so a small step takes
+// shares of at most 3 units (X / 12 of them) when that keeps at least half of
+// the warps free (they help the appending warps; the shares are spread over
+// the CTAs), else of at most 4 units (X / 16), a unit weighing 4: more shares
+// than that would only add partial states to merge.  The decode and combine
+// kernels both call this.
+__device__ __forceinline__ int warp_shares(int X, int n_warps) {
+  const int n3 = X / 12 + (X % 12 != 0), n4 = X / 16 + (X % 16 != 0);  // (X may be near 2^31)
+  if (2 * n3 <= n_warps) return max(1, n3);
+  return max(1, min(n_warps, n4));
+}
+
 // Position of flattened unit t: sequence (cursor b, advanced monotonically),
 // stream within the sequence and unit within the stream.
 struct UnitPos {

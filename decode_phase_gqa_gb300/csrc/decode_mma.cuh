@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   int T = 0;
   if (!plan_units<kDecodeThreads>(p, pref, misc, T, lens, poss, blockIdx.x == 0)) return;
   const int n_warps = min((int)gridDim.x * W, p.n_shares);
-  const int nwa = min(n_warps, max(1, (T + kMinUnitsPerShare - 1) / kMinUnitsPerShare));
+  const int nwa = warp_shares(4 * T + p.stream_cost * p.n_seq * spu, n_warps);
   const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, T, nwa);
   // A small batch leaves at least half of the warps idle: then the shares
   // are spread over the CTAs (warp slots 0..A-1 of every CTA; A <= W/2) and

@@ -18,9 +18,6 @@ namespace kvattn {
 constexpr int kUnitRows = 16;
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeThreads = kDecodeWarps * 32;
-// Work units a share is given at least when the step is small, so tiny
-// batches use few shares and merge few partial states.
-constexpr int kMinUnitsPerShare = 4;
 // Most 16-token units (over all streams) a step's block tables may hold.
 constexpr long long kMaxStepUnits = (1LL << 28) - 1;
 // shared memory a decode CTA may use so that 3 fit on one SM (228 KB, with
