@@ -191,7 +191,7 @@ class NativeCase:
     36 layer caches of the Qwen config), one workspace, one output buffer."""
 
     def __init__(self, name: str, seed: int, device, min_bytes: int = 4 * L2_BYTES,
-                 layers=None):
+                 layers=None, layered=False):
         from decode_phase_gqa_gb300 import kvattn as K
         self.K = K
         self.wl = W.make_workload(name, seed=seed)
@@ -199,7 +199,10 @@ class NativeCase:
         if layers is not None:   # fewer layer caches per step (profiling runs only)
             wl.layers = max(1, min(wl.layers, layers))
         self.device = device
-        self.calls_per_step = wl.layers
+        # a step of a multi-layer config: one kvattn_decode call per layer cache,
+        # or (layered) one kvattn_decode_layers call over all of them
+        self.layered = bool(layered) and wl.layers > 1
+        self.calls_per_step = 1 if self.layered else wl.layers
         per_cache = wl.kv_bytes
         if wl.layers > 1:
             self.copies = wl.layers           # a step reads every layer cache once
@@ -207,17 +210,45 @@ class NativeCase:
             # enough independent caches that a rotation reads min_bytes of KV;
             # capped for latency-bound toy shapes (their KV sits in L2 anyway)
             self.copies = min(64, max(2, math.ceil(min_bytes / max(per_cache, 1))))
-        self.l2_resident = self.copies * per_cache * self.calls_per_step < 2 * L2_BYTES
-        self.caches = [W.make_tensors(wl, layer=i, device=device) for i in range(self.copies)]
+        self.l2_resident = self.copies * per_cache * wl.layers < 2 * L2_BYTES
+        if wl.layers > 1:
+            # layer caches in layer-major arrays (what kvattn_decode_layers
+            # takes); the per-layer calls use views of them
+            self.stacked = {}
+            for i in range(self.copies):
+                t = W.make_tensors(wl, layer=i, device=device)
+                for k, v in t.items():
+                    if v is None:
+                        self.stacked[k] = None
+                        continue
+                    if k not in self.stacked:
+                        self.stacked[k] = torch.empty((self.copies,) + tuple(v.shape),
+                                                      dtype=v.dtype, device=device)
+                    self.stacked[k][i].copy_(v)
+                del t
+            self.caches = [{k: (None if v is None else v[i]) for k, v in self.stacked.items()}
+                           for i in range(self.copies)]
+        else:
+            self.caches = [W.make_tensors(wl, layer=i, device=device) for i in range(self.copies)]
         self.bt = torch.from_numpy(wl.block_table).to(device)
         self.sl = torch.from_numpy(wl.seq_lens).to(device)
         self.pos = torch.from_numpy(wl.positions).to(device)
-        self.out = torch.empty((wl.n_seq, wl.n_qh, wl.head_dim), dtype=torch.bfloat16,
+        lead = (wl.layers,) if self.layered else ()
+        self.out = torch.empty(lead + (wl.n_seq, wl.n_qh, wl.head_dim), dtype=torch.bfloat16,
                                device=device)
-        self.ws = K.alloc_workspace(wl.n_seq, wl.n_qh, wl.n_kvh, wl.head_dim, device=device)
+        self.ws = K.alloc_workspace(wl.n_seq, wl.n_qh, wl.n_kvh, wl.head_dim, device=device,
+                                    n_layers=wl.layers if self.layered else 1)
         self.graphs = []
 
     def call(self, i, stream=None, out=None):
+        if self.layered:
+            c = self.stacked
+            self.K.kvattn_decode_layers(
+                c["q"], c["k_new"], c["v_new"], c["k_pages"], c["v_pages"], self.bt, self.sl,
+                self.pos, self.out if out is None else out, rope_theta=self.wl.rope_theta,
+                scale=self.wl.scale, workspace=self.ws, k_scales=c["k_scales"],
+                v_scales=c["v_scales"], stream=stream)
+            return
         c = self.caches[i]
         self.K.kvattn_decode(c["q"], c["k_new"], c["v_new"], c["k_pages"], c["v_pages"],
                              self.bt, self.sl, self.pos, self.out if out is None else out,
@@ -227,6 +258,8 @@ class NativeCase:
 
     def step_groups(self):
         """Cache indices of each distinct step (a step = calls_per_step calls)."""
+        if self.layered:
+            return [[0]]
         if self.calls_per_step > 1:
             return [list(range(self.copies))]
         return [[i] for i in range(self.copies)]
@@ -411,8 +444,9 @@ def cpu_baseline(name: str, seed: int, budget_s: float = 10.0):
                       f"{wl.layers} layer(s) costs {wl.layers}x one layer"}
 
 
-def run_config(name, steps, warmup, rank, world, device, stream, with_e2e=True, layers=None):
-    case = NativeCase(name, seed=1000 * rank, device=device, layers=layers)
+def run_config(name, steps, warmup, rank, world, device, stream, with_e2e=True, layers=None,
+               layered=False):
+    case = NativeCase(name, seed=1000 * rank, device=device, layers=layers, layered=layered)
     case.capture(stream)
     st = case.check_status()
     if st:
@@ -496,20 +530,26 @@ def native(args, rank, world, local):
     if not args.no_extra_configs:
         extra = []
         for name in W.CONFIG_ORDER:
-            if name == args.config:
-                continue
             wl2 = W.make_workload(name)
-            call_ms_guess = max(wl2.kv_bytes * wl2.layers / (0.7 * peak * 1e9) * 1e3, 0.01)
-            k = max(10, min(2000, int(300.0 / call_ms_guess)))
-            r = run_config(name, k, max(3, k // 10), rank, world, device, stream, with_e2e=False)
-            extra.append({"config": name, "workload": workload_desc(r["case"].wl),
-                          "steps": k, "ms_per_step": r["ms_per_step"],
-                          "l2_resident": r["case"].l2_resident,
-                          "tokens_per_s": r["tokens_per_s"], "kv_read_gbs": r["kv_gbs"],
-                          "kv_read_frac_of_peak": r["kv_gbs"] / world / peak,
-                          "calls_per_step": r["calls_per_step"]})
-            del r
-            torch.cuda.empty_cache()
+            # a multi-layer step is timed both ways: a graph of one call per
+            # layer cache, and one kvattn_decode_layers call over all of them
+            for layered in ([False, True] if wl2.layers > 1 else [False]):
+                if name == args.config and not layered:
+                    continue
+                call_ms_guess = max(wl2.kv_bytes * wl2.layers / (0.7 * peak * 1e9) * 1e3, 0.01)
+                k = max(10, min(2000, int(300.0 / call_ms_guess)))
+                r = run_config(name, k, max(3, k // 10), rank, world, device, stream,
+                               with_e2e=False, layered=layered)
+                extra.append({"config": name, "workload": workload_desc(r["case"].wl),
+                              "entry": "kvattn_decode_layers (one call over the layer caches)"
+                                       if layered else "kvattn_decode",
+                              "steps": k, "ms_per_step": r["ms_per_step"],
+                              "l2_resident": r["case"].l2_resident,
+                              "tokens_per_s": r["tokens_per_s"], "kv_read_gbs": r["kv_gbs"],
+                              "kv_read_frac_of_peak": r["kv_gbs"] / world / peak,
+                              "calls_per_step": r["calls_per_step"]})
+                del r
+                torch.cuda.empty_cache()
         line["per_config"] = extra
     return line
 

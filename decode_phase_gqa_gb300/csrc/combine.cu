@@ -131,11 +131,12 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   // the unit list of T units is cut into nwa warp shares (WeightedSplit), and
   // stream sid's records sit in slots sid + (its first share) onwards, one
   // per share.
-  int T = 0;
-  const bool any = plan_units<kCombineThreads>(p, pref, scratch, T);
-  const int nwa = any ? warp_shares(4 * T + p.stream_cost * p.n_seq * spu, n_warps) : 1;
-  const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, any ? T : 1, nwa);
-  const int n_streams = p.n_seq * spu;
+  int TL = 0;  // units of one layer
+  const bool any = plan_units<kCombineThreads>(p, pref, scratch, TL);
+  const int nwa =
+      any ? warp_shares(p.n_layers * (4 * TL + p.stream_cost * p.n_seq * spu), n_warps) : 1;
+  const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, any ? TL : 1, p.n_layers, nwa);
+  const int n_streams = p.n_layers * p.n_seq * spu;  // stream sid: virtual sequence sid / spu
   // item it: chunk it / n_streams of stream it % n_streams; CTA c takes
   // items c, c + gridDim.x, ...
   const int n_items = any ? n_streams * kMaxChunks : 0;
@@ -147,10 +148,11 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
     const int it = base + tid * (int)gridDim.x;
     if (it < n_items) {
       const int q = it / n_streams, sid = it - q * n_streams;
-      const int b = sid / spu, si = sid % spu;
+      const int v = sid / spu, si = sid % spu;
+      const int l = v / p.n_seq, b = v - l * p.n_seq;
       const int units = pref[b + 1] - pref[b];
       if (units > 0) {
-        const int F = spu * pref[b] + si * units;
+        const int F = l * TL + spu * pref[b] + si * units;
         const int w0 = split.owner(F, sid);
         const int nseg = split.owner(F + units - 1, sid) - w0 + 1;
         int R = 1;
@@ -174,10 +176,10 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
       for (int i = gi; i < n_list; i += kGroups) {
         const int4 w = list[i];
         if (lseg[i] > kShort) continue;
-        const int b = w.x / spu, si = w.x % spu;
+        const int v = w.x / spu, si = w.x % spu;
         const int h0 = (si / p.n_sub) * GS * p.n_sub + (si % p.n_sub) * GS;
         const ColState st = merge_column<D, GS>(p.records + (size_t)(w.x + w.w) * RS, 0, 1, lseg[i], c);
-        store_column(p.out + ((size_t)b * p.n_qh + h0) * D + c * 4, st);
+        store_column(p.out + ((size_t)v * p.n_qh + h0) * D + c * 4, st);
       }
     }
     // long merges: the whole CTA, one item at a time
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
       const int nseg = lseg[i];
       if (nseg <= kShort) continue;
       const int sid = w.x, q = w.y, nch = w.z, w0 = w.w;
-      const int b = sid / spu, si = sid % spu;
+      const int v = sid / spu, si = sid % spu;
       const int h0 = (si / p.n_sub) * GS * p.n_sub + (si % p.n_sub) * GS;
       // thread (record lane rl, column cc of the chunk) merges records rl,
       // rl + R, ... of column c online
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
           }
           absorb_batch<8>(st, mm, ll, a);
         }
-        store_column(p.out + ((size_t)b * p.n_qh + h0) * D + c * 4, st);
+        store_column(p.out + ((size_t)v * p.n_qh + h0) * D + c * 4, st);
       }
       __syncthreads();
     }
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
 
 template <int D, int GS>
 cudaError_t launch_combine_t(const DecodeParams &p, int n_warps, int sms, cudaStream_t stream) {
-  const int n_streams = p.n_seq * p.n_kvh * p.n_sub;
+  const int n_streams = p.n_layers * p.n_seq * p.n_kvh * p.n_sub;
   constexpr int NC = GS * D / 4;
   const long long items = (long long)n_streams * (NC / (16 < NC ? 16 : NC));
   cudaLaunchConfig_t cfg = {};

@@ -102,33 +102,43 @@ __device__ __forceinline__ bool plan_units(const DecodeParams &p, int *pref, int
   return T > 0;
 }
 
+// Layers.  A call may decode L layer caches that share the lengths,
+// positions and block table (a layer-major batch): layer l's streams follow
+// layer l - 1's in the unit list.  Sequence b of layer l is the virtual
+// sequence v = l B + b; its queries, new rows, outputs and partial records are
+// row v of the layer-major arrays, its pages those of layer l's pool.
+//
 // The split actually used: a warp share is an equal part of a weighted unit
 // list, in which every unit weighs 4 and every stream weighs `sc` more (its
 // fixed costs: the query set-up at its start, the new token's row at its end),
-// placed after its last unit.  Unit t of stream s (s = b spu + si) sits at
-// weighted position 4 t + sc s; the list is X = 4 T + sc B spu long (the host
-// keeps X below 2^31).  Share c holds the units whose positions fall in
-// [split.begin(c), split.begin(c + 1)); its unit range is
-// [first_unit(split.begin(c)), first_unit(split.begin(c + 1))).
+// placed after its last unit.  Unit t of stream s (s = v spu + si) sits at
+// weighted position 4 t + sc s; a layer is XL = 4 TL + sc B spu long (TL: its
+// units) and the list L XL (the host keeps it below 2^31).  Share c holds the
+// units whose positions fall in [split.begin(c), split.begin(c + 1)); its
+// unit range is [first_unit(split.begin(c)), first_unit(split.begin(c + 1))).
 struct WeightedSplit {
-  const int *pref;  // units per stream, prefix over sequences
-  int B, spu, sc, T;
+  const int *pref;  // units per stream, prefix over the sequences of a layer
+  int B, spu, sc, TL, XL, L;
   Split split;
-  __device__ __forceinline__ WeightedSplit(const int *pref_, int B_, int spu_, int sc_, int T_, int n)
-      : pref(pref_), B(B_), spu(spu_), sc(sc_), T(T_), split(4 * T_ + sc_ * B_ * spu_, n) {}
-  // weighted position of sequence b's first stream
+  __device__ __forceinline__ WeightedSplit(const int *pref_, int B_, int spu_, int sc_, int TL_,
+                                           int L_, int n)
+      : pref(pref_), B(B_), spu(spu_), sc(sc_), TL(TL_), XL(4 * TL_ + sc_ * B_ * spu_), L(L_),
+        split(L_ * (4 * TL_ + sc_ * B_ * spu_), n) {}
+  // weighted position of sequence b's first stream within its layer
   __device__ __forceinline__ int seq_pos(int b) const { return 4 * spu * pref[b] + sc * spu * b; }
-  // First unit whose weighted position is >= y (T when there is none) and its
-  // sequence *b (the sequence of the unit; B - 1 when there is none), found by
-  // one lane: a binary search for the last sequence starting at or before y,
-  // the stream and unit inside it, and a second binary search that moves past
-  // sequences without units (the unit then belongs to the next sequence that
-  // has some).
-  __device__ __forceinline__ int first_unit(int y, int *b) const {
+  // First unit whose weighted position is >= y (L TL when there is none) and
+  // its virtual sequence *v (the sequence of the unit; L B - 1 when there is
+  // none), found by one lane: the layer, then a binary search for the last
+  // sequence of the layer starting at or before y, the stream and unit inside
+  // it, and a second binary search that moves past sequences without units
+  // (the unit then belongs to the next sequence that has some).
+  __device__ __forceinline__ int first_unit(int y, int *v) const {
     if (y >= split.T) {
-      *b = B - 1;
-      return T;
+      *v = L * B - 1;
+      return L * TL;
     }
+    const int l = y < XL ? 0 : y / XL;
+    y -= l * XL;
     int lo = 0, hi = B;  // seq_pos(lo) <= y; every sequence from hi on starts after y
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -150,11 +160,11 @@ struct WeightedSplit {
       else
         bh = mid;
     }
-    *b = bl;
-    return t;
+    *v = l * B + bl;
+    return l * TL + t;
   }
-  // Unit range [*t0, *t1) of share c and the sequences of its ends, for the
-  // whole warp: even lanes search the start, odd lanes the end, at once.
+  // Unit range [*t0, *t1) of share c and the virtual sequences of its ends,
+  // for the whole warp: even lanes search the start, odd lanes the end, at once.
   __device__ __forceinline__ void share_bounds(int c, int lane, int *t0, int *b0, int *t1,
                                                int *b1) const {
     int b = 0;
@@ -182,19 +192,30 @@ __device__ __forceinline__ int warp_shares(int X, int n_warps) {
   return max(1, min(n_warps, n4));
 }
 
-// Position of flattened unit t: sequence (cursor b, advanced monotonically),
-// stream within the sequence and unit within the stream.
+// Position of flattened unit t: virtual sequence (cursor v, advanced
+// monotonically), its layer and sequence within the layer, stream within the
+// sequence and unit within the stream (TL: units per layer).
 struct UnitPos {
-  int b, si, u, units;
+  int v, l, b, si, u, units;
   int first;  // flattened index of the stream's first unit
 };
 
-__device__ __forceinline__ UnitPos locate_unit(int t, int &b, const int *pref, int spu) {
-  while (spu * pref[b + 1] <= t) ++b;
+__device__ __forceinline__ UnitPos locate_unit(int t, int &v, const int *pref, int spu, int B,
+                                               int TL) {
+  int l = v < B ? 0 : v / B, b = v - l * B;
+  while (l * TL + spu * pref[b + 1] <= t) {  // unit t lies past sequence (l, b)
+    if (++b == B) {
+      b = 0;
+      ++l;
+    }
+  }
+  v = l * B + b;
   UnitPos r;
+  r.v = v;
+  r.l = l;
   r.b = b;
   r.units = pref[b + 1] - pref[b];
-  const int off = t - spu * pref[b];
+  const int off = t - (l * TL + spu * pref[b]);
   r.si = off / r.units;
   r.u = off - r.si * r.units;
   r.first = t - r.u;
@@ -221,11 +242,11 @@ __device__ __forceinline__ float frac_turns(int pos, float2 g) {
   return t - rintf(t);
 }
 
-// block-table entry (physical page, not yet range-checked) of flattened unit t
-// (cursor b advanced monotonically)
+// block-table entry (physical page within its layer's pool, not yet
+// range-checked) of flattened unit t (cursor v advanced monotonically)
 __device__ __forceinline__ int page_raw_of_unit(const DecodeParams &p, const int *pref, int spu,
-                                                int t, int &b) {
-  const UnitPos up = locate_unit(t, b, pref, spu);
+                                                int TL, int t, int &v) {
+  const UnitPos up = locate_unit(t, v, pref, spu, p.n_seq, TL);
   return __ldg(p.block_table + (size_t)up.b * p.max_pages + (up.u >> p.unit_shift));
 }
 

@@ -328,14 +328,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     // every CTA pulls its slice of the queries into L2, so that the warps'
     // query rows do not queue behind the flood of K/V requests
-    const size_t q_lines = ((size_t)p.n_seq * p.n_qh * D * 2 + 127) / 128;
+    const size_t q_lines = ((size_t)p.n_layers * p.n_seq * p.n_qh * D * 2 + 127) / 128;
     const size_t per = (q_lines + gridDim.x - 1) / gridDim.x;
     const char *qc = reinterpret_cast<const char *>(p.q);
 #pragma unroll 1
     for (size_t l = blockIdx.x * per + tid; l < min(q_lines, (blockIdx.x + 1) * per); l += kDecodeThreads)
       asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(qc + l * 128));
     // and the new keys and values, which the warps appending them read
-    const size_t kv_lines = ((size_t)p.n_seq * p.n_kvh * D * 2 + 127) / 128;
+    const size_t kv_lines = ((size_t)p.n_layers * p.n_seq * p.n_kvh * D * 2 + 127) / 128;
     const size_t kper = (kv_lines + gridDim.x - 1) / gridDim.x;
     const char *kc = reinterpret_cast<const char *>(p.k_new);
     const char *vc = reinterpret_cast<const char *>(p.v_new);
@@ -360,11 +360,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   pdl_launch_dependents();  // the combine grid may start planning at once
   // prefix sums of units per sequence, lengths and positions (its barriers
   // also publish the set-up above); shares are per warp here
-  int T = 0;
-  if (!plan_units<kDecodeThreads>(p, pref, misc, T, lens, poss, blockIdx.x == 0)) return;
+  int TL = 0;  // units of one layer
+  if (!plan_units<kDecodeThreads>(p, pref, misc, TL, lens, poss, blockIdx.x == 0)) return;
   const int n_warps = min((int)gridDim.x * W, p.n_shares);
-  const int nwa = warp_shares(4 * T + p.stream_cost * p.n_seq * spu, n_warps);
-  const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, T, nwa);
+  const int nwa = warp_shares(p.n_layers * (4 * TL + p.stream_cost * p.n_seq * spu), n_warps);
+  const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, TL, p.n_layers, nwa);
   // A small batch leaves at least half of the warps idle: then the shares
   // are spread over the CTAs (warp slots 0..A-1 of every CTA; A <= W/2) and
   // idle warp A + a of a CTA forms the new token's stored row of active warp
@@ -382,10 +382,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       int b = 0, b1 = 0, wa0 = 0, wa1 = 0;
       split.share_bounds(ga, lane, &wa0, &b, &wa1, &b1);
       if (wa0 >= wa1) b = 0;
-      const UnitPos up = locate_unit(wa0 < wa1 ? wa0 : 0, b, pref, spu);
+      const UnitPos up = locate_unit(wa0 < wa1 ? wa0 : 0, b, pref, spu, p.n_seq, TL);
       if (wa0 < wa1 && up.first + up.units <= wa1) {  // warp a appends its first stream's new token
         uint8_t *arow = smem + C::kNewOff + a * C::kNewBytes;
-        const size_t kv = ((size_t)up.b * p.n_kvh + up.si / p.n_sub) * D;
+        const size_t kv = ((size_t)up.v * p.n_kvh + up.si / p.n_sub) * D;
         const char *ks = reinterpret_cast<const char *>(p.k_new + kv);
         const char *vs = reinterpret_cast<const char *>(p.v_new + kv);
         for (int c = lane; c < 4 * D / 16; c += 32)
@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     return;
   }
-  int start_b = 0, end_b = 0, wt0 = 0, wt1 = 0;
-  split.share_bounds(g, lane, &wt0, &start_b, &wt1, &end_b);
+  int start_v = 0, end_v = 0, wt0 = 0, wt1 = 0;
+  split.share_bounds(g, lane, &wt0, &start_v, &wt1, &end_v);
   const int count = wt1 - wt0;
   if (count == 0) return;  // a share of stream costs only
   const uint64_t pol = l2_evict_first_policy();
@@ -410,9 +410,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // 0-7 issue the scale copies that the stage barriers track, so only lanes
   // kQLane0.. copy (and wait for) query rows.
   constexpr int kQLane0 = INT8 ? 8 : 0;
-  auto prefetch_queries = [&](int b, int h0) {
+  auto prefetch_queries = [&](int v, int h0) {  // (virtual sequence v)
     __syncwarp();
-    const char *src = reinterpret_cast<const char *>(p.q + ((size_t)b * p.n_qh + h0) * D);
+    const char *src = reinterpret_cast<const char *>(p.q + ((size_t)v * p.n_qh + h0) * D);
     if (lane >= kQLane0)
       for (int c = lane - kQLane0; c < C::kQBytes / 16; c += 32 - kQLane0)
         cp_async_16(reinterpret_cast<char *>(qbuf) + c * 16, src + c * 16);
@@ -422,8 +422,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // new-row buffer, the same way (any plain load issued once the SM's inbound
   // queue is full of tiles waits microseconds behind them)
   uint8_t *nrow = smem + C::kNewOff + warp * C::kNewBytes;
-  auto prefetch_new_raw = [&](int b, int j) {
-    const size_t kv = ((size_t)b * p.n_kvh + j) * D;
+  auto prefetch_new_raw = [&](int v, int j) {
+    const size_t kv = ((size_t)v * p.n_kvh + j) * D;
     const char *ks = reinterpret_cast<const char *>(p.k_new + kv);
     const char *vs = reinterpret_cast<const char *>(p.v_new + kv);
     if (lane >= kQLane0)
@@ -431,21 +431,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
         cp_async_16(nrow + c * 16, (c < 2 * D / 16 ? ks + c * 16 : vs + (c - 2 * D / 16) * 16));
     cp_async_commit();
   };
-  // position of the next unit to request: sequence, KV head, query-head group
-  // and unit of the stream, advanced one unit at a time by every lane alike
-  int cb_b, cb_j, cb_sub, cb_u, cb_units;
+  // position of the next unit to request: layer, sequence, KV head,
+  // query-head group and unit of the stream, advanced one unit at a time by
+  // every lane alike
+  int cb_l, cb_b, cb_j, cb_sub, cb_u, cb_units;
   {
-    int b = start_b;
-    const UnitPos up = locate_unit(wt0, b, pref, spu);
+    int v = start_v;
+    const UnitPos up = locate_unit(wt0, v, pref, spu, p.n_seq, TL);
+    cb_l = up.l;
     cb_b = up.b;
     cb_j = up.si / p.n_sub;
     cb_sub = up.si % p.n_sub;
     cb_u = up.u;
     cb_units = up.units;
-    prefetch_queries(up.b, cb_j * GS * p.n_sub + cb_sub * GS);
+    prefetch_queries(up.v, cb_j * GS * p.n_sub + cb_sub * GS);
     // the first stream's raw new rows, if this warp appends it and no idle
     // warp does the work
-    if (up.first + up.units <= wt1 && !(spread && warp + A < W)) prefetch_new_raw(up.b, cb_j);
+    if (up.first + up.units <= wt1 && !(spread && warp + A < W)) prefetch_new_raw(up.v, cb_j);
   }
   auto advance = [&]() {  // only while units remain in the share
     if (++cb_u < cb_units) return;
@@ -455,7 +457,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     if (++cb_j < p.n_kvh) return;
     cb_j = 0;
     do {
-      ++cb_b;
+      if (++cb_b == p.n_seq) {
+        cb_b = 0;
+        ++cb_l;
+      }
     } while (pref[cb_b + 1] == pref[cb_b]);
     cb_units = pref[cb_b + 1] - pref[cb_b];
   };
@@ -467,20 +472,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // memory itself (below): nothing waits for the pool write.
   // (raw block-table entries: the range check waits until a page is used, so
   // that the second window's load does not stall the first requests)
-  int pcur = start_b;  // per-lane cursor of the page windows
+  int pcur = start_v;  // per-lane cursor of the page windows
   int win_base = 0;
-  int win_page = lane < count ? page_raw_of_unit(p, pref, spu, wt0 + lane, pcur) : -1;
-  int nxt_page = 32 + lane < count ? page_raw_of_unit(p, pref, spu, wt0 + 32 + lane, pcur) : -1;
+  int win_page = lane < count ? page_raw_of_unit(p, pref, spu, TL, wt0 + lane, pcur) : -1;
+  int nxt_page = 32 + lane < count ? page_raw_of_unit(p, pref, spu, TL, wt0 + 32 + lane, pcur) : -1;
   auto issue = [&](int i) {  // called by the whole warp, in unit order
     if (i > 0) advance();
     if (i - win_base >= 32) {
       win_base += 32;
       win_page = nxt_page;
       const int tn = win_base + 32 + lane;
-      nxt_page = tn < count ? page_raw_of_unit(p, pref, spu, wt0 + tn, pcur) : -1;
+      nxt_page = tn < count ? page_raw_of_unit(p, pref, spu, TL, wt0 + tn, pcur) : -1;
     }
     int page = __shfl_sync(0xffffffffu, win_page, i - win_base);
-    page = (page >= 0 && page < p.num_pages) ? page : -1;
+    // range-checked in its layer's pool, then a page of the all-layer view
+    page = (page >= 0 && page < p.num_pages) ? page + cb_l * p.num_pages : -1;
     const int st = warp * C::kSW + i % C::kSW;
     const int row = (page * p.n_kvh + cb_j) * p.page_size + ((cb_u * kUnitRows) & (p.page_size - 1));
     if constexpr (INT8) {
@@ -527,16 +533,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   const int vcsel = INT8 ? kcsel : (lane >> 3) & 1;
   bool aborted = false;
   int consumed = 0;
-  int cb = start_b;
+  int cb = start_v;
   int t = wt0;
   while (t < wt1) {
-    const UnitPos sp = locate_unit(t, cb, pref, spu);
+    const UnitPos sp = locate_unit(t, cb, pref, spu, p.n_seq, TL);
     const int F = sp.first, E = F + sp.units;
     const int e = min(wt1, E);
     const int L = lens[sp.b];
     const int j = sp.si / p.n_sub, sub = sp.si % p.n_sub;
     const int h0 = j * GS * p.n_sub + sub * GS;
-    const int sid = sp.b * spu + sp.si;
+    const int sid = sp.v * spu + sp.si;  // (all layers' streams)
 
     // The warp that consumes the stream's last unit forms the stored key and
     // value of the new token (the storage recipe, storage.cuh) once that
@@ -570,13 +576,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       kbias[1] = acc[1];
     }
     if (E < wt1) {  // the share continues: fetch the next stream's query rows
-      int b = sp.b;
-      const UnitPos nx = locate_unit(E, b, pref, spu);
-      prefetch_queries(nx.b, (nx.si / p.n_sub) * GS * p.n_sub + (nx.si % p.n_sub) * GS);
+      int v = sp.v;
+      const UnitPos nx = locate_unit(E, v, pref, spu, p.n_seq, TL);
+      prefetch_queries(nx.v, (nx.si / p.n_sub) * GS * p.n_sub + (nx.si % p.n_sub) * GS);
     }
     // this stream's raw new rows (the first stream's came in the prologue),
     // after the query wait above so that it does not wait for them
-    if (own_last && t > wt0) prefetch_new_raw(sp.b, j);
+    if (own_last && t > wt0) prefetch_new_raw(sp.v, j);
     float o[C::kKSteps][4];
 #pragma unroll
     for (int dt = 0; dt < C::kKSteps; ++dt)
@@ -790,7 +796,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int dr = lane >> 2;
     const auto dA = [&](int dt) { return INT8 ? dt * 16 + 2 * dr : dt * 16 + dr; };
     const auto dB = [&](int dt) { return INT8 ? dt * 16 + 2 * dr + 1 : dt * 16 + dr + 8; };
-    __nv_bfloat16 *outp = p.out + ((size_t)sp.b * p.n_qh + h0 + hl) * D;
+    __nv_bfloat16 *outp = p.out + ((size_t)sp.v * p.n_qh + h0 + hl) * D;
     if (F >= wt0 && E <= wt1) {
       if (writer) {
         const float f = l > 0.f ? to_m / l : 0.f;

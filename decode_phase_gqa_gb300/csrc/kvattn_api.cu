@@ -172,34 +172,20 @@ cudaError_t decode_launcher(const DecodeParams &p, int head_dim, int gs, bool in
 
 }  // namespace
 
-extern "C" {
-
-size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim) {
-  if (n_seq < 0 || n_seq > KVATTN_MAX_SEQS || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 ||
-      (head_dim != 64 && head_dim != 128))
-    return 0;
-  return workspace_layout(n_seq, n_qh, n_kvh, head_dim).total;
-}
-
-int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return KVATTN_EWORKSPACE;
-  if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
-    return KVATTN_ECUDA;
-  return KVATTN_OK;
-}
-
-int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, void *k_pages,
-                         void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
-                         const int32_t *positions, void *out, int n_seq, int n_qh, int n_kvh,
-                         int head_dim, int page_size, float rope_theta, float scale,
-                         int kv_dtype, void *stream, int max_pages_per_seq, int num_pages,
-                         float *k_scales, float *v_scales, void *workspace,
-                         size_t workspace_bytes, int num_splits) {
+// One decode step over n_layers layer caches (layer-major arrays sharing the
+// block table, lengths and positions); kvattn_decode is n_layers = 1.
+static int decode_call(int n_layers, const void *q, const void *k_new, const void *v_new,
+                       void *k_pages, void *v_pages, const int32_t *block_table,
+                       const int32_t *seq_lens, const int32_t *positions, void *out, int n_seq,
+                       int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta,
+                       float scale, int kv_dtype, void *stream, int max_pages_per_seq,
+                       int num_pages, float *k_scales, float *v_scales, void *workspace,
+                       size_t workspace_bytes, int num_splits) {
   // ---- shape checks ----
-  if (n_seq < 0 || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 || max_pages_per_seq < 1 ||
-      num_pages < 1 || num_splits < 0 || num_splits > KVATTN_MAX_SPLITS)
+  if (n_layers < 1 || n_seq < 0 || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 ||
+      max_pages_per_seq < 1 || num_pages < 1 || num_splits < 0 || num_splits > KVATTN_MAX_SPLITS)
     return KVATTN_EINVAL;
+  if (n_layers > KVATTN_MAX_LAYERS) return KVATTN_EUNSUPPORTED;
   if (!std::isfinite(scale) || std::isnan(rope_theta) || std::isinf(rope_theta))
     return KVATTN_EINVAL;
   if (head_dim != 64 && head_dim != 128) return KVATTN_EUNSUPPORTED;
@@ -207,11 +193,13 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   if (kv_dtype != KVATTN_KV_BF16 && kv_dtype != KVATTN_KV_INT8) return KVATTN_EUNSUPPORTED;
   if (n_seq > KVATTN_MAX_SEQS || n_qh > 1024) return KVATTN_EUNSUPPORTED;
   if ((long long)max_pages_per_seq * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
-  // pool rows are addressed with 32-bit TMA coordinates
-  if ((long long)num_pages * n_kvh * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
+  // pool rows (all layers) are addressed with 32-bit TMA coordinates
+  if ((long long)n_layers * num_pages * n_kvh * page_size > (long long)INT_MAX)
+    return KVATTN_EUNSUPPORTED;
   // the work split weighs the 16-token units of all streams in 32-bit integers
   {
-    const long long streams = (long long)n_seq * n_kvh * (n_qh / n_kvh / group_split(n_qh / n_kvh));
+    const long long streams =
+        (long long)n_layers * n_seq * n_kvh * (n_qh / n_kvh / group_split(n_qh / n_kvh));
     const long long units = streams * ((long long)max_pages_per_seq * page_size / kUnitRows);
     if (units > kMaxStepUnits ||
         4 * units + streams * std::max(kStreamCostBf16, kStreamCostInt8) > (long long)INT_MAX)
@@ -229,7 +217,7 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
     return KVATTN_EINVAL;
   if (int8 && (!k_scales || !v_scales || !aligned(k_scales, 16) || !aligned(v_scales, 16)))
     return KVATTN_EINVAL;
-  const WorkspaceLayout wl = workspace_layout(n_seq, n_qh, n_kvh, head_dim);
+  const WorkspaceLayout wl = workspace_layout(n_layers * n_seq, n_qh, n_kvh, head_dim);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < wl.total)
     return KVATTN_EWORKSPACE;
 
@@ -264,11 +252,12 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   dp.page_size = page_size;
   dp.max_pages = max_pages_per_seq;
   dp.num_pages = num_pages;
+  dp.n_layers = n_layers;
   dp.n_sub = g / gs;
   for (int u = page_size / kUnitRows; u > 1; u >>= 1) ++dp.unit_shift;
   dp.stream_cost = int8 ? kStreamCostInt8 : kStreamCostBf16;
   {
-    const long long rows = (long long)num_pages * n_kvh * page_size;
+    const long long rows = (long long)n_layers * num_pages * n_kvh * page_size;
     if (!cached_pool_map(&dp.tmap_k, k_pages, rows, head_dim, int8) ||
         !cached_pool_map(&dp.tmap_v, v_pages, rows, head_dim, int8))
       return KVATTN_ECUDA;
@@ -290,6 +279,53 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   // ---- launch 2: merge of the streams the warp shares split ----
   if (launch_combine(dp, head_dim, gs, shares, sms, st) != cudaSuccess) return KVATTN_ECUDA;
   return KVATTN_OK;
+}
+
+extern "C" {
+
+size_t kvattn_workspace_size_layers(int n_layers, int n_seq, int n_qh, int n_kvh, int head_dim) {
+  if (n_layers < 1 || n_layers > KVATTN_MAX_LAYERS || n_seq < 0 || n_seq > KVATTN_MAX_SEQS ||
+      n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 || (head_dim != 64 && head_dim != 128))
+    return 0;
+  return workspace_layout(n_layers * n_seq, n_qh, n_kvh, head_dim).total;
+}
+
+size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim) {
+  return kvattn_workspace_size_layers(1, n_seq, n_qh, n_kvh, head_dim);
+}
+
+int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return KVATTN_EWORKSPACE;
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return KVATTN_ECUDA;
+  return KVATTN_OK;
+}
+
+int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                         void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                         const int32_t *positions, void *out, int n_seq, int n_qh, int n_kvh,
+                         int head_dim, int page_size, float rope_theta, float scale,
+                         int kv_dtype, void *stream, int max_pages_per_seq, int num_pages,
+                         float *k_scales, float *v_scales, void *workspace,
+                         size_t workspace_bytes, int num_splits) {
+  return decode_call(1, q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
+                     n_seq, n_qh, n_kvh, head_dim, page_size, rope_theta, scale, kv_dtype, stream,
+                     max_pages_per_seq, num_pages, k_scales, v_scales, workspace, workspace_bytes,
+                     num_splits);
+}
+
+int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const void *v_new,
+                         void *k_pages, void *v_pages, const int32_t *block_table,
+                         const int32_t *seq_lens, const int32_t *positions, void *out, int n_seq,
+                         int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta,
+                         float scale, int kv_dtype, void *stream, int max_pages_per_seq,
+                         int num_pages, float *k_scales, float *v_scales, void *workspace,
+                         size_t workspace_bytes) {
+  return decode_call(n_layers, q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
+                     positions, out, n_seq, n_qh, n_kvh, head_dim, page_size, rope_theta, scale,
+                     kv_dtype, stream, max_pages_per_seq, num_pages, k_scales, v_scales,
+                     workspace, workspace_bytes, 0);
 }
 
 int kvattn_decode(const void *q, const void *k_new, const void *v_new, void *k_pages,

@@ -33,8 +33,8 @@ constexpr long long kWaitCycles = 2000000000LL;
 inline int group_split(int g) { return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1; }
 
 struct DecodeParams {
-  // 2-D views [num_pages * n_kvh * page_size rows][head_dim] of the bf16
-  // K and V pools, boxes of 16 rows x 64 columns, 128-byte swizzle
+  // 2-D views [n_layers * num_pages * n_kvh * page_size rows][head_dim] of the
+  // K and V pools (all layers), [16 rows][128 or 64 bytes] boxes, swizzled
   CUtensorMap tmap_k, tmap_v;
   const int32_t *block_table, *seq_lens, *positions;
   const __nv_bfloat16 *q, *k_new, *v_new;
@@ -44,6 +44,8 @@ struct DecodeParams {
   float *records;      // partial softmax states of split streams
   uint32_t *status;
   int n_seq, n_qh, n_kvh, page_size, max_pages, num_pages;
+  int n_layers;        // layer caches decoded by the call (layer-major arrays,
+                       // one pool of num_pages pages per layer); 1 for one layer
   int n_sub;           // query-head groups per KV head (G / GS)
   int n_shares;        // the unit list is cut into at most this many shares
   int unit_shift;      // log2(page_size / 16): units per page

@@ -33,6 +33,7 @@ KVATTN_DEV_TIMEOUT = 4
 
 KVATTN_MAX_SPLITS = 4096
 KVATTN_MAX_SEQS = 8192
+KVATTN_MAX_LAYERS = 1024
 KVATTN_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
@@ -58,6 +59,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.kvattn_workspace_size.argtypes = [I, I, I, I]
         L.kvattn_workspace_size.restype = S
+        L.kvattn_workspace_size_layers.argtypes = [I, I, I, I, I]
+        L.kvattn_workspace_size_layers.restype = S
         L.kvattn_workspace_init.argtypes = [P, S, P]
         L.kvattn_workspace_init.restype = I
         dec = [P] * 9 + [I] * 5 + [F, F, I, P, I, I, P, P, P, S]
@@ -65,6 +68,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvattn_decode.restype = I
         L.kvattn_decode_splits.argtypes = dec + [I]
         L.kvattn_decode_splits.restype = I
+        L.kvattn_decode_layers.argtypes = [I] + dec
+        L.kvattn_decode_layers.restype = I
         L.kvattn_decode_noalloc.argtypes = dec[:-2] + [P]
         L.kvattn_decode_noalloc.restype = I
         L.kvattn_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
@@ -89,6 +94,11 @@ def kvattn_workspace_size(n_seq: int, n_qh: int, n_kvh: int, head_dim: int) -> i
     return int(load().kvattn_workspace_size(n_seq, n_qh, n_kvh, head_dim))
 
 
+def kvattn_workspace_size_layers(n_layers: int, n_seq: int, n_qh: int, n_kvh: int,
+                                 head_dim: int) -> int:
+    return int(load().kvattn_workspace_size_layers(n_layers, n_seq, n_qh, n_kvh, head_dim))
+
+
 def _stream_handle(stream, device) -> int:
     if stream is None:
         stream = torch.cuda.current_stream(device)
@@ -103,9 +113,9 @@ def kvattn_workspace_init(workspace: torch.Tensor, stream=None) -> None:
 
 
 def alloc_workspace(n_seq: int, n_qh: int, n_kvh: int, head_dim: int, device="cuda",
-                    stream=None) -> torch.Tensor:
+                    stream=None, n_layers: int = 1) -> torch.Tensor:
     """Device workspace for this shape (torch allocation, 256-byte aligned), initialised."""
-    size = kvattn_workspace_size(n_seq, n_qh, n_kvh, head_dim)
+    size = kvattn_workspace_size_layers(n_layers, n_seq, n_qh, n_kvh, head_dim)
     if size == 0:
         raise KvattnError(KVATTN_EINVAL, "kvattn_workspace_size")
     ws = torch.empty(size + 256, dtype=torch.uint8, device=device)
@@ -132,6 +142,46 @@ def _check(t: torch.Tensor, name: str, dtypes, ndim: int, device) -> None:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _marshal(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
+             k_scales, v_scales, layered: bool):
+    """Shape/dtype checks; returns (n_layers, n_seq, n_qh, n_kvh, d, page, num_pages, int8)."""
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kvattn_decode runs on CUDA tensors only")
+    bf = (torch.bfloat16,)
+    e = 1 if layered else 0
+    _check(q, "q", bf, 3 + e, dev)
+    _check(out, "out", bf, 3 + e, dev)
+    _check(k_new, "k_new", bf, 3 + e, dev)
+    _check(v_new, "v_new", bf, 3 + e, dev)
+    _check(k_pages, "k_pages", (torch.bfloat16, torch.int8), 4 + e, dev)
+    _check(v_pages, "v_pages", (k_pages.dtype,), 4 + e, dev)
+    _check(block_table, "block_table", (torch.int32,), 2, dev)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
+    _check(positions, "positions", (torch.int32,), 1, dev)
+    n_layers = q.shape[0] if layered else 1
+    n_seq, n_qh, d = q.shape[e:]
+    num_pages, n_kvh, page, d2 = k_pages.shape[e:]
+    lead = (n_layers,) if layered else ()
+    if (d2 != d or tuple(out.shape) != tuple(q.shape)
+            or tuple(k_new.shape) != lead + (n_seq, n_kvh, d)
+            or tuple(v_new.shape) != lead + (n_seq, n_kvh, d)
+            or tuple(k_pages.shape) != lead + (num_pages, n_kvh, page, d)
+            or tuple(v_pages.shape) != tuple(k_pages.shape)
+            or block_table.shape[0] != n_seq or seq_lens.shape[0] != n_seq
+            or positions.shape[0] != n_seq):
+        raise ValueError("inconsistent shapes")
+    int8 = k_pages.dtype == torch.int8
+    if int8:
+        for name, s in (("k_scales", k_scales), ("v_scales", v_scales)):
+            if s is None:
+                raise ValueError(f"{name} is required for an int8 cache")
+            _check(s, name, (torch.float32,), 3 + e, dev)
+            if tuple(s.shape) != lead + (num_pages, n_kvh, page):
+                raise ValueError(f"{name}: shape {tuple(s.shape)}")
+    return n_layers, n_seq, n_qh, n_kvh, d, page, num_pages, int8
+
+
 def kvattn_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
                   *, rope_theta: float, scale: float, workspace: torch.Tensor,
                   k_scales: Optional[torch.Tensor] = None, v_scales: Optional[torch.Tensor] = None,
@@ -143,44 +193,45 @@ def kvattn_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, posi
     seq_lens/positions [B] int32; k_scales/v_scales [num_pages, Hk, page] fp32
     (int8 only).  ``num_splits`` 0 = library default.
     """
-    dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("kvattn_decode runs on CUDA tensors only")
-    bf = (torch.bfloat16,)
-    _check(q, "q", bf, 3, dev)
-    _check(out, "out", bf, 3, dev)
-    _check(k_new, "k_new", bf, 3, dev)
-    _check(v_new, "v_new", bf, 3, dev)
-    _check(k_pages, "k_pages", (torch.bfloat16, torch.int8), 4, dev)
-    _check(v_pages, "v_pages", (k_pages.dtype,), 4, dev)
-    _check(block_table, "block_table", (torch.int32,), 2, dev)
-    _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
-    _check(positions, "positions", (torch.int32,), 1, dev)
-    n_seq, n_qh, d = q.shape
-    num_pages, n_kvh, page, d2 = k_pages.shape
-    if (d2 != d or tuple(out.shape) != tuple(q.shape) or tuple(k_new.shape) != (n_seq, n_kvh, d)
-            or tuple(v_new.shape) != (n_seq, n_kvh, d) or tuple(v_pages.shape) != tuple(k_pages.shape)
-            or block_table.shape[0] != n_seq or seq_lens.shape[0] != n_seq
-            or positions.shape[0] != n_seq):
-        raise ValueError("inconsistent shapes")
-    int8 = k_pages.dtype == torch.int8
-    if int8:
-        for name, s in (("k_scales", k_scales), ("v_scales", v_scales)):
-            if s is None:
-                raise ValueError(f"{name} is required for an int8 cache")
-            _check(s, name, (torch.float32,), 3, dev)
-            if tuple(s.shape) != (num_pages, n_kvh, page):
-                raise ValueError(f"{name}: shape {tuple(s.shape)}")
+    _, n_seq, n_qh, n_kvh, d, page, num_pages, int8 = _marshal(
+        q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
+        k_scales, v_scales, layered=False)
     rc = load().kvattn_decode_splits(
         q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
         block_table.data_ptr(), seq_lens.data_ptr(), positions.data_ptr(), out.data_ptr(),
         n_seq, n_qh, n_kvh, d, page, float(rope_theta), float(scale),
-        KVATTN_KV_INT8 if int8 else KVATTN_KV_BF16, _stream_handle(stream, dev),
+        KVATTN_KV_INT8 if int8 else KVATTN_KV_BF16, _stream_handle(stream, q.device),
         block_table.shape[1], num_pages, _ptr(k_scales) if int8 else None,
         _ptr(v_scales) if int8 else None, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), int(num_splits))
     if rc:
         raise KvattnError(rc, "kvattn_decode")
+
+
+def kvattn_decode_layers(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions,
+                         out, *, rope_theta: float, scale: float, workspace: torch.Tensor,
+                         k_scales: Optional[torch.Tensor] = None,
+                         v_scales: Optional[torch.Tensor] = None, stream=None) -> None:
+    """One decode step over L layer caches in one launch (kvattn_decode_layers).
+
+    Shapes as for ``kvattn_decode`` with a leading layer dimension L on q, out,
+    k_new, v_new, k_pages, v_pages and the scales; block_table, seq_lens and
+    positions are shared by all layers.  ``workspace`` from
+    ``alloc_workspace(..., n_layers=L)``.
+    """
+    n_layers, n_seq, n_qh, n_kvh, d, page, num_pages, int8 = _marshal(
+        q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
+        k_scales, v_scales, layered=True)
+    rc = load().kvattn_decode_layers(
+        n_layers, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(),
+        v_pages.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), positions.data_ptr(),
+        out.data_ptr(), n_seq, n_qh, n_kvh, d, page, float(rope_theta), float(scale),
+        KVATTN_KV_INT8 if int8 else KVATTN_KV_BF16, _stream_handle(stream, q.device),
+        block_table.shape[1], num_pages, _ptr(k_scales) if int8 else None,
+        _ptr(v_scales) if int8 else None, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size())
+    if rc:
+        raise KvattnError(rc, "kvattn_decode_layers")
 
 
 def kvattn_read_device_status(workspace: torch.Tensor, stream=None) -> int:

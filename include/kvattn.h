@@ -76,7 +76,8 @@ extern "C" {
 
 /* ---- limits ------------------------------------------------------------ */
 #define KVATTN_MAX_SPLITS 4096 /* largest num_splits of kvattn_decode_splits */
-#define KVATTN_MAX_SEQS 8192   /* largest n_seq of one call */
+#define KVATTN_MAX_SEQS 8192   /* largest n_seq of one call (per layer) */
+#define KVATTN_MAX_LAYERS 1024 /* largest n_layers of kvattn_decode_layers */
 
 /*
  * Bytes of device workspace one decode call needs for this shape.  The
@@ -85,6 +86,10 @@ extern "C" {
  * across warps.  0 when the shape is invalid.
  */
 size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim);
+
+/* Workspace bytes of kvattn_decode_layers over n_layers layer caches (0 when
+ * the shape is invalid); n_layers = 1 gives kvattn_workspace_size. */
+size_t kvattn_workspace_size_layers(int n_layers, int n_seq, int n_qh, int n_kvh, int head_dim);
 
 /*
  * Zero the workspace (all workspace_bytes, asynchronously on `stream`).  Must
@@ -152,7 +157,7 @@ int kvattn_decode(const void *q, const void *k_new, const void *v_new, void *k_p
 /*
  * kvattn_decode with an explicit work split: the flattened list of 16-token
  * units over all (sequence, KV head) pairs is cut into at most `num_splits`
- * equal shares, one per CTA; a sequence cut across shares is finished by a
+ * equal shares, one per warp; a sequence cut across shares is finished by a
  * log-sum-exp merge of the shares' partial softmax states.  num_splits = 0
  * picks the default (a multiple of the GPU's SM count); otherwise
  * 1 <= num_splits <= KVATTN_MAX_SPLITS.  Results for different splits agree
@@ -166,6 +171,40 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new,
                          int max_pages_per_seq, int num_pages, float *k_scales,
                          float *v_scales, void *workspace, size_t workspace_bytes,
                          int num_splits);
+
+/*
+ * One decode step over n_layers layer caches in one launch.  The decode phase
+ * pays for many small kernel launches ("Qwen3-8B inference engine from
+ * scratch in C++/CUDA", section 2.2): when the queries of several layers are
+ * ready together (for example a benchmark that runs every layer cache of a
+ * step), one call streams all of them in one balanced work split, so the
+ * start-up, tail and merge of a call are paid once instead of once per layer.
+ * The layers share the block table, lengths and positions (a paged cache keeps
+ * one page table for all layers; each layer has its own pool); each layer
+ * computes exactly what kvattn_decode computes for it.
+ *
+ * n_layers     1 <= n_layers <= KVATTN_MAX_LAYERS.
+ * q, out       device bf16 [n_layers, n_seq, n_qh, head_dim] (layer-major).
+ * k_new, v_new device bf16 [n_layers, n_seq, n_kvh, head_dim].
+ * k_pages,     device [n_layers, num_pages, n_kvh, page_size, head_dim]: layer
+ * v_pages      l's pool of num_pages pages, then layer l + 1's.
+ * k_scales,    device fp32 [n_layers, num_pages, n_kvh, page_size] (int8), or
+ * v_scales     NULL (bf16).
+ * block_table, seq_lens, positions: as for kvattn_decode, shared by all layers.
+ * workspace    >= kvattn_workspace_size_layers(n_layers, ...) bytes, set up as
+ *              for kvattn_decode.
+ * Other arguments, checks and errors as for kvattn_decode; additionally
+ * n_layers * num_pages * n_kvh * page_size must stay below 2^31 (pool rows are
+ * addressed with 32-bit coordinates), else KVATTN_EUNSUPPORTED.  With
+ * n_layers = 1 the call is kvattn_decode.
+ */
+int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const void *v_new,
+                         void *k_pages, void *v_pages, const int32_t *block_table,
+                         const int32_t *seq_lens, const int32_t *positions, void *out, int n_seq,
+                         int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta,
+                         float scale, int kv_dtype, void *stream, int max_pages_per_seq,
+                         int num_pages, float *k_scales, float *v_scales, void *workspace,
+                         size_t workspace_bytes);
 
 /*
  * kvattn_decode for callers that can neither pass a workspace nor let the

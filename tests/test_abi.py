@@ -31,10 +31,10 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
-        "kvattn_decode", "kvattn_decode_noalloc", "kvattn_decode_splits",
-        "kvattn_read_device_status",
+        "kvattn_decode", "kvattn_decode_layers", "kvattn_decode_noalloc",
+        "kvattn_decode_splits", "kvattn_read_device_status",
         "kvattn_status_string", "kvattn_version", "kvattn_workspace_init",
-        "kvattn_workspace_size"])
+        "kvattn_workspace_size", "kvattn_workspace_size_layers"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -159,3 +159,39 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.load(str(tmp_path / "nope.so"))
     finally:
         importlib.reload(K)
+
+
+def test_workspace_size_layers(lib):
+    s1, sl = K.kvattn_workspace_size, K.kvattn_workspace_size_layers
+    assert sl(1, 64, 32, 8, 128) == s1(64, 32, 8, 128)
+    # records for every layer's streams: as many as one layer of 36 x 64 sequences
+    assert sl(36, 64, 32, 8, 128) == s1(36 * 64, 32, 8, 128) > s1(64, 32, 8, 128)
+    for bad in ((0, 8, 4, 1, 64), (-1, 8, 4, 1, 64), (K.KVATTN_MAX_LAYERS + 1, 8, 4, 1, 64),
+                (2, 8, 4, 3, 64), (2, K.KVATTN_MAX_SEQS + 1, 4, 1, 64)):
+        assert sl(*bad) == 0, bad
+
+
+def call_layers(lib, n_layers, **kw):
+    a = args(**kw)
+    del a["num_splits"]
+    return lib.kvattn_decode_layers(n_layers, *a.values())
+
+
+@pytest.mark.parametrize("n_layers,kw,code", [
+    (0, {}, K.KVATTN_EINVAL),
+    (-3, {}, K.KVATTN_EINVAL),
+    (K.KVATTN_MAX_LAYERS + 1, {}, K.KVATTN_EUNSUPPORTED),
+    # every layer's pool rows must stay below 2^31: 1024 x 2^17 pages x 16 x 16
+    (1024, dict(num_pages=1 << 17, n_kvh=16, n_qh=16), K.KVATTN_EUNSUPPORTED),
+    # one layer's workspace is too small for 36 layers' partial states
+    (36, dict(workspace_bytes=None), K.KVATTN_EWORKSPACE),
+    (2, dict(head_dim=96), K.KVATTN_EUNSUPPORTED),
+    (2, dict(q=None), K.KVATTN_EINVAL),
+    (2, dict(n_seq=0), K.KVATTN_OK),
+])
+def test_layers_entry_fails_closed(lib, n_layers, kw, code):
+    if kw.get("workspace_bytes", 0) is None:
+        a = args()
+        kw = dict(workspace_bytes=K.kvattn_workspace_size(a["n_seq"], a["n_qh"], a["n_kvh"],
+                                                          a["head_dim"]))
+    assert call_layers(lib, n_layers, **kw) == code

@@ -1,0 +1,125 @@
+"""Parity of the multi-layer entry (kvattn_decode_layers) with the oracle (needs a GB300).
+
+Several layer caches that share the block table, lengths and positions are
+decoded in one call; every layer must come out as the oracle's decode step of
+that layer alone: its K/V pool (and int8 scales) bit for bit after the
+append, its output within max-abs 2e-2 / mean-abs 2e-3.  One layer through the
+multi-layer entry is the single-layer call bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from decode_phase_gqa_gb300 import kvattn as K
+from decode_phase_gqa_gb300 import workloads as W
+from tests.gpu_helpers import assert_close, out_f64, pool_bits, run_gpu, to_dev
+from tests.helpers import host_inputs, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+STACKED = ("q", "k_new", "v_new", "k_pages", "v_pages", "k_scales", "v_scales")
+
+
+def stack_layers(wl, n_layers, device="cuda", tensors=None):
+    """Layer-major device inputs of n_layers layer caches, and each layer's host copy."""
+    layers = tensors if tensors is not None else [
+        W.make_tensors(wl, layer=l, device="cpu") for l in range(n_layers)]
+    hosts = [host_inputs(wl, tensors=t) for t in layers]
+    d = {}
+    for k in STACKED:
+        d[k] = None if layers[0][k] is None else torch.stack(
+            [t[k].to(device) for t in layers]).contiguous()
+    for k in ("block_table", "seq_lens", "positions"):
+        d[k] = torch.from_numpy(np.ascontiguousarray(hosts[0][k])).to(device)
+    return d, hosts
+
+
+def run_layers(wl, d):
+    L, B, Hq, hd = d["q"].shape
+    ws = K.alloc_workspace(B, Hq, wl.n_kvh, hd, n_layers=L)
+    out = torch.full((L, B, Hq, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    K.kvattn_decode_layers(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
+                           d["block_table"], d["seq_lens"], d["positions"], out,
+                           rope_theta=wl.rope_theta, scale=wl.scale, workspace=ws,
+                           k_scales=d["k_scales"], v_scales=d["v_scales"])
+    return out, K.kvattn_read_device_status(ws)
+
+
+def check_layers(wl, d, hosts, out, seq_mask=None):
+    rows = None if seq_mask is None else np.flatnonzero(seq_mask)
+    for l, h in enumerate(hosts):
+        ref, ost, kp, vp, ks, vs = oracle_decode(wl, h, seq_mask=seq_mask)
+        assert ost == 0
+        assert np.array_equal(pool_bits(d["k_pages"][l]), kp), f"layer {l} K pool"
+        assert np.array_equal(pool_bits(d["v_pages"][l]), vp), f"layer {l} V pool"
+        if ks is not None:
+            assert np.array_equal(d["k_scales"][l].cpu().numpy().view(np.uint32), ks.view(np.uint32))
+            assert np.array_equal(d["v_scales"][l].cpu().numpy().view(np.uint32), vs.view(np.uint32))
+        got = out_f64(out[l])
+        assert np.all(np.isfinite(got if rows is None else got[rows])), f"layer {l} rows unwritten"
+        assert_close(got, ref, rows)
+
+
+def custom(n_qh, n_kvh, lens, d=128, kv="bf16", seed=0, page=16):
+    return W.make_workload("custom", seed=seed, n_seq=len(lens), n_qh=n_qh, n_kvh=n_kvh,
+                           head_dim=d, page_size=page, rope_theta=1e6, kv_dtype=kv,
+                           lengths=list(lens), spare=0.1)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n_layers", [2, 5])
+def test_every_layer_matches_the_oracle(kv, d, n_layers):
+    # ragged tails, a new token alone in a new page, an empty cache, several tiles
+    wl = custom(16, 4, [0, 15, 16, 17, 100, 257, 511], d=d, kv=kv, seed=n_layers + d)
+    dd, hosts = stack_layers(wl, n_layers)
+    out, status = run_layers(wl, dd)
+    assert status == 0
+    check_layers(wl, dd, hosts, out)
+
+
+@pytest.mark.parametrize("n_qh,n_kvh,lens", [
+    (4, 1, [256]),                      # the tiny shape: shares spread, helper warps
+    (32, 8, [3000, 1, 40]),             # streams cut across warps and across layers
+    (8, 8, [5] * 40),                   # many short sequences, no GQA sharing
+])
+def test_layer_boundaries_inside_shares(n_qh, n_kvh, lens):
+    wl = custom(n_qh, n_kvh, lens, d=64, seed=len(lens))
+    dd, hosts = stack_layers(wl, 3)
+    out, status = run_layers(wl, dd)
+    assert status == 0
+    check_layers(wl, dd, hosts, out)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_one_layer_is_the_single_layer_call(kv):
+    wl = custom(32, 8, [700, 3, 2048, 129], d=128, kv=kv, seed=11)
+    h = host_inputs(wl)
+    d1 = to_dev(h)
+    single, st1, _ = run_gpu(wl, d1)
+    dd, _ = stack_layers(wl, 1)
+    layered, st2 = run_layers(wl, dd)
+    assert st1 == st2 == 0
+    assert torch.equal(single.view(torch.int16), layered[0].view(torch.int16))
+    assert np.array_equal(pool_bits(d1["k_pages"]), pool_bits(dd["k_pages"][0]))
+    assert np.array_equal(pool_bits(d1["v_pages"]), pool_bits(dd["v_pages"][0]))
+
+
+def test_qwen3_shaped_layers_at_full_size():
+    """Four of the Qwen3-8B-shaped step's layer caches (batch 64, 32/8 heads,
+    d 128, lengths log-uniform in [128, 8192]) in one call with the default
+    split, as the benchmark times the step: every pool bit for bit, the
+    output on the longest, shortest and a seeded few sequences."""
+    wl = W.make_workload("qwen3", seed=0)
+    dev = torch.device("cuda")
+    layers = [W.make_tensors(wl, layer=l, device=dev) for l in range(4)]
+    dd, hosts = stack_layers(wl, 4, tensors=layers)
+    del layers
+    out, status = run_layers(wl, dd)
+    assert status == 0
+    L = wl.seq_lens
+    pick = {int(np.argmax(L)), int(np.argmin(L))}
+    pick.update(int(b) for b in np.random.default_rng(5).choice(wl.n_seq, 4, replace=False))
+    mask = np.zeros(wl.n_seq, np.uint8)
+    mask[sorted(pick)] = 1
+    check_layers(wl, dd, hosts, out, seq_mask=mask)
