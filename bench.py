@@ -333,13 +333,14 @@ def time_e2e(case: NativeCase, steps: int, warmup: int, world: int, stream):
     and the outputs of all calls are read back in one transfer, every step,
     inside the timed region."""
     n_calls = case.calls_per_step
-    n_sets = 1 if n_calls > 1 else 2  # packed input sets alternated over steps
+    layered = case.layered  # one call over every layer cache (layer-major inputs)
+    n_sets = 1 if (n_calls > 1 or layered) else 2  # packed input sets alternated over steps
 
     def layout():
         segs, off = [], 0
         for n in range(n_calls):
             for k in ("q", "k_new", "v_new"):
-                t = case.caches[0][k]
+                t = case.stacked[k] if layered else case.caches[0][k]
                 segs.append((("in", n, k), off, t.shape, t.dtype))
                 off += -(-t.numel() * t.element_size() // 256) * 256
         for name, t in (("bt", case.bt), ("sl", case.sl), ("pos", case.pos)):
@@ -363,7 +364,7 @@ def time_e2e(case: NativeCase, steps: int, warmup: int, world: int, stream):
         for n in range(n_calls):
             src = case.caches[(s * n_calls + n) % len(case.caches)]
             for k in ("q", "k_new", "v_new"):
-                v[("in", n, k)].copy_(src[k].cpu())
+                v[("in", n, k)].copy_((case.stacked[k] if layered else src[k]).cpu())
         v[("bt",)].copy_(case.bt.cpu())
         v[("sl",)].copy_(case.sl.cpu())
         v[("pos",)].copy_(case.pos.cpu())
@@ -378,6 +379,16 @@ def time_e2e(case: NativeCase, steps: int, warmup: int, world: int, stream):
 
     def one_step(s):
         dev_pack.copy_(host_packs[s % n_sets], non_blocking=True)
+        if layered:
+            c = case.stacked
+            case.K.kvattn_decode_layers(dv[("in", 0, "q")], dv[("in", 0, "k_new")],
+                                        dv[("in", 0, "v_new")], c["k_pages"], c["v_pages"],
+                                        dv[("bt",)], dv[("sl",)], dv[("pos",)], out_d[0],
+                                        rope_theta=case.wl.rope_theta, scale=case.wl.scale,
+                                        workspace=case.ws, k_scales=c["k_scales"],
+                                        v_scales=c["v_scales"], stream=stream)
+            out_h.copy_(out_d, non_blocking=True)
+            return
         idxs = case.step_groups()[s % len(case.step_groups())]
         for n, i in enumerate(idxs):
             c = case.caches[i]
@@ -481,11 +492,12 @@ def native(args, rank, world, local):
     peak, peak_kind = measured_peak()
     with ClockSampler(local) as clocks:
         main = run_config(args.config, args.steps, args.warmup, rank, world, device, stream,
-                          layers=args.layers)
+                          layers=args.layers, layered=args.layered)
     clk = clocks.summary(*main["window"])
     wl = main["case"].wl
     per_call_ms = main["ms_per_step"] / main["calls_per_step"]
-    achieved = wl.kv_bytes / (per_call_ms / 1e3) / 1e9   # GB/s over one call
+    call_bytes = main["kv_bytes_per_step"] / main["calls_per_step"]
+    achieved = call_bytes / (per_call_ms / 1e3) / 1e9   # GB/s over one call
     line = {
         "metric": METRIC,
         "value": main["tokens_per_s"],
@@ -503,6 +515,8 @@ def native(args, rank, world, local):
             "workload": workload_desc(wl), "n_seq": wl.n_seq, "n_qh": wl.n_qh,
             "n_kvh": wl.n_kvh, "head_dim": wl.head_dim, "page_size": wl.page_size,
             "kv_dtype": wl.kv_dtype, "layer_caches_per_step": wl.layers,
+            "entry": "kvattn_decode_layers (one call over the layer caches)"
+                     if main["case"].layered else "kvattn_decode",
             "kv_bytes_per_step": main["kv_bytes_per_step"],
             "kv_read_gbs": main["kv_gbs"],
             "kv_read_frac_of_peak": main["kv_gbs"] / world / peak,
@@ -515,7 +529,7 @@ def native(args, rank, world, local):
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_kind": peak_kind,
-            "traffic": recorded_traffic(args.config),
+            "traffic": recorded_traffic(args.config + ("_layers" if main["case"].layered else "")),
             "kernel": "kvattn decode call (decode kernel with RoPE/append + combine kernel, "
                       "timed together): algorithmic K+V bytes per call / call time",
         },
@@ -534,7 +548,7 @@ def native(args, rank, world, local):
             # a multi-layer step is timed both ways: a graph of one call per
             # layer cache, and one kvattn_decode_layers call over all of them
             for layered in ([False, True] if wl2.layers > 1 else [False]):
-                if name == args.config and not layered:
+                if name == args.config and layered == main["case"].layered:
                     continue
                 call_ms_guess = max(wl2.kv_bytes * wl2.layers / (0.7 * peak * 1e9) * 1e3, 0.01)
                 k = max(10, min(2000, int(300.0 / call_ms_guess)))
@@ -629,6 +643,8 @@ def main(argv=None):
     ap.add_argument("--config", choices=W.CONFIG_ORDER, default=PRIMARY)
     ap.add_argument("--no-extra-configs", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layered", action="store_true",
+                    help="time a multi-layer config's step as one kvattn_decode_layers call")
     ap.add_argument("--layers", type=int, default=None,
                     help="decode at most this many layer caches per step (a smaller case "
                          "for profiling; the default is the workload's own count)")
