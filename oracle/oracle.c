@@ -31,7 +31,7 @@
  *  [S8] "lightLLM, a pure-Python inference framework" (haoling.cc), section 1
  *       "Overview": Int8KV cache; the cache write around attention.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - frequency i of a head of size d is theta^(-2i/d), i < d/2; pair (i, i+d/2);
  *  - cached K are stored after RoPE; only q and the new k are rotated here;
  *  - seq_lens[b] = tokens cached before the step = slot of the new token;
