@@ -45,7 +45,7 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 SRC_FILES = ["decode_common.cuh", "decode_mma.cuh", "kvattn_internal.cuh", "angle_table.inc",
              "storage.cuh", "kvattn_api.cu", "decode_bf16.cu", "decode_int8.cu",
-             "combine.cu"]
+             "decode_bf16_layers.cu", "decode_int8_layers.cu", "combine.cu"]
 
 
 def workload_desc(wl: W.Workload) -> str:

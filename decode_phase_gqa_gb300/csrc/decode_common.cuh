@@ -131,13 +131,15 @@ struct WeightedSplit {
   // none), found by one lane: the layer, then a binary search for the last
   // sequence of the layer starting at or before y, the stream and unit inside
   // it, and a second binary search that moves past sequences without units
-  // (the unit then belongs to the next sequence that has some).
+  // (the unit then belongs to the next sequence that has some).  LAYERED:
+  // whether the list may hold more than one layer (else L is 1).
+  template <bool LAYERED>
   __device__ __forceinline__ int first_unit(int y, int *v) const {
     if (y >= split.T) {
       *v = L * B - 1;
       return L * TL;
     }
-    const int l = y < XL ? 0 : y / XL;
+    const int l = (LAYERED && y >= XL) ? y / XL : 0;
     y -= l * XL;
     int lo = 0, hi = B;  // seq_pos(lo) <= y; every sequence from hi on starts after y
     while (hi - lo > 1) {
@@ -165,10 +167,11 @@ struct WeightedSplit {
   }
   // Unit range [*t0, *t1) of share c and the virtual sequences of its ends,
   // for the whole warp: even lanes search the start, odd lanes the end, at once.
+  template <bool LAYERED>
   __device__ __forceinline__ void share_bounds(int c, int lane, int *t0, int *b0, int *t1,
                                                int *b1) const {
     int b = 0;
-    const int t = first_unit(split.begin(c + (lane & 1)), &b);
+    const int t = first_unit<LAYERED>(split.begin(c + (lane & 1)), &b);
     *t0 = __shfl_sync(0xffffffffu, t, 0);
     *b0 = __shfl_sync(0xffffffffu, b, 0);
     *t1 = __shfl_sync(0xffffffffu, t, 1);
@@ -200,11 +203,17 @@ struct UnitPos {
   int first;  // flattened index of the stream's first unit
 };
 
+template <bool LAYERED>  // (else l is 0 and v is b)
 __device__ __forceinline__ UnitPos locate_unit(int t, int &v, const int *pref, int spu, int B,
                                                int TL) {
-  int l = v < B ? 0 : v / B, b = v - l * B;
-  while (l * TL + spu * pref[b + 1] <= t) {  // unit t lies past sequence (l, b)
-    if (++b == B) {
+  int l = 0, b = v;
+  if (LAYERED && v >= B) {
+    l = v / B;
+    b = v - l * B;
+  }
+  while ((LAYERED ? l * TL : 0) + spu * pref[b + 1] <= t) {  // unit t lies past sequence (l, b)
+    ++b;
+    if (LAYERED && b == B) {
       b = 0;
       ++l;
     }
@@ -215,7 +224,7 @@ __device__ __forceinline__ UnitPos locate_unit(int t, int &v, const int *pref, i
   r.l = l;
   r.b = b;
   r.units = pref[b + 1] - pref[b];
-  const int off = t - (l * TL + spu * pref[b]);
+  const int off = t - ((LAYERED ? l * TL : 0) + spu * pref[b]);
   r.si = off / r.units;
   r.u = off - r.si * r.units;
   r.first = t - r.u;
@@ -244,9 +253,10 @@ __device__ __forceinline__ float frac_turns(int pos, float2 g) {
 
 // block-table entry (physical page within its layer's pool, not yet
 // range-checked) of flattened unit t (cursor v advanced monotonically)
+template <bool LAYERED>
 __device__ __forceinline__ int page_raw_of_unit(const DecodeParams &p, const int *pref, int spu,
                                                 int TL, int t, int &v) {
-  const UnitPos up = locate_unit(t, v, pref, spu, p.n_seq, TL);
+  const UnitPos up = locate_unit<LAYERED>(t, v, pref, spu, p.n_seq, TL);
   return __ldg(p.block_table + (size_t)up.b * p.max_pages + (up.u >> p.unit_shift));
 }
 

@@ -168,14 +168,14 @@ __device__ __forceinline__ float pow2i(int k) { return __uint_as_float((uint32_t
 // RoPE of the query, fp32 only (the query needs fp32 accuracy): lane l holds
 // cos/sin of angles l + 32k of position `pos`, from frac_turns and sincospif.
 template <int D>
-__device__ __forceinline__ void warp_query_angles(const DecodeParams &p, const float2 *turns,
-                                                  int pos, int lane, float (&cr)[D / 64],
+__device__ __forceinline__ void warp_query_angles(const float2 *turns, int pos, bool rope,
+                                                  int lane, float (&cr)[D / 64],
                                                   float (&sr)[D / 64]) {
 #pragma unroll
   for (int k = 0; k < D / 64; ++k) {
     cr[k] = 1.f;
     sr[k] = 0.f;
-    if (p.use_rope) sincospif(2.f * frac_turns(pos, turns[lane + 32 * k]), &sr[k], &cr[k]);
+    if (rope) sincospif(2.f * frac_turns(pos, turns[lane + 32 * k]), &sr[k], &cr[k]);
   }
 }
 
@@ -269,7 +269,7 @@ __device__ __forceinline__ void warp_query_fragments(const DecodeParams &p, cons
   }
 }
 
-template <int D, int GS, bool INT8>
+template <int D, int GS, bool INT8, bool LAYERED>
 // at most 3 CTAs fit an SM's shared memory: let each thread have 1/384 of the
 // register file
 __global__ void __launch_bounds__(kDecodeThreads, 3)
@@ -363,8 +363,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   int TL = 0;  // units of one layer
   if (!plan_units<kDecodeThreads>(p, pref, misc, TL, lens, poss, blockIdx.x == 0)) return;
   const int n_warps = min((int)gridDim.x * W, p.n_shares);
-  const int nwa = warp_shares(p.n_layers * (4 * TL + p.stream_cost * p.n_seq * spu), n_warps);
-  const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, TL, p.n_layers, nwa);
+  // (LAYERED: the call decodes several layer caches, else one)
+  const int n_layers = LAYERED ? p.n_layers : 1;
+  const int nwa = warp_shares(n_layers * (4 * TL + p.stream_cost * p.n_seq * spu), n_warps);
+  const WeightedSplit split(pref, p.n_seq, spu, p.stream_cost, TL, n_layers, nwa);
+  const auto rope_of = [&](int l) { return LAYERED ? layer_rope(p, l) : p.use_rope != 0; };
   // A small batch leaves at least half of the warps idle: then the shares
   // are spread over the CTAs (warp slots 0..A-1 of every CTA; A <= W/2) and
   // idle warp A + a of a CTA forms the new token's stored row of active warp
@@ -380,9 +383,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int ga = a * (int)gridDim.x + (int)blockIdx.x;
     if (spread && a >= 0 && a < A && ga < nwa) {
       int b = 0, b1 = 0, wa0 = 0, wa1 = 0;
-      split.share_bounds(ga, lane, &wa0, &b, &wa1, &b1);
+      split.share_bounds<LAYERED>(ga, lane, &wa0, &b, &wa1, &b1);
       if (wa0 >= wa1) b = 0;
-      const UnitPos up = locate_unit(wa0 < wa1 ? wa0 : 0, b, pref, spu, p.n_seq, TL);
+      const UnitPos up = locate_unit<LAYERED>(wa0 < wa1 ? wa0 : 0, b, pref, spu, p.n_seq, TL);
       if (wa0 < wa1 && up.first + up.units <= wa1) {  // warp a appends its first stream's new token
         uint8_t *arow = smem + C::kNewOff + a * C::kNewBytes;
         const size_t kv = ((size_t)up.v * p.n_kvh + up.si / p.n_sub) * D;
@@ -392,14 +395,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
           cp_async_16(arow + c * 16, (c < 2 * D / 16 ? ks + c * 16 : vs + (c - 2 * D / 16) * 16));
         cp_async_wait_all();
         __syncwarp();
-        stage_new_row<D, INT8>(poss[up.b], inv_freq, angle_tab, p.use_rope != 0, lane, arow);
+        stage_new_row<D, INT8>(poss[up.b], inv_freq, angle_tab, rope_of(up.l), lane, arow);
         if (lane == 0) mbar_arrive(&row_ready[a]);  // (release: the row is visible)
       }
     }
     return;
   }
   int start_v = 0, end_v = 0, wt0 = 0, wt1 = 0;
-  split.share_bounds(g, lane, &wt0, &start_v, &wt1, &end_v);
+  split.share_bounds<LAYERED>(g, lane, &wt0, &start_v, &wt1, &end_v);
   const int count = wt1 - wt0;
   if (count == 0) return;  // a share of stream costs only
   const uint64_t pol = l2_evict_first_policy();
@@ -437,7 +440,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   int cb_l, cb_b, cb_j, cb_sub, cb_u, cb_units;
   {
     int v = start_v;
-    const UnitPos up = locate_unit(wt0, v, pref, spu, p.n_seq, TL);
+    const UnitPos up = locate_unit<LAYERED>(wt0, v, pref, spu, p.n_seq, TL);
     cb_l = up.l;
     cb_b = up.b;
     cb_j = up.si / p.n_sub;
@@ -457,7 +460,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     if (++cb_j < p.n_kvh) return;
     cb_j = 0;
     do {
-      if (++cb_b == p.n_seq) {
+      ++cb_b;
+      if (LAYERED && cb_b == p.n_seq) {
         cb_b = 0;
         ++cb_l;
       }
@@ -474,19 +478,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // that the second window's load does not stall the first requests)
   int pcur = start_v;  // per-lane cursor of the page windows
   int win_base = 0;
-  int win_page = lane < count ? page_raw_of_unit(p, pref, spu, TL, wt0 + lane, pcur) : -1;
-  int nxt_page = 32 + lane < count ? page_raw_of_unit(p, pref, spu, TL, wt0 + 32 + lane, pcur) : -1;
+  int win_page = lane < count ? page_raw_of_unit<LAYERED>(p, pref, spu, TL, wt0 + lane, pcur) : -1;
+  int nxt_page = 32 + lane < count ? page_raw_of_unit<LAYERED>(p, pref, spu, TL, wt0 + 32 + lane, pcur) : -1;
   auto issue = [&](int i) {  // called by the whole warp, in unit order
     if (i > 0) advance();
     if (i - win_base >= 32) {
       win_base += 32;
       win_page = nxt_page;
       const int tn = win_base + 32 + lane;
-      nxt_page = tn < count ? page_raw_of_unit(p, pref, spu, TL, wt0 + tn, pcur) : -1;
+      nxt_page = tn < count ? page_raw_of_unit<LAYERED>(p, pref, spu, TL, wt0 + tn, pcur) : -1;
     }
     int page = __shfl_sync(0xffffffffu, win_page, i - win_base);
     // range-checked in its layer's pool, then a page of the all-layer view
-    page = (page >= 0 && page < p.num_pages) ? page + cb_l * p.num_pages : -1;
+    page = (page >= 0 && page < p.num_pages) ? page + (LAYERED ? cb_l * p.num_pages : 0) : -1;
     const int st = warp * C::kSW + i % C::kSW;
     const int row = (page * p.n_kvh + cb_j) * p.page_size + ((cb_u * kUnitRows) & (p.page_size - 1));
     if constexpr (INT8) {
@@ -536,7 +540,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   int cb = start_v;
   int t = wt0;
   while (t < wt1) {
-    const UnitPos sp = locate_unit(t, cb, pref, spu, p.n_seq, TL);
+    const UnitPos sp = locate_unit<LAYERED>(t, cb, pref, spu, p.n_seq, TL);
     const int F = sp.first, E = F + sp.units;
     const int e = min(wt1, E);
     const int L = lens[sp.b];
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     uint32_t qb[C::kKSteps][2];
     float inv_sq;
     float cr[D / 64], sr[D / 64];
-    warp_query_angles<D>(p, turns, poss[sp.b], lane, cr, sr);  // while the rows land
+    warp_query_angles<D>(turns, poss[sp.b], rope_of(sp.l), lane, cr, sr);  // while the rows land
     if (lane >= kQLane0) cp_async_wait_all();
     __syncwarp();
     warp_query_fragments<D, GS, INT8>(p, cr, sr, qbuf, lane, qb, inv_sq);
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     if (E < wt1) {  // the share continues: fetch the next stream's query rows
       int v = sp.v;
-      const UnitPos nx = locate_unit(E, v, pref, spu, p.n_seq, TL);
+      const UnitPos nx = locate_unit<LAYERED>(E, v, pref, spu, p.n_seq, TL);
       prefetch_queries(nx.v, (nx.si / p.n_sub) * GS * p.n_sub + (nx.si % p.n_sub) * GS);
     }
     // this stream's raw new rows (the first stream's came in the prologue),
@@ -599,7 +603,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       if (own_last && tt == tab_at && !helped) {
         if (lane >= kQLane0) cp_async_wait_all();  // the raw rows
         __syncwarp();
-        stage_new_row<D, INT8>(poss[sp.b], inv_freq, angle_tab, p.use_rope != 0, lane, nrow);
+        stage_new_row<D, INT8>(poss[sp.b], inv_freq, angle_tab, rope_of(sp.l), lane, nrow);
       }
       const int i = (int)(tt - wt0);
       const int st = warp * C::kSW + i % C::kSW;
@@ -832,11 +836,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   }
 }
 
-template <int D, int GS, bool INT8>
+template <int D, int GS, bool INT8, bool LAYERED>
 cudaError_t launch_decode_mma_t(const DecodeParams &p, int grid, cudaStream_t stream,
                                 int *ctas_per_sm, bool launch) {
   using C = MmaCfg<D, GS, INT8>;
-  auto kern = decode_mma_kernel<D, GS, INT8>;
+  auto kern = decode_mma_kernel<D, GS, INT8, LAYERED>;
   const int smem = C::kFixedSmem + (int)align_up((size_t)(3 * p.n_seq + 1) * 4, 16);
   static std::mutex mu;
   static std::map<std::pair<int, int>, int> occupancy;  // (device, smem) -> CTAs/SM

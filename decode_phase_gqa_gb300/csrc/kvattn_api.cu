@@ -180,7 +180,7 @@ static int decode_call(int n_layers, const void *q, const void *k_new, const voi
                        int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta,
                        float scale, int kv_dtype, void *stream, int max_pages_per_seq,
                        int num_pages, float *k_scales, float *v_scales, void *workspace,
-                       size_t workspace_bytes, int num_splits) {
+                       size_t workspace_bytes, int num_splits, const uint8_t *layer_rope) {
   // ---- shape checks ----
   if (n_layers < 1 || n_seq < 0 || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 ||
       max_pages_per_seq < 1 || num_pages < 1 || num_splits < 0 || num_splits > KVATTN_MAX_SPLITS)
@@ -243,6 +243,10 @@ static int decode_call(int n_layers, const void *q, const void *k_new, const voi
   dp.records = reinterpret_cast<float *>(ws + wl.records_off);
   dp.status = reinterpret_cast<uint32_t *>(ws + wl.status_off);
   dp.use_rope = use_rope ? 1 : 0;
+  // layers whose entry of layer_rope is 0 skip RoPE (a NoPE layer)
+  if (layer_rope)
+    for (int l = 0; l < n_layers; ++l)
+      if (!layer_rope[l]) dp.nope[l >> 5] |= 1u << (l & 31);
   // scores are formed in log2 units: fold scale * log2(e) into the query
   dp.qscale = (float)((double)scale * 1.4426950408889634);
   freq_tables(rope_theta, head_dim, dp.inv_freq, dp.turns);
@@ -312,7 +316,7 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, vo
   return decode_call(1, q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
                      n_seq, n_qh, n_kvh, head_dim, page_size, rope_theta, scale, kv_dtype, stream,
                      max_pages_per_seq, num_pages, k_scales, v_scales, workspace, workspace_bytes,
-                     num_splits);
+                     num_splits, nullptr);
 }
 
 int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const void *v_new,
@@ -321,11 +325,11 @@ int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const v
                          int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta,
                          float scale, int kv_dtype, void *stream, int max_pages_per_seq,
                          int num_pages, float *k_scales, float *v_scales, void *workspace,
-                         size_t workspace_bytes) {
+                         size_t workspace_bytes, const uint8_t *layer_rope) {
   return decode_call(n_layers, q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
                      positions, out, n_seq, n_qh, n_kvh, head_dim, page_size, rope_theta, scale,
                      kv_dtype, stream, max_pages_per_seq, num_pages, k_scales, v_scales,
-                     workspace, workspace_bytes, 0);
+                     workspace, workspace_bytes, 0, layer_rope);
 }
 
 int kvattn_decode(const void *q, const void *k_new, const void *v_new, void *k_pages,

@@ -51,7 +51,8 @@ struct DecodeParams {
   int unit_shift;      // log2(page_size / 16): units per page
   int stream_cost;     // weight of a stream's fixed costs in the work split
                        // (quarters of a unit's weight)
-  int use_rope;
+  int use_rope;        // rope_theta > 0
+  uint32_t nope[KVATTN_MAX_LAYERS / 32];  // bit l: layer l has no RoPE
   float qscale;        // scale * log2(e): scores come out in log2 units
   // turns per position of rotation pair i, rope_theta^(-2i/d) / (2 pi), as an
   // fp32 head and remainder (host-computed in double)
@@ -93,6 +94,11 @@ cudaError_t launch_decode_bf16(const DecodeParams &p, int head_dim, int gs, int 
                                cudaStream_t stream, int *ctas_per_sm, bool launch);
 cudaError_t launch_decode_int8(const DecodeParams &p, int head_dim, int gs, int grid,
                                cudaStream_t stream, int *ctas_per_sm, bool launch);
+// the same for several layer caches (p.n_layers > 1)
+cudaError_t launch_decode_bf16_layers(const DecodeParams &p, int head_dim, int gs, int grid,
+                                      cudaStream_t stream, int *ctas_per_sm, bool launch);
+cudaError_t launch_decode_int8_layers(const DecodeParams &p, int head_dim, int gs, int grid,
+                                      cudaStream_t stream, int *ctas_per_sm, bool launch);
 // Merge of the partial records of the streams the decode kernel's work split
 // cut (sms = the GPU's SM count).
 cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int n_warps, int sms,
@@ -178,6 +184,11 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Whether layer l's query and new key are rotated.
+__device__ __forceinline__ bool layer_rope(const DecodeParams &p, int l) {
+  return p.use_rope != 0 && ((p.nope[l >> 5] >> (l & 31)) & 1u) == 0;
 }
 
 // Number of 16-token units a sequence with L cached tokens spans (the new

@@ -68,7 +68,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvattn_decode.restype = I
         L.kvattn_decode_splits.argtypes = dec + [I]
         L.kvattn_decode_splits.restype = I
-        L.kvattn_decode_layers.argtypes = [I] + dec
+        L.kvattn_decode_layers.argtypes = [I] + dec + [P]
         L.kvattn_decode_layers.restype = I
         L.kvattn_decode_noalloc.argtypes = dec[:-2] + [P]
         L.kvattn_decode_noalloc.restype = I
@@ -211,17 +211,24 @@ def kvattn_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, posi
 def kvattn_decode_layers(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions,
                          out, *, rope_theta: float, scale: float, workspace: torch.Tensor,
                          k_scales: Optional[torch.Tensor] = None,
-                         v_scales: Optional[torch.Tensor] = None, stream=None) -> None:
+                         v_scales: Optional[torch.Tensor] = None, layer_rope=None,
+                         stream=None) -> None:
     """One decode step over L layer caches in one launch (kvattn_decode_layers).
 
     Shapes as for ``kvattn_decode`` with a leading layer dimension L on q, out,
     k_new, v_new, k_pages, v_pages and the scales; block_table, seq_lens and
     positions are shared by all layers.  ``workspace`` from
-    ``alloc_workspace(..., n_layers=L)``.
+    ``alloc_workspace(..., n_layers=L)``.  ``layer_rope``: None (every layer
+    rotated) or L flags, false for a layer without RoPE.
     """
     n_layers, n_seq, n_qh, n_kvh, d, page, num_pages, int8 = _marshal(
         q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
         k_scales, v_scales, layered=True)
+    flags = None
+    if layer_rope is not None:
+        if len(layer_rope) != n_layers:
+            raise ValueError(f"layer_rope: {len(layer_rope)} flags for {n_layers} layers")
+        flags = (ctypes.c_uint8 * n_layers)(*[1 if f else 0 for f in layer_rope])
     rc = load().kvattn_decode_layers(
         n_layers, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(),
         v_pages.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), positions.data_ptr(),
@@ -229,7 +236,8 @@ def kvattn_decode_layers(q, k_new, v_new, k_pages, v_pages, block_table, seq_len
         KVATTN_KV_INT8 if int8 else KVATTN_KV_BF16, _stream_handle(stream, q.device),
         block_table.shape[1], num_pages, _ptr(k_scales) if int8 else None,
         _ptr(v_scales) if int8 else None, workspace.data_ptr(),
-        workspace.numel() * workspace.element_size())
+        workspace.numel() * workspace.element_size(),
+        None if flags is None else ctypes.cast(flags, ctypes.c_void_p))
     if rc:
         raise KvattnError(rc, "kvattn_decode_layers")
 

@@ -193,6 +193,12 @@ int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new,
  * block_table, seq_lens, positions: as for kvattn_decode, shared by all layers.
  * workspace    >= kvattn_workspace_size_layers(n_layers, ...) bytes, set up as
  *              for kvattn_decode.
+ * layer_rope   host uint8 [n_layers] or NULL: a layer whose entry is 0 has no
+ *              RoPE (its query and new key are not rotated), as in a model whose
+ *              RoPE and NoPE layers alternate ("LLM inference from smollm3.go",
+ *              section "Positional encoding: why the model knows order");
+ *              NULL: every layer is rotated (unless rope_theta <= 0, which turns
+ *              RoPE off for all).  Read during the call only.
  * Other arguments, checks and errors as for kvattn_decode; additionally
  * n_layers * num_pages * n_kvh * page_size must stay below 2^31 (pool rows are
  * addressed with 32-bit coordinates), else KVATTN_EUNSUPPORTED.  With
@@ -204,7 +210,7 @@ int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const v
                          int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta,
                          float scale, int kv_dtype, void *stream, int max_pages_per_seq,
                          int num_pages, float *k_scales, float *v_scales, void *workspace,
-                         size_t workspace_bytes);
+                         size_t workspace_bytes, const uint8_t *layer_rope);
 
 /*
  * kvattn_decode for callers that can neither pass a workspace nor let the

@@ -174,7 +174,7 @@ def test_workspace_size_layers(lib):
 def call_layers(lib, n_layers, **kw):
     a = args(**kw)
     del a["num_splits"]
-    return lib.kvattn_decode_layers(n_layers, *a.values())
+    return lib.kvattn_decode_layers(n_layers, *a.values(), None)
 
 
 @pytest.mark.parametrize("n_layers,kw,code", [

@@ -6,6 +6,8 @@ that layer alone: its K/V pool (and int8 scales) bit for bit after the
 append, its output within max-abs 2e-2 / mean-abs 2e-3.  One layer through the
 multi-layer entry is the single-layer call bit for bit.
 """
+from dataclasses import replace
+
 import numpy as np
 import pytest
 import torch
@@ -34,21 +36,24 @@ def stack_layers(wl, n_layers, device="cuda", tensors=None):
     return d, hosts
 
 
-def run_layers(wl, d):
+def run_layers(wl, d, layer_rope=None):
     L, B, Hq, hd = d["q"].shape
     ws = K.alloc_workspace(B, Hq, wl.n_kvh, hd, n_layers=L)
     out = torch.full((L, B, Hq, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
     K.kvattn_decode_layers(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
                            d["block_table"], d["seq_lens"], d["positions"], out,
                            rope_theta=wl.rope_theta, scale=wl.scale, workspace=ws,
-                           k_scales=d["k_scales"], v_scales=d["v_scales"])
+                           k_scales=d["k_scales"], v_scales=d["v_scales"],
+                           layer_rope=layer_rope)
     return out, K.kvattn_read_device_status(ws)
 
 
-def check_layers(wl, d, hosts, out, seq_mask=None):
+def check_layers(wl, d, hosts, out, seq_mask=None, layer_rope=None):
     rows = None if seq_mask is None else np.flatnonzero(seq_mask)
     for l, h in enumerate(hosts):
-        ref, ost, kp, vp, ks, vs = oracle_decode(wl, h, seq_mask=seq_mask)
+        # a layer without RoPE is the oracle's step with RoPE off (theta <= 0)
+        wl_l = wl if layer_rope is None or layer_rope[l] else replace(wl, rope_theta=0.0)
+        ref, ost, kp, vp, ks, vs = oracle_decode(wl_l, h, seq_mask=seq_mask)
         assert ost == 0
         assert np.array_equal(pool_bits(d["k_pages"][l]), kp), f"layer {l} K pool"
         assert np.array_equal(pool_bits(d["v_pages"][l]), vp), f"layer {l} V pool"
@@ -123,3 +128,15 @@ def test_qwen3_shaped_layers_at_full_size():
     mask = np.zeros(wl.n_seq, np.uint8)
     mask[sorted(pick)] = 1
     check_layers(wl, dd, hosts, out, seq_mask=mask)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_rope_and_nope_layers(kv):
+    """SmolLM3's pattern: RoPE on three layers, none on the fourth (its query
+    and new key are not rotated), in one call."""
+    pattern = [True, True, True, False, True, True, True, False]
+    wl = custom(16, 4, [3, 64, 200, 1000], d=128, kv=kv, seed=21)
+    dd, hosts = stack_layers(wl, len(pattern))
+    out, status = run_layers(wl, dd, layer_rope=pattern)
+    assert status == 0
+    check_layers(wl, dd, hosts, out, layer_rope=pattern)

@@ -5,6 +5,8 @@ seeded inputs, then checks: the whole K/V pool (and int8 scales) bit for bit
 after the append, the attention output within max-abs 2e-2 / mean-abs 2e-3,
 and a clean device status word.
 """
+from dataclasses import replace
+
 import numpy as np
 import pytest
 import torch
@@ -286,3 +288,32 @@ def test_back_to_back_steps_see_the_previous_append(kv):
         assert np.array_equal(d1["v_scales"].cpu().numpy().view(np.uint32), vs.view(np.uint32))
     assert_close(out_f64(outs[0]), ref1)
     assert_close(out_f64(outs[1]), ref2)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_selective_kv_over_a_sparse_block_table(kv):
+    """Decode over a selectively kept cache ("C17 CPU-first LLM inference
+    engine", section 5.3: initial tokens, recent tokens and a few important
+    ones are kept, the rest evicted).  At page granularity the kept cache is a
+    sparse block table: the sequence's first page, three middle pages and its
+    last four.  seq_lens is the kept token count and positions the new token's
+    true position, so the new token lands in the same physical slot, rotated
+    the same way, as in the full cache, and attends over exactly the kept
+    tokens."""
+    L = 1000
+    wl, h_full = custom(16, 4, [L], d=128, kv=kv, seed=9)
+    keep = [0, 10, 31, 47, 59, 60, 61, 62]       # logical pages; 62 holds slot L
+    assert L // wl.page_size == keep[-1]
+    sparse = np.full_like(wl.block_table, -1)
+    sparse[0, :len(keep)] = wl.block_table[0, keep]
+    L_kept = wl.page_size * (len(keep) - 1) + L % wl.page_size
+    wl_s = replace(W.with_lengths(wl, [L_kept], positions=[L]), block_table=sparse)
+    h = dict(h_full)
+    h["block_table"], h["seq_lens"], h["positions"] = sparse, wl_s.seq_lens, wl_s.positions
+    check_against_oracle(wl_s, h)
+    # the appended row is the full cache's: same slot, same position
+    d = to_dev(h)
+    run_gpu(wl_s, d)
+    _, _, kp, vp, _, _ = oracle_decode(wl, h_full)
+    assert np.array_equal(pool_bits(d["k_pages"]), kp)
+    assert np.array_equal(pool_bits(d["v_pages"]), vp)
