@@ -140,3 +140,57 @@ def test_rope_and_nope_layers(kv):
     out, status = run_layers(wl, dd, layer_rope=pattern)
     assert status == 0
     check_layers(wl, dd, hosts, out, layer_rope=pattern)
+
+
+def test_bad_length_and_bad_page_in_every_layer():
+    """The layers share the lengths and the block table, so a bad length or
+    page is bad in every layer: each layer skips the same sequence and leaves
+    out the same page's tokens as its own decode step would, and the status
+    word reports both."""
+    wl = custom(8, 2, [50, 60, 70, 90], d=64, seed=8)
+    layers = [W.make_tensors(wl, layer=l, device="cpu") for l in range(3)]
+    bt = wl.block_table.copy()
+    bt[2, 1] = 10 ** 6      # out of range: tokens 16-31 of sequence 2 left out
+    bt[3, 0] = -7           # negative: tokens 0-15 of sequence 3 left out
+    wl = replace(wl, block_table=bt, seq_lens=np.array([50, -3, 70, 90], np.int32))
+    dd, hosts = stack_layers(wl, 3, tensors=layers)
+    out, status = run_layers(wl, dd)
+    assert status & K.KVATTN_DEV_BAD_LEN and status & K.KVATTN_DEV_BAD_PAGE
+    for l, h in enumerate(hosts):
+        ref, ost, kp, vp, _, _ = oracle_decode(wl, h)
+        assert ost & 1 and ost & 2
+        o = out_f64(out[l])
+        assert np.all(np.isnan(o[1])), "the skipped sequence's rows were written"
+        assert_close(o, ref, rows=[0, 2, 3])
+        assert np.array_equal(pool_bits(dd["k_pages"][l]), kp)
+        assert np.array_equal(pool_bits(dd["v_pages"][l]), vp)
+
+
+def test_layers_captured_in_cuda_graph():
+    """One layered call captured in a CUDA graph and replayed twice (the append
+    rewrites the same slot with the same row, so a replay repeats the step)."""
+    wl = custom(32, 8, [1000, 20, 333, 4096], d=128, seed=13)
+    dd, hosts = stack_layers(wl, 4)
+    L, B, Hq, hd = dd["q"].shape
+    ws = K.alloc_workspace(B, Hq, wl.n_kvh, hd, n_layers=L)
+    out = torch.empty((L, B, Hq, hd), dtype=torch.bfloat16, device="cuda")
+
+    def call(stream):
+        K.kvattn_decode_layers(dd["q"], dd["k_new"], dd["v_new"], dd["k_pages"], dd["v_pages"],
+                               dd["block_table"], dd["seq_lens"], dd["positions"], out,
+                               rope_theta=wl.rope_theta, scale=wl.scale, workspace=ws,
+                               stream=stream)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call(s)            # the library's per-device set-up, outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(s)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert K.kvattn_read_device_status(ws) == 0
+        check_layers(wl, dd, hosts, out)
