@@ -19,7 +19,7 @@ LIB = os.path.join(BUILD, "libkvattn.so")
 HEADER = os.path.join(ROOT, "include", "kvattn.h")
 
 SOURCES = ["kvattn_api.cu", "decode_bf16.cu", "decode_int8.cu", "decode_bf16_layers.cu",
-           "decode_int8_layers.cu", "kvattn_noalloc.cu", "combine.cu"]
+           "decode_int8_layers.cu", "kvattn_noalloc.cu", "combine.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I", os.path.join(ROOT, "include")]

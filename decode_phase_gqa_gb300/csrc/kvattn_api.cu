@@ -172,6 +172,13 @@ cudaError_t decode_launcher(const DecodeParams &p, int head_dim, int gs, bool in
 
 }  // namespace
 
+namespace kvattn {
+// the frequency tables for the prefill kernels (prefill.cu)
+void rope_tables(float rope_theta, int head_dim, double *inv_freq, float2 *turns) {
+  freq_tables(rope_theta, head_dim, inv_freq, turns);
+}
+}  // namespace kvattn
+
 // One decode step over n_layers layer caches (layer-major arrays sharing the
 // block table, lengths and positions); kvattn_decode is n_layers = 1.
 static int decode_call(int n_layers, const void *q, const void *k_new, const void *v_new,

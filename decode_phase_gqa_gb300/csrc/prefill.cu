@@ -1,0 +1,433 @@
+// Paged chunked-prefill attention: each sequence b brings n_b >= 1 new tokens
+// after the ctx_b tokens its pages already hold (a prompt, or the next chunk of
+// one, or the k draft tokens of a speculative step to verify).  Two kernels on
+// the caller's stream:
+//
+//  * append: the new keys and values go into slots ctx_b .. ctx_b + n_b - 1 of
+//    the sequence's pages, the keys rotated by the same storage recipe as the
+//    decode step's append (storage.cuh), new token i at RoPE position ctx_b + i;
+//  * attention: new token i attends over the keys 0 .. ctx_b + i (its own
+//    included, the later new ones masked), the causal attention of a prefill
+//    ("LLM inference from smollm3.go", section "Prefill: the whole prompt at
+//    once"; "Qwen3-8B inference engine from scratch in C++/CUDA", section
+//    4.4.1: the blockwise softmax over key blocks, never the whole score
+//    matrix).  With n_b = 1 it is the decode step.
+//
+// Attention kernel: a CTA takes 16 new tokens of one sequence and the 4 query
+// heads of one group (a warp per head), so one staged K/V tile serves the 4
+// heads (section 4.4.2 of the Qwen3-8B page: a group's KV is read once).
+// Key tiles of 64 tokens are gathered page by page with 16-byte cp.async into
+// a double-buffered, XOR-swizzled shared-memory ring; per tile a warp forms
+// S = Q K^T (16 x 64, m16n8k16 bf16 MMAs, fp32), the online softmax of its 16
+// rows in the log2 domain, and O += P V.  Query rows are rotated in fp32 and
+// scaled by scale * log2(e) before they are rounded to bf16.
+#include <climits>
+#include <cmath>
+
+#include "decode_common.cuh"
+#include "storage.cuh"
+
+namespace kvattn {
+
+namespace {
+
+constexpr int kPfWarps = 4;                  // query heads per CTA, one warp each
+constexpr int kPfThreads = 32 * kPfWarps;
+constexpr int kPfRows = 16;                  // new tokens per CTA (the MMA's M)
+constexpr int kPfKeys = 64;                  // keys per staged tile
+
+struct PrefillParams {
+  const __nv_bfloat16 *q, *k_new, *v_new;
+  __nv_bfloat16 *k_pages, *v_pages, *out;
+  const int32_t *block_table, *seq_starts, *ctx_lens;
+  uint32_t *status;  // KVATTN_DEV_* bits (NULL: not reported)
+  int n_seq, n_tok, n_qh, n_kvh, page_size, page_shift, max_pages, num_pages;
+  int tiles_per_seq;  // 16-token tiles the grid gives each sequence
+  int use_rope;
+  float qscale;       // scale * log2(e)
+  float2 turns[64];   // rope_theta^(-2i/d) / (2 pi) as fp32 head + remainder
+  double inv_freq[64];
+};
+
+__device__ __forceinline__ void report(const PrefillParams &p, uint32_t bits) {
+  if (p.status) atomicOr(p.status, bits);
+}
+
+// Sequence b's rows of the new-token arrays [start, start + n_new) and cached
+// count ctx; false when they do not fit the arrays or the block table.
+__device__ __forceinline__ bool seq_span(const PrefillParams &p, int b, int &start, int &n_new,
+                                         int &ctx) {
+  start = __ldg(p.seq_starts + b);
+  const int end = __ldg(p.seq_starts + b + 1);
+  ctx = __ldg(p.ctx_lens + b);
+  n_new = end - start;
+  const long long cap = (long long)p.max_pages << p.page_shift;
+  return start >= 0 && end <= p.n_tok && n_new >= 0 && ctx >= 0 && (long long)ctx + n_new <= cap;
+}
+
+// ---- append ------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid_constant__ PrefillParams p) {
+  __shared__ double inv_freq[64];
+  __shared__ float4 table[sizeof(kSinCosStep) / 16];
+  __shared__ __align__(16) uint8_t rowbuf[kPfWarps][4 * D];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < 64) inv_freq[tid] = p.inv_freq[tid];
+  for (int i = tid; i < (int)(sizeof(kSinCosStep) / 16); i += kPfThreads) table[i] = kSinCosStep[i];
+  __syncthreads();
+  const long long item = (long long)blockIdx.x * kPfWarps + warp;  // (new-token row, KV head)
+  if (item >= (long long)p.n_tok * p.n_kvh) return;
+  const int r = (int)(item / p.n_kvh), j = (int)(item - (long long)r * p.n_kvh);
+  // the sequence of row r: the last b with seq_starts[b] <= r
+  int lo = 0, hi = p.n_seq;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.seq_starts + mid) <= r)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  int start, n_new, ctx;
+  if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new) {
+    if (lane == 0) report(p, KVATTN_DEV_BAD_LEN);  // a row no valid sequence owns
+    return;
+  }
+  const int slot = ctx + (r - start);  // also the RoPE position
+  const int page = __ldg(p.block_table + (size_t)lo * p.max_pages + (slot >> p.page_shift));
+  if (page < 0 || page >= p.num_pages) {
+    if (lane == 0) report(p, KVATTN_DEV_BAD_PAGE);
+    return;
+  }
+  constexpr int CH = 2 * D / 16;  // 16-byte chunks of a row
+  uint8_t *buf = rowbuf[warp];
+  const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + ((size_t)r * p.n_kvh + j) * D);
+  const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + ((size_t)r * p.n_kvh + j) * D);
+  for (int c = lane; c < 2 * CH; c += 32)
+    reinterpret_cast<uint4 *>(buf)[c] = c < CH ? ks[c] : vs[c - CH];
+  __syncwarp();
+  stage_new_row<D, false>(slot, inv_freq, table, p.use_rope != 0, lane, buf);
+  const size_t prow = ((size_t)page * p.n_kvh + j) * p.page_size + (slot & (p.page_size - 1));
+  for (int c = lane; c < 2 * CH; c += 32) {
+    const uint4 x = reinterpret_cast<const uint4 *>(buf)[c];
+    if (c < CH)
+      reinterpret_cast<uint4 *>(p.k_pages + prow * D)[c] = x;
+    else
+      reinterpret_cast<uint4 *>(p.v_pages + prow * D)[c - CH] = x;
+  }
+}
+
+// ---- attention ---------------------------------------------------------------
+template <int D>
+struct PfCfg {
+  static constexpr int kRowB = 2 * D;                        // bytes of a bf16 row
+  static constexpr int kQBytes = kPfWarps * kPfRows * kRowB;  // the warps' query rows
+  static constexpr int kTile = kPfKeys * kRowB;              // one K or V tile
+  static constexpr int kStage = 2 * kTile;                   // K then V
+  static constexpr int kSmem = kQBytes + 2 * kStage + 2 * kPfKeys * 4 + 64 * 8;
+};
+
+// Byte offset of 16-byte chunk c of row r in a [rows][2 D] tile: the low three
+// bits of the chunk index are XORed with the row's, so the 8 rows an ldmatrix
+// reads at one chunk hit 8 different bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t sw(int r, int c) {
+  return (uint32_t)(r * PfCfg<D>::kRowB + (((c & ~7) | ((c ^ r) & 7)) << 4));
+}
+
+// 16-byte cp.async that copies `bytes` (16 or 0) and zero-fills the rest
+__device__ __forceinline__ void cp_async_16_zfill(void *dst, const void *src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_one() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_constant__ PrefillParams p) {
+  using C = PfCfg<D>;
+  constexpr int KS = D / 16;  // k-steps of Q K^T
+  constexpr int ND = D / 8;   // n-tiles of O
+  constexpr int CH = D / 8;   // 16-byte chunks of a row
+  const float kFloor = -1e30f;  // initial running maximum, below any score
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t *qs = smem;
+  uint8_t *stages = smem + C::kQBytes;
+  int *rvalid = reinterpret_cast<int *>(stages + 2 * C::kStage);  // [2][kPfKeys]
+  float2 *turns = reinterpret_cast<float2 *>(rvalid + 2 * kPfKeys);  // [64]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x / p.tiles_per_seq, qt = blockIdx.x % p.tiles_per_seq;
+  const int g = p.n_qh / p.n_kvh;
+  const int j = blockIdx.y / (g / kPfWarps);
+  const int h = j * g + (blockIdx.y % (g / kPfWarps)) * kPfWarps + warp;  // this warp's head
+  int start, n_new, ctx;
+  if (!seq_span(p, b, start, n_new, ctx)) {
+    if (qt == 0 && blockIdx.y == 0 && tid == 0) report(p, KVATTN_DEV_BAD_LEN);
+    return;
+  }
+  // more new tokens than the grid's tiles cover (a bound the caller gave)
+  if (qt == 0 && blockIdx.y == 0 && tid == 0 && n_new > p.tiles_per_seq * kPfRows)
+    report(p, KVATTN_DEV_BAD_LEN);
+  const int t0 = qt * kPfRows;
+  if (t0 >= n_new) return;
+  if (tid < 64) turns[tid] = p.turns[tid];
+  __syncthreads();
+
+  // ---- the warp's 16 query rows: rotated in fp32, scaled, rounded to bf16 ----
+  uint8_t *qw = qs + warp * kPfRows * C::kRowB;
+  for (int e = lane; e < kPfRows * (D / 2); e += 32) {
+    const int r = e / (D / 2), i = e % (D / 2);
+    float lo = 0.f, hi = 0.f;
+    if (t0 + r < n_new) {
+      const __nv_bfloat16 *qr = p.q + ((size_t)(start + t0 + r) * p.n_qh + h) * D;
+      lo = __bfloat162float(qr[i]);
+      hi = __bfloat162float(qr[i + D / 2]);
+      if (p.use_rope) {
+        float sn, cs;
+        sincospif(2.f * frac_turns(ctx + t0 + r, turns[i]), &sn, &cs);
+        const float a = lo * cs - hi * sn, bb = hi * cs + lo * sn;
+        lo = a;
+        hi = bb;
+      }
+    }
+    *reinterpret_cast<__nv_bfloat16 *>(qw + sw<D>(r, i / 8) + (i % 8) * 2) =
+        __float2bfloat16_rn(lo * p.qscale);
+    *reinterpret_cast<__nv_bfloat16 *>(qw + sw<D>(r, (i + D / 2) / 8) + ((i + D / 2) % 8) * 2) =
+        __float2bfloat16_rn(hi * p.qscale);
+  }
+  __syncwarp();
+  uint32_t qf[KS][4];  // A fragments: rows g, g + 8; k 2t.., 2t + 8..
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+    ldmatrix_x4(qf[ks], smem_addr(qw) + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)));
+
+  // ---- key tiles ----------------------------------------------------------------
+  // keys the CTA's last valid row sees: 0 .. ctx + min(n_new, t0 + 16) - 1
+  const int n_keys = ctx + min(n_new, t0 + kPfRows);
+  const int n_tiles = (n_keys + kPfKeys - 1) / kPfKeys;
+  auto load_tile = [&](int kt, int s) {
+    uint8_t *Ks = stages + s * C::kStage, *Vs = Ks + C::kTile;
+    for (int idx = tid; idx < kPfKeys * CH; idx += kPfThreads) {
+      const int r = idx / CH, c = idx % CH;
+      const int tok = kt * kPfKeys + r;
+      const __nv_bfloat16 *srck = p.k_pages, *srcv = p.v_pages;
+      int bytes = 0;
+      if (tok < n_keys) {
+        const int page = __ldg(p.block_table + (size_t)b * p.max_pages + (tok >> p.page_shift));
+        if (page >= 0 && page < p.num_pages) {
+          const size_t prow = ((size_t)page * p.n_kvh + j) * p.page_size + (tok & (p.page_size - 1));
+          srck = p.k_pages + prow * D + c * 8;
+          srcv = p.v_pages + prow * D + c * 8;
+          bytes = 16;
+        } else if (c == 0) {
+          report(p, KVATTN_DEV_BAD_PAGE);
+        }
+      }
+      cp_async_16_zfill(Ks + sw<D>(r, c), srck, bytes);
+      cp_async_16_zfill(Vs + sw<D>(r, c), srcv, bytes);
+      if (c == 0) rvalid[s * kPfKeys + r] = bytes != 0;
+    }
+    cp_async_commit();
+  };
+
+  float o[ND][4];
+#pragma unroll
+  for (int nd = 0; nd < ND; ++nd)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[nd][k] = 0.f;
+  float m[2] = {kFloor, kFloor}, l[2] = {0.f, 0.f};
+  // absolute positions of this lane's rows g and g + 8
+  const int qpos[2] = {ctx + t0 + (lane >> 2), ctx + t0 + (lane >> 2) + 8};
+
+  load_tile(0, 0);
+  for (int kt = 0; kt < n_tiles; ++kt) {
+    if (kt + 1 < n_tiles)
+      load_tile(kt + 1, (kt + 1) & 1);
+    else
+      cp_async_commit();  // (an empty group: the wait below still means tile kt)
+    cp_async_wait_one();
+    __syncthreads();
+    const uint8_t *Ks = stages + (kt & 1) * C::kStage, *Vs = Ks + C::kTile;
+    const int *rv = rvalid + (kt & 1) * kPfKeys;
+    const uint32_t kb = smem_addr(Ks), vb = smem_addr(Vs);
+
+    // S = Q K^T over the tile's 64 keys: 8 n-tiles of 8 keys
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) s[nt][k] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; nt += 2) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        // matrices: keys nt*8.. at chunks 2ks, 2ks+1, then keys (nt+1)*8.. at the same
+        uint32_t kf[4];
+        const int mi = lane >> 3;
+        ldmatrix_x4(kf, kb + sw<D>((nt + (mi >> 1)) * 8 + (lane & 7), 2 * ks + (mi & 1)));
+        mma_bf16_16816(s[nt], qf[ks], kf[0], kf[1]);
+        mma_bf16_16816(s[nt + 1], qf[ks], kf[2], kf[3]);
+      }
+    }
+    // causal and page masks, running maxima of rows g and g + 8
+    const int key0 = kt * kPfKeys;
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
+        const bool ok = key0 + kr <= qpos[e >> 1] && rv[kr] != 0;
+        s[nt][e] = ok ? s[nt][e] : -INFINITY;
+        mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+      }
+    float alpha[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+      const float mn = fmaxf(m[rr], mx[rr]);
+      alpha[rr] = ex2_approx(m[rr] - mn);
+      m[rr] = mn;
+      l[rr] *= alpha[rr];
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[nt][e] = ex2_approx(s[nt][e] - m[e >> 1]);
+        l[e >> 1] += s[nt][e];
+      }
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd) {
+      o[nd][0] *= alpha[0];
+      o[nd][1] *= alpha[0];
+      o[nd][2] *= alpha[1];
+      o[nd][3] *= alpha[1];
+    }
+    // O += P V: P's accumulator layout is the next MMA's A layout, keys
+    // 16 kk .. 16 kk + 15 from n-tiles 2 kk, 2 kk + 1
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t a[4] = {pack_bf16(s[2 * kk][0], s[2 * kk][1]), pack_bf16(s[2 * kk][2], s[2 * kk][3]),
+                             pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                             pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+#pragma unroll
+      for (int nd = 0; nd < ND; nd += 2) {
+        // matrices: keys 16kk..+7 and 16kk+8..+15 at chunk nd, then at chunk nd+1
+        uint32_t vf[4];
+        ldmatrix_x4_trans(vf, vb + sw<D>(16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8, nd + (lane >> 4)));
+        mma_bf16_16816(o[nd], a, vf[0], vf[1]);
+        mma_bf16_16816(o[nd + 1], a, vf[2], vf[3]);
+      }
+    }
+    __syncthreads();  // the stage is rewritten two tiles on
+  }
+  cp_async_wait_all();
+
+  // ---- rows g and g + 8 of head h: O / l, rounded to bf16 ----------------------
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
+  }
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int t = t0 + (lane >> 2) + 8 * rr;
+    if (t >= n_new) continue;
+    const float f = l[rr] > 0.f ? 1.f / l[rr] : 0.f;  // no visible key: a zero row
+    __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
+        p.out + ((size_t)(start + t) * p.n_qh + h) * D + 2 * (lane & 3));
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd)
+      dst[4 * nd] = __floats2bfloat162_rn(o[nd][2 * rr] * f, o[nd][2 * rr + 1] * f);
+  }
+}
+
+template <int D>
+cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
+  using C = PfCfg<D>;
+  // (set on every call: the attribute belongs to the current device)
+  cudaError_t err = cudaFuncSetAttribute(prefill_attn_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (err != cudaSuccess) return err;
+  const long long items = (long long)p.n_tok * p.n_kvh;
+  prefill_append_kernel<D><<<(unsigned)((items + kPfWarps - 1) / kPfWarps), kPfThreads, 0, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const dim3 grid((unsigned)(p.n_seq * p.tiles_per_seq), (unsigned)(p.n_qh / kPfWarps));
+  prefill_attn_kernel<D><<<grid, kPfThreads, C::kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+bool pf_aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+}  // namespace
+
+// host frequency tables (kvattn_api.cu)
+void rope_tables(float rope_theta, int head_dim, double *inv_freq, float2 *turns);
+
+}  // namespace kvattn
+
+extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                              void *v_pages, const int32_t *block_table,
+                              const int32_t *seq_starts, const int32_t *ctx_lens, void *out,
+                              int n_seq, int n_tok, int n_qh, int n_kvh, int head_dim,
+                              int page_size, float rope_theta, float scale, void *stream,
+                              int max_pages_per_seq, int num_pages, int max_new_tokens,
+                              uint32_t *dev_status) {
+  using namespace kvattn;
+  if (n_seq < 0 || n_tok < 0 || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 ||
+      max_pages_per_seq < 1 || num_pages < 1 || max_new_tokens < 0)
+    return KVATTN_EINVAL;
+  if (!std::isfinite(scale) || std::isnan(rope_theta) || std::isinf(rope_theta))
+    return KVATTN_EINVAL;
+  if (head_dim != 64 && head_dim != 128) return KVATTN_EUNSUPPORTED;
+  if ((n_qh / n_kvh) % kPfWarps != 0) return KVATTN_EUNSUPPORTED;  // 4 heads to a CTA
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128 &&
+      page_size != 256)
+    return KVATTN_EUNSUPPORTED;
+  if (n_seq > KVATTN_MAX_SEQS || n_qh > 1024) return KVATTN_EUNSUPPORTED;
+  if ((long long)max_pages_per_seq * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
+  if ((long long)num_pages * n_kvh * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
+  const long long tiles = ((long long)max_new_tokens + kPfRows - 1) / kPfRows;
+  if ((long long)n_seq * tiles > (long long)INT_MAX || (long long)n_tok * n_kvh > (1LL << 40))
+    return KVATTN_EUNSUPPORTED;
+  if (n_seq == 0 || n_tok == 0 || max_new_tokens == 0) return KVATTN_OK;  // nothing to do
+  if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_starts ||
+      !ctx_lens || !out)
+    return KVATTN_EINVAL;
+  if (!pf_aligned(q, 16) || !pf_aligned(k_new, 16) || !pf_aligned(v_new, 16) ||
+      !pf_aligned(k_pages, 16) || !pf_aligned(v_pages, 16) || !pf_aligned(out, 4) ||
+      !pf_aligned(block_table, 4) || !pf_aligned(seq_starts, 4) || !pf_aligned(ctx_lens, 4) ||
+      (dev_status && !pf_aligned(dev_status, 4)))
+    return KVATTN_EINVAL;
+  PrefillParams p = {};
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  p.k_pages = static_cast<__nv_bfloat16 *>(k_pages);
+  p.v_pages = static_cast<__nv_bfloat16 *>(v_pages);
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.block_table = block_table;
+  p.seq_starts = seq_starts;
+  p.ctx_lens = ctx_lens;
+  p.status = dev_status;
+  p.n_seq = n_seq;
+  p.n_tok = n_tok;
+  p.n_qh = n_qh;
+  p.n_kvh = n_kvh;
+  p.page_size = page_size;
+  for (int s = page_size; s > 1; s >>= 1) ++p.page_shift;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.tiles_per_seq = (int)tiles;
+  p.use_rope = rope_theta > 0.0f ? 1 : 0;
+  p.qscale = (float)((double)scale * 1.4426950408889634);
+  rope_tables(rope_theta, head_dim, p.inv_freq, p.turns);
+  const cudaError_t err = head_dim == 64 ? launch_prefill_t<64>(p, static_cast<cudaStream_t>(stream))
+                                         : launch_prefill_t<128>(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KVATTN_OK : KVATTN_ECUDA;
+}

@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvattn_decode_layers.argtypes = [I] + dec + [P]
         L.kvattn_decode_layers.restype = I
         L.kvattn_decode_noalloc.argtypes = dec[:-2] + [P]
+        L.kvattn_prefill.argtypes = [P] * 9 + [I] * 6 + [F, F, P, I, I, I, P]
+        L.kvattn_prefill.restype = I
         L.kvattn_decode_noalloc.restype = I
         L.kvattn_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         L.kvattn_read_device_status.restype = I
@@ -240,6 +242,50 @@ def kvattn_decode_layers(q, k_new, v_new, k_pages, v_pages, block_table, seq_len
         None if flags is None else ctypes.cast(flags, ctypes.c_void_p))
     if rc:
         raise KvattnError(rc, "kvattn_decode_layers")
+
+
+def kvattn_prefill(q, k_new, v_new, k_pages, v_pages, block_table, seq_starts, ctx_lens, out,
+                   *, rope_theta: float, scale: float, max_new_tokens: int,
+                   dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Paged chunked prefill (kvattn_prefill): append the new tokens, then
+    causal attention over the cache and the earlier new tokens.
+
+    Shapes: q/out [T, Hq, d] bf16 (the new tokens of all sequences back to
+    back); k_new/v_new [T, Hk, d] bf16; k_pages/v_pages [num_pages, Hk, page, d]
+    bf16; block_table [B, max_pages] int32; seq_starts [B + 1] int32; ctx_lens
+    [B] int32; dev_status: None or a 1-element uint32/int32 device tensor that
+    receives KVATTN_DEV_* bits.
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kvattn_prefill runs on CUDA tensors only")
+    bf = (torch.bfloat16,)
+    _check(q, "q", bf, 3, dev)
+    _check(out, "out", bf, 3, dev)
+    _check(k_new, "k_new", bf, 3, dev)
+    _check(v_new, "v_new", bf, 3, dev)
+    _check(k_pages, "k_pages", bf, 4, dev)
+    _check(v_pages, "v_pages", bf, 4, dev)
+    _check(block_table, "block_table", (torch.int32,), 2, dev)
+    _check(seq_starts, "seq_starts", (torch.int32,), 1, dev)
+    _check(ctx_lens, "ctx_lens", (torch.int32,), 1, dev)
+    n_tok, n_qh, d = q.shape
+    num_pages, n_kvh, page, d2 = k_pages.shape
+    n_seq = ctx_lens.shape[0]
+    if (d2 != d or tuple(out.shape) != tuple(q.shape) or tuple(k_new.shape) != (n_tok, n_kvh, d)
+            or tuple(v_new.shape) != (n_tok, n_kvh, d) or tuple(v_pages.shape) != tuple(k_pages.shape)
+            or block_table.shape[0] != n_seq or seq_starts.shape[0] != n_seq + 1):
+        raise ValueError("inconsistent shapes")
+    if dev_status is not None:
+        _check(dev_status, "dev_status", (torch.int32, torch.uint32), 1, dev)
+    rc = load().kvattn_prefill(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+        block_table.data_ptr(), seq_starts.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
+        n_seq, n_tok, n_qh, n_kvh, d, page, float(rope_theta), float(scale),
+        _stream_handle(stream, dev), block_table.shape[1], num_pages, int(max_new_tokens),
+        _ptr(dev_status))
+    if rc:
+        raise KvattnError(rc, "kvattn_prefill")
 
 
 def kvattn_read_device_status(workspace: torch.Tensor, stream=None) -> int:

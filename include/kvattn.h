@@ -213,6 +213,49 @@ int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const v
                          size_t workspace_bytes, const uint8_t *layer_rope);
 
 /*
+ * Paged chunked prefill: each sequence b brings n_b >= 0 new tokens after the
+ * ctx_lens[b] tokens its pages already hold (a prompt, the next chunk of a
+ * long one, or the draft tokens of a speculative step to verify).  The new
+ * keys and values are appended to slots ctx_lens[b] .. ctx_lens[b] + n_b - 1
+ * (keys rotated at those positions with the storage recipe of kvattn_decode),
+ * then new token i attends over keys 0 .. ctx_lens[b] + i: causal attention
+ * over the cache and the earlier new tokens ("LLM inference from
+ * smollm3.go", section "Prefill: the whole prompt at once"; "Qwen3-8B
+ * inference engine from scratch in C++/CUDA", section 4.4.1).  A sequence
+ * with n_b = 1 gets exactly the decode step (with seq_lens = positions =
+ * ctx_lens).  bf16 cache only.
+ *
+ * q, out       device bf16 [n_tok, n_qh, head_dim]: the new tokens of all
+ *              sequences back to back, 16-byte aligned (out 4-byte).
+ * k_new, v_new device bf16 [n_tok, n_kvh, head_dim], 16-byte aligned.
+ * k_pages,     device bf16 [num_pages, n_kvh, page_size, head_dim], as for
+ * v_pages      kvattn_decode; the pages of every appended slot must be
+ *              assigned in block_table.
+ * block_table  device int32 [n_seq, max_pages_per_seq].
+ * seq_starts   device int32 [n_seq + 1]: sequence b's new tokens are rows
+ *              seq_starts[b] .. seq_starts[b + 1] - 1 of q, k_new, v_new, out.
+ * ctx_lens     device int32 [n_seq]: tokens cached before the call; new token
+ *              i has slot and RoPE position ctx_lens[b] + i.
+ * n_qh / n_kvh must be a multiple of 4 (a CTA serves 4 query heads of a group),
+ *              else KVATTN_EUNSUPPORTED.
+ * max_new_tokens  an upper bound on every n_b; it sizes the launch (a
+ *              sequence with more new tokens has the rest left out and
+ *              reported as KVATTN_DEV_BAD_LEN).
+ * dev_status   device uint32, 4-byte aligned, or NULL: KVATTN_DEV_BAD_LEN is
+ *              OR-ed in for a sequence whose rows or slots do not fit (it is
+ *              skipped), KVATTN_DEV_BAD_PAGE for a page outside [0, num_pages)
+ *              (its tokens are left out, no append lands there).
+ * Other arguments, checks and errors as for kvattn_decode.  No workspace: a
+ * CTA finishes its tokens' attention itself.
+ */
+int kvattn_prefill(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                   void *v_pages, const int32_t *block_table, const int32_t *seq_starts,
+                   const int32_t *ctx_lens, void *out, int n_seq, int n_tok, int n_qh, int n_kvh,
+                   int head_dim, int page_size, float rope_theta, float scale, void *stream,
+                   int max_pages_per_seq, int num_pages, int max_new_tokens,
+                   uint32_t *dev_status);
+
+/*
  * kvattn_decode for callers that can neither pass a workspace nor let the
  * library allocate one.  The source pages have no counterpart of this entry
  * point.

@@ -36,3 +36,35 @@ def oracle_decode(wl: W.Workload, h, seq_mask=None, n_threads=0):
                             h["seq_lens"], h["positions"], wl.rope_theta, wl.scale,
                             ks, vs, seq_mask=seq_mask, n_threads=n_threads)
     return out, st, kp, vp, ks, vs
+
+
+def oracle_prefill(h, seq_starts, ctx_lens, rope_theta, scale, seqs=None):
+    """The oracle's chunked prefill, as the decode steps it is made of: step i
+    appends new token i of every sequence that has one (slot and RoPE position
+    ctx + i) and attends over the cache up to it, which is the causal
+    attention over the cache and the earlier new tokens.
+
+    h: q [T, Hq, d], k_new / v_new [T, Hk, d] (bf16 bits), k_pages / v_pages,
+    block_table [B, max_pages].  `seqs`: the sequences to run (default all).
+    Returns (out float64 [T, Hq, d], NaN for rows not run; status; the pools
+    after the appends).
+    """
+    import oracle
+    kp, vp = h["k_pages"].copy(), h["v_pages"].copy()
+    starts = np.asarray(seq_starts, np.int64)
+    ctx = np.asarray(ctx_lens, np.int64)
+    n_new = np.diff(starts)
+    chosen = np.arange(len(ctx)) if seqs is None else np.asarray(seqs)
+    out = np.full(h["q"].shape, np.nan)
+    st = 0
+    for i in range(int(n_new[chosen].max(initial=0))):
+        act = chosen[n_new[chosen] > i]
+        rows = starts[act] + i
+        o, s = oracle.decode(np.ascontiguousarray(h["q"][rows]), np.ascontiguousarray(h["k_new"][rows]),
+                             np.ascontiguousarray(h["v_new"][rows]), kp, vp,
+                             np.ascontiguousarray(h["block_table"][act]),
+                             (ctx[act] + i).astype(np.int32), (ctx[act] + i).astype(np.int32),
+                             rope_theta, scale)
+        out[rows] = o
+        st |= s
+    return out, st, kp, vp

@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "kvattn_decode", "kvattn_decode_layers", "kvattn_decode_noalloc",
-        "kvattn_decode_splits", "kvattn_read_device_status",
+        "kvattn_decode_splits", "kvattn_prefill", "kvattn_read_device_status",
         "kvattn_status_string", "kvattn_version", "kvattn_workspace_init",
         "kvattn_workspace_size", "kvattn_workspace_size_layers"])
 
@@ -195,3 +195,32 @@ def test_layers_entry_fails_closed(lib, n_layers, kw, code):
         kw = dict(workspace_bytes=K.kvattn_workspace_size(a["n_seq"], a["n_qh"], a["n_kvh"],
                                                           a["head_dim"]))
     assert call_layers(lib, n_layers, **kw) == code
+
+
+def prefill_args(**kw):
+    a = dict(q=FAKE, k_new=FAKE, v_new=FAKE, k_pages=FAKE, v_pages=FAKE, block_table=FAKE,
+             seq_starts=FAKE, ctx_lens=FAKE, out=FAKE, n_seq=2, n_tok=40, n_qh=8, n_kvh=2,
+             head_dim=64, page_size=16, rope_theta=1e4, scale=0.125, stream=None,
+             max_pages_per_seq=4, num_pages=8, max_new_tokens=32, dev_status=None)
+    a.update(kw)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_seq=-1), K.KVATTN_EINVAL),
+    (dict(n_tok=-1), K.KVATTN_EINVAL),
+    (dict(n_qh=6, n_kvh=4), K.KVATTN_EINVAL),
+    (dict(n_qh=6, n_kvh=2), K.KVATTN_EUNSUPPORTED),     # groups of 3 heads
+    (dict(head_dim=96), K.KVATTN_EUNSUPPORTED),
+    (dict(page_size=8), K.KVATTN_EUNSUPPORTED),
+    (dict(max_new_tokens=-1), K.KVATTN_EINVAL),
+    (dict(scale=float("nan")), K.KVATTN_EINVAL),
+    (dict(q=None), K.KVATTN_EINVAL),
+    (dict(seq_starts=None), K.KVATTN_EINVAL),
+    (dict(k_new=FAKE + 8), K.KVATTN_EINVAL),
+    (dict(dev_status=FAKE + 2), K.KVATTN_EINVAL),
+    (dict(n_tok=0), K.KVATTN_OK),
+    (dict(n_seq=0), K.KVATTN_OK),
+])
+def test_prefill_entry_fails_closed(lib, kw, code):
+    assert lib.kvattn_prefill(*prefill_args(**kw).values()) == code

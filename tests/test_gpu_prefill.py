@@ -1,0 +1,125 @@
+"""Paged chunked prefill (kvattn_prefill) against the oracle (needs a GB300).
+
+The oracle's prefill is the decode steps it is made of (tests/helpers.py,
+oracle_prefill): step i appends new token i of every sequence and attends over
+the cache up to it.  Checks: the whole pool bit for bit after the appends,
+every output row within max-abs 2e-2 / mean-abs 2e-3, the status word.
+"""
+import numpy as np
+import pytest
+import torch
+
+from decode_phase_gqa_gb300 import kvattn as K
+from decode_phase_gqa_gb300 import workloads as W
+from tests.gpu_helpers import assert_close, out_f64, pool_bits, run_gpu, to_dev
+from tests.helpers import bits, host_inputs, oracle_decode, oracle_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def make_case(n_qh, n_kvh, ctx, n_new, d=128, page=16, seed=0, theta=1e6):
+    """A pool and table covering ctx + n_new tokens per sequence, and the new
+    tokens' q / k / v (N(0,1), bf16), back to back."""
+    ctx = np.asarray(ctx, np.int32)
+    n_new = np.asarray(n_new, np.int32)
+    wl = W.make_workload("custom", seed=seed, n_seq=len(ctx), n_qh=n_qh, n_kvh=n_kvh,
+                         head_dim=d, page_size=page, rope_theta=theta, kv_dtype="bf16",
+                         lengths=[int(x) for x in np.maximum(ctx + n_new - 1, 0)], spare=0.1)
+    h = host_inputs(wl)
+    g = torch.Generator().manual_seed(1000 + seed)
+    T = int(n_new.sum())
+    h["q"] = bits(torch.randn((T, n_qh, d), generator=g).to(torch.bfloat16))
+    h["k_new"] = bits(torch.randn((T, n_kvh, d), generator=g).to(torch.bfloat16))
+    h["v_new"] = bits(torch.randn((T, n_kvh, d), generator=g).to(torch.bfloat16))
+    starts = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    return wl, h, starts, ctx
+
+
+def run_prefill(wl, h, starts, ctx, max_new=None):
+    d = to_dev(h)
+    ss = torch.from_numpy(starts).cuda()
+    cl = torch.from_numpy(np.ascontiguousarray(ctx)).cuda()
+    out = torch.full_like(d["q"], float("nan"))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mx = int(np.diff(starts).max(initial=0)) if max_new is None else max_new
+    K.kvattn_prefill(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
+                     d["block_table"], ss, cl, out, rope_theta=wl.rope_theta, scale=wl.scale,
+                     max_new_tokens=mx, dev_status=st)
+    torch.cuda.synchronize()
+    return out, int(st.item()), d
+
+
+def check(wl, h, starts, ctx):
+    out, st, d = run_prefill(wl, h, starts, ctx)
+    ref, ost, kp, vp = oracle_prefill(h, starts, ctx, wl.rope_theta, wl.scale)
+    assert st == 0 and ost == 0, (st, ost)
+    assert np.array_equal(pool_bits(d["k_pages"]), kp)
+    assert np.array_equal(pool_bits(d["v_pages"]), vp)
+    return assert_close(out_f64(out), ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n_qh,n_kvh", [(4, 1), (16, 4), (8, 2)])
+def test_prompts_into_empty_caches(d, n_qh, n_kvh):
+    # ragged prompts: one token, exactly a 16-token tile, one past, several key tiles
+    wl, h, starts, ctx = make_case(n_qh, n_kvh, [0, 0, 0, 0], [1, 16, 17, 150], d=d, seed=d + n_qh)
+    check(wl, h, starts, ctx)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_chunked_prefill_after_cached_tokens(d):
+    wl, h, starts, ctx = make_case(16, 4, [100, 0, 37, 511], [20, 5, 64, 33], d=d, seed=3)
+    check(wl, h, starts, ctx)
+
+
+def test_speculative_verification_of_draft_tokens():
+    """Four draft tokens per sequence over long caches (Qwen3-8B-shaped heads)."""
+    wl, h, starts, ctx = make_case(32, 8, [1000, 3, 257, 4000], [4, 4, 4, 4], d=128, seed=5)
+    check(wl, h, starts, ctx)
+
+
+@pytest.mark.parametrize("page", [32, 64, 256])
+def test_page_sizes(page):
+    wl, h, starts, ctx = make_case(8, 2, [30, 300, 0], [40, 9, 70], d=64, page=page, seed=page)
+    check(wl, h, starts, ctx)
+
+
+def test_long_prompt():
+    wl, h, starts, ctx = make_case(16, 4, [0, 64], [600, 333], d=128, seed=7)
+    check(wl, h, starts, ctx)
+
+
+def test_one_new_token_is_the_decode_step():
+    """n_b = 1 is kvattn_decode with seq_lens = positions = ctx: the same
+    appended rows bit for bit, outputs within the tolerance of the oracle."""
+    wl, h, starts, ctx = make_case(16, 4, [50, 0, 300, 1023], [1, 1, 1, 1], d=128, seed=9)
+    out, st, d = run_prefill(wl, h, starts, ctx)
+    hd = dict(h, seq_lens=ctx.copy(), positions=ctx.copy())
+    wld = W.with_lengths(wl, ctx)
+    dd = to_dev(hd)
+    dec, st2, _ = run_gpu(wld, dd)
+    assert st == st2 == 0
+    assert np.array_equal(pool_bits(d["k_pages"]), pool_bits(dd["k_pages"]))
+    assert np.array_equal(pool_bits(d["v_pages"]), pool_bits(dd["v_pages"]))
+    ref, *_ = oracle_decode(wld, hd)
+    assert_close(out_f64(out), ref)
+    assert_close(out_f64(dec), ref)
+
+
+def test_bad_page_and_overfull_sequence_are_reported():
+    wl, h, starts, ctx = make_case(8, 2, [40, 20, 10], [30, 10, 10], d=64, seed=11)
+    bt = h["block_table"].copy()
+    bt[0, 1] = 10 ** 6           # cached tokens 16-31 of sequence 0 left out
+    h["block_table"] = bt
+    cap = bt.shape[1] * wl.page_size
+    ctx = ctx.copy()
+    ctx[2] = cap - 5             # 10 new tokens cannot fit: sequence 2 is skipped
+    out, st, d = run_prefill(wl, h, starts, ctx)
+    assert st & K.KVATTN_DEV_BAD_PAGE and st & K.KVATTN_DEV_BAD_LEN
+    got = out_f64(out)
+    assert np.all(np.isnan(got[starts[2]:starts[3]])), "the skipped sequence's rows were written"
+    ref, ost, kp, vp = oracle_prefill(h, starts, ctx, wl.rope_theta, wl.scale, seqs=[0, 1])
+    assert ost & 2
+    assert_close(got[:starts[2]], ref[:starts[2]])
+    assert np.array_equal(pool_bits(d["k_pages"]), kp)
+    assert np.array_equal(pool_bits(d["v_pages"]), vp)
