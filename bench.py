@@ -455,6 +455,91 @@ def cpu_baseline(name: str, seed: int, budget_s: float = 10.0):
                       f"{wl.layers} layer(s) costs {wl.layers}x one layer"}
 
 
+def measured_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def run_prefill_config(kind, steps, warmup, device, stream, seed=0):
+    """kvattn_prefill timed from a CUDA graph of one call.
+
+    prefill: SmolLM3-3B-shaped heads (16/4, d 128), 8 prompts of 2048 tokens
+             into empty caches (compute-bound: causal attention FLOPs);
+    verify:  Qwen3-8B-shaped heads (32/8, d 128) over the Qwen3 workload's 64
+             cache lengths, 4 draft tokens each (a speculative step's check;
+             bandwidth-bound: the cached K/V are read once per group).
+    """
+    from decode_phase_gqa_gb300 import kvattn as K
+    if kind == "prefill":
+        n_qh, n_kvh, d, theta = 16, 4, 128, 1e6
+        ctx = np.zeros(8, np.int64)
+        n_new = np.full(8, 2048, np.int64)
+    else:
+        q3 = W.make_workload("qwen3", seed=seed)
+        n_qh, n_kvh, d, theta = q3.n_qh, q3.n_kvh, q3.head_dim, q3.rope_theta
+        ctx = q3.seq_lens.astype(np.int64)
+        n_new = np.full(len(ctx), 4, np.int64)
+    wl = W.make_workload("custom", seed=seed, n_seq=len(ctx), n_qh=n_qh, n_kvh=n_kvh,
+                         head_dim=d, page_size=16, rope_theta=theta, kv_dtype="bf16",
+                         lengths=[int(x) for x in ctx + n_new - 1], spare=0.05)
+    t = W.make_tensors(wl, device=device)
+    g = torch.Generator(device=device).manual_seed(seed + 77)
+    T = int(n_new.sum())
+    q = torch.randn((T, n_qh, d), generator=g, device=device).to(torch.bfloat16)
+    kn = torch.randn((T, n_kvh, d), generator=g, device=device).to(torch.bfloat16)
+    vn = torch.randn((T, n_kvh, d), generator=g, device=device).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    bt = torch.from_numpy(wl.block_table).to(device)
+    ss = torch.from_numpy(np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)).to(device)
+    cl = torch.from_numpy(ctx.astype(np.int32)).to(device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def call():
+        K.kvattn_prefill(q, kn, vn, t["k_pages"], t["v_pages"], bt, ss, cl, out,
+                         rope_theta=theta, scale=1.0 / math.sqrt(d), max_new_tokens=int(n_new.max()),
+                         dev_status=st, stream=stream)
+
+    with torch.cuda.stream(stream):
+        call()   # per-device set-up outside the capture
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            call()
+        for _ in range(warmup):
+            gr.replay()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            gr.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"prefill device status {int(st.item()):#x}")
+    ms = t0.elapsed_time(t1) / steps
+    keys = float(np.sum(n_new * ctx + n_new * (n_new + 1) // 2))  # sum over new tokens of keys seen
+    flops = 4.0 * d * n_qh * keys
+    kv_bytes = float(np.sum(ctx + n_new)) * n_kvh * d * 2 * 2
+    peak_tf, peak_kind = measured_bf16_peak()
+    peak_gb, _ = measured_peak()
+    res = {"config": kind, "entry": "kvattn_prefill",
+           "workload": ("SmolLM3-3B-shaped heads 16/4, d128: 8 prompts x 2048 new tokens, empty caches"
+                        if kind == "prefill" else
+                        "Qwen3-8B-shaped heads 32/8, d128: 64 sequences, L log-uniform [128,8192], "
+                        "4 draft tokens each"),
+           "steps": steps, "ms_per_step": ms, "new_tokens_per_s": T / (ms / 1e3),
+           "attn_tflops": flops / (ms / 1e3) / 1e12, "bf16_peak_tflops": peak_tf,
+           "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / peak_tf, "peak_kind": peak_kind,
+           "kv_read_gbs": kv_bytes / (ms / 1e3) / 1e9,
+           "kv_read_frac_of_peak": kv_bytes / (ms / 1e3) / 1e9 / peak_gb}
+    del t, q, kn, vn, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_config(name, steps, warmup, rank, world, device, stream, with_e2e=True, layers=None,
                layered=False):
     case = NativeCase(name, seed=1000 * rank, device=device, layers=layers, layered=layered)
@@ -564,6 +649,8 @@ def native(args, rank, world, local):
                               "calls_per_step": r["calls_per_step"]})
                 del r
                 torch.cuda.empty_cache()
+        for kind, k in (("prefill", 20), ("verify", 200)):
+            extra.append(run_prefill_config(kind, k, 3, device, stream))
         line["per_config"] = extra
     return line
 
