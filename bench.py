@@ -496,11 +496,12 @@ def run_prefill_config(kind, steps, warmup, device, stream, seed=0):
     ss = torch.from_numpy(np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)).to(device)
     cl = torch.from_numpy(ctx.astype(np.int32)).to(device)
     st = torch.zeros(1, dtype=torch.int32, device=device)
+    ws = torch.empty(K.kvattn_prefill_workspace_size(T, n_qh, d), dtype=torch.uint8, device=device)
 
     def call():
         K.kvattn_prefill(q, kn, vn, t["k_pages"], t["v_pages"], bt, ss, cl, out,
                          rope_theta=theta, scale=1.0 / math.sqrt(d), max_new_tokens=int(n_new.max()),
-                         dev_status=st, stream=stream)
+                         dev_status=st, workspace=ws, stream=stream)
 
     with torch.cuda.stream(stream):
         call()   # per-device set-up outside the capture
@@ -535,7 +536,7 @@ def run_prefill_config(kind, steps, warmup, device, stream, seed=0):
            "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / peak_tf, "peak_kind": peak_kind,
            "kv_read_gbs": kv_bytes / (ms / 1e3) / 1e9,
            "kv_read_frac_of_peak": kv_bytes / (ms / 1e3) / 1e9 / peak_gb}
-    del t, q, kn, vn, out
+    del t, q, kn, vn, out, ws
     torch.cuda.empty_cache()
     return res
 

@@ -21,6 +21,7 @@
 // S = Q K^T (16 x 64, m16n8k16 bf16 MMAs, fp32), the online softmax of its 16
 // rows in the log2 domain, and O += P V.  Query rows are rotated in fp32 and
 // scaled by scale * log2(e) before they are rounded to bf16.
+#include <algorithm>
 #include <climits>
 #include <cmath>
 
@@ -43,6 +44,9 @@ struct PrefillParams {
   uint32_t *status;  // KVATTN_DEV_* bits (NULL: not reported)
   int n_seq, n_tok, n_qh, n_kvh, page_size, page_shift, max_pages, num_pages;
   int tiles_per_seq;  // 16-token tiles the grid gives each sequence
+  int n_splits;       // CTAs sharing one query tile's key tiles (strided)
+  float *part;        // n_splits > 1: [n_splits][n_tok][n_qh][D + 2] partial
+                      // states (o relative to 2^m, m, l; log2 units)
   int use_rope;
   float qscale;       // scale * log2(e)
   float2 turns[64];   // rope_theta^(-2i/d) / (2 pi) as fp32 head + remainder
@@ -241,16 +245,21 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_c
   // absolute positions of this lane's rows g and g + 8
   const int qpos[2] = {ctx + t0 + (lane >> 2), ctx + t0 + (lane >> 2) + 8};
 
-  load_tile(0, 0);
-  for (int kt = 0; kt < n_tiles; ++kt) {
-    if (kt + 1 < n_tiles)
-      load_tile(kt + 1, (kt + 1) & 1);
+  // this CTA's key tiles: z, z + S, z + 2 S, ... (split z of S)
+  const int z = blockIdx.z, S = p.n_splits;
+  if (z < n_tiles)
+    load_tile(z, 0);
+  else
+    cp_async_commit();
+  for (int it = 0, kt = z; kt < n_tiles; ++it, kt += S) {
+    if (kt + S < n_tiles)
+      load_tile(kt + S, (it + 1) & 1);
     else
       cp_async_commit();  // (an empty group: the wait below still means tile kt)
     cp_async_wait_one();
     __syncthreads();
-    const uint8_t *Ks = stages + (kt & 1) * C::kStage, *Vs = Ks + C::kTile;
-    const int *rv = rvalid + (kt & 1) * kPfKeys;
+    const uint8_t *Ks = stages + (it & 1) * C::kStage, *Vs = Ks + C::kTile;
+    const int *rv = rvalid + (it & 1) * kPfKeys;
     const uint32_t kb = smem_addr(Ks), vb = smem_addr(Vs);
 
     // S = Q K^T over the tile's 64 keys: 8 n-tiles of 8 keys
@@ -333,6 +342,20 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_c
     l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
     l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
   }
+  if (S > 1) {  // a partial state per row, merged by prefill_merge_kernel
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int t = t0 + (lane >> 2) + 8 * rr;
+      if (t >= n_new) continue;
+      float *rec = p.part + (((size_t)z * p.n_tok + start + t) * p.n_qh + h) * (D + 2);
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd)
+        *reinterpret_cast<float2 *>(rec + 8 * nd + 2 * (lane & 3)) =
+            make_float2(o[nd][2 * rr], o[nd][2 * rr + 1]);
+      if ((lane & 3) == 0) *reinterpret_cast<float2 *>(rec + D) = make_float2(m[rr], l[rr]);
+    }
+    return;
+  }
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int t = t0 + (lane >> 2) + 8 * rr;
@@ -346,6 +369,48 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_c
   }
 }
 
+// ---- merge of the splits' partial states -------------------------------------
+// A warp per (new-token row, query head): M = max_z m_z, w_z = 2^(m_z - M),
+// out = sum_z w_z o_z / sum_z w_z l_z (the blockwise softmax's recombination,
+// "Qwen3-8B inference engine from scratch in C++/CUDA", section 4.4.1).
+template <int D>
+__global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_constant__ PrefillParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * kPfWarps + warp;  // (row, query head)
+  if (item >= (long long)p.n_tok * p.n_qh) return;
+  const int r = (int)(item / p.n_qh), h = (int)(item - (long long)r * p.n_qh);
+  int lo = 0, hi = p.n_seq;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.seq_starts + mid) <= r)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  int start, n_new, ctx;
+  // rows of skipped sequences, and past the tiles the grid covered, stay unwritten
+  if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new ||
+      r - start >= p.tiles_per_seq * kPfRows)
+    return;
+  constexpr int E = D / 32;  // output columns per lane
+  const size_t stride = (size_t)p.n_tok * p.n_qh * (D + 2);
+  const float *rec = p.part + ((size_t)r * p.n_qh + h) * (D + 2);
+  float M = -INFINITY;
+  for (int zz = 0; zz < p.n_splits; ++zz) M = fmaxf(M, __ldg(rec + zz * stride + D));
+  float L = 0.f, acc[E] = {};
+  for (int zz = 0; zz < p.n_splits; ++zz) {
+    const float *rz = rec + zz * stride;
+    const float w = ex2_approx(__ldg(rz + D) - M);
+    L += w * __ldg(rz + D + 1);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] += w * __ldg(rz + lane + 32 * e);
+  }
+  const float f = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16 *dst = p.out + ((size_t)r * p.n_qh + h) * D;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(acc[e] * f);
+}
+
 template <int D>
 cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
   using C = PfCfg<D>;
@@ -357,8 +422,13 @@ cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
   prefill_append_kernel<D><<<(unsigned)((items + kPfWarps - 1) / kPfWarps), kPfThreads, 0, stream>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const dim3 grid((unsigned)(p.n_seq * p.tiles_per_seq), (unsigned)(p.n_qh / kPfWarps));
+  const dim3 grid((unsigned)(p.n_seq * p.tiles_per_seq), (unsigned)(p.n_qh / kPfWarps),
+                  (unsigned)p.n_splits);
   prefill_attn_kernel<D><<<grid, kPfThreads, C::kSmem, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || p.n_splits == 1) return err;
+  const long long rows = (long long)p.n_tok * p.n_qh;
+  prefill_merge_kernel<D><<<(unsigned)((rows + kPfWarps - 1) / kPfWarps), kPfThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -371,13 +441,25 @@ void rope_tables(float rope_theta, int head_dim, double *inv_freq, float2 *turns
 
 }  // namespace kvattn
 
+namespace {
+constexpr int kPfMaxSplits = 16;
+size_t split_bytes(long long n_tok, int n_qh, int head_dim) {
+  return (size_t)n_tok * n_qh * (head_dim + 2) * sizeof(float);
+}
+}  // namespace
+
+extern "C" size_t kvattn_prefill_workspace_size(int n_tok, int n_qh, int head_dim) {
+  if (n_tok < 0 || n_qh < 1 || (head_dim != 64 && head_dim != 128)) return 0;
+  return kPfMaxSplits * split_bytes(n_tok, n_qh, head_dim);
+}
+
 extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_new, void *k_pages,
                               void *v_pages, const int32_t *block_table,
                               const int32_t *seq_starts, const int32_t *ctx_lens, void *out,
                               int n_seq, int n_tok, int n_qh, int n_kvh, int head_dim,
                               int page_size, float rope_theta, float scale, void *stream,
                               int max_pages_per_seq, int num_pages, int max_new_tokens,
-                              uint32_t *dev_status) {
+                              uint32_t *dev_status, void *workspace, size_t workspace_bytes) {
   using namespace kvattn;
   if (n_seq < 0 || n_tok < 0 || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 ||
       max_pages_per_seq < 1 || num_pages < 1 || max_new_tokens < 0)
@@ -402,7 +484,7 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   if (!pf_aligned(q, 16) || !pf_aligned(k_new, 16) || !pf_aligned(v_new, 16) ||
       !pf_aligned(k_pages, 16) || !pf_aligned(v_pages, 16) || !pf_aligned(out, 4) ||
       !pf_aligned(block_table, 4) || !pf_aligned(seq_starts, 4) || !pf_aligned(ctx_lens, 4) ||
-      (dev_status && !pf_aligned(dev_status, 4)))
+      (dev_status && !pf_aligned(dev_status, 4)) || (workspace && !pf_aligned(workspace, 16)))
     return KVATTN_EINVAL;
   PrefillParams p = {};
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -424,6 +506,26 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   p.max_pages = max_pages_per_seq;
   p.num_pages = num_pages;
   p.tiles_per_seq = (int)tiles;
+  // Splits of a query tile's key tiles: short chunks over long contexts
+  // (speculative verification, small decode-like chunks) share them among 16
+  // CTAs so every context streams at once; long prompts, whose query tiles
+  // already fill the GPU, take one, as does a call without a workspace.
+  {
+    int S = 1;
+    if (max_new_tokens <= 64) {
+      S = kPfMaxSplits;
+    } else {
+      int dev = 0, sms = 152;
+      if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      const long long base = (long long)n_seq * tiles * (n_qh / kPfWarps);
+      S = (int)std::min<long long>(kPfMaxSplits, std::max<long long>(1, (4LL * sms + base - 1) / base));
+    }
+    const size_t per = split_bytes(n_tok, n_qh, head_dim);
+    if (S > 1) S = workspace ? (int)std::min<size_t>((size_t)S, workspace_bytes / per) : 1;
+    p.n_splits = std::max(1, S);
+    p.part = static_cast<float *>(workspace);
+  }
   p.use_rope = rope_theta > 0.0f ? 1 : 0;
   p.qscale = (float)((double)scale * 1.4426950408889634);
   rope_tables(rope_theta, head_dim, p.inv_freq, p.turns);

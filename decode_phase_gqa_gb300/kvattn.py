@@ -71,8 +71,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvattn_decode_layers.argtypes = [I] + dec + [P]
         L.kvattn_decode_layers.restype = I
         L.kvattn_decode_noalloc.argtypes = dec[:-2] + [P]
-        L.kvattn_prefill.argtypes = [P] * 9 + [I] * 6 + [F, F, P, I, I, I, P]
+        L.kvattn_prefill.argtypes = [P] * 9 + [I] * 6 + [F, F, P, I, I, I, P, P, S]
         L.kvattn_prefill.restype = I
+        L.kvattn_prefill_workspace_size.argtypes = [I, I, I]
+        L.kvattn_prefill_workspace_size.restype = S
         L.kvattn_decode_noalloc.restype = I
         L.kvattn_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         L.kvattn_read_device_status.restype = I
@@ -246,7 +248,8 @@ def kvattn_decode_layers(q, k_new, v_new, k_pages, v_pages, block_table, seq_len
 
 def kvattn_prefill(q, k_new, v_new, k_pages, v_pages, block_table, seq_starts, ctx_lens, out,
                    *, rope_theta: float, scale: float, max_new_tokens: int,
-                   dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+                   dev_status: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """Paged chunked prefill (kvattn_prefill): append the new tokens, then
     causal attention over the cache and the earlier new tokens.
 
@@ -254,7 +257,8 @@ def kvattn_prefill(q, k_new, v_new, k_pages, v_pages, block_table, seq_starts, c
     back); k_new/v_new [T, Hk, d] bf16; k_pages/v_pages [num_pages, Hk, page, d]
     bf16; block_table [B, max_pages] int32; seq_starts [B + 1] int32; ctx_lens
     [B] int32; dev_status: None or a 1-element uint32/int32 device tensor that
-    receives KVATTN_DEV_* bits.
+    receives KVATTN_DEV_* bits; workspace: None or a device tensor of
+    ``kvattn_prefill_workspace_size(T, Hq, d)`` bytes (for short chunks).
     """
     dev = q.device
     if dev.type != "cuda":
@@ -283,9 +287,14 @@ def kvattn_prefill(q, k_new, v_new, k_pages, v_pages, block_table, seq_starts, c
         block_table.data_ptr(), seq_starts.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
         n_seq, n_tok, n_qh, n_kvh, d, page, float(rope_theta), float(scale),
         _stream_handle(stream, dev), block_table.shape[1], num_pages, int(max_new_tokens),
-        _ptr(dev_status))
+        _ptr(dev_status), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size())
     if rc:
         raise KvattnError(rc, "kvattn_prefill")
+
+
+def kvattn_prefill_workspace_size(n_tok: int, n_qh: int, head_dim: int) -> int:
+    return int(load().kvattn_prefill_workspace_size(n_tok, n_qh, head_dim))
 
 
 def kvattn_read_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -245,15 +245,27 @@ int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const v
  *              OR-ed in for a sequence whose rows or slots do not fit (it is
  *              skipped), KVATTN_DEV_BAD_PAGE for a page outside [0, num_pages)
  *              (its tokens are left out, no append lands there).
- * Other arguments, checks and errors as for kvattn_decode.  No workspace: a
- * CTA finishes its tokens' attention itself.
+ * workspace    device, 16-byte aligned, or NULL; workspace_bytes its size.  With
+ *              max_new_tokens <= 64 (short chunks over long contexts: a
+ *              speculative check) the key tiles of a query tile are shared
+ *              among up to 16 CTAs whose partial softmax states are merged by
+ *              a third kernel; they need kvattn_prefill_workspace_size(...)
+ *              bytes (fewer splits when the workspace is smaller, none
+ *              without one).  Its contents need no initialisation and are
+ *              not kept between calls; calls sharing a workspace must not
+ *              overlap on the GPU.
+ * Other arguments, checks and errors as for kvattn_decode.
  */
 int kvattn_prefill(const void *q, const void *k_new, const void *v_new, void *k_pages,
                    void *v_pages, const int32_t *block_table, const int32_t *seq_starts,
                    const int32_t *ctx_lens, void *out, int n_seq, int n_tok, int n_qh, int n_kvh,
                    int head_dim, int page_size, float rope_theta, float scale, void *stream,
                    int max_pages_per_seq, int num_pages, int max_new_tokens,
-                   uint32_t *dev_status);
+                   uint32_t *dev_status, void *workspace, size_t workspace_bytes);
+
+/* Workspace bytes kvattn_prefill can use for n_tok new tokens (0 when the
+ * shape is invalid). */
+size_t kvattn_prefill_workspace_size(int n_tok, int n_qh, int head_dim);
 
 /*
  * kvattn_decode for callers that can neither pass a workspace nor let the

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "kvattn_decode", "kvattn_decode_layers", "kvattn_decode_noalloc",
-        "kvattn_decode_splits", "kvattn_prefill", "kvattn_read_device_status",
+        "kvattn_decode_splits", "kvattn_prefill", "kvattn_prefill_workspace_size",
+        "kvattn_read_device_status",
         "kvattn_status_string", "kvattn_version", "kvattn_workspace_init",
         "kvattn_workspace_size", "kvattn_workspace_size_layers"])
 
@@ -201,7 +202,8 @@ def prefill_args(**kw):
     a = dict(q=FAKE, k_new=FAKE, v_new=FAKE, k_pages=FAKE, v_pages=FAKE, block_table=FAKE,
              seq_starts=FAKE, ctx_lens=FAKE, out=FAKE, n_seq=2, n_tok=40, n_qh=8, n_kvh=2,
              head_dim=64, page_size=16, rope_theta=1e4, scale=0.125, stream=None,
-             max_pages_per_seq=4, num_pages=8, max_new_tokens=32, dev_status=None)
+             max_pages_per_seq=4, num_pages=8, max_new_tokens=32, dev_status=None,
+             workspace=None, workspace_bytes=0)
     a.update(kw)
     return a
 
@@ -219,6 +221,7 @@ def prefill_args(**kw):
     (dict(seq_starts=None), K.KVATTN_EINVAL),
     (dict(k_new=FAKE + 8), K.KVATTN_EINVAL),
     (dict(dev_status=FAKE + 2), K.KVATTN_EINVAL),
+    (dict(workspace=FAKE + 8, workspace_bytes=1 << 20), K.KVATTN_EINVAL),
     (dict(n_tok=0), K.KVATTN_OK),
     (dict(n_seq=0), K.KVATTN_OK),
 ])

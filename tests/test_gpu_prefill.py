@@ -35,22 +35,26 @@ def make_case(n_qh, n_kvh, ctx, n_new, d=128, page=16, seed=0, theta=1e6):
     return wl, h, starts, ctx
 
 
-def run_prefill(wl, h, starts, ctx, max_new=None):
+def run_prefill(wl, h, starts, ctx, max_new=None, split=True):
     d = to_dev(h)
     ss = torch.from_numpy(starts).cuda()
     cl = torch.from_numpy(np.ascontiguousarray(ctx)).cuda()
     out = torch.full_like(d["q"], float("nan"))
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     mx = int(np.diff(starts).max(initial=0)) if max_new is None else max_new
+    ws = None
+    if split:   # NaN-filled: no split may read what it did not write
+        n = K.kvattn_prefill_workspace_size(d["q"].shape[0], d["q"].shape[1], d["q"].shape[2])
+        ws = torch.full((n // 4,), float("nan"), dtype=torch.float32, device="cuda")
     K.kvattn_prefill(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
                      d["block_table"], ss, cl, out, rope_theta=wl.rope_theta, scale=wl.scale,
-                     max_new_tokens=mx, dev_status=st)
+                     max_new_tokens=mx, dev_status=st, workspace=ws)
     torch.cuda.synchronize()
     return out, int(st.item()), d
 
 
-def check(wl, h, starts, ctx):
-    out, st, d = run_prefill(wl, h, starts, ctx)
+def check(wl, h, starts, ctx, split=True):
+    out, st, d = run_prefill(wl, h, starts, ctx, split=split)
     ref, ost, kp, vp = oracle_prefill(h, starts, ctx, wl.rope_theta, wl.scale)
     assert st == 0 and ost == 0, (st, ost)
     assert np.array_equal(pool_bits(d["k_pages"]), kp)
@@ -72,10 +76,12 @@ def test_chunked_prefill_after_cached_tokens(d):
     check(wl, h, starts, ctx)
 
 
-def test_speculative_verification_of_draft_tokens():
-    """Four draft tokens per sequence over long caches (Qwen3-8B-shaped heads)."""
+@pytest.mark.parametrize("split", [True, False])
+def test_speculative_verification_of_draft_tokens(split):
+    """Four draft tokens per sequence over long caches (Qwen3-8B-shaped heads),
+    with the key tiles split among 16 CTAs and merged, and without."""
     wl, h, starts, ctx = make_case(32, 8, [1000, 3, 257, 4000], [4, 4, 4, 4], d=128, seed=5)
-    check(wl, h, starts, ctx)
+    check(wl, h, starts, ctx, split=split)
 
 
 @pytest.mark.parametrize("page", [32, 64, 256])
