@@ -129,3 +129,48 @@ def test_bad_page_and_overfull_sequence_are_reported():
     assert_close(got[:starts[2]], ref[:starts[2]])
     assert np.array_equal(pool_bits(d["k_pages"]), kp)
     assert np.array_equal(pool_bits(d["v_pages"]), vp)
+
+
+@pytest.mark.parametrize("kind", ["prefill", "verify"])
+def test_benchmark_shapes_at_full_size(kind):
+    """The two shapes the benchmark times, drawn as it draws them (on the GPU,
+    same seeds) and run with its workspace: 8 SmolLM3-shaped prompts of 2048
+    tokens into empty caches, and 4 draft tokens over each of the Qwen3-shaped
+    batch's 64 caches.  Every pool bit for bit, every output row in tolerance."""
+    import math
+    if kind == "prefill":
+        n_qh, n_kvh, d, theta = 16, 4, 128, 1e6
+        ctx = np.zeros(8, np.int64)
+        n_new = np.full(8, 2048, np.int64)
+    else:
+        q3 = W.make_workload("qwen3", seed=0)
+        n_qh, n_kvh, d, theta = q3.n_qh, q3.n_kvh, q3.head_dim, q3.rope_theta
+        ctx = q3.seq_lens.astype(np.int64)
+        n_new = np.full(len(ctx), 4, np.int64)
+    wl = W.make_workload("custom", seed=0, n_seq=len(ctx), n_qh=n_qh, n_kvh=n_kvh, head_dim=d,
+                         page_size=16, rope_theta=theta, kv_dtype="bf16",
+                         lengths=[int(x) for x in ctx + n_new - 1], spare=0.05)
+    dev = torch.device("cuda")
+    t = W.make_tensors(wl, device=dev)
+    g = torch.Generator(device=dev).manual_seed(77)
+    T = int(n_new.sum())
+    q = torch.randn((T, n_qh, d), generator=g, device=dev).to(torch.bfloat16)
+    kn = torch.randn((T, n_kvh, d), generator=g, device=dev).to(torch.bfloat16)
+    vn = torch.randn((T, n_kvh, d), generator=g, device=dev).to(torch.bfloat16)
+    h = {"q": bits(q), "k_new": bits(kn), "v_new": bits(vn), "k_pages": bits(t["k_pages"]),
+         "v_pages": bits(t["v_pages"]), "block_table": wl.block_table.copy()}
+    starts = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    out = torch.full_like(q, float("nan"))
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(K.kvattn_prefill_workspace_size(T, n_qh, d), dtype=torch.uint8, device=dev)
+    K.kvattn_prefill(q, kn, vn, t["k_pages"], t["v_pages"], torch.from_numpy(wl.block_table).to(dev),
+                     torch.from_numpy(starts).to(dev), torch.from_numpy(ctx.astype(np.int32)).to(dev),
+                     out, rope_theta=theta, scale=1.0 / math.sqrt(d),
+                     max_new_tokens=int(n_new.max()), dev_status=st, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref, ost, kp, vp = oracle_prefill(h, starts, ctx, theta, 1.0 / math.sqrt(d))
+    assert ost == 0
+    assert np.array_equal(pool_bits(t["k_pages"]), kp)
+    assert np.array_equal(pool_bits(t["v_pages"]), vp)
+    assert_close(out_f64(out), ref)
