@@ -16,9 +16,9 @@
 // Attention kernel: a CTA takes 16 new tokens of one sequence and the 4 query
 // heads of one group (a warp per head), so one staged K/V tile serves the 4
 // heads (section 4.4.2 of the Qwen3-8B page: a group's KV is read once).
-// Key tiles of 64 tokens are gathered page by page with 16-byte cp.async into
+// Key tiles of 32 tokens are gathered page by page with 16-byte cp.async into
 // a double-buffered, XOR-swizzled shared-memory ring; per tile a warp forms
-// S = Q K^T (16 x 64, m16n8k16 bf16 MMAs, fp32), the online softmax of its 16
+// S = Q K^T (16 x 32, m16n8k16 bf16 MMAs, fp32), the online softmax of its 16
 // rows in the log2 domain, and O += P V.  Query rows are rotated in fp32 and
 // scaled by scale * log2(e) before they are rounded to bf16.
 #include <algorithm>
@@ -35,7 +35,9 @@ namespace {
 constexpr int kPfWarps = 4;                  // query heads per CTA, one warp each
 constexpr int kPfThreads = 32 * kPfWarps;
 constexpr int kPfRows = 16;                  // new tokens per CTA (the MMA's M)
-constexpr int kPfKeys = 64;                  // keys per staged tile
+constexpr int kPfKeys = 32;                  // keys per staged tile
+constexpr int kPfNT = kPfKeys / 8;           // its n-tiles of 8 keys (Q K^T)
+constexpr int kPfKK = kPfKeys / 16;          // its k-steps of 16 keys (P V)
 
 struct PrefillParams {
   const __nv_bfloat16 *q, *k_new, *v_new;
@@ -149,7 +151,7 @@ __device__ __forceinline__ void cp_async_wait_one() {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __grid_constant__ PrefillParams p) {
   using C = PfCfg<D>;
   constexpr int KS = D / 16;  // k-steps of Q K^T
   constexpr int ND = D / 8;   // n-tiles of O
@@ -262,14 +264,14 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_c
     const int *rv = rvalid + (it & 1) * kPfKeys;
     const uint32_t kb = smem_addr(Ks), vb = smem_addr(Vs);
 
-    // S = Q K^T over the tile's 64 keys: 8 n-tiles of 8 keys
-    float s[8][4];
+    // S = Q K^T over the tile's keys, n-tiles of 8 keys
+    float s[kPfNT][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < kPfNT; ++nt)
 #pragma unroll
       for (int k = 0; k < 4; ++k) s[nt][k] = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 8; nt += 2) {
+    for (int nt = 0; nt < kPfNT; nt += 2) {
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         // matrices: keys nt*8.. at chunks 2ks, 2ks+1, then keys (nt+1)*8.. at the same
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_c
     const int key0 = kt * kPfKeys;
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < kPfNT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_c
       l[rr] *= alpha[rr];
     }
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < kPfNT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         s[nt][e] = ex2_approx(s[nt][e] - m[e >> 1]);
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(const __grid_c
     // O += P V: P's accumulator layout is the next MMA's A layout, keys
     // 16 kk .. 16 kk + 15 from n-tiles 2 kk, 2 kk + 1
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
+    for (int kk = 0; kk < kPfKK; ++kk) {
       const uint32_t a[4] = {pack_bf16(s[2 * kk][0], s[2 * kk][1]), pack_bf16(s[2 * kk][2], s[2 * kk][3]),
                              pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
                              pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3])};
