@@ -164,17 +164,22 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
   float2 *turns = reinterpret_cast<float2 *>(rvalid + 2 * kPfKeys);  // [64]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x / p.tiles_per_seq, qt = blockIdx.x % p.tiles_per_seq;
+  // CTA x: head group x % G, then sequence, then query tile from the last:
+  // the latest tiles of every sequence and group (the most keys) are placed
+  // first, so the longest CTAs do not start last
+  const int G = p.n_qh / kPfWarps;
+  const int grp = (int)(blockIdx.x % G), rest = (int)(blockIdx.x / G);
+  const int b = rest % p.n_seq, qt = p.tiles_per_seq - 1 - rest / p.n_seq;
   const int g = p.n_qh / p.n_kvh;
-  const int j = blockIdx.y / (g / kPfWarps);
-  const int h = j * g + (blockIdx.y % (g / kPfWarps)) * kPfWarps + warp;  // this warp's head
+  const int j = grp / (g / kPfWarps);
+  const int h = j * g + (grp % (g / kPfWarps)) * kPfWarps + warp;  // this warp's head
   int start, n_new, ctx;
   if (!seq_span(p, b, start, n_new, ctx)) {
-    if (qt == 0 && blockIdx.y == 0 && tid == 0) report(p, KVATTN_DEV_BAD_LEN);
+    if (qt == 0 && grp == 0 && tid == 0) report(p, KVATTN_DEV_BAD_LEN);
     return;
   }
   // more new tokens than the grid's tiles cover (a bound the caller gave)
-  if (qt == 0 && blockIdx.y == 0 && tid == 0 && n_new > p.tiles_per_seq * kPfRows)
+  if (qt == 0 && grp == 0 && tid == 0 && n_new > p.tiles_per_seq * kPfRows)
     report(p, KVATTN_DEV_BAD_LEN);
   const int t0 = qt * kPfRows;
   if (t0 >= n_new) return;
@@ -424,7 +429,7 @@ cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
   prefill_append_kernel<D><<<(unsigned)((items + kPfWarps - 1) / kPfWarps), kPfThreads, 0, stream>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const dim3 grid((unsigned)(p.n_seq * p.tiles_per_seq), (unsigned)(p.n_qh / kPfWarps),
+  const dim3 grid((unsigned)((long long)p.n_seq * p.tiles_per_seq * (p.n_qh / kPfWarps)), 1u,
                   (unsigned)p.n_splits);
   prefill_attn_kernel<D><<<grid, kPfThreads, C::kSmem, stream>>>(p);
   err = cudaGetLastError();
@@ -477,7 +482,8 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   if ((long long)max_pages_per_seq * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
   if ((long long)num_pages * n_kvh * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
   const long long tiles = ((long long)max_new_tokens + kPfRows - 1) / kPfRows;
-  if ((long long)n_seq * tiles > (long long)INT_MAX || (long long)n_tok * n_kvh > (1LL << 40))
+  if ((long long)n_seq * tiles * (n_qh / kPfWarps) > (long long)INT_MAX ||
+      (long long)n_tok * n_kvh > (1LL << 40))
     return KVATTN_EUNSUPPORTED;
   if (n_seq == 0 || n_tok == 0 || max_new_tokens == 0) return KVATTN_OK;  // nothing to do
   if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_starts ||
