@@ -38,6 +38,7 @@ constexpr int kPfRows = 16;                  // new tokens per CTA (the MMA's M)
 constexpr int kPfKeys = 32;                  // keys per staged tile
 constexpr int kPfNT = kPfKeys / 8;           // its n-tiles of 8 keys (Q K^T)
 constexpr int kPfKK = kPfKeys / 16;          // its k-steps of 16 keys (P V)
+constexpr int kPfMinTiles = 8;               // key tiles a split takes at least
 
 struct PrefillParams {
   const __nv_bfloat16 *q, *k_new, *v_new;
@@ -69,6 +70,16 @@ __device__ __forceinline__ bool seq_span(const PrefillParams &p, int b, int &sta
   n_new = end - start;
   const long long cap = (long long)p.max_pages << p.page_shift;
   return start >= 0 && end <= p.n_tok && n_new >= 0 && ctx >= 0 && (long long)ctx + n_new <= cap;
+}
+
+// Key tiles of the query tile starting at new token t0 (n_new new tokens after
+// ctx cached ones), and the splits sharing them: S at most, each with at least
+// kPfMinTiles tiles (the attention and merge kernels both use this).
+__device__ __forceinline__ int query_tile_keys(int ctx, int n_new, int t0) {
+  return ctx + min(n_new, t0 + kPfRows);
+}
+__device__ __forceinline__ int tile_splits(int n_tiles, int S) {
+  return max(1, min(S, (n_tiles + kPfMinTiles - 1) / kPfMinTiles));
 }
 
 // ---- append ------------------------------------------------------------------
@@ -183,6 +194,15 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
     report(p, KVATTN_DEV_BAD_LEN);
   const int t0 = qt * kPfRows;
   if (t0 >= n_new) return;
+  // keys the CTA's last valid row sees: 0 .. ctx + min(n_new, t0 + 16) - 1, in
+  // tiles; split z of the query tile takes a contiguous range of them (a split
+  // past the query tile's count has nothing to do)
+  const int n_keys = query_tile_keys(ctx, n_new, t0);
+  const int n_tiles = (n_keys + kPfKeys - 1) / kPfKeys;
+  const int z = blockIdx.z, nz = tile_splits(n_tiles, p.n_splits);
+  if (z >= nz) return;
+  const int per = (n_tiles + nz - 1) / nz;
+  const int kt_begin = z * per, kt_end = min(n_tiles, kt_begin + per);
   if (tid < 64) turns[tid] = p.turns[tid];
   __syncthreads();
 
@@ -215,9 +235,6 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
     ldmatrix_x4(qf[ks], smem_addr(qw) + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)));
 
   // ---- key tiles ----------------------------------------------------------------
-  // keys the CTA's last valid row sees: 0 .. ctx + min(n_new, t0 + 16) - 1
-  const int n_keys = ctx + min(n_new, t0 + kPfRows);
-  const int n_tiles = (n_keys + kPfKeys - 1) / kPfKeys;
   auto load_tile = [&](int kt, int s) {
     uint8_t *Ks = stages + s * C::kStage, *Vs = Ks + C::kTile;
     for (int idx = tid; idx < kPfKeys * CH; idx += kPfThreads) {
@@ -252,15 +269,14 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
   // absolute positions of this lane's rows g and g + 8
   const int qpos[2] = {ctx + t0 + (lane >> 2), ctx + t0 + (lane >> 2) + 8};
 
-  // this CTA's key tiles: z, z + S, z + 2 S, ... (split z of S)
-  const int z = blockIdx.z, S = p.n_splits;
-  if (z < n_tiles)
-    load_tile(z, 0);
+  // this CTA's key tiles: kt_begin .. kt_end - 1 (split z of nz)
+  if (kt_begin < kt_end)
+    load_tile(kt_begin, 0);
   else
     cp_async_commit();
-  for (int it = 0, kt = z; kt < n_tiles; ++it, kt += S) {
-    if (kt + S < n_tiles)
-      load_tile(kt + S, (it + 1) & 1);
+  for (int it = 0, kt = kt_begin; kt < kt_end; ++it, ++kt) {
+    if (kt + 1 < kt_end)
+      load_tile(kt + 1, (it + 1) & 1);
     else
       cp_async_commit();  // (an empty group: the wait below still means tile kt)
     cp_async_wait_one();
@@ -349,7 +365,7 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
     l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
     l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
   }
-  if (S > 1) {  // a partial state per row, merged by prefill_merge_kernel
+  if (p.n_splits > 1) {  // a partial state per row, merged by prefill_merge_kernel
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const int t = t0 + (lane >> 2) + 8 * rr;
@@ -402,10 +418,13 @@ __global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_
   constexpr int E = D / 32;  // output columns per lane
   const size_t stride = (size_t)p.n_tok * p.n_qh * (D + 2);
   const float *rec = p.part + ((size_t)r * p.n_qh + h) * (D + 2);
+  // the splits of the row's query tile, as the attention kernel formed them
+  const int t0 = ((r - start) / kPfRows) * kPfRows;
+  const int nz = tile_splits((query_tile_keys(ctx, n_new, t0) + kPfKeys - 1) / kPfKeys, p.n_splits);
   float M = -INFINITY;
-  for (int zz = 0; zz < p.n_splits; ++zz) M = fmaxf(M, __ldg(rec + zz * stride + D));
+  for (int zz = 0; zz < nz; ++zz) M = fmaxf(M, __ldg(rec + zz * stride + D));
   float L = 0.f, acc[E] = {};
-  for (int zz = 0; zz < p.n_splits; ++zz) {
+  for (int zz = 0; zz < nz; ++zz) {
     const float *rz = rec + zz * stride;
     const float w = ex2_approx(__ldg(rz + D) - M);
     L += w * __ldg(rz + D + 1);
@@ -515,9 +534,10 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   p.num_pages = num_pages;
   p.tiles_per_seq = (int)tiles;
   // Splits of a query tile's key tiles: short chunks over long contexts
-  // (speculative verification, small decode-like chunks) share them among 16
-  // CTAs so every context streams at once; long prompts, whose query tiles
-  // already fill the GPU, take one, as does a call without a workspace.
+  // (speculative verification, small decode-like chunks) share them among up
+  // to 16 CTAs, each with at least 8 tiles, so every context streams at once;
+  // long prompts, whose query tiles already fill the GPU, take one, as does a
+  // call without a workspace.
   {
     int S = 1;
     if (max_new_tokens <= 64) {
