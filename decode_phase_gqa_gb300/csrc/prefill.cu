@@ -38,7 +38,7 @@ constexpr int kPfRows = 16;                  // new tokens per CTA (the MMA's M)
 constexpr int kPfKeys = 32;                  // keys per staged tile
 constexpr int kPfNT = kPfKeys / 8;           // its n-tiles of 8 keys (Q K^T)
 constexpr int kPfKK = kPfKeys / 16;          // its k-steps of 16 keys (P V)
-constexpr int kPfMinTiles = 8;               // key tiles a split takes at least
+constexpr int kPfMinTiles = 16;              // key tiles a split takes at least
 
 struct PrefillParams {
   const __nv_bfloat16 *q, *k_new, *v_new;
@@ -535,7 +535,7 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   p.tiles_per_seq = (int)tiles;
   // Splits of a query tile's key tiles: short chunks over long contexts
   // (speculative verification, small decode-like chunks) share them among up
-  // to 16 CTAs, each with at least 8 tiles, so every context streams at once;
+  // to 16 CTAs, each with at least 16 tiles, so every context streams at once;
   // long prompts, whose query tiles already fill the GPU, take one, as does a
   // call without a workspace.
   {
