@@ -174,3 +174,39 @@ def test_benchmark_shapes_at_full_size(kind):
     assert np.array_equal(pool_bits(t["k_pages"]), kp)
     assert np.array_equal(pool_bits(t["v_pages"]), vp)
     assert_close(out_f64(out), ref)
+
+
+def test_decode_after_prefill_reads_the_prefilled_cache():
+    """A prompt through kvattn_prefill, then two decode steps through
+    kvattn_decode: the steps attend over the keys the prefill appended, and
+    the whole sequence equals the oracle's decode steps one token at a time."""
+    n_qh, n_kvh, d = 16, 4, 128
+    ctx0, prompt, steps = np.array([0, 40], np.int32), np.array([70, 9], np.int32), 2
+    # pages for the prompt and the decode steps that follow
+    wl, h, starts, ctx = make_case(n_qh, n_kvh, ctx0, prompt + steps, d=d, seed=17)
+    T = int(prompt.sum())
+    rows = np.concatenate([np.arange(starts[b], starts[b] + prompt[b]) for b in range(2)])
+    later = [starts[:-1] + prompt + s for s in range(steps)]  # rows of each decode token
+    hp = dict(h, q=h["q"][rows].copy(), k_new=h["k_new"][rows].copy(), v_new=h["v_new"][rows].copy())
+    pstarts = np.concatenate([[0], np.cumsum(prompt)]).astype(np.int32)
+    out, st, dv = run_prefill(wl, hp, pstarts, ctx0)
+    assert st == 0
+    ref_p, ost, kp, vp = oracle_prefill(hp, pstarts, ctx0, wl.rope_theta, wl.scale)
+    assert ost == 0
+    assert_close(out_f64(out), ref_p)
+    hd = {"k_pages": kp, "v_pages": vp, "block_table": h["block_table"], "k_scales": None,
+          "v_scales": None}
+    for s in range(steps):
+        L = (ctx0 + prompt + s).astype(np.int32)
+        hs = dict(hd, q=h["q"][later[s]].copy(), k_new=h["k_new"][later[s]].copy(),
+                  v_new=h["v_new"][later[s]].copy(), seq_lens=L, positions=L)
+        wls = W.with_lengths(wl, L)
+        dd = to_dev(hs)
+        dd["k_pages"], dd["v_pages"] = dv["k_pages"], dv["v_pages"]   # the GPU's own cache
+        dec, st2, _ = run_gpu(wls, dd)
+        ref, ost2, kp, vp, _, _ = oracle_decode(wls, hs)
+        assert st2 == 0 and ost2 == 0
+        assert np.array_equal(pool_bits(dv["k_pages"]), kp)
+        assert np.array_equal(pool_bits(dv["v_pages"]), vp)
+        assert_close(out_f64(dec), ref)
+        hd = dict(hd, k_pages=kp, v_pages=vp)
