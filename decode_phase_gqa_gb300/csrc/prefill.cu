@@ -105,8 +105,11 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
       hi = mid;
   }
   int start, n_new, ctx;
-  if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new) {
-    if (lane == 0) report(p, KVATTN_DEV_BAD_LEN);  // a row no valid sequence owns
+  // a row no valid sequence owns, or past the tokens the launch covers (the
+  // attention kernel leaves those out too)
+  if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new ||
+      r - start >= p.tiles_per_seq * kPfRows) {
+    if (lane == 0) report(p, KVATTN_DEV_BAD_LEN);
     return;
   }
   const int slot = ctx + (r - start);  // also the RoPE position
@@ -501,8 +504,9 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   if ((long long)max_pages_per_seq * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
   if ((long long)num_pages * n_kvh * page_size > (long long)INT_MAX) return KVATTN_EUNSUPPORTED;
   const long long tiles = ((long long)max_new_tokens + kPfRows - 1) / kPfRows;
+  // grid sizes: query tiles x head groups, and a warp per (new token, head)
   if ((long long)n_seq * tiles * (n_qh / kPfWarps) > (long long)INT_MAX ||
-      (long long)n_tok * n_kvh > (1LL << 40))
+      (long long)n_tok * n_qh > (long long)kPfWarps * INT_MAX)
     return KVATTN_EUNSUPPORTED;
   if (n_seq == 0 || n_tok == 0 || max_new_tokens == 0) return KVATTN_OK;  // nothing to do
   if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_starts ||

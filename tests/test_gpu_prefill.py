@@ -210,3 +210,23 @@ def test_decode_after_prefill_reads_the_prefilled_cache():
         assert np.array_equal(pool_bits(dv["v_pages"]), vp)
         assert_close(out_f64(dec), ref)
         hd = dict(hd, k_pages=kp, v_pages=vp)
+
+
+def test_tokens_past_max_new_tokens_are_left_out():
+    """A sequence with more new tokens than max_new_tokens: the first
+    max_new_tokens are appended and attended, the rest neither, and the status
+    says so; the other sequences are untouched by it."""
+    wl, h, starts, ctx = make_case(8, 2, [10, 30], [20, 50], d=64, seed=19)
+    out, st, d = run_prefill(wl, h, starts, ctx, max_new=32)
+    assert st & K.KVATTN_DEV_BAD_LEN
+    got = out_f64(out)
+    cut = starts[1] + 32            # rows of sequence 1 past the launch's 32 tokens
+    assert np.all(np.isnan(got[cut:starts[2]]))
+    short = np.concatenate([[0], np.cumsum([20, 32])]).astype(np.int32)
+    keep = np.r_[0:starts[1] + 32]
+    hs = dict(h, q=h["q"][keep].copy(), k_new=h["k_new"][keep].copy(), v_new=h["v_new"][keep].copy())
+    ref, ost, kp, vp = oracle_prefill(hs, short, ctx, wl.rope_theta, wl.scale)
+    assert ost == 0
+    assert_close(got[:cut], ref)
+    assert np.array_equal(pool_bits(d["k_pages"]), kp)
+    assert np.array_equal(pool_bits(d["v_pages"]), vp)
