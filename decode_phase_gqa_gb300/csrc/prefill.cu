@@ -42,7 +42,9 @@ constexpr int kPfMinTiles = 16;              // key tiles a split takes at least
 
 struct PrefillParams {
   const __nv_bfloat16 *q, *k_new, *v_new;
-  __nv_bfloat16 *k_pages, *v_pages, *out;
+  void *k_pages, *v_pages;  // bf16, or int8 codes with k_scales / v_scales
+  float *k_scales, *v_scales;
+  __nv_bfloat16 *out;
   const int32_t *block_table, *seq_starts, *ctx_lens;
   uint32_t *status;  // KVATTN_DEV_* bits (NULL: not reported)
   int n_seq, n_tok, n_qh, n_kvh, page_size, page_shift, max_pages, num_pages;
@@ -83,7 +85,7 @@ __device__ __forceinline__ int tile_splits(int n_tiles, int S) {
 }
 
 // ---- append ------------------------------------------------------------------
-template <int D>
+template <int D, bool INT8>
 __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid_constant__ PrefillParams p) {
   __shared__ double inv_freq[64];
   __shared__ float4 table[sizeof(kSinCosStep) / 16];
@@ -125,33 +127,74 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
   for (int c = lane; c < 2 * CH; c += 32)
     reinterpret_cast<uint4 *>(buf)[c] = c < CH ? ks[c] : vs[c - CH];
   __syncwarp();
-  stage_new_row<D, false>(slot, inv_freq, table, p.use_rope != 0, lane, buf);
+  stage_new_row<D, INT8>(slot, inv_freq, table, p.use_rope != 0, lane, buf);
   const size_t prow = ((size_t)page * p.n_kvh + j) * p.page_size + (slot & (p.page_size - 1));
-  for (int c = lane; c < 2 * CH; c += 32) {
+  // the stored key row, then the value row (int8: codes, the two scales after)
+  constexpr int RB = INT8 ? D : 2 * D, SCH = RB / 16;
+  for (int c = lane; c < 2 * SCH; c += 32) {
     const uint4 x = reinterpret_cast<const uint4 *>(buf)[c];
-    if (c < CH)
-      reinterpret_cast<uint4 *>(p.k_pages + prow * D)[c] = x;
-    else
-      reinterpret_cast<uint4 *>(p.v_pages + prow * D)[c - CH] = x;
+    uint8_t *dst = static_cast<uint8_t *>(c < SCH ? p.k_pages : p.v_pages) + prow * RB;
+    reinterpret_cast<uint4 *>(dst)[c < SCH ? c : c - SCH] = x;
+  }
+  if (INT8 && lane == 0) {
+    const float *sc = reinterpret_cast<const float *>(buf + 2 * D);
+    p.k_scales[prow] = sc[0];
+    p.v_scales[prow] = sc[1];
   }
 }
 
 // ---- attention ---------------------------------------------------------------
-template <int D>
+template <int D, bool INT8>
 struct PfCfg {
-  static constexpr int kRowB = 2 * D;                        // bytes of a bf16 row
+  static constexpr int kRowB = 2 * D;                        // bytes of a 16-bit row
   static constexpr int kQBytes = kPfWarps * kPfRows * kRowB;  // the warps' query rows
-  static constexpr int kTile = kPfKeys * kRowB;              // one K or V tile
+  static constexpr int kTile = kPfKeys * kRowB;              // one K or V tile (16-bit)
   static constexpr int kStage = 2 * kTile;                   // K then V
-  static constexpr int kSmem = kQBytes + 2 * kStage + 2 * kPfKeys * 4 + 64 * 8;
+  // int8 cache: a stage's codes (K, V) and row scales (K, V) as copied
+  static constexpr int kRaw = INT8 ? 2 * kPfKeys * D + 2 * kPfKeys * 4 : 0;
+  static constexpr int kSmem = kQBytes + 2 * (kStage + kRaw) + 2 * kPfKeys * 4 + 64 * 8;
 };
+
+// The MMAs' 16-bit type: bf16 for the bf16 cache; f16 for the int8 cache,
+// whose rows are dequantised (code * scale) into f16 tiles.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  } else {
+    return pack_bf16(lo, hi);
+  }
+}
+template <bool F16>
+__device__ __forceinline__ uint16_t to16(float x) {
+  if constexpr (F16) {
+    __half v = __float2half_rn(x);
+    return *reinterpret_cast<uint16_t *>(&v);
+  } else {
+    __nv_bfloat16 v = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&v);
+  }
+}
+template <bool F16>
+__device__ __forceinline__ void mma16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    mma_bf16_16816(d, a, b0, b1);
+  }
+}
 
 // Byte offset of 16-byte chunk c of row r in a [rows][2 D] tile: the low three
 // bits of the chunk index are XORed with the row's, so the 8 rows an ldmatrix
 // reads at one chunk hit 8 different bank groups.
 template <int D>
 __device__ __forceinline__ uint32_t sw(int r, int c) {
-  return (uint32_t)(r * PfCfg<D>::kRowB + (((c & ~7) | ((c ^ r) & 7)) << 4));
+  return (uint32_t)(r * 2 * D + (((c & ~7) | ((c ^ r) & 7)) << 4));
 }
 
 // 16-byte cp.async that copies `bytes` (16 or 0) and zero-fills the rest
@@ -164,9 +207,9 @@ __device__ __forceinline__ void cp_async_wait_one() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
-template <int D>
+template <int D, bool INT8>
 __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __grid_constant__ PrefillParams p) {
-  using C = PfCfg<D>;
+  using C = PfCfg<D, INT8>;
   constexpr int KS = D / 16;  // k-steps of Q K^T
   constexpr int ND = D / 8;   // n-tiles of O
   constexpr int CH = D / 8;   // 16-byte chunks of a row
@@ -174,7 +217,8 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *qs = smem;
   uint8_t *stages = smem + C::kQBytes;
-  int *rvalid = reinterpret_cast<int *>(stages + 2 * C::kStage);  // [2][kPfKeys]
+  uint8_t *raws = stages + 2 * C::kStage;  // int8: [2][codes K, codes V, scales K, scales V]
+  int *rvalid = reinterpret_cast<int *>(raws + 2 * C::kRaw);  // [2][kPfKeys]
   float2 *turns = reinterpret_cast<float2 *>(rvalid + 2 * kPfKeys);  // [64]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -226,10 +270,9 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
         hi = bb;
       }
     }
-    *reinterpret_cast<__nv_bfloat16 *>(qw + sw<D>(r, i / 8) + (i % 8) * 2) =
-        __float2bfloat16_rn(lo * p.qscale);
-    *reinterpret_cast<__nv_bfloat16 *>(qw + sw<D>(r, (i + D / 2) / 8) + ((i + D / 2) % 8) * 2) =
-        __float2bfloat16_rn(hi * p.qscale);
+    *reinterpret_cast<uint16_t *>(qw + sw<D>(r, i / 8) + (i % 8) * 2) = to16<INT8>(lo * p.qscale);
+    *reinterpret_cast<uint16_t *>(qw + sw<D>(r, (i + D / 2) / 8) + ((i + D / 2) % 8) * 2) =
+        to16<INT8>(hi * p.qscale);
   }
   __syncwarp();
   uint32_t qf[KS][4];  // A fragments: rows g, g + 8; k 2t.., 2t + 8..
@@ -238,27 +281,47 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
     ldmatrix_x4(qf[ks], smem_addr(qw) + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)));
 
   // ---- key tiles ----------------------------------------------------------------
+  // pool row of key token tok, or -1 (past the keys, or an out-of-range page)
+  auto pool_row = [&](int tok, bool rep) -> long long {
+    if (tok >= n_keys) return -1;
+    const int page = __ldg(p.block_table + (size_t)b * p.max_pages + (tok >> p.page_shift));
+    if (page < 0 || page >= p.num_pages) {
+      if (rep) report(p, KVATTN_DEV_BAD_PAGE);
+      return -1;
+    }
+    return ((long long)page * p.n_kvh + j) * p.page_size + (tok & (p.page_size - 1));
+  };
   auto load_tile = [&](int kt, int s) {
-    uint8_t *Ks = stages + s * C::kStage, *Vs = Ks + C::kTile;
-    for (int idx = tid; idx < kPfKeys * CH; idx += kPfThreads) {
-      const int r = idx / CH, c = idx % CH;
-      const int tok = kt * kPfKeys + r;
-      const __nv_bfloat16 *srck = p.k_pages, *srcv = p.v_pages;
-      int bytes = 0;
-      if (tok < n_keys) {
-        const int page = __ldg(p.block_table + (size_t)b * p.max_pages + (tok >> p.page_shift));
-        if (page >= 0 && page < p.num_pages) {
-          const size_t prow = ((size_t)page * p.n_kvh + j) * p.page_size + (tok & (p.page_size - 1));
-          srck = p.k_pages + prow * D + c * 8;
-          srcv = p.v_pages + prow * D + c * 8;
-          bytes = 16;
-        } else if (c == 0) {
-          report(p, KVATTN_DEV_BAD_PAGE);
-        }
+    constexpr int RB = INT8 ? D : 2 * D;  // bytes of a cached row
+    constexpr int RCH = RB / 16;
+    // bf16: straight into the swizzled tiles; int8: the codes into the raw area
+    uint8_t *Kd = INT8 ? raws + s * C::kRaw : stages + s * C::kStage;
+    uint8_t *Vd = INT8 ? Kd + kPfKeys * D : Kd + C::kTile;
+    for (int idx = tid; idx < kPfKeys * RCH; idx += kPfThreads) {
+      const int r = idx / RCH, c = idx % RCH;
+      const long long prow = pool_row(kt * kPfKeys + r, c == 0);
+      const uint8_t *srck = static_cast<const uint8_t *>(p.k_pages);
+      const uint8_t *srcv = static_cast<const uint8_t *>(p.v_pages);
+      if (prow >= 0) {
+        srck += prow * RB + c * 16;
+        srcv += prow * RB + c * 16;
       }
-      cp_async_16_zfill(Ks + sw<D>(r, c), srck, bytes);
-      cp_async_16_zfill(Vs + sw<D>(r, c), srcv, bytes);
-      if (c == 0) rvalid[s * kPfKeys + r] = bytes != 0;
+      const uint32_t off = INT8 ? (uint32_t)(r * D + c * 16) : sw<D>(r, c);
+      cp_async_16_zfill(Kd + off, srck, prow >= 0 ? 16 : 0);
+      cp_async_16_zfill(Vd + off, srcv, prow >= 0 ? 16 : 0);
+      if (c == 0) rvalid[s * kPfKeys + r] = prow >= 0;
+    }
+    if constexpr (INT8) {
+      // row scales: each 16-key half of the tile lies in one page (64 bytes
+      // of K scales, 64 of V); 16-byte copies, zero-filled past the keys
+      if (tid < 4 * (kPfKeys / 16) * 2) {
+        const int half = tid >> 3, v = (tid >> 2) & 1, part = tid & 3;
+        const long long prow = pool_row(kt * kPfKeys + 16 * half, false);
+        const float *src = v ? p.v_scales : p.k_scales;
+        if (prow >= 0) src += prow + 4 * part;
+        float *dst = reinterpret_cast<float *>(Kd + 2 * kPfKeys * D) + v * kPfKeys + 16 * half + 4 * part;
+        cp_async_16_zfill(dst, src, prow >= 0 ? 16 : 0);
+      }
     }
     cp_async_commit();
   };
@@ -286,6 +349,26 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
     __syncthreads();
     const uint8_t *Ks = stages + (it & 1) * C::kStage, *Vs = Ks + C::kTile;
     const int *rv = rvalid + (it & 1) * kPfKeys;
+    if constexpr (INT8) {
+      // the stage's codes times their row scales -> f16 tiles (rows not to be
+      // read: zero, whatever their scale slot holds)
+      const int8_t *raw = reinterpret_cast<const int8_t *>(raws + (it & 1) * C::kRaw);
+      const float *scl = reinterpret_cast<const float *>(raws + (it & 1) * C::kRaw + 2 * kPfKeys * D);
+      for (int idx = tid; idx < 2 * kPfKeys * CH; idx += kPfThreads) {
+        const int v = idx / (kPfKeys * CH), rest = idx - v * kPfKeys * CH;
+        const int r = rest / CH, c = rest % CH;
+        const float sc = rv[r] ? scl[v * kPfKeys + r] : 0.f;
+        const uint2 w = *reinterpret_cast<const uint2 *>(raw + v * kPfKeys * D + r * D + c * 8);
+        const int8_t *e = reinterpret_cast<const int8_t *>(&w);
+        uint4 o4;
+        o4.x = pack16<true>(e[0] * sc, e[1] * sc);
+        o4.y = pack16<true>(e[2] * sc, e[3] * sc);
+        o4.z = pack16<true>(e[4] * sc, e[5] * sc);
+        o4.w = pack16<true>(e[6] * sc, e[7] * sc);
+        *reinterpret_cast<uint4 *>(const_cast<uint8_t *>(v ? Vs : Ks) + sw<D>(r, c)) = o4;
+      }
+      __syncthreads();
+    }
     const uint32_t kb = smem_addr(Ks), vb = smem_addr(Vs);
 
     // S = Q K^T over the tile's keys, n-tiles of 8 keys
@@ -302,8 +385,8 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
         uint32_t kf[4];
         const int mi = lane >> 3;
         ldmatrix_x4(kf, kb + sw<D>((nt + (mi >> 1)) * 8 + (lane & 7), 2 * ks + (mi & 1)));
-        mma_bf16_16816(s[nt], qf[ks], kf[0], kf[1]);
-        mma_bf16_16816(s[nt + 1], qf[ks], kf[2], kf[3]);
+        mma16<INT8>(s[nt], qf[ks], kf[0], kf[1]);
+        mma16<INT8>(s[nt + 1], qf[ks], kf[2], kf[3]);
       }
     }
     // causal and page masks, running maxima of rows g and g + 8
@@ -346,16 +429,17 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
     // 16 kk .. 16 kk + 15 from n-tiles 2 kk, 2 kk + 1
 #pragma unroll
     for (int kk = 0; kk < kPfKK; ++kk) {
-      const uint32_t a[4] = {pack_bf16(s[2 * kk][0], s[2 * kk][1]), pack_bf16(s[2 * kk][2], s[2 * kk][3]),
-                             pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                             pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+      const uint32_t a[4] = {pack16<INT8>(s[2 * kk][0], s[2 * kk][1]),
+                             pack16<INT8>(s[2 * kk][2], s[2 * kk][3]),
+                             pack16<INT8>(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                             pack16<INT8>(s[2 * kk + 1][2], s[2 * kk + 1][3])};
 #pragma unroll
       for (int nd = 0; nd < ND; nd += 2) {
         // matrices: keys 16kk..+7 and 16kk+8..+15 at chunk nd, then at chunk nd+1
         uint32_t vf[4];
         ldmatrix_x4_trans(vf, vb + sw<D>(16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8, nd + (lane >> 4)));
-        mma_bf16_16816(o[nd], a, vf[0], vf[1]);
-        mma_bf16_16816(o[nd + 1], a, vf[2], vf[3]);
+        mma16<INT8>(o[nd], a, vf[0], vf[1]);
+        mma16<INT8>(o[nd + 1], a, vf[2], vf[3]);
       }
     }
     __syncthreads();  // the stage is rewritten two tiles on
@@ -440,20 +524,20 @@ __global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_
   for (int e = 0; e < E; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(acc[e] * f);
 }
 
-template <int D>
+template <int D, bool INT8>
 cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
-  using C = PfCfg<D>;
+  using C = PfCfg<D, INT8>;
   // (set on every call: the attribute belongs to the current device)
-  cudaError_t err = cudaFuncSetAttribute(prefill_attn_kernel<D>,
+  cudaError_t err = cudaFuncSetAttribute(prefill_attn_kernel<D, INT8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (err != cudaSuccess) return err;
   const long long items = (long long)p.n_tok * p.n_kvh;
-  prefill_append_kernel<D><<<(unsigned)((items + kPfWarps - 1) / kPfWarps), kPfThreads, 0, stream>>>(p);
+  prefill_append_kernel<D, INT8><<<(unsigned)((items + kPfWarps - 1) / kPfWarps), kPfThreads, 0, stream>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const dim3 grid((unsigned)((long long)p.n_seq * p.tiles_per_seq * (p.n_qh / kPfWarps)), 1u,
                   (unsigned)p.n_splits);
-  prefill_attn_kernel<D><<<grid, kPfThreads, C::kSmem, stream>>>(p);
+  prefill_attn_kernel<D, INT8><<<grid, kPfThreads, C::kSmem, stream>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess || p.n_splits == 1) return err;
   const long long rows = (long long)p.n_tok * p.n_qh;
@@ -486,10 +570,13 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
                               void *v_pages, const int32_t *block_table,
                               const int32_t *seq_starts, const int32_t *ctx_lens, void *out,
                               int n_seq, int n_tok, int n_qh, int n_kvh, int head_dim,
-                              int page_size, float rope_theta, float scale, void *stream,
-                              int max_pages_per_seq, int num_pages, int max_new_tokens,
+                              int page_size, float rope_theta, float scale, int kv_dtype,
+                              void *stream, int max_pages_per_seq, int num_pages,
+                              float *k_scales, float *v_scales, int max_new_tokens,
                               uint32_t *dev_status, void *workspace, size_t workspace_bytes) {
   using namespace kvattn;
+  if (kv_dtype != KVATTN_KV_BF16 && kv_dtype != KVATTN_KV_INT8) return KVATTN_EUNSUPPORTED;
+  const bool int8 = kv_dtype == KVATTN_KV_INT8;
   if (n_seq < 0 || n_tok < 0 || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 ||
       max_pages_per_seq < 1 || num_pages < 1 || max_new_tokens < 0)
     return KVATTN_EINVAL;
@@ -517,12 +604,16 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
       !pf_aligned(block_table, 4) || !pf_aligned(seq_starts, 4) || !pf_aligned(ctx_lens, 4) ||
       (dev_status && !pf_aligned(dev_status, 4)) || (workspace && !pf_aligned(workspace, 16)))
     return KVATTN_EINVAL;
+  if (int8 && (!k_scales || !v_scales || !pf_aligned(k_scales, 16) || !pf_aligned(v_scales, 16)))
+    return KVATTN_EINVAL;
   PrefillParams p = {};
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
   p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-  p.k_pages = static_cast<__nv_bfloat16 *>(k_pages);
-  p.v_pages = static_cast<__nv_bfloat16 *>(v_pages);
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.k_scales = int8 ? k_scales : nullptr;
+  p.v_scales = int8 ? v_scales : nullptr;
   p.out = static_cast<__nv_bfloat16 *>(out);
   p.block_table = block_table;
   p.seq_starts = seq_starts;
@@ -561,7 +652,8 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   p.use_rope = rope_theta > 0.0f ? 1 : 0;
   p.qscale = (float)((double)scale * 1.4426950408889634);
   rope_tables(rope_theta, head_dim, p.inv_freq, p.turns);
-  const cudaError_t err = head_dim == 64 ? launch_prefill_t<64>(p, static_cast<cudaStream_t>(stream))
-                                         : launch_prefill_t<128>(p, static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t err = head_dim == 64 ? (int8 ? launch_prefill_t<64, true>(p, st) : launch_prefill_t<64, false>(p, st))
+                                         : (int8 ? launch_prefill_t<128, true>(p, st) : launch_prefill_t<128, false>(p, st));
   return err == cudaSuccess ? KVATTN_OK : KVATTN_ECUDA;
 }

@@ -71,7 +71,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvattn_decode_layers.argtypes = [I] + dec + [P]
         L.kvattn_decode_layers.restype = I
         L.kvattn_decode_noalloc.argtypes = dec[:-2] + [P]
-        L.kvattn_prefill.argtypes = [P] * 9 + [I] * 6 + [F, F, P, I, I, I, P, P, S]
+        L.kvattn_prefill.argtypes = [P] * 9 + [I] * 6 + [F, F, I, P, I, I, P, P, I, P, P, S]
         L.kvattn_prefill.restype = I
         L.kvattn_prefill_workspace_size.argtypes = [I, I, I]
         L.kvattn_prefill_workspace_size.restype = S
@@ -248,6 +248,7 @@ def kvattn_decode_layers(q, k_new, v_new, k_pages, v_pages, block_table, seq_len
 
 def kvattn_prefill(q, k_new, v_new, k_pages, v_pages, block_table, seq_starts, ctx_lens, out,
                    *, rope_theta: float, scale: float, max_new_tokens: int,
+                   k_scales: Optional[torch.Tensor] = None, v_scales: Optional[torch.Tensor] = None,
                    dev_status: Optional[torch.Tensor] = None,
                    workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """Paged chunked prefill (kvattn_prefill): append the new tokens, then
@@ -255,7 +256,7 @@ def kvattn_prefill(q, k_new, v_new, k_pages, v_pages, block_table, seq_starts, c
 
     Shapes: q/out [T, Hq, d] bf16 (the new tokens of all sequences back to
     back); k_new/v_new [T, Hk, d] bf16; k_pages/v_pages [num_pages, Hk, page, d]
-    bf16; block_table [B, max_pages] int32; seq_starts [B + 1] int32; ctx_lens
+    bf16 or int8 (then k_scales/v_scales [num_pages, Hk, page] fp32); block_table [B, max_pages] int32; seq_starts [B + 1] int32; ctx_lens
     [B] int32; dev_status: None or a 1-element uint32/int32 device tensor that
     receives KVATTN_DEV_* bits; workspace: None or a device tensor of
     ``kvattn_prefill_workspace_size(T, Hq, d)`` bytes (for short chunks).
@@ -268,8 +269,8 @@ def kvattn_prefill(q, k_new, v_new, k_pages, v_pages, block_table, seq_starts, c
     _check(out, "out", bf, 3, dev)
     _check(k_new, "k_new", bf, 3, dev)
     _check(v_new, "v_new", bf, 3, dev)
-    _check(k_pages, "k_pages", bf, 4, dev)
-    _check(v_pages, "v_pages", bf, 4, dev)
+    _check(k_pages, "k_pages", (torch.bfloat16, torch.int8), 4, dev)
+    _check(v_pages, "v_pages", (k_pages.dtype,), 4, dev)
     _check(block_table, "block_table", (torch.int32,), 2, dev)
     _check(seq_starts, "seq_starts", (torch.int32,), 1, dev)
     _check(ctx_lens, "ctx_lens", (torch.int32,), 1, dev)
@@ -280,14 +281,23 @@ def kvattn_prefill(q, k_new, v_new, k_pages, v_pages, block_table, seq_starts, c
             or tuple(v_new.shape) != (n_tok, n_kvh, d) or tuple(v_pages.shape) != tuple(k_pages.shape)
             or block_table.shape[0] != n_seq or seq_starts.shape[0] != n_seq + 1):
         raise ValueError("inconsistent shapes")
+    int8 = k_pages.dtype == torch.int8
+    if int8:
+        for name, s in (("k_scales", k_scales), ("v_scales", v_scales)):
+            if s is None:
+                raise ValueError(f"{name} is required for an int8 cache")
+            _check(s, name, (torch.float32,), 3, dev)
+            if tuple(s.shape) != (num_pages, n_kvh, page):
+                raise ValueError(f"{name}: shape {tuple(s.shape)}")
     if dev_status is not None:
         _check(dev_status, "dev_status", (torch.int32, torch.uint32), 1, dev)
     rc = load().kvattn_prefill(
         q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
         block_table.data_ptr(), seq_starts.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
         n_seq, n_tok, n_qh, n_kvh, d, page, float(rope_theta), float(scale),
-        _stream_handle(stream, dev), block_table.shape[1], num_pages, int(max_new_tokens),
-        _ptr(dev_status), _ptr(workspace),
+        KVATTN_KV_INT8 if int8 else KVATTN_KV_BF16, _stream_handle(stream, dev),
+        block_table.shape[1], num_pages, _ptr(k_scales) if int8 else None,
+        _ptr(v_scales) if int8 else None, int(max_new_tokens), _ptr(dev_status), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size())
     if rc:
         raise KvattnError(rc, "kvattn_prefill")

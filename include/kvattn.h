@@ -223,14 +223,17 @@ int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const v
  * smollm3.go", section "Prefill: the whole prompt at once"; "Qwen3-8B
  * inference engine from scratch in C++/CUDA", section 4.4.1).  A sequence
  * with n_b = 1 gets exactly the decode step (with seq_lens = positions =
- * ctx_lens).  bf16 cache only.
+ * ctx_lens), for the bf16 and the int8 cache alike (the int8 rows are
+ * dequantised to f16 for the tensor cores: code * scale, rounded once).
  *
  * q, out       device bf16 [n_tok, n_qh, head_dim]: the new tokens of all
  *              sequences back to back, 16-byte aligned (out 4-byte).
  * k_new, v_new device bf16 [n_tok, n_kvh, head_dim], 16-byte aligned.
- * k_pages,     device bf16 [num_pages, n_kvh, page_size, head_dim], as for
- * v_pages      kvattn_decode; the pages of every appended slot must be
- *              assigned in block_table.
+ * k_pages,     device [num_pages, n_kvh, page_size, head_dim], bf16 or int8
+ * v_pages      per kv_dtype, as for kvattn_decode; the pages of every appended
+ *              slot must be assigned in block_table.
+ * k_scales,    as for kvattn_decode (int8 only).
+ * v_scales
  * block_table  device int32 [n_seq, max_pages_per_seq].
  * seq_starts   device int32 [n_seq + 1]: sequence b's new tokens are rows
  *              seq_starts[b] .. seq_starts[b + 1] - 1 of q, k_new, v_new, out.
@@ -259,9 +262,10 @@ int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const v
 int kvattn_prefill(const void *q, const void *k_new, const void *v_new, void *k_pages,
                    void *v_pages, const int32_t *block_table, const int32_t *seq_starts,
                    const int32_t *ctx_lens, void *out, int n_seq, int n_tok, int n_qh, int n_kvh,
-                   int head_dim, int page_size, float rope_theta, float scale, void *stream,
-                   int max_pages_per_seq, int num_pages, int max_new_tokens,
-                   uint32_t *dev_status, void *workspace, size_t workspace_bytes);
+                   int head_dim, int page_size, float rope_theta, float scale, int kv_dtype,
+                   void *stream, int max_pages_per_seq, int num_pages, float *k_scales,
+                   float *v_scales, int max_new_tokens, uint32_t *dev_status, void *workspace,
+                   size_t workspace_bytes);
 
 /* Workspace bytes kvattn_prefill can use for n_tok new tokens (0 when the
  * shape is invalid). */

@@ -47,10 +47,13 @@ def oracle_prefill(h, seq_starts, ctx_lens, rope_theta, scale, seqs=None):
     h: q [T, Hq, d], k_new / v_new [T, Hk, d] (bf16 bits), k_pages / v_pages,
     block_table [B, max_pages].  `seqs`: the sequences to run (default all).
     Returns (out float64 [T, Hq, d], NaN for rows not run; status; the pools
-    after the appends).
+    after the appends); int8 caches: h["k_scales"] / h["v_scales"] are
+    updated copies too, returned as oracle_prefill.scales.
     """
     import oracle
     kp, vp = h["k_pages"].copy(), h["v_pages"].copy()
+    ks = None if h.get("k_scales") is None else h["k_scales"].copy()
+    vs = None if h.get("v_scales") is None else h["v_scales"].copy()
     starts = np.asarray(seq_starts, np.int64)
     ctx = np.asarray(ctx_lens, np.int64)
     n_new = np.diff(starts)
@@ -64,7 +67,8 @@ def oracle_prefill(h, seq_starts, ctx_lens, rope_theta, scale, seqs=None):
                              np.ascontiguousarray(h["v_new"][rows]), kp, vp,
                              np.ascontiguousarray(h["block_table"][act]),
                              (ctx[act] + i).astype(np.int32), (ctx[act] + i).astype(np.int32),
-                             rope_theta, scale)
+                             rope_theta, scale, ks, vs)
         out[rows] = o
         st |= s
+    oracle_prefill.scales = (ks, vs)
     return out, st, kp, vp

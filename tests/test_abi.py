@@ -201,9 +201,9 @@ def test_layers_entry_fails_closed(lib, n_layers, kw, code):
 def prefill_args(**kw):
     a = dict(q=FAKE, k_new=FAKE, v_new=FAKE, k_pages=FAKE, v_pages=FAKE, block_table=FAKE,
              seq_starts=FAKE, ctx_lens=FAKE, out=FAKE, n_seq=2, n_tok=40, n_qh=8, n_kvh=2,
-             head_dim=64, page_size=16, rope_theta=1e4, scale=0.125, stream=None,
-             max_pages_per_seq=4, num_pages=8, max_new_tokens=32, dev_status=None,
-             workspace=None, workspace_bytes=0)
+             head_dim=64, page_size=16, rope_theta=1e4, scale=0.125, kv_dtype=0, stream=None,
+             max_pages_per_seq=4, num_pages=8, k_scales=None, v_scales=None, max_new_tokens=32,
+             dev_status=None, workspace=None, workspace_bytes=0)
     a.update(kw)
     return a
 
@@ -222,6 +222,9 @@ def prefill_args(**kw):
     (dict(k_new=FAKE + 8), K.KVATTN_EINVAL),
     (dict(dev_status=FAKE + 2), K.KVATTN_EINVAL),
     (dict(workspace=FAKE + 8, workspace_bytes=1 << 20), K.KVATTN_EINVAL),
+    (dict(kv_dtype=2), K.KVATTN_EUNSUPPORTED),
+    (dict(kv_dtype=1), K.KVATTN_EINVAL),                      # int8 without scales
+    (dict(kv_dtype=1, k_scales=FAKE, v_scales=FAKE + 4), K.KVATTN_EINVAL),
     (dict(n_tok=0), K.KVATTN_OK),
     (dict(n_seq=0), K.KVATTN_OK),
 ])

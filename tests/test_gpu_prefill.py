@@ -17,13 +17,13 @@ from tests.helpers import bits, host_inputs, oracle_decode, oracle_prefill
 pytestmark = pytest.mark.gpu
 
 
-def make_case(n_qh, n_kvh, ctx, n_new, d=128, page=16, seed=0, theta=1e6):
+def make_case(n_qh, n_kvh, ctx, n_new, d=128, page=16, seed=0, theta=1e6, kv="bf16"):
     """A pool and table covering ctx + n_new tokens per sequence, and the new
     tokens' q / k / v (N(0,1), bf16), back to back."""
     ctx = np.asarray(ctx, np.int32)
     n_new = np.asarray(n_new, np.int32)
     wl = W.make_workload("custom", seed=seed, n_seq=len(ctx), n_qh=n_qh, n_kvh=n_kvh,
-                         head_dim=d, page_size=page, rope_theta=theta, kv_dtype="bf16",
+                         head_dim=d, page_size=page, rope_theta=theta, kv_dtype=kv,
                          lengths=[int(x) for x in np.maximum(ctx + n_new - 1, 0)], spare=0.1)
     h = host_inputs(wl)
     g = torch.Generator().manual_seed(1000 + seed)
@@ -48,7 +48,8 @@ def run_prefill(wl, h, starts, ctx, max_new=None, split=True):
         ws = torch.full((n // 4,), float("nan"), dtype=torch.float32, device="cuda")
     K.kvattn_prefill(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
                      d["block_table"], ss, cl, out, rope_theta=wl.rope_theta, scale=wl.scale,
-                     max_new_tokens=mx, dev_status=st, workspace=ws)
+                     max_new_tokens=mx, k_scales=d["k_scales"], v_scales=d["v_scales"],
+                     dev_status=st, workspace=ws)
     torch.cuda.synchronize()
     return out, int(st.item()), d
 
@@ -59,6 +60,10 @@ def check(wl, h, starts, ctx, split=True):
     assert st == 0 and ost == 0, (st, ost)
     assert np.array_equal(pool_bits(d["k_pages"]), kp)
     assert np.array_equal(pool_bits(d["v_pages"]), vp)
+    ks, vs = oracle_prefill.scales
+    if ks is not None:
+        assert np.array_equal(d["k_scales"].cpu().numpy().view(np.uint32), ks.view(np.uint32))
+        assert np.array_equal(d["v_scales"].cpu().numpy().view(np.uint32), vs.view(np.uint32))
     return assert_close(out_f64(out), ref)
 
 
@@ -230,3 +235,30 @@ def test_tokens_past_max_new_tokens_are_left_out():
     assert_close(got[:cut], ref)
     assert np.array_equal(pool_bits(d["k_pages"]), kp)
     assert np.array_equal(pool_bits(d["v_pages"]), vp)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("ctx,n_new", [([0, 0, 0], [1, 17, 150]),            # prompts
+                                       ([100, 37, 511], [20, 64, 33]),       # chunks
+                                       ([1000, 3, 4000], [4, 4, 4])])        # drafts
+def test_int8_cache(d, ctx, n_new):
+    """The int8 cache: appended rows quantised by the decode step's recipe
+    (codes and scales bit for bit), attention over the dequantised rows."""
+    wl, h, starts, ctx = make_case(16, 4, ctx, n_new, d=d, seed=d + len(n_new), kv="int8")
+    check(wl, h, starts, ctx)
+
+
+def test_int8_one_new_token_is_the_decode_step():
+    wl, h, starts, ctx = make_case(32, 8, [50, 0, 300, 1023], [1, 1, 1, 1], d=128, seed=23, kv="int8")
+    out, st, d = run_prefill(wl, h, starts, ctx)
+    hd = dict(h, seq_lens=ctx.copy(), positions=ctx.copy())
+    wld = W.with_lengths(wl, ctx)
+    dd = to_dev(hd)
+    dec, st2, _ = run_gpu(wld, dd)
+    assert st == st2 == 0
+    for k in ("k_pages", "v_pages"):
+        assert np.array_equal(pool_bits(d[k]), pool_bits(dd[k]))
+    for k in ("k_scales", "v_scales"):
+        assert torch.equal(d[k], dd[k])
+    ref, *_ = oracle_decode(wld, hd)
+    assert_close(out_f64(out), ref)
