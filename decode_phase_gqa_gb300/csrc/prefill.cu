@@ -39,6 +39,12 @@ constexpr int kPfKeys = 32;                  // keys per staged tile
 constexpr int kPfNT = kPfKeys / 8;           // its n-tiles of 8 keys (Q K^T)
 constexpr int kPfKK = kPfKeys / 16;          // its k-steps of 16 keys (P V)
 constexpr int kPfMinTiles = 16;              // key tiles a split takes at least
+// short chunks (at most 4 new tokens a sequence: speculative drafts)
+constexpr int kPsTok = 4;                    // new tokens a CTA (x 4 heads: the MMA's 16 rows)
+constexpr int kPsWarpKeys = 16;              // keys of a stage each warp takes
+constexpr int kPsKeys = kPfWarps * kPsWarpKeys;  // keys a stage holds
+constexpr int kPsStages = 3;
+constexpr int kPsMinTiles = 8;               // stages a split takes at least
 
 struct PrefillParams {
   const __nv_bfloat16 *q, *k_new, *v_new;
@@ -48,8 +54,9 @@ struct PrefillParams {
   const int32_t *block_table, *seq_starts, *ctx_lens;
   uint32_t *status;  // KVATTN_DEV_* bits (NULL: not reported)
   int n_seq, n_tok, n_qh, n_kvh, page_size, page_shift, max_pages, num_pages;
-  int tiles_per_seq;  // 16-token tiles the grid gives each sequence
-  int n_splits;       // CTAs sharing one query tile's key tiles (strided)
+  int tiles_per_seq;  // query tiles the grid gives each sequence
+  int tile_rows;      // new tokens a query tile holds: 16, or kPsTok (short chunks)
+  int n_splits;       // CTAs sharing one query tile's key tiles
   float *part;        // n_splits > 1: [n_splits][n_tok][n_qh][D + 2] partial
                       // states (o relative to 2^m, m, l; log2 units)
   int use_rope;
@@ -83,6 +90,11 @@ __device__ __forceinline__ int query_tile_keys(int ctx, int n_new, int t0) {
 __device__ __forceinline__ int tile_splits(int n_tiles, int S) {
   return max(1, min(S, (n_tiles + kPfMinTiles - 1) / kPfMinTiles));
 }
+// the same for the short-chunk kernel's query tiles and 64-key stages
+__device__ __forceinline__ int short_tile_keys(int ctx, int n_new) { return ctx + min(n_new, kPsTok); }
+__device__ __forceinline__ int short_splits(int n_stages, int S) {
+  return max(1, min(S, (n_stages + kPsMinTiles - 1) / kPsMinTiles));
+}
 
 // ---- append ------------------------------------------------------------------
 template <int D, bool INT8>
@@ -110,7 +122,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
   // a row no valid sequence owns, or past the tokens the launch covers (the
   // attention kernel leaves those out too)
   if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new ||
-      r - start >= p.tiles_per_seq * kPfRows) {
+      r - start >= p.tiles_per_seq * p.tile_rows) {
     if (lane == 0) report(p, KVATTN_DEV_BAD_LEN);
     return;
   }
@@ -479,6 +491,248 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
   }
 }
 
+// ---- short chunks: at most 4 new tokens a sequence ------------------------------
+// The 16 MMA rows are the 4 new tokens x the 4 query heads of a group (row
+// 4 t + i: token t, head i), so no row is padding when the chunk is a
+// speculative step's drafts.  A 64-key stage is split among the 4 warps (16
+// keys each); each warp gathers and uses its own 16 keys of every stage (one
+// page lookup, two 256-byte rows a copy instruction) through a private
+// three-deep cp.async ring, so warps stream independently with no CTA barrier
+// per stage.  Each warp keeps its own online-softmax state of all 16 rows; the
+// four states are merged in shared memory at the end.
+template <int D>
+struct PsCfg {
+  static constexpr int kRowB = 2 * D;
+  static constexpr int kQBytes = 16 * kRowB;
+  static constexpr int kPart = kPsWarpKeys * kRowB;  // a warp's K (or V) rows of a stage
+  static constexpr int kRing = kPsStages * 2 * kPart;  // a warp's ring
+  static constexpr int kSmem = kQBytes + kPfWarps * kRing + 64 * 8;
+  // the end-of-kernel merge borrows the rings: [4 warps][16 rows][D] + (m, l)
+  static_assert(kPfWarps * 16 * (D + 2) * 4 <= kPfWarps * kRing, "merge buffer");
+};
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_n() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 2) prefill_short_kernel(const __grid_constant__ PrefillParams p) {
+  using C = PsCfg<D>;
+  constexpr int KS = D / 16;
+  constexpr int ND = D / 8;
+  constexpr int RCH = 2 * D / 16;  // 16-byte chunks of a row
+  const float kFloor = -1e30f;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t *qs = smem;
+  uint8_t *rings = smem + C::kQBytes;
+  float2 *turns = reinterpret_cast<float2 *>(rings + kPfWarps * C::kRing);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.n_qh / kPfWarps;  // head quads
+  const int grp = (int)(blockIdx.x % G), b = (int)(blockIdx.x / G);
+  const int g = p.n_qh / p.n_kvh;
+  const int j = grp / (g / kPfWarps);
+  const int h0 = j * g + (grp % (g / kPfWarps)) * kPfWarps;  // the quad's first head
+  int start, n_new, ctx;
+  if (!seq_span(p, b, start, n_new, ctx)) {
+    if (grp == 0 && blockIdx.z == 0 && tid == 0) report(p, KVATTN_DEV_BAD_LEN);
+    return;
+  }
+  if (grp == 0 && blockIdx.z == 0 && tid == 0 && n_new > kPsTok) report(p, KVATTN_DEV_BAD_LEN);
+  if (n_new <= 0) return;
+  const int n_keys = short_tile_keys(ctx, n_new);
+  const int n_tiles = (n_keys + kPsKeys - 1) / kPsKeys;
+  const int z = blockIdx.z, nz = short_splits(n_tiles, p.n_splits);
+  if (z >= nz) return;
+  const int per = (n_tiles + nz - 1) / nz;
+  const int kt_begin = z * per, kt_end = min(n_tiles, kt_begin + per);
+  if (tid < 64) turns[tid] = p.turns[tid];
+  __syncthreads();
+
+  const int wk = warp * kPsWarpKeys;  // the warp's keys within a stage
+  uint8_t *ring = rings + warp * C::kRing;
+  uint32_t bad = 0;  // bit s: stage s's keys lie in an out-of-range page
+  // the warp's 16 keys of stage kt (in one page: pages hold 16 keys or more)
+  auto load_part = [&](int kt, int s) {
+    const int key = kt * kPsKeys + wk;
+    long long base = -1;
+    if (key < n_keys) {
+      const int page = __ldg(p.block_table + (size_t)b * p.max_pages + (key >> p.page_shift));
+      if (page >= 0 && page < p.num_pages)
+        base = ((long long)page * p.n_kvh + j) * p.page_size + (key & (p.page_size - 1));
+      else if (lane == 0)
+        report(p, KVATTN_DEV_BAD_PAGE);
+    }
+    bad = base >= 0 ? bad & ~(1u << s) : bad | (1u << s);
+    uint8_t *Kd = ring + s * 2 * C::kPart, *Vd = Kd + C::kPart;
+#pragma unroll
+    for (int idx = lane; idx < kPsWarpKeys * RCH; idx += 32) {
+      const int r = idx / RCH, c = idx % RCH;
+      const bool ok = base >= 0 && key + r < n_keys;
+      const size_t off = ok ? (size_t)(base + r) * (2 * D) + c * 16 : 0;
+      cp_async_16_zfill(Kd + sw<D>(r, c), static_cast<const uint8_t *>(p.k_pages) + off, ok ? 16 : 0);
+      cp_async_16_zfill(Vd + sw<D>(r, c), static_cast<const uint8_t *>(p.v_pages) + off, ok ? 16 : 0);
+    }
+  };
+  // the first stages go out before the queries are formed
+#pragma unroll
+  for (int i = 0; i < kPsStages - 1; ++i) {
+    if (kt_begin + i < kt_end) load_part(kt_begin + i, i);
+    cp_async_commit();
+  }
+
+  // ---- the 16 query rows (token r / 4, head h0 + r % 4): rotated, scaled ----
+  for (int e = tid; e < 16 * (D / 2); e += kPfThreads) {
+    const int r = e / (D / 2), i = e % (D / 2);
+    const int t = r >> 2;
+    float lo = 0.f, hi = 0.f;
+    if (t < n_new) {
+      const __nv_bfloat16 *qr = p.q + ((size_t)(start + t) * p.n_qh + h0 + (r & 3)) * D;
+      lo = __bfloat162float(qr[i]);
+      hi = __bfloat162float(qr[i + D / 2]);
+      if (p.use_rope) {
+        float sn, cs;
+        sincospif(2.f * frac_turns(ctx + t, turns[i]), &sn, &cs);
+        const float a = lo * cs - hi * sn, bb = hi * cs + lo * sn;
+        lo = a;
+        hi = bb;
+      }
+    }
+    *reinterpret_cast<uint16_t *>(qs + sw<D>(r, i / 8) + (i % 8) * 2) = to16<false>(lo * p.qscale);
+    *reinterpret_cast<uint16_t *>(qs + sw<D>(r, (i + D / 2) / 8) + ((i + D / 2) % 8) * 2) =
+        to16<false>(hi * p.qscale);
+  }
+  __syncthreads();
+  uint32_t qf[KS][4];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+    ldmatrix_x4(qf[ks], smem_addr(qs) + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)));
+
+  float o[ND][4];
+#pragma unroll
+  for (int nd = 0; nd < ND; ++nd)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[nd][k] = 0.f;
+  float m[2] = {kFloor, kFloor}, l[2] = {0.f, 0.f};
+  // this lane's rows g and g + 8: tokens g / 4 and 2 + g / 4
+  const int qpos[2] = {ctx + (lane >> 4), ctx + 2 + (lane >> 4)};
+
+  for (int it = 0, kt = kt_begin; kt < kt_end; ++it, ++kt) {
+    if (kt + kPsStages - 1 < kt_end) load_part(kt + kPsStages - 1, (it + kPsStages - 1) % kPsStages);
+    cp_async_commit();
+    cp_async_wait_n<kPsStages - 1>();
+    __syncwarp();  // the other lanes' copies of this stage
+    const int st = it % kPsStages;
+    const uint32_t kb = smem_addr(ring + st * 2 * C::kPart), vb = kb + C::kPart;
+    const bool pg_ok = !((bad >> st) & 1u);
+
+    float s[2][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t kf[4];
+      const int mi = lane >> 3;
+      ldmatrix_x4(kf, kb + sw<D>((mi >> 1) * 8 + (lane & 7), 2 * ks + (mi & 1)));
+      mma16<false>(s[0], qf[ks], kf[0], kf[1]);
+      mma16<false>(s[1], qf[ks], kf[2], kf[3]);
+    }
+    const int key0 = kt * kPsKeys + wk;
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
+        const bool ok = key0 + kr <= qpos[e >> 1] && pg_ok;  // (keys past n_keys: past qpos)
+        s[nt][e] = ok ? s[nt][e] : -INFINITY;
+        mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+      }
+    float alpha[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+      const float mn = fmaxf(m[rr], mx[rr]);
+      alpha[rr] = ex2_approx(m[rr] - mn);
+      m[rr] = mn;
+      l[rr] *= alpha[rr];
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[nt][e] = ex2_approx(s[nt][e] - m[e >> 1]);
+        l[e >> 1] += s[nt][e];
+      }
+    const uint32_t a[4] = {pack16<false>(s[0][0], s[0][1]), pack16<false>(s[0][2], s[0][3]),
+                           pack16<false>(s[1][0], s[1][1]), pack16<false>(s[1][2], s[1][3])};
+#pragma unroll
+    for (int nd = 0; nd < ND; nd += 2) {
+      o[nd][0] *= alpha[0];
+      o[nd][1] *= alpha[0];
+      o[nd][2] *= alpha[1];
+      o[nd][3] *= alpha[1];
+      o[nd + 1][0] *= alpha[0];
+      o[nd + 1][1] *= alpha[0];
+      o[nd + 1][2] *= alpha[1];
+      o[nd + 1][3] *= alpha[1];
+      uint32_t vf[4];
+      ldmatrix_x4_trans(vf, vb + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, nd + (lane >> 4)));
+      mma16<false>(o[nd], a, vf[0], vf[1]);
+      mma16<false>(o[nd + 1], a, vf[2], vf[3]);
+    }
+    __syncwarp();  // the stage is rewritten kPsStages stages on
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- the four warps' states of each row: M = max m_w, weights 2^(m_w - M) ----
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
+  }
+  float *ob = reinterpret_cast<float *>(rings);  // [warp][row][D]
+  float2 *ml = reinterpret_cast<float2 *>(ob + kPfWarps * 16 * D);  // [warp][row]
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int r = (lane >> 2) + 8 * rr;
+    float *dst = ob + (warp * 16 + r) * D + 2 * (lane & 3);
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd)
+      *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][2 * rr], o[nd][2 * rr + 1]);
+    if ((lane & 3) == 0) ml[warp * 16 + r] = make_float2(m[rr], l[rr]);
+  }
+  __syncthreads();
+  for (int e = tid; e < 16 * (D / 2); e += kPfThreads) {
+    const int r = e / (D / 2), c = 2 * (e % (D / 2));
+    const int t = r >> 2, h = h0 + (r & 3);
+    if (t >= n_new || t >= kPsTok) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kPfWarps; ++w) M = fmaxf(M, ml[w * 16 + r].x);
+    float L = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPfWarps; ++w) {
+      const float2 st = ml[w * 16 + r];
+      const float wt = ex2_approx(st.x - M);
+      const float2 ov = *reinterpret_cast<const float2 *>(ob + (w * 16 + r) * D + c);
+      L += wt * st.y;
+      a0 += wt * ov.x;
+      a1 += wt * ov.y;
+    }
+    if (p.n_splits > 1) {  // the split's partial state, merged by prefill_merge_kernel
+      float *rec = p.part + (((size_t)z * p.n_tok + start + t) * p.n_qh + h) * (D + 2);
+      *reinterpret_cast<float2 *>(rec + c) = make_float2(a0, a1);
+      if (c == 0) *reinterpret_cast<float2 *>(rec + D) = make_float2(M, L);
+    } else {
+      const float f = L > 0.f ? 1.f / L : 0.f;
+      *reinterpret_cast<__nv_bfloat162 *>(p.out + ((size_t)(start + t) * p.n_qh + h) * D + c) =
+          __floats2bfloat162_rn(a0 * f, a1 * f);
+    }
+  }
+}
+
 // ---- merge of the splits' partial states -------------------------------------
 // A warp per (new-token row, query head): M = max_z m_z, w_z = 2^(m_z - M),
 // out = sum_z w_z o_z / sum_z w_z l_z (the blockwise softmax's recombination,
@@ -500,14 +754,16 @@ __global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_
   int start, n_new, ctx;
   // rows of skipped sequences, and past the tiles the grid covered, stay unwritten
   if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new ||
-      r - start >= p.tiles_per_seq * kPfRows)
+      r - start >= p.tiles_per_seq * p.tile_rows)
     return;
   constexpr int E = D / 32;  // output columns per lane
   const size_t stride = (size_t)p.n_tok * p.n_qh * (D + 2);
   const float *rec = p.part + ((size_t)r * p.n_qh + h) * (D + 2);
   // the splits of the row's query tile, as the attention kernel formed them
-  const int t0 = ((r - start) / kPfRows) * kPfRows;
-  const int nz = tile_splits((query_tile_keys(ctx, n_new, t0) + kPfKeys - 1) / kPfKeys, p.n_splits);
+  const int t0 = ((r - start) / p.tile_rows) * p.tile_rows;
+  const int nz = p.tile_rows == kPsTok
+                     ? short_splits((short_tile_keys(ctx, n_new) + kPsKeys - 1) / kPsKeys, p.n_splits)
+                     : tile_splits((query_tile_keys(ctx, n_new, t0) + kPfKeys - 1) / kPfKeys, p.n_splits);
   float M = -INFINITY;
   for (int zz = 0; zz < nz; ++zz) M = fmaxf(M, __ldg(rec + zz * stride + D));
   float L = 0.f, acc[E] = {};
@@ -537,7 +793,14 @@ cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const dim3 grid((unsigned)((long long)p.n_seq * p.tiles_per_seq * (p.n_qh / kPfWarps)), 1u,
                   (unsigned)p.n_splits);
-  prefill_attn_kernel<D, INT8><<<grid, kPfThreads, C::kSmem, stream>>>(p);
+  if (!INT8 && p.tile_rows == kPsTok) {
+    err = cudaFuncSetAttribute(prefill_short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PsCfg<D>::kSmem);
+    if (err != cudaSuccess) return err;
+    prefill_short_kernel<D><<<grid, kPfThreads, PsCfg<D>::kSmem, stream>>>(p);
+  } else {
+    prefill_attn_kernel<D, INT8><<<grid, kPfThreads, C::kSmem, stream>>>(p);
+  }
   err = cudaGetLastError();
   if (err != cudaSuccess || p.n_splits == 1) return err;
   const long long rows = (long long)p.n_tok * p.n_qh;
@@ -627,7 +890,11 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   for (int s = page_size; s > 1; s >>= 1) ++p.page_shift;
   p.max_pages = max_pages_per_seq;
   p.num_pages = num_pages;
-  p.tiles_per_seq = (int)tiles;
+  // short chunks over a bf16 cache (at most kPsTok new tokens a sequence)
+  // take the kernel whose MMA rows are tokens x heads; the rest 16-token tiles
+  const bool short_chunks = !int8 && max_new_tokens <= kPsTok;
+  p.tiles_per_seq = short_chunks ? 1 : (int)tiles;
+  p.tile_rows = short_chunks ? kPsTok : kPfRows;
   // Splits of a query tile's key tiles: short chunks over long contexts
   // (speculative verification, small decode-like chunks) share them among up
   // to 16 CTAs, each with at least 16 tiles, so every context streams at once;

@@ -262,3 +262,43 @@ def test_int8_one_new_token_is_the_decode_step():
         assert torch.equal(d[k], dd[k])
     ref, *_ = oracle_decode(wld, hd)
     assert_close(out_f64(out), ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n_qh,n_kvh", [(4, 1), (32, 8), (16, 2)])
+def test_short_chunks(d, n_qh, n_kvh):
+    """At most 4 new tokens a sequence (the kernel whose MMA rows are tokens x
+    heads): ragged chunks of 1..4 and none, caches from empty to several
+    64-key stages and splits, groups of one and of two head quads."""
+    wl, h, starts, ctx = make_case(n_qh, n_kvh, [0, 63, 64, 700, 5, 2000], [4, 1, 3, 2, 0, 4],
+                                   d=d, seed=d + n_qh + n_kvh)
+    check(wl, h, starts, ctx)
+    check(wl, h, starts, ctx, split=False)
+
+
+@pytest.mark.parametrize("page", [16, 64, 256])
+def test_short_chunks_page_sizes(page):
+    wl, h, starts, ctx = make_case(8, 2, [30, 600, 0, 4095], [4, 2, 1, 3], d=128, page=page, seed=page + 1)
+    check(wl, h, starts, ctx)
+
+
+def test_short_chunks_bad_page_and_tokens_past_the_bound():
+    """max_new_tokens = 4 with a 6-token sequence: its first 4 tokens only,
+    and the status says so; a page out of range is reported, its keys left out."""
+    wl, h, starts, ctx = make_case(8, 2, [40, 300], [3, 6], d=64, seed=29)
+    bt = h["block_table"].copy()
+    bt[0, 1] = 10 ** 6           # cached tokens 16-31 of sequence 0
+    h["block_table"] = bt
+    out, st, d = run_prefill(wl, h, starts, ctx, max_new=4)
+    assert st & K.KVATTN_DEV_BAD_PAGE and st & K.KVATTN_DEV_BAD_LEN
+    got = out_f64(out)
+    cut = starts[1] + 4
+    assert np.all(np.isnan(got[cut:]))
+    keep = np.r_[0:cut]
+    hs = dict(h, q=h["q"][keep].copy(), k_new=h["k_new"][keep].copy(), v_new=h["v_new"][keep].copy())
+    short = np.array([0, 3, 7], np.int32)
+    ref, ost, kp, vp = oracle_prefill(hs, short, ctx, wl.rope_theta, wl.scale)
+    assert ost & 2
+    assert_close(got[:cut], ref)
+    assert np.array_equal(pool_bits(d["k_pages"]), kp)
+    assert np.array_equal(pool_bits(d["v_pages"]), vp)
