@@ -43,8 +43,8 @@ constexpr int kPfMinTiles = 16;              // key tiles a split takes at least
 constexpr int kPsTok = 4;                    // new tokens a CTA (x 4 heads: the MMA's 16 rows)
 constexpr int kPsWarpKeys = 16;              // keys of a stage each warp takes
 constexpr int kPsKeys = kPfWarps * kPsWarpKeys;  // keys a stage holds
-constexpr int kPsStages = 3;
-constexpr int kPsMinTiles = 8;               // stages a split takes at least
+constexpr int kPsStages = 2;
+constexpr int kPsMinTiles = 16;              // stages a split takes at least
 
 struct PrefillParams {
   const __nv_bfloat16 *q, *k_new, *v_new;
@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
   __shared__ float4 table[sizeof(kSinCosStep) / 16];
   __shared__ __align__(16) uint8_t rowbuf[kPfWarps][4 * D];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_launch_dependents();  // the short-chunk attention grid may start at once
   if (tid < 64) inv_freq[tid] = p.inv_freq[tid];
   for (int i = tid; i < (int)(sizeof(kSinCosStep) / 16); i += kPfThreads) table[i] = kSinCosStep[i];
   __syncthreads();
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
 // speculative step's drafts.  A 64-key stage is split among the 4 warps (16
 // keys each); each warp gathers and uses its own 16 keys of every stage (one
 // page lookup, two 256-byte rows a copy instruction) through a private
-// three-deep cp.async ring, so warps stream independently with no CTA barrier
+// double-buffered cp.async ring, so warps stream independently with no CTA barrier
 // per stage.  Each warp keeps its own online-softmax state of all 16 rows; the
 // four states are merged in shared memory at the end.
 template <int D>
@@ -517,7 +518,7 @@ __device__ __forceinline__ void cp_async_wait_n() {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPfThreads, 2) prefill_short_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __grid_constant__ PrefillParams p) {
   using C = PsCfg<D>;
   constexpr int KS = D / 16;
   constexpr int ND = D / 8;
@@ -535,16 +536,23 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_short_kernel(const __gr
   const int j = grp / (g / kPfWarps);
   const int h0 = j * g + (grp % (g / kPfWarps)) * kPfWarps;  // the quad's first head
   int start, n_new, ctx;
+  // Launched as the append kernel's programmatic dependent: the cached keys
+  // (slots below ctx) are read while the append runs; a warp waits for the
+  // append grid before its first slice that holds new slots, and every
+  // thread waits before it leaves, so the grid ends after the append's.
   if (!seq_span(p, b, start, n_new, ctx)) {
     if (grp == 0 && blockIdx.z == 0 && tid == 0) report(p, KVATTN_DEV_BAD_LEN);
+    pdl_wait_primary();
     return;
   }
   if (grp == 0 && blockIdx.z == 0 && tid == 0 && n_new > kPsTok) report(p, KVATTN_DEV_BAD_LEN);
-  if (n_new <= 0) return;
   const int n_keys = short_tile_keys(ctx, n_new);
   const int n_tiles = (n_keys + kPsKeys - 1) / kPsKeys;
   const int z = blockIdx.z, nz = short_splits(n_tiles, p.n_splits);
-  if (z >= nz) return;
+  if (n_new <= 0 || z >= nz) {
+    pdl_wait_primary();
+    return;
+  }
   const int per = (n_tiles + nz - 1) / nz;
   const int kt_begin = z * per, kt_end = min(n_tiles, kt_begin + per);
   if (tid < 64) turns[tid] = p.turns[tid];
@@ -553,9 +561,14 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_short_kernel(const __gr
   const int wk = warp * kPsWarpKeys;  // the warp's keys within a stage
   uint8_t *ring = rings + warp * C::kRing;
   uint32_t bad = 0;  // bit s: stage s's keys lie in an out-of-range page
+  bool appended = false;  // the append grid is complete and its rows visible
   // the warp's 16 keys of stage kt (in one page: pages hold 16 keys or more)
   auto load_part = [&](int kt, int s) {
     const int key = kt * kPsKeys + wk;
+    if (!appended && key + kPsWarpKeys > ctx) {
+      pdl_wait_primary();
+      appended = true;
+    }
     long long base = -1;
     if (key < n_keys) {
       const int page = __ldg(p.block_table + (size_t)b * p.max_pages + (key >> p.page_shift));
@@ -684,6 +697,8 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_short_kernel(const __gr
     __syncwarp();  // the stage is rewritten kPsStages stages on
   }
   cp_async_wait_all();
+  if (!appended) pdl_wait_primary();
+  pdl_launch_dependents();  // the merge grid may be placed
   __syncthreads();
 
   // ---- the four warps' states of each row: M = max m_w, weights 2^(m_w - M) ----
@@ -704,6 +719,10 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_short_kernel(const __gr
     if ((lane & 3) == 0) ml[warp * 16 + r] = make_float2(m[rr], l[rr]);
   }
   __syncthreads();
+  // one split: the output; several: this split's state, merged by
+  // prefill_merge_kernel (a warp per row there hides the loads' latency better
+  // than the last split to finish merging, or a CTA per head quad)
+  const bool direct = p.n_splits == 1;
   for (int e = tid; e < 16 * (D / 2); e += kPfThreads) {
     const int r = e / (D / 2), c = 2 * (e % (D / 2));
     const int t = r >> 2, h = h0 + (r & 3);
@@ -721,7 +740,7 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_short_kernel(const __gr
       a0 += wt * ov.x;
       a1 += wt * ov.y;
     }
-    if (p.n_splits > 1) {  // the split's partial state, merged by prefill_merge_kernel
+    if (!direct) {
       float *rec = p.part + (((size_t)z * p.n_tok + start + t) * p.n_qh + h) * (D + 2);
       *reinterpret_cast<float2 *>(rec + c) = make_float2(a0, a1);
       if (c == 0) *reinterpret_cast<float2 *>(rec + D) = make_float2(M, L);
@@ -740,6 +759,7 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_short_kernel(const __gr
 template <int D>
 __global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_constant__ PrefillParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait_primary();  // the attention grid's partial states are complete and visible
   const long long item = (long long)blockIdx.x * kPfWarps + warp;  // (row, query head)
   if (item >= (long long)p.n_tok * p.n_qh) return;
   const int r = (int)(item / p.n_qh), h = (int)(item - (long long)r * p.n_qh);
@@ -780,6 +800,23 @@ __global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_
   for (int e = 0; e < E; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(acc[e] * f);
 }
 
+// a launch that may overlap the end of the stream's previous kernel (its
+// threads wait for that kernel with griddepcontrol.wait)
+template <typename K>
+cudaError_t launch_pdl(K kern, dim3 grid, int smem, cudaStream_t stream, const PrefillParams &p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <int D, bool INT8>
 cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
   using C = PfCfg<D, INT8>;
@@ -797,15 +834,16 @@ cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
     err = cudaFuncSetAttribute(prefill_short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                PsCfg<D>::kSmem);
     if (err != cudaSuccess) return err;
-    prefill_short_kernel<D><<<grid, kPfThreads, PsCfg<D>::kSmem, stream>>>(p);
+    err = launch_pdl(prefill_short_kernel<D>, grid, PsCfg<D>::kSmem, stream, p);
+    if (err != cudaSuccess) return err;
   } else {
     prefill_attn_kernel<D, INT8><<<grid, kPfThreads, C::kSmem, stream>>>(p);
   }
   err = cudaGetLastError();
   if (err != cudaSuccess || p.n_splits == 1) return err;
   const long long rows = (long long)p.n_tok * p.n_qh;
-  prefill_merge_kernel<D><<<(unsigned)((rows + kPfWarps - 1) / kPfWarps), kPfThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(prefill_merge_kernel<D>, dim3((unsigned)((rows + kPfWarps - 1) / kPfWarps)), 0,
+                    stream, p);
 }
 
 bool pf_aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }

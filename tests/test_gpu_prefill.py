@@ -181,12 +181,15 @@ def test_benchmark_shapes_at_full_size(kind):
     assert_close(out_f64(out), ref)
 
 
-def test_decode_after_prefill_reads_the_prefilled_cache():
-    """A prompt through kvattn_prefill, then two decode steps through
-    kvattn_decode: the steps attend over the keys the prefill appended, and
-    the whole sequence equals the oracle's decode steps one token at a time."""
+@pytest.mark.parametrize("ctx0,prompt", [([0, 40], [70, 9]),      # 16-token query tiles
+                                         ([100, 700], [3, 4])])   # the short-chunk kernel
+def test_decode_after_prefill_reads_the_prefilled_cache(ctx0, prompt):
+    """A prompt (or drafts) through kvattn_prefill, then two decode steps
+    through kvattn_decode: the steps attend over the keys the prefill
+    appended, and the whole sequence equals the oracle's decode steps one
+    token at a time."""
     n_qh, n_kvh, d = 16, 4, 128
-    ctx0, prompt, steps = np.array([0, 40], np.int32), np.array([70, 9], np.int32), 2
+    ctx0, prompt, steps = np.array(ctx0, np.int32), np.array(prompt, np.int32), 2
     # pages for the prompt and the decode steps that follow
     wl, h, starts, ctx = make_case(n_qh, n_kvh, ctx0, prompt + steps, d=d, seed=17)
     T = int(prompt.sum())
@@ -302,3 +305,27 @@ def test_short_chunks_bad_page_and_tokens_past_the_bound():
     assert_close(got[:cut], ref)
     assert np.array_equal(pool_bits(d["k_pages"]), kp)
     assert np.array_equal(pool_bits(d["v_pages"]), vp)
+
+
+def test_short_chunks_workspace_reused_across_calls():
+    """The split counters live in the workspace and are reset by every call:
+    two calls on one workspace (the second re-appends the same rows) give the
+    oracle's outputs both times."""
+    wl, h, starts, ctx = make_case(32, 8, [3000, 1500, 5000], [4, 3, 4], d=128, seed=31)
+    d = to_dev(h)
+    ss = torch.from_numpy(starts).cuda()
+    cl = torch.from_numpy(np.ascontiguousarray(ctx)).cuda()
+    n = K.kvattn_prefill_workspace_size(d["q"].shape[0], d["q"].shape[1], d["q"].shape[2])
+    ws = torch.full((n // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    ref, ost, kp, vp = oracle_prefill(h, starts, ctx, wl.rope_theta, wl.scale)
+    assert ost == 0
+    for _ in range(2):
+        out = torch.full_like(d["q"], float("nan"))
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        K.kvattn_prefill(d["q"], d["k_new"], d["v_new"], d["k_pages"], d["v_pages"],
+                         d["block_table"], ss, cl, out, rope_theta=wl.rope_theta, scale=wl.scale,
+                         max_new_tokens=4, dev_status=st, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert np.array_equal(pool_bits(d["k_pages"]), kp)
+        assert_close(out_f64(out), ref)
