@@ -81,6 +81,24 @@ __device__ __forceinline__ bool seq_span(const PrefillParams &p, int b, int &sta
   return start >= 0 && end <= p.n_tok && n_new >= 0 && ctx >= 0 && (long long)ctx + n_new <= cap;
 }
 
+// The sequence of new-token row r: the last b < n_seq with seq_starts[b] <= r
+// (the answer of a binary search when the starts ascend; a row the sequence
+// does not hold is caught by the caller's seq_span check).  Called by a whole
+// warp: each round its 32 lanes probe 32 evenly spaced starts of the range
+// left and keep the piece after the last probe <= r, so 64 sequences take
+// two rounds of loads instead of six dependent ones.
+__device__ __forceinline__ int seq_of_row(const PrefillParams &p, int r, int lane) {
+  int lo = 0, hi = p.n_seq;
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const unsigned le = __ballot_sync(0xffffffffu, idx < hi && __ldg(p.seq_starts + idx) <= r);
+    lo += le ? (31 - __clz(le)) * step : 0;
+    hi = min(hi, lo + step);
+  }
+  return lo;
+}
+
 // Key tiles of the query tile starting at new token t0 (n_new new tokens after
 // ctx cached ones), and the splits sharing them: S at most, each with at least
 // kPfMinTiles tiles (the attention and merge kernels both use this).
@@ -110,15 +128,18 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
   const long long item = (long long)blockIdx.x * kPfWarps + warp;  // (new-token row, KV head)
   if (item >= (long long)p.n_tok * p.n_kvh) return;
   const int r = (int)(item / p.n_kvh), j = (int)(item - (long long)r * p.n_kvh);
-  // the sequence of row r: the last b with seq_starts[b] <= r
-  int lo = 0, hi = p.n_seq;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(p.seq_starts + mid) <= r)
-      lo = mid;
-    else
-      hi = mid;
+  // the new key and value rows are fetched (a 16-byte chunk a lane, held in
+  // registers) while the row's sequence is found
+  constexpr int CH = 2 * D / 16;  // 16-byte chunks of a row
+  static_assert(2 * CH <= 32, "a chunk a lane");
+  uint8_t *buf = rowbuf[warp];
+  uint4 chunk = make_uint4(0u, 0u, 0u, 0u);
+  if (lane < 2 * CH) {
+    const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + ((size_t)r * p.n_kvh + j) * D);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + ((size_t)r * p.n_kvh + j) * D);
+    chunk = lane < CH ? ks[lane] : vs[lane - CH];
   }
+  const int lo = seq_of_row(p, r, lane);
   int start, n_new, ctx;
   // a row no valid sequence owns, or past the tokens the launch covers (the
   // attention kernel leaves those out too)
@@ -133,12 +154,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
     if (lane == 0) report(p, KVATTN_DEV_BAD_PAGE);
     return;
   }
-  constexpr int CH = 2 * D / 16;  // 16-byte chunks of a row
-  uint8_t *buf = rowbuf[warp];
-  const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + ((size_t)r * p.n_kvh + j) * D);
-  const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + ((size_t)r * p.n_kvh + j) * D);
-  for (int c = lane; c < 2 * CH; c += 32)
-    reinterpret_cast<uint4 *>(buf)[c] = c < CH ? ks[c] : vs[c - CH];
+  if (lane < 2 * CH) reinterpret_cast<uint4 *>(buf)[lane] = chunk;
   __syncwarp();
   stage_new_row<D, INT8>(slot, inv_freq, table, p.use_rope != 0, lane, buf);
   const size_t prow = ((size_t)page * p.n_kvh + j) * p.page_size + (slot & (p.page_size - 1));
@@ -763,14 +779,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_
   const long long item = (long long)blockIdx.x * kPfWarps + warp;  // (row, query head)
   if (item >= (long long)p.n_tok * p.n_qh) return;
   const int r = (int)(item / p.n_qh), h = (int)(item - (long long)r * p.n_qh);
-  int lo = 0, hi = p.n_seq;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(p.seq_starts + mid) <= r)
-      lo = mid;
-    else
-      hi = mid;
-  }
+  const int lo = seq_of_row(p, r, lane);
   int start, n_new, ctx;
   // rows of skipped sequences, and past the tiles the grid covered, stay unwritten
   if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new ||

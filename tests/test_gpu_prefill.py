@@ -329,3 +329,17 @@ def test_short_chunks_workspace_reused_across_calls():
         assert int(st.item()) == 0
         assert np.array_equal(pool_bits(d["k_pages"]), kp)
         assert_close(out_f64(out), ref)
+
+
+@pytest.mark.parametrize("max_new", [3, 20])
+def test_many_sequences_with_empty_chunks(max_new):
+    """1100 sequences (three rounds of the row -> sequence search), a third of
+    them with no new token (equal starts), short caches: both kernels."""
+    rng = np.random.default_rng(37 + max_new)
+    n_new = rng.integers(0, 4, 1100)
+    n_new[-1] = 3
+    if max_new > 4:
+        n_new[::97] = 20
+    ctx = rng.integers(0, 41, 1100)
+    wl, h, starts, ctx = make_case(4, 1, ctx, n_new, d=64, seed=41 + max_new)
+    check(wl, h, starts, ctx)
