@@ -115,48 +115,118 @@ __device__ __forceinline__ int short_splits(int n_stages, int S) {
 }
 
 // ---- append ------------------------------------------------------------------
+// A warp per (new-token row, KV head); the CTA's four warps hold at most four
+// tokens (one when n_kvh >= 4 divides evenly), and the RoPE angles of each token
+// (an fp64 product reduced and rounded per pair, costly at this part's fp64
+// rate) are formed once by the first warp holding it and shared: the row
+// recipe is the decode step's (store_angle, rot_store, quant_row_warp), so the
+// stored bits are the same.
+template <int D, bool INT8>
+__device__ __forceinline__ void stage_row_cs(const float2 *cs, bool use_rope, int lane, uint8_t *buf) {
+  constexpr int PPL = D / 64;
+  float xk[D / 32], xv[D / 32];
+  const __nv_bfloat16 *raw = reinterpret_cast<const __nv_bfloat16 *>(buf);
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) {
+    xk[k] = __bfloat162float(raw[row_elem<D>(lane, k)]);
+    xv[k] = __bfloat162float(raw[D + row_elem<D>(lane, k)]);
+  }
+  __syncwarp();  // every lane has read the raw rows before the buffer is rewritten
+  if (use_rope) {
+#pragma unroll
+    for (int k = 0; k < PPL; ++k) {
+      const float2 a = cs[lane + 32 * k];
+      rot_store(xk[k], xk[PPL + k], a.x, a.y, xk[k], xk[PPL + k]);
+    }
+  }
+  if constexpr (INT8) {
+    int8_t kc[D / 32], vc[D / 32];
+    const float ksc = quant_row_warp<D>(xk, kc);
+    const float vsc = quant_row_warp<D>(xv, vc);
+    int8_t *kr = reinterpret_cast<int8_t *>(buf), *vr = kr + D;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) {
+      kr[row_elem<D>(lane, k)] = kc[k];
+      vr[row_elem<D>(lane, k)] = vc[k];
+    }
+    if (lane == 0) {
+      float *sc = reinterpret_cast<float *>(buf + 2 * D);
+      sc[0] = ksc;
+      sc[1] = vsc;
+    }
+  } else {
+    __nv_bfloat16 *kr = reinterpret_cast<__nv_bfloat16 *>(buf), *vr = kr + D;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) {
+      kr[row_elem<D>(lane, k)] = __float2bfloat16_rn(xk[k]);
+      vr[row_elem<D>(lane, k)] = __float2bfloat16_rn(xv[k]);
+    }
+  }
+  __syncwarp();
+}
+
 template <int D, bool INT8>
 __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid_constant__ PrefillParams p) {
   __shared__ double inv_freq[64];
   __shared__ float4 table[sizeof(kSinCosStep) / 16];
   __shared__ __align__(16) uint8_t rowbuf[kPfWarps][4 * D];
+  __shared__ float2 cs[kPfWarps][D / 2];  // (cos, sin) per pair, by the warp that formed them
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();  // the short-chunk attention grid may start at once
   if (tid < 64) inv_freq[tid] = p.inv_freq[tid];
   for (int i = tid; i < (int)(sizeof(kSinCosStep) / 16); i += kPfThreads) table[i] = kSinCosStep[i];
-  __syncthreads();
-  const long long item = (long long)blockIdx.x * kPfWarps + warp;  // (new-token row, KV head)
-  if (item >= (long long)p.n_tok * p.n_kvh) return;
-  const int r = (int)(item / p.n_kvh), j = (int)(item - (long long)r * p.n_kvh);
+  const long long item0 = (long long)blockIdx.x * kPfWarps;
+  const long long item = item0 + warp;  // (new-token row, KV head)
+  const bool live = item < (long long)p.n_tok * p.n_kvh;
+  const int r = live ? (int)(item / p.n_kvh) : 0, j = live ? (int)(item - (long long)r * p.n_kvh) : 0;
   // the new key and value rows are fetched (a 16-byte chunk a lane, held in
   // registers) while the row's sequence is found
   constexpr int CH = 2 * D / 16;  // 16-byte chunks of a row
   static_assert(2 * CH <= 32, "a chunk a lane");
-  uint8_t *buf = rowbuf[warp];
   uint4 chunk = make_uint4(0u, 0u, 0u, 0u);
-  if (lane < 2 * CH) {
+  if (live && lane < 2 * CH) {
     const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + ((size_t)r * p.n_kvh + j) * D);
     const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + ((size_t)r * p.n_kvh + j) * D);
     chunk = lane < CH ? ks[lane] : vs[lane - CH];
   }
-  const int lo = seq_of_row(p, r, lane);
-  int start, n_new, ctx;
-  // a row no valid sequence owns, or past the tokens the launch covers (the
-  // attention kernel leaves those out too)
-  if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new ||
-      r - start >= p.tiles_per_seq * p.tile_rows) {
-    if (lane == 0) report(p, KVATTN_DEV_BAD_LEN);
-    return;
+  // (every test below depends on the token only, so all warps of a token agree)
+  bool ok = false;
+  int lo = 0, slot = 0, page = 0;
+  if (live) {
+    lo = seq_of_row(p, r, lane);
+    int start, n_new, ctx;
+    // a row no valid sequence owns, or past the tokens the launch covers (the
+    // attention kernel leaves those out too)
+    if (!seq_span(p, lo, start, n_new, ctx) || r < start || r >= start + n_new ||
+        r - start >= p.tiles_per_seq * p.tile_rows) {
+      if (lane == 0 && j == 0) report(p, KVATTN_DEV_BAD_LEN);
+    } else {
+      slot = ctx + (r - start);  // also the RoPE position
+      page = __ldg(p.block_table + (size_t)lo * p.max_pages + (slot >> p.page_shift));
+      if (page < 0 || page >= p.num_pages) {
+        if (lane == 0 && j == 0) report(p, KVATTN_DEV_BAD_PAGE);
+      } else {
+        ok = true;
+      }
+    }
   }
-  const int slot = ctx + (r - start);  // also the RoPE position
-  const int page = __ldg(p.block_table + (size_t)lo * p.max_pages + (slot >> p.page_shift));
-  if (page < 0 || page >= p.num_pages) {
-    if (lane == 0) report(p, KVATTN_DEV_BAD_PAGE);
-    return;
+  __syncthreads();  // the tables
+  // the token's first warp in this CTA forms its angles
+  const int owner = (int)(max((long long)r * p.n_kvh, item0) - item0);
+  if (ok && p.use_rope && owner == warp) {
+#pragma unroll
+    for (int k = 0; k < D / 64; ++k) {
+      float c, sn;
+      store_angle(slot, inv_freq[lane + 32 * k], table, c, sn);
+      cs[warp][lane + 32 * k] = make_float2(c, sn);
+    }
   }
+  __syncthreads();
+  if (!ok) return;
+  uint8_t *buf = rowbuf[warp];
   if (lane < 2 * CH) reinterpret_cast<uint4 *>(buf)[lane] = chunk;
   __syncwarp();
-  stage_new_row<D, INT8>(slot, inv_freq, table, p.use_rope != 0, lane, buf);
+  stage_row_cs<D, INT8>(cs[owner], p.use_rope != 0, lane, buf);
   const size_t prow = ((size_t)page * p.n_kvh + j) * p.page_size + (slot & (p.page_size - 1));
   // the stored key row, then the value row (int8: codes, the two scales after)
   constexpr int RB = INT8 ? D : 2 * D, SCH = RB / 16;
