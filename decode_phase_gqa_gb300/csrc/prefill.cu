@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
   __shared__ __align__(16) uint8_t rowbuf[kPfWarps][4 * D];
   __shared__ float2 cs[kPfWarps][D / 2];  // (cos, sin) per pair, by the warp that formed them
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_launch_dependents();  // the short-chunk attention grid may start at once
+  pdl_launch_dependents();  // the attention grid may start at once
   if (tid < 64) inv_freq[tid] = p.inv_freq[tid];
   for (int i = tid; i < (int)(sizeof(kSinCosStep) / 16); i += kPfThreads) table[i] = kSinCosStep[i];
   const long long item0 = (long long)blockIdx.x * kPfWarps;
@@ -330,23 +330,33 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
   const int g = p.n_qh / p.n_kvh;
   const int j = grp / (g / kPfWarps);
   const int h = j * g + (grp % (g / kPfWarps)) * kPfWarps + warp;  // this warp's head
+  // Launched as the append kernel's programmatic dependent: the queries are
+  // formed while the append runs, and every thread waits for the append grid
+  // before the first key tile (or before it leaves).
   int start, n_new, ctx;
   if (!seq_span(p, b, start, n_new, ctx)) {
     if (qt == 0 && grp == 0 && tid == 0) report(p, KVATTN_DEV_BAD_LEN);
+    pdl_wait_primary();
     return;
   }
   // more new tokens than the grid's tiles cover (a bound the caller gave)
   if (qt == 0 && grp == 0 && tid == 0 && n_new > p.tiles_per_seq * kPfRows)
     report(p, KVATTN_DEV_BAD_LEN);
   const int t0 = qt * kPfRows;
-  if (t0 >= n_new) return;
+  if (t0 >= n_new) {
+    pdl_wait_primary();
+    return;
+  }
   // keys the CTA's last valid row sees: 0 .. ctx + min(n_new, t0 + 16) - 1, in
   // tiles; split z of the query tile takes a contiguous range of them (a split
   // past the query tile's count has nothing to do)
   const int n_keys = query_tile_keys(ctx, n_new, t0);
   const int n_tiles = (n_keys + kPfKeys - 1) / kPfKeys;
   const int z = blockIdx.z, nz = tile_splits(n_tiles, p.n_splits);
-  if (z >= nz) return;
+  if (z >= nz) {
+    pdl_wait_primary();
+    return;
+  }
   const int per = (n_tiles + nz - 1) / nz;
   const int kt_begin = z * per, kt_end = min(n_tiles, kt_begin + per);
   if (tid < 64) turns[tid] = p.turns[tid];
@@ -435,6 +445,7 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
   const int qpos[2] = {ctx + t0 + (lane >> 2), ctx + t0 + (lane >> 2) + 8};
 
   // this CTA's key tiles: kt_begin .. kt_end - 1 (split z of nz)
+  pdl_wait_primary();  // the appended rows are complete and visible
   if (kt_begin < kt_end)
     load_tile(kt_begin, 0);
   else
@@ -916,7 +927,8 @@ cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
     err = launch_pdl(prefill_short_kernel<D>, grid, PsCfg<D>::kSmem, stream, p);
     if (err != cudaSuccess) return err;
   } else {
-    prefill_attn_kernel<D, INT8><<<grid, kPfThreads, C::kSmem, stream>>>(p);
+    err = launch_pdl(prefill_attn_kernel<D, INT8>, grid, C::kSmem, stream, p);
+    if (err != cudaSuccess) return err;
   }
   err = cudaGetLastError();
   if (err != cudaSuccess || p.n_splits == 1) return err;
