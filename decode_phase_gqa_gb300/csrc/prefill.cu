@@ -598,12 +598,15 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
 // double-buffered cp.async ring, so warps stream independently with no CTA barrier
 // per stage.  Each warp keeps its own online-softmax state of all 16 rows; the
 // four states are merged in shared memory at the end.
-template <int D>
+template <int D, bool INT8>
 struct PsCfg {
   static constexpr int kRowB = 2 * D;
   static constexpr int kQBytes = 16 * kRowB;
-  static constexpr int kPart = kPsWarpKeys * kRowB;  // a warp's K (or V) rows of a stage
-  static constexpr int kRing = kPsStages * 2 * kPart;  // a warp's ring
+  static constexpr int kPart = kPsWarpKeys * kRowB;  // a warp's K (or V) rows of a stage (16-bit)
+  // int8 cache: a stage is the codes (K, V) and row scales (K, V) as copied,
+  // dequantised into one f16 K/V tile pair after the ring
+  static constexpr int kRaw = 2 * kPsWarpKeys * D + 2 * kPsWarpKeys * 4;
+  static constexpr int kRing = INT8 ? kPsStages * kRaw + 2 * kPart : kPsStages * 2 * kPart;  // a warp's
   static constexpr int kSmem = kQBytes + kPfWarps * kRing + 64 * 8;
   // the end-of-kernel merge borrows the rings: [4 warps][16 rows][D] + (m, l)
   static_assert(kPfWarps * 16 * (D + 2) * 4 <= kPfWarps * kRing, "merge buffer");
@@ -614,9 +617,9 @@ __device__ __forceinline__ void cp_async_wait_n() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int D>
+template <int D, bool INT8>
 __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __grid_constant__ PrefillParams p) {
-  using C = PsCfg<D>;
+  using C = PsCfg<D, INT8>;
   constexpr int KS = D / 16;
   constexpr int ND = D / 8;
   constexpr int RCH = 2 * D / 16;  // 16-byte chunks of a row
@@ -675,6 +678,25 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         report(p, KVATTN_DEV_BAD_PAGE);
     }
     bad = base >= 0 ? bad & ~(1u << s) : bad | (1u << s);
+    if constexpr (INT8) {
+      // codes row by row (plain layout), then the 16 K and 16 V scales
+      uint8_t *Kd = ring + s * C::kRaw, *Vd = Kd + kPsWarpKeys * D;
+      constexpr int CC = D / 16;  // 16-byte chunks of a code row
+#pragma unroll
+      for (int idx = lane; idx < kPsWarpKeys * CC; idx += 32) {
+        const int r = idx / CC, c = idx % CC;
+        const bool ok = base >= 0 && key + r < n_keys;
+        const size_t off = ok ? (size_t)(base + r) * D + c * 16 : 0;
+        cp_async_16_zfill(Kd + r * D + c * 16, static_cast<const uint8_t *>(p.k_pages) + off, ok ? 16 : 0);
+        cp_async_16_zfill(Vd + r * D + c * 16, static_cast<const uint8_t *>(p.v_pages) + off, ok ? 16 : 0);
+      }
+      if (lane < 8) {
+        const float *src = lane < 4 ? p.k_scales : p.v_scales;
+        const size_t off = base >= 0 ? (size_t)base + 4 * (lane & 3) : 0;
+        cp_async_16_zfill(Vd + kPsWarpKeys * D + 16 * lane, src + off, base >= 0 ? 16 : 0);
+      }
+      return;
+    }
     uint8_t *Kd = ring + s * 2 * C::kPart, *Vd = Kd + C::kPart;
 #pragma unroll
     for (int idx = lane; idx < kPsWarpKeys * RCH; idx += 32) {
@@ -709,9 +731,9 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         hi = bb;
       }
     }
-    *reinterpret_cast<uint16_t *>(qs + sw<D>(r, i / 8) + (i % 8) * 2) = to16<false>(lo * p.qscale);
+    *reinterpret_cast<uint16_t *>(qs + sw<D>(r, i / 8) + (i % 8) * 2) = to16<INT8>(lo * p.qscale);
     *reinterpret_cast<uint16_t *>(qs + sw<D>(r, (i + D / 2) / 8) + ((i + D / 2) % 8) * 2) =
-        to16<false>(hi * p.qscale);
+        to16<INT8>(hi * p.qscale);
   }
   __syncthreads();
   uint32_t qf[KS][4];
@@ -734,8 +756,33 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
     cp_async_wait_n<kPsStages - 1>();
     __syncwarp();  // the other lanes' copies of this stage
     const int st = it % kPsStages;
-    const uint32_t kb = smem_addr(ring + st * 2 * C::kPart), vb = kb + C::kPart;
+    uint32_t kb = smem_addr(ring + st * 2 * C::kPart), vb = kb + C::kPart;
     const bool pg_ok = !((bad >> st) & 1u);
+    if constexpr (INT8) {
+      // the slice's codes times their row scales -> the warp's f16 tiles (rows
+      // past the keys: zero, whatever their scale slot holds)
+      const int8_t *raw = reinterpret_cast<const int8_t *>(ring + st * C::kRaw);
+      const float *scl = reinterpret_cast<const float *>(raw + 2 * kPsWarpKeys * D);
+      uint8_t *tile = ring + kPsStages * C::kRaw;
+      const int key0 = kt * kPsKeys + wk;
+#pragma unroll 4
+      for (int idx = lane; idx < 2 * kPsWarpKeys * (D / 8); idx += 32) {
+        const int v = idx / (kPsWarpKeys * (D / 8)), rest = idx - v * kPsWarpKeys * (D / 8);
+        const int r = rest / (D / 8), c = rest % (D / 8);
+        const float sc = key0 + r < n_keys ? scl[v * kPsWarpKeys + r] : 0.f;
+        const uint2 w = *reinterpret_cast<const uint2 *>(raw + v * kPsWarpKeys * D + r * D + c * 8);
+        const int8_t *e = reinterpret_cast<const int8_t *>(&w);
+        uint4 o4;
+        o4.x = pack16<true>(e[0] * sc, e[1] * sc);
+        o4.y = pack16<true>(e[2] * sc, e[3] * sc);
+        o4.z = pack16<true>(e[4] * sc, e[5] * sc);
+        o4.w = pack16<true>(e[6] * sc, e[7] * sc);
+        *reinterpret_cast<uint4 *>(tile + v * C::kPart + sw<D>(r, c)) = o4;
+      }
+      __syncwarp();
+      kb = smem_addr(tile);
+      vb = kb + C::kPart;
+    }
 
     float s[2][4] = {};
 #pragma unroll
@@ -743,8 +790,8 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
       uint32_t kf[4];
       const int mi = lane >> 3;
       ldmatrix_x4(kf, kb + sw<D>((mi >> 1) * 8 + (lane & 7), 2 * ks + (mi & 1)));
-      mma16<false>(s[0], qf[ks], kf[0], kf[1]);
-      mma16<false>(s[1], qf[ks], kf[2], kf[3]);
+      mma16<INT8>(s[0], qf[ks], kf[0], kf[1]);
+      mma16<INT8>(s[1], qf[ks], kf[2], kf[3]);
     }
     const int key0 = kt * kPsKeys + wk;
     float mx[2] = {-INFINITY, -INFINITY};
@@ -774,8 +821,8 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         s[nt][e] = ex2_approx(s[nt][e] - m[e >> 1]);
         l[e >> 1] += s[nt][e];
       }
-    const uint32_t a[4] = {pack16<false>(s[0][0], s[0][1]), pack16<false>(s[0][2], s[0][3]),
-                           pack16<false>(s[1][0], s[1][1]), pack16<false>(s[1][2], s[1][3])};
+    const uint32_t a[4] = {pack16<INT8>(s[0][0], s[0][1]), pack16<INT8>(s[0][2], s[0][3]),
+                           pack16<INT8>(s[1][0], s[1][1]), pack16<INT8>(s[1][2], s[1][3])};
 #pragma unroll
     for (int nd = 0; nd < ND; nd += 2) {
       o[nd][0] *= alpha[0];
@@ -788,8 +835,8 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
       o[nd + 1][3] *= alpha[1];
       uint32_t vf[4];
       ldmatrix_x4_trans(vf, vb + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, nd + (lane >> 4)));
-      mma16<false>(o[nd], a, vf[0], vf[1]);
-      mma16<false>(o[nd + 1], a, vf[2], vf[3]);
+      mma16<INT8>(o[nd], a, vf[0], vf[1]);
+      mma16<INT8>(o[nd + 1], a, vf[2], vf[3]);
     }
     __syncwarp();  // the stage is rewritten kPsStages stages on
   }
@@ -920,11 +967,12 @@ cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const dim3 grid((unsigned)((long long)p.n_seq * p.tiles_per_seq * (p.n_qh / kPfWarps)), 1u,
                   (unsigned)p.n_splits);
-  if (!INT8 && p.tile_rows == kPsTok) {
-    err = cudaFuncSetAttribute(prefill_short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               PsCfg<D>::kSmem);
+  if (p.tile_rows == kPsTok) {
+    using S = PsCfg<D, INT8>;
+    err = cudaFuncSetAttribute(prefill_short_kernel<D, INT8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               S::kSmem);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(prefill_short_kernel<D>, grid, PsCfg<D>::kSmem, stream, p);
+    err = launch_pdl(prefill_short_kernel<D, INT8>, grid, S::kSmem, stream, p);
     if (err != cudaSuccess) return err;
   } else {
     err = launch_pdl(prefill_attn_kernel<D, INT8>, grid, C::kSmem, stream, p);
@@ -1019,9 +1067,9 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   for (int s = page_size; s > 1; s >>= 1) ++p.page_shift;
   p.max_pages = max_pages_per_seq;
   p.num_pages = num_pages;
-  // short chunks over a bf16 cache (at most kPsTok new tokens a sequence)
-  // take the kernel whose MMA rows are tokens x heads; the rest 16-token tiles
-  const bool short_chunks = !int8 && max_new_tokens <= kPsTok;
+  // short chunks (at most kPsTok new tokens a sequence) take the kernel whose
+  // MMA rows are tokens x heads; the rest 16-token tiles
+  const bool short_chunks = max_new_tokens <= kPsTok;
   p.tiles_per_seq = short_chunks ? 1 : (int)tiles;
   p.tile_rows = short_chunks ? kPsTok : kPfRows;
   // Splits of a query tile's key tiles: short chunks over long contexts

@@ -279,10 +279,22 @@ def test_short_chunks(d, n_qh, n_kvh):
     check(wl, h, starts, ctx, split=False)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
 @pytest.mark.parametrize("page", [16, 64, 256])
-def test_short_chunks_page_sizes(page):
-    wl, h, starts, ctx = make_case(8, 2, [30, 600, 0, 4095], [4, 2, 1, 3], d=128, page=page, seed=page + 1)
+def test_short_chunks_page_sizes(page, kv):
+    wl, h, starts, ctx = make_case(8, 2, [30, 600, 0, 4095], [4, 2, 1, 3], d=128, page=page,
+                                   seed=page + 1, kv=kv)
     check(wl, h, starts, ctx)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_short_chunks_int8(d):
+    """Short chunks over an int8 cache: ragged 0..4 new tokens, caches from
+    empty to several splits, with and without splits."""
+    wl, h, starts, ctx = make_case(16, 4, [0, 63, 64, 700, 5, 2000], [4, 1, 3, 2, 0, 4], d=d,
+                                   seed=d + 43, kv="int8")
+    check(wl, h, starts, ctx)
+    check(wl, h, starts, ctx, split=False)
 
 
 def test_short_chunks_bad_page_and_tokens_past_the_bound():
