@@ -241,9 +241,13 @@ int kvattn_decode_layers(int n_layers, const void *q, const void *k_new, const v
  *              i has slot and RoPE position ctx_lens[b] + i.
  * n_qh / n_kvh must be a multiple of 4 (a CTA serves 4 query heads of a group),
  *              else KVATTN_EUNSUPPORTED.
- * max_new_tokens  an upper bound on every n_b; it sizes the launch (a
- *              sequence with more new tokens has the rest neither appended nor
- *              attended, and KVATTN_DEV_BAD_LEN is reported).
+ * max_new_tokens  an upper bound on every n_b; it sizes the launch: up to 4
+ *              (speculative drafts), 4 new tokens a sequence are covered, by a
+ *              kernel whose MMA rows are 4 tokens x 4 heads; above, the bound
+ *              rounded up to a multiple of 16, by 16-token query tiles.  A
+ *              sequence with more new tokens than the launch covers has the
+ *              rest neither appended nor attended, and KVATTN_DEV_BAD_LEN is
+ *              reported.
  * dev_status   device uint32, 4-byte aligned, or NULL: KVATTN_DEV_BAD_LEN is
  *              OR-ed in for a sequence whose rows or slots do not fit (it is
  *              skipped), KVATTN_DEV_BAD_PAGE for a page outside [0, num_pages)
