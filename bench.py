@@ -470,7 +470,8 @@ def run_prefill_config(kind, steps, warmup, device, stream, seed=0):
              into empty caches (compute-bound: causal attention FLOPs);
     verify:  Qwen3-8B-shaped heads (32/8, d 128) over the Qwen3 workload's 64
              cache lengths, 4 draft tokens each (a speculative step's check;
-             bandwidth-bound: the cached K/V are read once per group).
+             bandwidth-bound: the cached K/V are read once per group);
+    verify_int8: the same over an int8 cache (codes + per-row fp32 scales).
     """
     from decode_phase_gqa_gb300 import kvattn as K
     if kind == "prefill":
@@ -483,7 +484,8 @@ def run_prefill_config(kind, steps, warmup, device, stream, seed=0):
         ctx = q3.seq_lens.astype(np.int64)
         n_new = np.full(len(ctx), 4, np.int64)
     wl = W.make_workload("custom", seed=seed, n_seq=len(ctx), n_qh=n_qh, n_kvh=n_kvh,
-                         head_dim=d, page_size=16, rope_theta=theta, kv_dtype="bf16",
+                         head_dim=d, page_size=16, rope_theta=theta,
+                         kv_dtype="int8" if kind == "verify_int8" else "bf16",
                          lengths=[int(x) for x in ctx + n_new - 1], spare=0.05)
     t = W.make_tensors(wl, device=device)
     g = torch.Generator(device=device).manual_seed(seed + 77)
@@ -501,6 +503,7 @@ def run_prefill_config(kind, steps, warmup, device, stream, seed=0):
     def call():
         K.kvattn_prefill(q, kn, vn, t["k_pages"], t["v_pages"], bt, ss, cl, out,
                          rope_theta=theta, scale=1.0 / math.sqrt(d), max_new_tokens=int(n_new.max()),
+                         k_scales=t.get("k_scales"), v_scales=t.get("v_scales"),
                          dev_status=st, workspace=ws, stream=stream)
 
     with torch.cuda.stream(stream):
@@ -523,14 +526,15 @@ def run_prefill_config(kind, steps, warmup, device, stream, seed=0):
     ms = t0.elapsed_time(t1) / steps
     keys = float(np.sum(n_new * ctx + n_new * (n_new + 1) // 2))  # sum over new tokens of keys seen
     flops = 4.0 * d * n_qh * keys
-    kv_bytes = float(np.sum(ctx + n_new)) * n_kvh * d * 2 * 2
+    row_bytes = 2 * d + 8 if kind == "verify_int8" else 2 * d * 2  # a K and a V row (+ scales)
+    kv_bytes = float(np.sum(ctx + n_new)) * n_kvh * row_bytes
     peak_tf, peak_kind = measured_bf16_peak()
     peak_gb, _ = measured_peak()
     res = {"config": kind, "entry": "kvattn_prefill",
            "workload": ("SmolLM3-3B-shaped heads 16/4, d128: 8 prompts x 2048 new tokens, empty caches"
                         if kind == "prefill" else
                         "Qwen3-8B-shaped heads 32/8, d128: 64 sequences, L log-uniform [128,8192], "
-                        "4 draft tokens each"),
+                        "4 draft tokens each" + (", int8 cache" if kind == "verify_int8" else "")),
            "steps": steps, "ms_per_step": ms, "new_tokens_per_s": T / (ms / 1e3),
            "attn_tflops": flops / (ms / 1e3) / 1e12, "bf16_peak_tflops": peak_tf,
            "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / peak_tf, "peak_kind": peak_kind,
@@ -650,7 +654,7 @@ def native(args, rank, world, local):
                               "calls_per_step": r["calls_per_step"]})
                 del r
                 torch.cuda.empty_cache()
-        for kind, k in (("prefill", 20), ("verify", 200)):
+        for kind, k in (("prefill", 20), ("verify", 200), ("verify_int8", 200)):
             extra.append(run_prefill_config(kind, k, 3, device, stream))
         line["per_config"] = extra
     return line
