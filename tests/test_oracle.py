@@ -364,6 +364,53 @@ def test_append_touches_only_the_new_slot():
         assert np.array_equal(vp[wl.block_table[b, L // 16], :, L % 16], h["v_new"][b])
 
 
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("n_kvh,d,page,theta", [(1, 64, 16, 1e4), (2, 128, 16, 1e6),
+                                                 (4, 64, 32, 5e5), (2, 128, 8, 0.0)])
+def test_append_stores_the_recipe_values(kv, n_kvh, d, page, theta):
+    # Every appended slot is rebuilt from the storage recipe of the pages
+    # ("LLM inference from smollm3.go": the new k/v are written at the current
+    # slot after RoPE, section "KV cache"; a quantised row is int8 codes with
+    # one fp32 scale max|x|/127, section "int8 weight-only quantization"),
+    # replayed in numpy float32 by tests/refmath.py, and compared bit for bit
+    # with what the oracle wrote.  RoPE positions differ from the slots, so a
+    # key rotated at its slot (or not at all) shows; one key row and one value
+    # row are zero, so the zero-row rule of the quantiser shows.
+    rng = np.random.default_rng(d * 7 + page + n_kvh)
+    lens = [0, 5, page - 1, page, 3 * page + 2]
+    wl, h = _tiny(2 * n_kvh, n_kvh, lens, d=d, page=page, kv=kv, theta=theta,
+                  seed=d + n_kvh)
+    pos = (wl.seq_lens + rng.integers(1, 40000, size=len(lens))).astype(np.int32)
+    h["positions"] = pos
+    wl.positions = pos
+    h["k_new"][1, 0, :] = 0
+    h["v_new"][2, n_kvh - 1, :] = 0
+    kp, vp = h["k_pages"].copy(), h["v_pages"].copy()
+    ks = None if h["k_scales"] is None else h["k_scales"].copy()
+    vs = None if h["v_scales"] is None else h["v_scales"].copy()
+    st = oracle.append(h["k_new"], h["v_new"], kp, vp, wl.block_table, wl.seq_lens, pos,
+                       theta, ks, vs)
+    assert st == 0
+    for b, L in enumerate(wl.seq_lens):
+        pg, off = wl.block_table[b, L // page], L % page
+        for j in range(n_kvh):
+            kf = R.store_key_f32(h["k_new"][b, j], int(pos[b]), theta)
+            if kv == "bf16":
+                assert np.array_equal(kp[pg, j, off], R.f32_to_bf16_bits(kf))
+                assert np.array_equal(vp[pg, j, off], h["v_new"][b, j])
+            else:
+                kc, kscale = R.quant_row_int8(kf)
+                vc, vscale = R.quant_row_int8(R.bf16_bits_to_f64(h["v_new"][b, j]))
+                assert np.array_equal(kp[pg, j, off], kc)
+                assert np.array_equal(vp[pg, j, off], vc)
+                assert ks[pg, j, off].view(np.uint32) == np.float32(kscale).view(np.uint32)
+                assert vs[pg, j, off].view(np.uint32) == np.float32(vscale).view(np.uint32)
+    # the zero rows really are zero after storage
+    if kv == "int8":
+        b1 = wl.block_table[1, wl.seq_lens[1] // page]
+        assert ks[b1, 0, wl.seq_lens[1] % page] == 0 and not kp[b1, 0, wl.seq_lens[1] % page].any()
+
+
 def test_tiny_config_end_to_end_against_numpy():
     wl = W.make_workload("tiny", seed=0)
     assert wl.num_pages == 17 and list(wl.seq_lens) == [256]

@@ -28,6 +28,12 @@ MUTATIONS = {
                     "return (((size_t)j * g->num_pages + page) * g->page + off);"),
     "append_offset": ("int off = L % page;", "int off = (L + 1) % page;"),
     "int8_round_half_away": ("float r = rintf(t);", "float r = roundf(t);"),
+    "append_unrotated": ("oracle_rope_store_f32(kx, d, positions[b], rope_theta, kr);",
+                         "oracle_rope_store_f32(kx, d, 0, rope_theta, kr);"),
+    "append_rotated_at_slot": ("oracle_rope_store_f32(kx, d, positions[b], rope_theta, kr);",
+                               "oracle_rope_store_f32(kx, d, L, rope_theta, kr);"),
+    "int8_value_from_key": ("oracle_quant_int8(vr, d, codes, &v_scales[s]);",
+                            "oracle_quant_int8(kr, d, codes, &v_scales[s]);"),
     "store_fused": ("volatile float a = lc - hs, b = hc + ls;",
                     "volatile float a = fmaf(-hi, s, lo * c), b = fmaf(lo, s, hi * c);"),
 }
