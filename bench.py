@@ -2,16 +2,21 @@
 """Benchmark of one decode step of GQA attention over a paged KV cache on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                    [--config NAME] [--no-extra-configs]
+                    [--config NAME] [--per-call] [--no-extra-configs]
 
 A step is one pass of the whole hot path (RoPE + append + split-KV attention
-+ merge: one kvattn_decode call per layer cache) over one batch.  The default
-workload is the SmolLM3-3B-shaped layer (16/4 heads, d 128, batch 8, cached
-lengths U[512, 4096], page 16).  Inputs are seeded synthetic N(0, 1) draws
-already resident in HBM; consecutive steps rotate over independent caches
-whose total size is far above the 129 MB L2, so every step reads its KV from
-HBM.  Steps are replayed from CUDA graphs (one graph per cache) and timed with
-CUDA events on the launching stream; rank 0 prints one JSON line.
++ merge) over one batch.  The default workload is the largest configuration:
+the Qwen3-8B-shaped continuous batch (32/8 heads, d 128, batch 64, cached
+lengths log-uniform in [128, 8192], page 16) over its 36 independent layer
+caches, decoded by one kvattn_decode_layers call per step (``--per-call``:
+one kvattn_decode call per layer cache instead).  Inputs are seeded synthetic
+N(0, 1) draws already resident in HBM; a step reads 18 GB of K/V, far above
+the 129 MB L2 (single-layer configs rotate over independent caches whose
+total is at least 4x L2).  The timed window is replayed from CUDA graphs that
+each hold many consecutive steps, so no host launch gap falls inside it, and
+is timed with CUDA events on the launching stream; rank 0 prints one JSON
+line.  Every other configuration is timed in the same run under
+``per_config``, each with its own roofline and end-to-end figure.
 
 With N > 1 (torchrun) every rank decodes its own batch (weak scaling, no data
 exchange); the timing is the max over ranks.  ``--impl reference`` times the
@@ -40,7 +45,7 @@ import torch  # noqa: E402
 from decode_phase_gqa_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attn tokens/s and KV-read HBM GB/s (% of GB300 peak) per config"
-PRIMARY = "smollm3"
+PRIMARY = "qwen3"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 SRC_FILES = ["decode_common.cuh", "decode_mma.cuh", "kvattn_internal.cuh", "angle_table.inc",
@@ -58,6 +63,8 @@ def workload_desc(wl: W.Workload) -> str:
                    "half L=32768, half L~U[1,2048], page 16",
         "int8": "Int8 KV cache, Qwen3-8B-shaped: 32/8 heads, d128, batch 128, "
                 "L~U[1024,4096], page 16, per-token-per-head fp32 scales",
+        "qwen3_b512": "Qwen3-8B-shaped large continuous batch: 32/8 heads, d128, batch 512, "
+                      "L log-uniform [128,8192], page 16, one layer cache",
     }.get(wl.name, wl.name)
 
 
@@ -265,8 +272,7 @@ class NativeCase:
         return [[i] for i in range(self.copies)]
 
     def capture(self, stream):
-        """One graph per step (a step's calls), plus one graph of a whole
-        rotation (every step once, in order) to cut graph-launch gaps."""
+        """One graph per step (its calls), used for the warm-up steps."""
         for grp in self.step_groups():
             for i in grp:          # warm the library's per-device set-up first
                 self.call(i, stream)
@@ -277,37 +283,47 @@ class NativeCase:
                 for i in grp:
                     self.call(i, stream)
             self.graphs.append(g)
-        self.rotation = None
-        if len(self.graphs) > 1:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for grp in self.step_groups():
-                    for i in grp:
-                        self.call(i, stream)
-            self.rotation = g
         torch.cuda.synchronize()
 
     def replay(self, step):
         self.graphs[step % len(self.graphs)].replay()
 
-    def replay_steps(self, first, n):
-        """Replay steps first .. first + n - 1 (rotation order), whole
-        rotations from the rotation graph."""
-        s, end = first, first + n
-        r = len(self.graphs)
-        while s < end:
-            if self.rotation is not None and s % r == 0 and end - s >= r:
-                self.rotation.replay()
-                s += r
-            else:
-                self.graphs[s % r].replay()
-                s += 1
+    def capture_window(self, stream, first, n, max_calls=1024):
+        """Graphs that replay steps first .. first + n - 1 (rotation order) with
+        no host launch gap inside: a graph of C consecutive steps (C a multiple
+        of the rotation's length, so every replay starts at the same cache),
+        replayed n // C times, then a graph of the n % C steps left.  A graph
+        holds at most max_calls library calls (two kernels each)."""
+        groups = self.step_groups()
+        r = len(groups)
+        cap = max(1, max_calls // self.calls_per_step)
+        assert r <= cap, "a rotation must fit one graph"
+        chunk = n if n <= cap else r * (cap // r)
+
+        def graph_of(k):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(first, first + k):
+                    for i in groups[s % r]:
+                        self.call(i, stream)
+            return g
+
+        self.window = [(graph_of(chunk), n // chunk)]
+        if n % chunk:
+            self.window.append((graph_of(n % chunk), 1))
+        torch.cuda.synchronize()
+
+    def replay_window(self):
+        for g, reps in self.window:
+            for _ in range(reps):
+                g.replay()
 
     def check_status(self):
         return self.K.kvattn_read_device_status(self.ws)
 
 
 def time_steps(case: NativeCase, steps: int, warmup: int, world: int, stream):
+    case.capture_window(stream, warmup, steps)
     with torch.cuda.stream(stream):
         for s in range(warmup):
             case.replay(s)
@@ -317,11 +333,12 @@ def time_steps(case: NativeCase, steps: int, warmup: int, world: int, stream):
         t0 = time.time()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        case.replay_steps(warmup, steps)
+        case.replay_window()
         end.record(stream)
         torch.cuda.synchronize()
         t1 = time.time()
         barrier(world)
+    case.window = None
     return start.elapsed_time(end), (t0, t1)
 
 
@@ -545,6 +562,10 @@ def run_prefill_config(kind, steps, warmup, device, stream, seed=0):
     return res
 
 
+ENTRY_LAYERS = "kvattn_decode_layers (one call over the layer caches)"
+ENTRY_CALL = "kvattn_decode"
+
+
 def run_config(name, steps, warmup, rank, world, device, stream, with_e2e=True, layers=None,
                layered=False):
     case = NativeCase(name, seed=1000 * rank, device=device, layers=layers, layered=layered)
@@ -573,6 +594,49 @@ def run_config(name, steps, warmup, rank, world, device, stream, with_e2e=True, 
     return res
 
 
+def roofline_of(r, world, peak, peak_kind):
+    """Roofline of the dominant kernel of one library call: algorithmic K+V
+    bytes of the call / the call's event-timed duration (its decode kernel and
+    the small merge kernel that follows it, timed together)."""
+    case = r["case"]
+    per_call_ms = r["ms_per_step"] / r["calls_per_step"]
+    call_bytes = r["kv_bytes_per_step"] / r["calls_per_step"]
+    achieved = call_bytes / (per_call_ms / 1e3) / 1e9
+    return {
+        "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "frac": achieved / peak, "peak_kind": peak_kind,
+        "algorithmic_bytes_per_launch": call_bytes,
+        "launch_us": per_call_ms * 1e3,
+        "traffic": recorded_traffic(r["name"] + ("_layers" if case.layered else "")),
+        "kernel": "decode_mma_kernel (RoPE, append, split-KV attention) with its merge "
+                  "kernel, timed together per library call",
+    }
+
+
+def config_entry(r, world, peak, peak_kind):
+    """per_config entry of a timed decode configuration."""
+    case = r["case"]
+    wl = case.wl
+    e = {"config": r["name"], "workload": workload_desc(wl),
+         "entry": ENTRY_LAYERS if case.layered else ENTRY_CALL,
+         "steps": r["steps"], "ms_per_step": r["ms_per_step"],
+         "l2_resident": case.l2_resident,
+         "tokens_per_s": r["tokens_per_s"], "kv_read_gbs": r["kv_gbs"],
+         "kv_read_frac_of_peak": r["kv_gbs"] / world / peak,
+         "calls_per_step": r["calls_per_step"],
+         "roofline": roofline_of(r, world, peak, peak_kind)}
+    if "e2e" in r:
+        e["e2e"] = r["e2e"]
+    return e
+
+
+def steps_for(name, layered, peak, budget_ms=300.0):
+    """Timed steps of an extra configuration: about budget_ms of device time."""
+    wl = W.make_workload(name)
+    step_ms = max(wl.kv_bytes * wl.layers / (0.7 * peak * 1e9) * 1e3, 0.01)
+    return max(10, min(2000, int(budget_ms / step_ms)))
+
+
 def native(args, rank, world, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
@@ -580,14 +644,13 @@ def native(args, rank, world, local):
     B.build()
     stream = torch.cuda.Stream(device)
     peak, peak_kind = measured_peak()
+    layered_main = not args.per_call
     with ClockSampler(local) as clocks:
         main = run_config(args.config, args.steps, args.warmup, rank, world, device, stream,
-                          layers=args.layers, layered=args.layered)
+                          layers=args.layers, layered=layered_main)
+    main["steps"] = args.steps
     clk = clocks.summary(*main["window"])
     wl = main["case"].wl
-    per_call_ms = main["ms_per_step"] / main["calls_per_step"]
-    call_bytes = main["kv_bytes_per_step"] / main["calls_per_step"]
-    achieved = call_bytes / (per_call_ms / 1e3) / 1e9   # GB/s over one call
     line = {
         "metric": METRIC,
         "value": main["tokens_per_s"],
@@ -605,53 +668,44 @@ def native(args, rank, world, local):
             "workload": workload_desc(wl), "n_seq": wl.n_seq, "n_qh": wl.n_qh,
             "n_kvh": wl.n_kvh, "head_dim": wl.head_dim, "page_size": wl.page_size,
             "kv_dtype": wl.kv_dtype, "layer_caches_per_step": wl.layers,
-            "entry": "kvattn_decode_layers (one call over the layer caches)"
-                     if main["case"].layered else "kvattn_decode",
+            "entry": ENTRY_LAYERS if main["case"].layered else ENTRY_CALL,
             "kv_bytes_per_step": main["kv_bytes_per_step"],
             "kv_read_gbs": main["kv_gbs"],
             "kv_read_frac_of_peak": main["kv_gbs"] / world / peak,
-            "l2": f"inputs larger than L2: {main['copies']} independent caches rotated, "
-                  f"{main['copies'] * wl.kv_bytes / 2**20:.0f} MiB of KV per rotation",
+            "l2": (f"inputs larger than L2: each step reads "
+                   f"{main['kv_bytes_per_step'] / 2**20:.0f} MiB of KV"
+                   + (f" ({main['copies']} independent caches rotated)"
+                      if wl.layers == 1 else f" over {wl.layers} layer caches")),
             "timing": "CUDA events on the launching stream around K steps replayed from "
-                      "CUDA graphs (a graph per rotation of the caches, a graph per step)",
+                      "CUDA graphs of many consecutive steps (no host launch gap inside)",
             "parallelism": f"{world} independent replica(s), one batch per GPU",
         },
-        "roofline": {
-            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "peak_kind": peak_kind,
-            "traffic": recorded_traffic(args.config + ("_layers" if main["case"].layered else "")),
-            "kernel": "kvattn decode call (decode kernel with RoPE/append + combine kernel, "
-                      "timed together): algorithmic K+V bytes per call / call time",
-        },
+        "roofline": roofline_of(main, world, peak, peak_kind),
         "e2e": main["e2e"],
         # decode (with the append) and combine kernels per call
         "gpu_launches": 2 * main["calls_per_step"] * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "impl": "native",
     }
+    main_layered = main["case"].layered
+    del main["case"]
+    torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config, seed=0)
     if not args.no_extra_configs:
         extra = []
-        for name in W.CONFIG_ORDER:
+        for name in W.CONFIG_ORDER + W.EXTRA_CONFIGS:
             wl2 = W.make_workload(name)
-            # a multi-layer step is timed both ways: a graph of one call per
-            # layer cache, and one kvattn_decode_layers call over all of them
-            for layered in ([False, True] if wl2.layers > 1 else [False]):
-                if name == args.config and layered == main["case"].layered:
+            # a multi-layer step is timed both ways: one kvattn_decode_layers
+            # call over all layer caches, and one kvattn_decode call per cache
+            for layered in ([True, False] if wl2.layers > 1 else [False]):
+                if name == args.config and layered == main_layered:
                     continue
-                call_ms_guess = max(wl2.kv_bytes * wl2.layers / (0.7 * peak * 1e9) * 1e3, 0.01)
-                k = max(10, min(2000, int(300.0 / call_ms_guess)))
+                k = steps_for(name, layered, peak)
                 r = run_config(name, k, max(3, k // 10), rank, world, device, stream,
-                               with_e2e=False, layered=layered)
-                extra.append({"config": name, "workload": workload_desc(r["case"].wl),
-                              "entry": "kvattn_decode_layers (one call over the layer caches)"
-                                       if layered else "kvattn_decode",
-                              "steps": k, "ms_per_step": r["ms_per_step"],
-                              "l2_resident": r["case"].l2_resident,
-                              "tokens_per_s": r["tokens_per_s"], "kv_read_gbs": r["kv_gbs"],
-                              "kv_read_frac_of_peak": r["kv_gbs"] / world / peak,
-                              "calls_per_step": r["calls_per_step"]})
+                               layered=layered)
+                r["steps"] = k
+                extra.append(config_entry(r, world, peak, peak_kind))
                 del r
                 torch.cuda.empty_cache()
         for kind, k in (("prefill", 20), ("verify", 200), ("verify_int8", 200)):
@@ -729,14 +783,15 @@ def reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--config", choices=W.CONFIG_ORDER, default=PRIMARY)
+    ap.add_argument("--config", choices=W.CONFIG_ORDER + W.EXTRA_CONFIGS, default=PRIMARY)
     ap.add_argument("--no-extra-configs", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--layered", action="store_true",
-                    help="time a multi-layer config's step as one kvattn_decode_layers call")
+    ap.add_argument("--per-call", action="store_true",
+                    help="time a multi-layer config's step as one kvattn_decode call per "
+                         "layer cache (default: one kvattn_decode_layers call)")
     ap.add_argument("--layers", type=int, default=None,
                     help="decode at most this many layer caches per step (a smaller case "
                          "for profiling; the default is the workload's own count)")

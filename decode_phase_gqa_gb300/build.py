@@ -19,7 +19,8 @@ LIB = os.path.join(BUILD, "libkvattn.so")
 HEADER = os.path.join(ROOT, "include", "kvattn.h")
 
 SOURCES = ["kvattn_api.cu", "decode_bf16.cu", "decode_int8.cu", "decode_bf16_layers.cu",
-           "decode_int8_layers.cu", "kvattn_noalloc.cu", "combine.cu", "prefill.cu"]
+           "decode_int8_layers.cu", "kvattn_noalloc.cu", "combine.cu", "prefill.cu",
+           "prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I", os.path.join(ROOT, "include")]
@@ -37,8 +38,8 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def _compile(src: str, nvcc: str, extra, verbose: bool) -> str:
-    obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+def _compile(src: str, nvcc: str, extra, verbose: bool, build_dir: str) -> str:
+    obj = os.path.join(build_dir, src.replace(".cu", ".o"))
     srcp = os.path.join(CSRC, src)
     if (os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(srcp)
             and os.path.getmtime(obj) >= _deps_mtime()):
@@ -53,25 +54,30 @@ def _compile(src: str, nvcc: str, extra, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = None) -> str:
+    """Compile and link the library; returns its path.
+
+    ``variant``: a named build with ``extra_flags`` (e.g. a test-only macro),
+    kept apart in ``_build/<variant>/`` so it never replaces the library."""
+    build_dir = BUILD if variant is None else os.path.join(BUILD, variant)
+    lib = os.path.join(build_dir, "libkvattn.so")
+    os.makedirs(build_dir, exist_ok=True)
     if force:
-        for f in os.listdir(BUILD):
+        for f in os.listdir(build_dir):
             if f.endswith((".o", ".so")):
-                os.remove(os.path.join(BUILD, f))
+                os.remove(os.path.join(build_dir, f))
     nvcc = _nvcc()
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, nvcc, extra_flags, verbose), SOURCES))
-    if not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        cmd = [nvcc] + ARCH + ["-shared", "-o", LIB + ".tmp"] + objs
+        objs = list(ex.map(lambda s: _compile(s, nvcc, extra_flags, verbose, build_dir), SOURCES))
+    if not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        cmd = [nvcc] + ARCH + ["-shared", "-o", lib + ".tmp"] + objs
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":

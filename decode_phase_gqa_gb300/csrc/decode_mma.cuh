@@ -84,7 +84,8 @@ struct MmaCfg {
   static constexpr int kBarOff = kScaleOff + W * kSW * kScales;
   static constexpr int kFreqOff = kBarOff + W * kSW * 8;  // rope turns per position, float2[D/2]
   static constexpr int kInvOff = kFreqOff + 512;   // rope_theta^(-2i/d), double[D/2]
-  // 4 ints of scratch; the warps' new-row barriers (uint64[W]) at +32
+  // 4 ints of scratch; test builds' never-completed barrier at +16; the warps'
+  // new-row barriers (uint64[W]) at +32
   static constexpr int kMiscOff = kInvOff + 512;
   static constexpr int kQOff = kMiscOff + 64;             // [W][GS][D] bf16
   static constexpr int kNewOff = kQOff + W * kQBytes;     // [W][kNewBytes]
@@ -310,6 +311,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   if (tid == 0) {
     for (int s = 0; s < W * C::kSW; ++s) mbar_init(&bars[s], 1);
     for (int w = 0; w < W; ++w) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 32) + w, 1);
+#ifdef KVATTN_TEST_STALL
+    mbar_init(reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 16), 1);  // never arrived at
+#endif
     fence_barrier_init();
     prefetch_tensormap(&p.tmap_k);
     prefetch_tensormap(&p.tmap_v);
@@ -536,6 +540,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   const int vrow = INT8 ? krow : (lane & 7) + (lane >> 4) * 8;
   const int vcsel = INT8 ? kcsel : (lane >> 3) & 1;
   bool aborted = false;
+#ifdef KVATTN_TEST_STALL
+  if ((__ldcg(p.status) & kTestStallRequest) != 0 &&
+      !__all_sync(0xffffffffu, mbar_wait_bounded(reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 16),
+                                                  0, kTestStallCycles))) {
+    aborted = true;
+    if (lane == 0) atomicOr(p.status, KVATTN_DEV_TIMEOUT);
+  }
+#endif
   int consumed = 0;
   int cb = start_v;
   int t = wt0;
@@ -614,8 +626,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
           aborted = true;
           if (lane == 0) atomicOr(p.status, KVATTN_DEV_TIMEOUT);
         }
+        consumed = i + 1;  // stages waited for (or given up on) so far
       }
-      consumed = i + 1;
       const int tok0 = (int)(tt - F) * kUnitRows;
       const int upage = spage[i % C::kSW];
       if (ok && upage >= 0) {
@@ -831,6 +843,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
 
   cp_async_wait_all();  // no copy may land after the warp has left
   if (aborted && lane == 0) {
+    // copies issued to stages no wait has looked at since are still in
+    // flight: let them land before the warp leaves
     for (int i = consumed; i < issued; ++i)
       (void)mbar_wait_bounded(&bars[warp * C::kSW + i % C::kSW], (uint32_t)((i / C::kSW) & 1));
   }

@@ -173,21 +173,37 @@ cudaError_t decode_launcher(const DecodeParams &p, int head_dim, int gs, bool in
 }  // namespace
 
 namespace kvattn {
+namespace {
+thread_local int g_last_cuda_error = 0;
+}
+// Record the CUDA error behind a KVATTN_ECUDA return (kvattn_last_cuda_error)
+// and return KVATTN_ECUDA.
+int cuda_fail(cudaError_t err) {
+  g_last_cuda_error = (int)(err == cudaSuccess ? cudaErrorUnknown : err);
+  return KVATTN_ECUDA;
+}
+
 // the frequency tables for the prefill kernels (prefill.cu)
 void rope_tables(float rope_theta, int head_dim, double *inv_freq, float2 *turns) {
   freq_tables(rope_theta, head_dim, inv_freq, turns);
 }
+// the pools' TMA view for the tcgen05 prefill kernel (prefill_tc.cu)
+bool pool_tensor_map(CUtensorMap *map, const void *base, long long rows, int head_dim, bool int8) {
+  return cached_pool_map(map, base, rows, head_dim, int8);
+}
 }  // namespace kvattn
 
-// One decode step over n_layers layer caches (layer-major arrays sharing the
-// block table, lengths and positions); kvattn_decode is n_layers = 1.
-static int decode_call(int n_layers, const void *q, const void *k_new, const void *v_new,
-                       void *k_pages, void *v_pages, const int32_t *block_table,
-                       const int32_t *seq_lens, const int32_t *positions, void *out, int n_seq,
-                       int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta,
-                       float scale, int kv_dtype, void *stream, int max_pages_per_seq,
-                       int num_pages, float *k_scales, float *v_scales, void *workspace,
-                       size_t workspace_bytes, int num_splits, const uint8_t *layer_rope) {
+namespace kvattn {
+// The host checks of a decode call (sizes, pointers, alignment, workspace),
+// in the order decode_call makes them; KVATTN_OK when a launch may follow.
+// Queues nothing.
+int decode_check(int n_layers, const void *q, const void *k_new, const void *v_new,
+                 const void *k_pages, const void *v_pages, const int32_t *block_table,
+                 const int32_t *seq_lens, const int32_t *positions, const void *out, int n_seq,
+                 int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta, float scale,
+                 int kv_dtype, int max_pages_per_seq, int num_pages, const float *k_scales,
+                 const float *v_scales, const void *workspace, size_t workspace_bytes,
+                 int num_splits) {
   // ---- shape checks ----
   if (n_layers < 1 || n_seq < 0 || n_qh < 1 || n_kvh < 1 || n_qh % n_kvh != 0 ||
       max_pages_per_seq < 1 || num_pages < 1 || num_splits < 0 || num_splits > KVATTN_MAX_SPLITS)
@@ -227,7 +243,29 @@ static int decode_call(int n_layers, const void *q, const void *k_new, const voi
   const WorkspaceLayout wl = workspace_layout(n_layers * n_seq, n_qh, n_kvh, head_dim);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < wl.total)
     return KVATTN_EWORKSPACE;
+  return KVATTN_OK;
+}
+}  // namespace kvattn
 
+// One decode step over n_layers layer caches (layer-major arrays sharing the
+// block table, lengths and positions); kvattn_decode is n_layers = 1.
+static int decode_call(int n_layers, const void *q, const void *k_new, const void *v_new,
+                       void *k_pages, void *v_pages, const int32_t *block_table,
+                       const int32_t *seq_lens, const int32_t *positions, void *out, int n_seq,
+                       int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta,
+                       float scale, int kv_dtype, void *stream, int max_pages_per_seq,
+                       int num_pages, float *k_scales, float *v_scales, void *workspace,
+                       size_t workspace_bytes, int num_splits, const uint8_t *layer_rope) {
+  {
+    const int rc = decode_check(n_layers, q, k_new, v_new, k_pages, v_pages, block_table,
+                                seq_lens, positions, out, n_seq, n_qh, n_kvh, head_dim,
+                                page_size, rope_theta, scale, kv_dtype, max_pages_per_seq,
+                                num_pages, k_scales, v_scales, workspace, workspace_bytes,
+                                num_splits);
+    if (rc != KVATTN_OK || n_seq == 0) return rc;
+  }
+  const bool int8 = kv_dtype == KVATTN_KV_INT8;
+  const WorkspaceLayout wl = workspace_layout(n_layers * n_seq, n_qh, n_kvh, head_dim);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int g = n_qh / n_kvh;
@@ -271,24 +309,26 @@ static int decode_call(int n_layers, const void *q, const void *k_new, const voi
     const long long rows = (long long)n_layers * num_pages * n_kvh * page_size;
     if (!cached_pool_map(&dp.tmap_k, k_pages, rows, head_dim, int8) ||
         !cached_pool_map(&dp.tmap_v, v_pages, rows, head_dim, int8))
-      return KVATTN_ECUDA;
+      return cuda_fail(cudaErrorInvalidValue);  // the tensor map could not be encoded
   }
   // the first call for a configuration on a device sets the kernel's shared
   // memory limit and caches its occupancy; later calls only launch.  A share
   // of the unit list is one warp's work.
   int sms = 0, per_sm = 0;
-  if (sm_count(&sms) != cudaSuccess) return KVATTN_ECUDA;
-  if (decode_launcher(dp, head_dim, gs, int8, 0, st, &per_sm, false) != cudaSuccess)
-    return KVATTN_ECUDA;
+  cudaError_t err = sm_count(&sms);
+  if (err != cudaSuccess) return cuda_fail(err);
+  err = decode_launcher(dp, head_dim, gs, int8, 0, st, &per_sm, false);
+  if (err != cudaSuccess) return cuda_fail(err);
   int shares = num_splits;
   if (shares == 0) shares = sms * (per_sm > 0 ? per_sm : 1) * kDecodeWarps;
   if (shares > KVATTN_MAX_SPLITS) shares = KVATTN_MAX_SPLITS;
   dp.n_shares = shares;
   const int grid = (shares + kDecodeWarps - 1) / kDecodeWarps;
-  if (decode_launcher(dp, head_dim, gs, int8, grid, st, nullptr, true) != cudaSuccess)
-    return KVATTN_ECUDA;
+  err = decode_launcher(dp, head_dim, gs, int8, grid, st, nullptr, true);
+  if (err != cudaSuccess) return cuda_fail(err);
   // ---- launch 2: merge of the streams the warp shares split ----
-  if (launch_combine(dp, head_dim, gs, shares, sms, st) != cudaSuccess) return KVATTN_ECUDA;
+  err = launch_combine(dp, head_dim, gs, shares, sms, st);
+  if (err != cudaSuccess) return cuda_fail(err);
   return KVATTN_OK;
 }
 
@@ -307,10 +347,9 @@ size_t kvattn_workspace_size(int n_seq, int n_qh, int n_kvh, int head_dim) {
 
 int kvattn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return KVATTN_EWORKSPACE;
-  if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
-    return KVATTN_ECUDA;
-  return KVATTN_OK;
+  const cudaError_t err =
+      cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KVATTN_OK : cuda_fail(err);
 }
 
 int kvattn_decode_splits(const void *q, const void *k_new, const void *v_new, void *k_pages,
@@ -356,11 +395,11 @@ int kvattn_read_device_status(void *workspace, void *stream, uint32_t *bits) {
   if (!workspace || !aligned(workspace, 256)) return KVATTN_EWORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t host = 0;
-  if (cudaMemcpyAsync(&host, workspace, sizeof host, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return KVATTN_ECUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return KVATTN_ECUDA;
-  if (cudaMemsetAsync(workspace, 0, sizeof host, st) != cudaSuccess) return KVATTN_ECUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return KVATTN_ECUDA;
+  cudaError_t err = cudaMemcpyAsync(&host, workspace, sizeof host, cudaMemcpyDeviceToHost, st);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+  if (err == cudaSuccess) err = cudaMemsetAsync(workspace, 0, sizeof host, st);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+  if (err != cudaSuccess) return cuda_fail(err);
   *bits = host;
   return KVATTN_OK;
 }
@@ -376,6 +415,8 @@ const char *kvattn_status_string(int status) {
   }
 }
 
-int kvattn_version(void) { return 100; }
+int kvattn_version(void) { return 101; }
+
+int kvattn_last_cuda_error(void) { return g_last_cuda_error; }
 
 }  // extern "C"

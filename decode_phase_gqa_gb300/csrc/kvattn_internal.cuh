@@ -28,6 +28,15 @@ constexpr int kCtaSmemBudget = 75 * 1024;
 constexpr long long kTablePrefetchLines = 8192;
 // A bounded wait gives up after this many SM clocks (about one second).
 constexpr long long kWaitCycles = 2000000000LL;
+#ifdef KVATTN_TEST_STALL
+// Test builds only (the macro is never defined in the library build): when a
+// call finds kTestStallRequest set in its status word, every decode warp
+// first waits, with this short limit (about a millisecond), on a barrier that
+// nothing ever arrives at and that no copy is ever issued to, so the wait runs
+// out, KVATTN_DEV_TIMEOUT is recorded and the kernel takes its give-up path.
+constexpr long long kTestStallCycles = 2000000LL;
+constexpr uint32_t kTestStallRequest = 0x80000000u;
+#endif
 
 // Query heads per CTA group: the largest of 4, 2, 1 dividing the GQA group.
 inline int group_split(int g) { return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1; }
@@ -104,6 +113,20 @@ cudaError_t launch_decode_int8_layers(const DecodeParams &p, int head_dim, int g
 cudaError_t launch_combine(const DecodeParams &p, int head_dim, int gs, int n_warps, int sms,
                            cudaStream_t stream);
 
+// Record `err` as this thread's last CUDA error (kvattn_last_cuda_error) and
+// return KVATTN_ECUDA (kvattn_api.cu).
+int cuda_fail(cudaError_t err);
+
+// The host checks of kvattn_decode / kvattn_decode_layers (kvattn_api.cu):
+// KVATTN_OK when the arguments may be launched on; queues nothing.
+int decode_check(int n_layers, const void *q, const void *k_new, const void *v_new,
+                 const void *k_pages, const void *v_pages, const int32_t *block_table,
+                 const int32_t *seq_lens, const int32_t *positions, const void *out, int n_seq,
+                 int n_qh, int n_kvh, int head_dim, int page_size, float rope_theta, float scale,
+                 int kv_dtype, int max_pages_per_seq, int num_pages, const float *k_scales,
+                 const float *v_scales, const void *workspace, size_t workspace_bytes,
+                 int num_splits);
+
 #ifdef __CUDACC__
 // ---- device helpers ----------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -146,12 +169,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of an mbarrier; false if it did not complete within
-// kWaitCycles (the caller records KVATTN_DEV_TIMEOUT and stops using data).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// `limit` SM clocks (the caller records KVATTN_DEV_TIMEOUT and stops using data).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }

@@ -12,7 +12,11 @@
 // The array is a file-scope __device__ variable.  In host code its name only
 // stands in for the symbol, it is not a device address, so the address is
 // looked up with cudaGetSymbolAddress once per device (with that device
-// current) and that address is what the kernels receive.
+// current) and that address is what the kernels receive.  The looked-up
+// address is kept for the life of the process: after cudaDeviceReset (or
+// anything else that destroys and re-creates the device's primary context)
+// the array may sit elsewhere, so this entry point must not be used across
+// such a reset.
 #include <mutex>
 
 #include "kvattn_internal.cuh"
@@ -64,19 +68,36 @@ extern "C" int kvattn_decode_noalloc(const void *q, const void *k_new, const voi
   if (need > KVATTN_NOALLOC_SCRATCH_BYTES) return KVATTN_EUNSUPPORTED;
   if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) % 4) != 0) return KVATTN_EINVAL;
   void *scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return KVATTN_ECUDA;
+  {
+    const cudaError_t err = scratch_address(&scratch);
+    if (err != cudaSuccess) return kvattn::cuda_fail(err);
+  }
+  // every host check of the decode step first, so that a rejected call has
+  // queued nothing (not even the status clear below)
+  {
+    const int rc = kvattn::decode_check(1, q, k_new, v_new, k_pages, v_pages, block_table,
+                                        seq_lens, positions, out, n_seq, n_qh, n_kvh, head_dim,
+                                        page_size, rope_theta, scale, kv_dtype,
+                                        max_pages_per_seq, num_pages, k_scales, v_scales,
+                                        scratch, KVATTN_NOALLOC_SCRATCH_BYTES, 0);
+    if (rc != KVATTN_OK) return rc;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: the status word must start
   // at zero (every record the combine kernel reads is rewritten by the step)
-  if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) return KVATTN_ECUDA;
+  {
+    const cudaError_t err = cudaMemsetAsync(scratch, 0, 256, st);
+    if (err != cudaSuccess) return kvattn::cuda_fail(err);
+  }
   const int rc = kvattn_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
                                positions, out, n_seq, n_qh, n_kvh, head_dim, page_size,
                                rope_theta, scale, kv_dtype, stream, max_pages_per_seq, num_pages,
                                k_scales, v_scales, scratch, KVATTN_NOALLOC_SCRATCH_BYTES);
   if (rc != KVATTN_OK) return rc;
-  if (dev_status &&
-      cudaMemcpyAsync(dev_status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) !=
-          cudaSuccess)
-    return KVATTN_ECUDA;
+  if (dev_status) {
+    const cudaError_t err =
+        cudaMemcpyAsync(dev_status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st);
+    if (err != cudaSuccess) return kvattn::cuda_fail(err);
+  }
   return KVATTN_OK;
 }

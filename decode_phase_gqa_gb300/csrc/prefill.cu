@@ -25,61 +25,12 @@
 #include <climits>
 #include <cmath>
 
-#include "decode_common.cuh"
+#include "prefill_common.cuh"
 #include "storage.cuh"
 
 namespace kvattn {
 
 namespace {
-
-constexpr int kPfWarps = 4;                  // query heads per CTA, one warp each
-constexpr int kPfThreads = 32 * kPfWarps;
-constexpr int kPfRows = 16;                  // new tokens per CTA (the MMA's M)
-constexpr int kPfKeys = 32;                  // keys per staged tile
-constexpr int kPfNT = kPfKeys / 8;           // its n-tiles of 8 keys (Q K^T)
-constexpr int kPfKK = kPfKeys / 16;          // its k-steps of 16 keys (P V)
-constexpr int kPfMinTiles = 16;              // key tiles a split takes at least
-// short chunks (at most 4 new tokens a sequence: speculative drafts)
-constexpr int kPsTok = 4;                    // new tokens a CTA (x 4 heads: the MMA's 16 rows)
-constexpr int kPsWarpKeys = 16;              // keys of a stage each warp takes
-constexpr int kPsKeys = kPfWarps * kPsWarpKeys;  // keys a stage holds
-constexpr int kPsStages = 2;
-constexpr int kPsMinTiles = 16;              // stages a split takes at least
-
-struct PrefillParams {
-  const __nv_bfloat16 *q, *k_new, *v_new;
-  void *k_pages, *v_pages;  // bf16, or int8 codes with k_scales / v_scales
-  float *k_scales, *v_scales;
-  __nv_bfloat16 *out;
-  const int32_t *block_table, *seq_starts, *ctx_lens;
-  uint32_t *status;  // KVATTN_DEV_* bits (NULL: not reported)
-  int n_seq, n_tok, n_qh, n_kvh, page_size, page_shift, max_pages, num_pages;
-  int tiles_per_seq;  // query tiles the grid gives each sequence
-  int tile_rows;      // new tokens a query tile holds: 16, or kPsTok (short chunks)
-  int n_splits;       // CTAs sharing one query tile's key tiles
-  float *part;        // n_splits > 1: [n_splits][n_tok][n_qh][D + 2] partial
-                      // states (o relative to 2^m, m, l; log2 units)
-  int use_rope;
-  float qscale;       // scale * log2(e)
-  float2 turns[64];   // rope_theta^(-2i/d) / (2 pi) as fp32 head + remainder
-  double inv_freq[64];
-};
-
-__device__ __forceinline__ void report(const PrefillParams &p, uint32_t bits) {
-  if (p.status) atomicOr(p.status, bits);
-}
-
-// Sequence b's rows of the new-token arrays [start, start + n_new) and cached
-// count ctx; false when they do not fit the arrays or the block table.
-__device__ __forceinline__ bool seq_span(const PrefillParams &p, int b, int &start, int &n_new,
-                                         int &ctx) {
-  start = __ldg(p.seq_starts + b);
-  const int end = __ldg(p.seq_starts + b + 1);
-  ctx = __ldg(p.ctx_lens + b);
-  n_new = end - start;
-  const long long cap = (long long)p.max_pages << p.page_shift;
-  return start >= 0 && end <= p.n_tok && n_new >= 0 && ctx >= 0 && (long long)ctx + n_new <= cap;
-}
 
 // The sequence of new-token row r: the last b < n_seq with seq_starts[b] <= r
 // (the answer of a binary search when the starts ascend; a row the sequence
@@ -918,9 +869,16 @@ __global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_
   const float *rec = p.part + ((size_t)r * p.n_qh + h) * (D + 2);
   // the splits of the row's query tile, as the attention kernel formed them
   const int t0 = ((r - start) / p.tile_rows) * p.tile_rows;
-  const int nz = p.tile_rows == kPsTok
-                     ? short_splits((short_tile_keys(ctx, n_new) + kPsKeys - 1) / kPsKeys, p.n_splits)
-                     : tile_splits((query_tile_keys(ctx, n_new, t0) + kPfKeys - 1) / kPfKeys, p.n_splits);
+  int nz;
+  if (p.tile_rows == kPsTok) {
+    nz = short_splits((short_tile_keys(ctx, n_new) + kPsKeys - 1) / kPsKeys, p.n_splits);
+  } else if (p.tc_tiles) {
+    const int n_rows = min(n_new, p.tiles_per_seq * p.tile_rows);
+    const int tc0 = ((r - start) / kTcTok) * kTcTok;
+    nz = tc_splits((tc_tile_keys(ctx, n_rows, tc0) + kTcKeys - 1) / kTcKeys, p.n_splits);
+  } else {
+    nz = tile_splits((query_tile_keys(ctx, n_new, t0) + kPfKeys - 1) / kPfKeys, p.n_splits);
+  }
   float M = -INFINITY;
   for (int zz = 0; zz < nz; ++zz) M = fmaxf(M, __ldg(rec + zz * stride + D));
   float L = 0.f, acc[E] = {};
@@ -973,6 +931,10 @@ cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
                                S::kSmem);
     if (err != cudaSuccess) return err;
     err = launch_pdl(prefill_short_kernel<D, INT8>, grid, S::kSmem, stream, p);
+    if (err != cudaSuccess) return err;
+  } else if (p.tc_tiles) {
+    // long prompts over a bf16 cache: the tcgen05 kernel (prefill_tc.cu)
+    err = launch_prefill_tc(p, D, p.tiles_per_seq * kPfRows, stream);
     if (err != cudaSuccess) return err;
   } else {
     err = launch_pdl(prefill_attn_kernel<D, INT8>, grid, C::kSmem, stream, p);
@@ -1077,6 +1039,9 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   // to 16 CTAs, each with at least 16 tiles, so every context streams at once;
   // long prompts, whose query tiles already fill the GPU, take one, as does a
   // call without a workspace.
+  // Long prompts over a bf16 cache take the tcgen05 kernel (32-token query
+  // tiles, one CTA an SM): their splits aim at two CTAs an SM.
+  p.tc_tiles = (!int8 && !short_chunks && max_new_tokens > 64) ? 1 : 0;
   {
     int S = 1;
     if (max_new_tokens <= 64) {
@@ -1085,8 +1050,11 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
       int dev = 0, sms = 152;
       if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      const long long base = (long long)n_seq * tiles * (n_qh / kPfWarps);
-      S = (int)std::min<long long>(kPfMaxSplits, std::max<long long>(1, (4LL * sms + base - 1) / base));
+      const long long base =
+          p.tc_tiles ? (long long)n_seq * ((tiles * kPfRows + kTcTok - 1) / kTcTok) * (n_qh / kPfWarps)
+                     : (long long)n_seq * tiles * (n_qh / kPfWarps);
+      const long long want = p.tc_tiles ? 2LL * sms : 4LL * sms;
+      S = (int)std::min<long long>(kPfMaxSplits, std::max<long long>(1, (want + base - 1) / base));
     }
     const size_t per = split_bytes(n_tok, n_qh, head_dim);
     if (S > 1) S = workspace ? (int)std::min<size_t>((size_t)S, workspace_bytes / per) : 1;
@@ -1099,5 +1067,5 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t err = head_dim == 64 ? (int8 ? launch_prefill_t<64, true>(p, st) : launch_prefill_t<64, false>(p, st))
                                          : (int8 ? launch_prefill_t<128, true>(p, st) : launch_prefill_t<128, false>(p, st));
-  return err == cudaSuccess ? KVATTN_OK : KVATTN_ECUDA;
+  return err == cudaSuccess ? KVATTN_OK : cuda_fail(err);
 }

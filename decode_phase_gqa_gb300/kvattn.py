@@ -42,48 +42,57 @@ _lock = threading.Lock()
 
 class KvattnError(RuntimeError):
     def __init__(self, code: int, what: str):
-        super().__init__(f"{what}: status {code} ({kvattn_status_string(code)})")
+        msg = f"{what}: status {code} ({kvattn_status_string(code)})"
+        if code == KVATTN_ECUDA:
+            msg += f", cudaError {kvattn_last_cuda_error()}"
+        super().__init__(msg)
         self.code = code
+
+
+def bind(path: str) -> ctypes.CDLL:
+    """Open a build of the library at `path` and declare its entry points."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "decode_phase_gqa_gb300.build.build() (nvcc, sm_103a)")
+    L = ctypes.CDLL(path)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.kvattn_workspace_size.argtypes = [I, I, I, I]
+    L.kvattn_workspace_size.restype = S
+    L.kvattn_workspace_size_layers.argtypes = [I, I, I, I, I]
+    L.kvattn_workspace_size_layers.restype = S
+    L.kvattn_workspace_init.argtypes = [P, S, P]
+    L.kvattn_workspace_init.restype = I
+    dec = [P] * 9 + [I] * 5 + [F, F, I, P, I, I, P, P, P, S]
+    L.kvattn_decode.argtypes = dec
+    L.kvattn_decode.restype = I
+    L.kvattn_decode_splits.argtypes = dec + [I]
+    L.kvattn_decode_splits.restype = I
+    L.kvattn_decode_layers.argtypes = [I] + dec + [P]
+    L.kvattn_decode_layers.restype = I
+    L.kvattn_decode_noalloc.argtypes = dec[:-2] + [P]
+    L.kvattn_decode_noalloc.restype = I
+    L.kvattn_prefill.argtypes = [P] * 9 + [I] * 6 + [F, F, I, P, I, I, P, P, I, P, P, S]
+    L.kvattn_prefill.restype = I
+    L.kvattn_prefill_workspace_size.argtypes = [I, I, I]
+    L.kvattn_prefill_workspace_size.restype = S
+    L.kvattn_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+    L.kvattn_read_device_status.restype = I
+    L.kvattn_status_string.argtypes = [I]
+    L.kvattn_status_string.restype = ctypes.c_char_p
+    L.kvattn_version.argtypes = []
+    L.kvattn_version.restype = I
+    L.kvattn_last_cuda_error.argtypes = []
+    L.kvattn_last_cuda_error.restype = I
+    return L
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     """Load the CUDA library (fails loudly when it has not been built)."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        if not os.path.exists(path):
-            raise RuntimeError(f"{path} is missing: build it with "
-                               "decode_phase_gqa_gb300.build.build() (nvcc, sm_103a)")
-        L = ctypes.CDLL(path)
-        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-        L.kvattn_workspace_size.argtypes = [I, I, I, I]
-        L.kvattn_workspace_size.restype = S
-        L.kvattn_workspace_size_layers.argtypes = [I, I, I, I, I]
-        L.kvattn_workspace_size_layers.restype = S
-        L.kvattn_workspace_init.argtypes = [P, S, P]
-        L.kvattn_workspace_init.restype = I
-        dec = [P] * 9 + [I] * 5 + [F, F, I, P, I, I, P, P, P, S]
-        L.kvattn_decode.argtypes = dec
-        L.kvattn_decode.restype = I
-        L.kvattn_decode_splits.argtypes = dec + [I]
-        L.kvattn_decode_splits.restype = I
-        L.kvattn_decode_layers.argtypes = [I] + dec + [P]
-        L.kvattn_decode_layers.restype = I
-        L.kvattn_decode_noalloc.argtypes = dec[:-2] + [P]
-        L.kvattn_prefill.argtypes = [P] * 9 + [I] * 6 + [F, F, I, P, I, I, P, P, I, P, P, S]
-        L.kvattn_prefill.restype = I
-        L.kvattn_prefill_workspace_size.argtypes = [I, I, I]
-        L.kvattn_prefill_workspace_size.restype = S
-        L.kvattn_decode_noalloc.restype = I
-        L.kvattn_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
-        L.kvattn_read_device_status.restype = I
-        L.kvattn_status_string.argtypes = [I]
-        L.kvattn_status_string.restype = ctypes.c_char_p
-        L.kvattn_version.argtypes = []
-        L.kvattn_version.restype = I
-        _lib = L
-        return L
+        if _lib is None:
+            _lib = bind(path)
+        return _lib
 
 
 def kvattn_status_string(code: int) -> str:
@@ -92,6 +101,11 @@ def kvattn_status_string(code: int) -> str:
 
 def kvattn_version() -> int:
     return load().kvattn_version()
+
+
+def kvattn_last_cuda_error() -> int:
+    """cudaError_t value behind this thread's last KVATTN_ECUDA return (0: none)."""
+    return int(load().kvattn_last_cuda_error())
 
 
 def kvattn_workspace_size(n_seq: int, n_qh: int, n_kvh: int, head_dim: int) -> int:
@@ -146,23 +160,60 @@ def _check(t: torch.Tensor, name: str, dtypes, ndim: int, device) -> None:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+_BF = (torch.bfloat16,)
+_POOL = (torch.bfloat16, torch.int8)
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+_sig_lock = threading.Lock()
+_sig_cache = {}  # argument signature -> the marshalled sizes (checks passed)
+
+
+def _signature(tensors, layered: bool):
+    """What the checks of _marshal depend on: shape, dtype, device index and
+    contiguity of every tensor argument (None kept as None)."""
+    return (layered,) + tuple(
+        None if t is None else (t.shape, t.dtype, t.get_device(), t.is_contiguous())
+        for t in tensors)
+
+
 def _marshal(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
              k_scales, v_scales, layered: bool):
-    """Shape/dtype checks; returns (n_layers, n_seq, n_qh, n_kvh, d, page, num_pages, int8)."""
+    """Shape/dtype checks; returns (n_layers, n_seq, n_qh, n_kvh, d, page, num_pages, int8).
+
+    The checks run once per argument signature; a repeated signature (same
+    shapes, dtypes, device and contiguity) reuses their result."""
+    tensors = (q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
+               k_scales, v_scales)
+    try:
+        key = _signature(tensors, layered)
+    except AttributeError:
+        raise TypeError("tensor arguments must be torch.Tensor or None") from None
+    hit = _sig_cache.get(key)
+    if hit is not None:
+        return hit
+    res = _marshal_checked(*tensors, layered)
+    with _sig_lock:
+        if len(_sig_cache) > 256:
+            _sig_cache.clear()
+        _sig_cache[key] = res
+    return res
+
+
+def _marshal_checked(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions, out,
+                     k_scales, v_scales, layered: bool):
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("kvattn_decode runs on CUDA tensors only")
-    bf = (torch.bfloat16,)
     e = 1 if layered else 0
-    _check(q, "q", bf, 3 + e, dev)
-    _check(out, "out", bf, 3 + e, dev)
-    _check(k_new, "k_new", bf, 3 + e, dev)
-    _check(v_new, "v_new", bf, 3 + e, dev)
-    _check(k_pages, "k_pages", (torch.bfloat16, torch.int8), 4 + e, dev)
+    _check(q, "q", _BF, 3 + e, dev)
+    _check(out, "out", _BF, 3 + e, dev)
+    _check(k_new, "k_new", _BF, 3 + e, dev)
+    _check(v_new, "v_new", _BF, 3 + e, dev)
+    _check(k_pages, "k_pages", _POOL, 4 + e, dev)
     _check(v_pages, "v_pages", (k_pages.dtype,), 4 + e, dev)
-    _check(block_table, "block_table", (torch.int32,), 2, dev)
-    _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
-    _check(positions, "positions", (torch.int32,), 1, dev)
+    _check(block_table, "block_table", _I32, 2, dev)
+    _check(seq_lens, "seq_lens", _I32, 1, dev)
+    _check(positions, "positions", _I32, 1, dev)
     n_layers = q.shape[0] if layered else 1
     n_seq, n_qh, d = q.shape[e:]
     num_pages, n_kvh, page, d2 = k_pages.shape[e:]
@@ -180,7 +231,7 @@ def _marshal(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, positions
         for name, s in (("k_scales", k_scales), ("v_scales", v_scales)):
             if s is None:
                 raise ValueError(f"{name} is required for an int8 cache")
-            _check(s, name, (torch.float32,), 3 + e, dev)
+            _check(s, name, _F32, 3 + e, dev)
             if tuple(s.shape) != lead + (num_pages, n_kvh, page):
                 raise ValueError(f"{name}: shape {tuple(s.shape)}")
     return n_layers, n_seq, n_qh, n_kvh, d, page, num_pages, int8

@@ -57,10 +57,18 @@ CONFIGS = {
     "int8": dict(n_seq=128, n_qh=32, n_kvh=8, head_dim=128, page_size=16,
                  rope_theta=1e6, scale=1 / math.sqrt(128), kv_dtype="int8",
                  layers=1, lengths=("uniform", 1024, 4096), spare=0.05),
+    # A large continuous batch of the Qwen3-8B shape: 512 sequences, L
+    # log-uniform in [128, 8192], one layer cache (what a serving engine's
+    # batch grows to; checks that throughput holds above 128 sequences).
+    "qwen3_b512": dict(n_seq=512, n_qh=32, n_kvh=8, head_dim=128, page_size=16,
+                       rope_theta=1e6, scale=1 / math.sqrt(128), kv_dtype="bf16",
+                       layers=1, lengths=("loguniform", 128, 8192), spare=0.05),
 }
 
 # The configs in the order the benchmark configuration list states them.
 CONFIG_ORDER = ["tiny", "smollm3", "qwen3", "llama1b", "int8"]
+# Further shapes the benchmark times beside them.
+EXTRA_CONFIGS = ["qwen3_b512"]
 
 
 @dataclass

@@ -297,7 +297,12 @@ size_t kvattn_prefill_workspace_size(int n_tok, int n_qh, int head_dim);
  * kvattn_workspace_size(n_seq, n_qh, n_kvh, head_dim) >
  * KVATTN_NOALLOC_SCRATCH_BYTES.
  * The first call on a device (with that device current) looks up the array's
- * device address; make that first call before any stream capture.
+ * device address; make that first call before any stream capture.  That
+ * address is kept until the process exits: do not use this entry point
+ * across cudaDeviceReset (or any other destruction of the device's primary
+ * context), after which the array may lie elsewhere.
+ * Every host check of kvattn_decode is made before anything is queued: a
+ * call that returns an error has queued no work.
  * Every call uses the same array and finds the previous call's contents in it:
  * calls that overlap on the GPU (other streams, other host threads) race and
  * corrupt each other's results, so order them on one stream.
@@ -323,6 +328,14 @@ const char *kvattn_status_string(int status);
 
 /* Library ABI version (major * 100 + minor). */
 int kvattn_version(void);
+
+/*
+ * The cudaError_t value behind this thread's most recent KVATTN_ECUDA return
+ * (0 when no call on this thread has returned KVATTN_ECUDA).  A pool whose
+ * tensor map could not be encoded reports cudaErrorInvalidValue (1).  Not a
+ * step of the method: a diagnostic for callers that receive KVATTN_ECUDA.
+ */
+int kvattn_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "kvattn_decode", "kvattn_decode_layers", "kvattn_decode_noalloc",
-        "kvattn_decode_splits", "kvattn_prefill", "kvattn_prefill_workspace_size",
+        "kvattn_decode_splits", "kvattn_last_cuda_error", "kvattn_prefill",
+        "kvattn_prefill_workspace_size",
         "kvattn_read_device_status",
         "kvattn_status_string", "kvattn_version", "kvattn_workspace_init",
         "kvattn_workspace_size", "kvattn_workspace_size_layers"])
@@ -58,7 +59,8 @@ def test_status_strings(lib):
     for code in range(5):
         assert K.kvattn_status_string(code)
     assert K.kvattn_status_string(99) == "unknown status"
-    assert K.kvattn_version() >= 100
+    assert K.kvattn_version() >= 101
+    assert K.kvattn_last_cuda_error() == 0   # no call has failed in CUDA here
 
 
 def test_workspace_size(lib):

@@ -2,8 +2,8 @@
 
 Each benchmark workload (SmolLM3-3B-shaped layer, two of the Qwen3-8B-shaped
 layer caches, the Llama-3.2-1B-shaped skewed long-context batch, the int8
-cache) is drawn on the GPU exactly as the benchmark draws it, decoded through
-a CUDA graph of kvattn_decode calls with the default work split (one shared
+cache, and a Qwen3-8B-shaped batch of 512 sequences) is drawn on the GPU
+exactly as the benchmark draws it, decoded through a CUDA graph of kvattn_decode calls with the default work split (one shared
 workspace, as the benchmark replays them), and checked against the oracle:
 
 * the whole K/V pool (and the int8 scales) bit for bit after the append, for
@@ -24,7 +24,7 @@ from tests.helpers import host_inputs, oracle_decode
 pytestmark = pytest.mark.gpu
 
 # config -> layer caches decoded (the Qwen3 step has 36; two keep the test short)
-CASES = {"smollm3": 1, "qwen3": 2, "llama1b": 1, "int8": 1}
+CASES = {"smollm3": 1, "qwen3": 2, "llama1b": 1, "int8": 1, "qwen3_b512": 1}
 
 
 def sample_mask(wl, n_random=4, seed=0):

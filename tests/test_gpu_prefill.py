@@ -100,6 +100,48 @@ def test_long_prompt():
     check(wl, h, starts, ctx)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_long_prompts_without_splits(d):
+    # no workspace: every query tile's keys go through one CTA of the
+    # tensor-core kernel (prompts above 64 new tokens over a bf16 cache)
+    wl, h, starts, ctx = make_case(16, 4, [0, 0, 130, 0], [65, 200, 97, 300], d=d, seed=13)
+    check(wl, h, starts, ctx, split=False)
+
+
+def test_long_prompt_eight_query_heads_per_kv_head():
+    # a group of 8 query heads is two CTAs of 4 heads each
+    wl, h, starts, ctx = make_case(16, 2, [0, 40], [400, 129], d=128, seed=17)
+    check(wl, h, starts, ctx)
+    check(wl, h, starts, ctx, split=False)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_pool_slots_past_the_keys_may_hold_nan(d):
+    # every pool slot no key occupies (before or after the step) is a NaN:
+    # the rows past a sequence's last key inside its last 16-key block must
+    # not reach the weighted sum
+    wl, h, starts, ctx = make_case(16, 4, [0, 0, 0], [77, 130, 250], d=d, seed=19)
+    nan = np.uint16(0x7FC1)
+    h["k_pages"][:] = nan
+    h["v_pages"][:] = nan
+    check(wl, h, starts, ctx)
+    check(wl, h, starts, ctx, split=False)
+
+
+def test_bad_page_in_a_long_prompt_is_reported():
+    wl, h, starts, ctx = make_case(8, 2, [64, 0], [100, 180], d=128, seed=23)
+    bt = h["block_table"].copy()
+    bt[0, 2] = -7                # cached tokens 32-47 of sequence 0 left out
+    h["block_table"] = bt
+    out, st, d = run_prefill(wl, h, starts, ctx, split=False)
+    assert st & K.KVATTN_DEV_BAD_PAGE
+    ref, ost, kp, vp = oracle_prefill(h, starts, ctx, wl.rope_theta, wl.scale)
+    assert ost & 2
+    assert_close(out_f64(out), ref)
+    assert np.array_equal(pool_bits(d["k_pages"]), kp)
+    assert np.array_equal(pool_bits(d["v_pages"]), vp)
+
+
 def test_one_new_token_is_the_decode_step():
     """n_b = 1 is kvattn_decode with seq_lens = positions = ctx: the same
     appended rows bit for bit, outputs within the tolerance of the oracle."""

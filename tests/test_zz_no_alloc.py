@@ -5,7 +5,9 @@ reserved nearly all of HBM for its KV-page pool up front, or a plugin whose
 host framework owns every device allocation and forbids cudaMalloc.  For them
 the library keeps the step's scratch in a fixed array of its own.  These tests
 call that entry point through the C ABI (ctypes, raw pointers) and compare it
-with kvattn_decode given a normal workspace, on two calls in a row.
+with kvattn_decode given a normal workspace and with the oracle, on two calls
+in a row, and check that a call's device status bits reach the caller and do
+not leak into the next call.
 
 The file is named so that pytest collects it last.
 """
@@ -18,8 +20,8 @@ import torch
 from decode_phase_gqa_gb300 import build as B
 from decode_phase_gqa_gb300 import kvattn as K
 from decode_phase_gqa_gb300 import workloads as W
-from tests.gpu_helpers import MAX_ABS, MEAN_ABS, out_f64, pool_bits, to_dev
-from tests.helpers import host_inputs
+from tests.gpu_helpers import MAX_ABS, MEAN_ABS, assert_close, out_f64, pool_bits, to_dev
+from tests.helpers import host_inputs, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -52,10 +54,20 @@ def _case(seed, kv, d):
     return wl, host_inputs(wl)
 
 
-def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(lib):
+def _assert_pools_equal(d, kp, vp, ks, vs):
+    assert np.array_equal(pool_bits(d["k_pages"]), kp)
+    assert np.array_equal(pool_bits(d["v_pages"]), vp)
+    if ks is not None:
+        assert np.array_equal(d["k_scales"].cpu().numpy().view(np.uint32), ks.view(np.uint32))
+        assert np.array_equal(d["v_scales"].cpu().numpy().view(np.uint32), vs.view(np.uint32))
+
+
+def test_noalloc_matches_workspace_entry_and_oracle_on_two_calls_in_a_row(lib):
     stream = torch.cuda.current_stream().cuda_stream
     for seed, kv, d in ((21, "bf16", 128), (22, "int8", 64)):
         wl, h = _case(seed, kv, d)
+        ref, ost, kp, vp, ks, vs = oracle_decode(wl, h)
+        assert ost == 0
         # the existing entry point, with a workspace from the caller
         d_ws = to_dev(h)
         out_ws = torch.empty(d_ws["q"].shape, dtype=torch.bfloat16, device="cuda")
@@ -77,6 +89,39 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(lib):
         assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS
         assert np.array_equal(pool_bits(d_na["k_pages"]), pool_bits(d_ws["k_pages"]))
         assert np.array_equal(pool_bits(d_na["v_pages"]), pool_bits(d_ws["v_pages"]))
+        # and both against the oracle: pools (and int8 scales) bit for bit,
+        # outputs within the stated tolerance
+        _assert_pools_equal(d_na, kp, vp, ks, vs)
+        assert_close(a, ref)
+
+
+def test_noalloc_status_word_is_reported_then_cleared(lib):
+    # a block-table entry outside the pool makes the device skip that page and
+    # set KVATTN_DEV_BAD_PAGE in the array's status word; the next call on the
+    # same stream starts from a cleared word and reports 0
+    stream = torch.cuda.current_stream().cuda_stream
+    wl, h = _case(23, "bf16", 128)
+    bad = dict(h)
+    bad["block_table"] = h["block_table"].copy()
+    bad["block_table"][0, 3] = -1
+    d_bad = to_dev(bad)
+    out_bad = torch.zeros(d_bad["q"].shape, dtype=torch.bfloat16, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    rc = lib.kvattn_decode_noalloc(*_common_args(wl, d_bad, out_bad, stream), status.data_ptr())
+    assert rc == K.KVATTN_OK
+    torch.cuda.synchronize()
+    assert status.item() & K.KVATTN_DEV_BAD_PAGE
+    # the clean call: status 0 and the oracle's result
+    ref, ost, kp, vp, ks, vs = oracle_decode(wl, h)
+    d_ok = to_dev(h)
+    out_ok = torch.full(d_ok["q"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    status.fill_(-1)
+    rc = lib.kvattn_decode_noalloc(*_common_args(wl, d_ok, out_ok, stream), status.data_ptr())
+    assert rc == K.KVATTN_OK
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    _assert_pools_equal(d_ok, kp, vp, ks, vs)
+    assert_close(out_f64(out_ok), ref)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
