@@ -1039,7 +1039,7 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   // to 16 CTAs, each with at least 16 tiles, so every context streams at once;
   // long prompts, whose query tiles already fill the GPU, take one, as does a
   // call without a workspace.
-  // Long prompts over a bf16 cache take the tcgen05 kernel (32-token query
+  // Long prompts over a bf16 cache take the tcgen05 kernel (64-token query
   // tiles, one CTA an SM): their splits aim at two CTAs an SM.
   p.tc_tiles = (!int8 && !short_chunks && max_new_tokens > 64) ? 1 : 0;
   {

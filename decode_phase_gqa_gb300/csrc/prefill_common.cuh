@@ -22,11 +22,11 @@ constexpr int kPsKeys = kPfWarps * kPsWarpKeys;  // keys a stage holds
 constexpr int kPsStages = 2;
 constexpr int kPsMinTiles = 16;              // stages a split takes at least
 
-// the tcgen05 attention kernel (prefill_tc.cu): 32 new tokens x 4 heads = 128
-// MMA rows a CTA, 64-key tiles, splits of at least 8 tiles
-constexpr int kTcTok = 32;
-constexpr int kTcKeys = 64;
-constexpr int kTcMinTiles = 8;
+// the tcgen05 attention kernel (prefill_tc.cu): 64 new tokens x 4 heads (two
+// halves of 128 MMA rows) a CTA, 128-key tiles, splits of at least 4 tiles
+constexpr int kTcTok = 64;
+constexpr int kTcKeys = 128;
+constexpr int kTcMinTiles = 4;
 
 struct PrefillParams {
   const __nv_bfloat16 *q, *k_new, *v_new;
@@ -67,7 +67,7 @@ __device__ __forceinline__ bool seq_span(const PrefillParams &p, int b, int &sta
 
 // The tcgen05 kernel's query tile starting at new token t0 (n_rows new tokens
 // attended, after ctx cached ones): the keys its last row sees, and the
-// splits sharing its 64-key tiles (at most S, each of at least kTcMinTiles).
+// splits sharing its 128-key tiles (at most S, each of at least kTcMinTiles).
 __device__ __forceinline__ int tc_tile_keys(int ctx, int n_rows, int t0) {
   return ctx + min(n_rows, t0 + kTcTok);
 }
@@ -77,7 +77,7 @@ __device__ __forceinline__ int tc_splits(int n_tiles, int S) {
 
 // Launch of the tcgen05 attention kernel (prefill_tc.cu) for the long-prompt
 // path over a bf16 cache: new tokens 0 .. cover - 1 of every sequence in
-// 32-token query tiles, p.n_splits splits at most; the append kernel has been
+// 64-token query tiles, p.n_splits splits at most; the append kernel has been
 // queued before it.
 cudaError_t launch_prefill_tc(const PrefillParams &p, int head_dim, int cover,
                               cudaStream_t stream);

@@ -5,56 +5,71 @@
 // "LLM inference from smollm3.go", section "Prefill: the whole prompt at once"
 // (new token i of a sequence attends over keys 0 .. ctx + i).
 //
-// A CTA owns 128 MMA rows: 32 new tokens of one sequence x the 4 query heads
-// of one group (row 32 hh + tl: head hh of the group, token tl), so every
-// staged K/V tile serves the whole group (section 4.4.2 of the Qwen3-8B page).
-// Keys come in tiles of 64.  Six warps:
-//   * warps 0-3 (one thread per row, TMEM lanes 32 w ..): rotate and scale the
-//     query rows into shared memory; per tile read the scores S from tensor
-//     memory, mask them, keep the row's running maximum m and normaliser l
-//     (log2 units; the maximum moves lazily, by more than 8, so the
-//     accumulator is rarely rescaled), write P = 2^(S - m) as bf16 into
-//     shared memory; at the end read O, divide by l, store bf16;
-//   * warp 4: TMA tensor copies of the K and V tiles (16-key page blocks,
-//     [16 rows][128 bytes] boxes, 128-byte swizzle) into a 3-stage ring;
-//   * warp 5, one thread: issues the MMAs, S = Q K^T into one of two TMEM
-//     score buffers (M 128, N 64, K d) and O += P V into the TMEM accumulator
-//     (M 128, N 64 per half of d, K 64), and commits them to mbarriers.
-// S of tile i + 1 is computed while the softmax warps work on tile i; P is
-// double-buffered so that the softmax of tile i + 1 need not wait for the
-// P V products of tile i.  Every wait is bounded (KVATTN_DEV_TIMEOUT).
+// A CTA owns 64 new tokens of one sequence x the 4 query heads of one group:
+// two halves of 128 MMA rows (row 32 hh + tl of half hf: head hh of the group,
+// token 32 hf + tl), so every staged K/V tile serves the whole group (section
+// 4.4.2 of the Qwen3-8B page) and both halves.  Keys come in tiles of 128.
+// Eleven warps:
+//   * warps 0-3 (half 0) and 4-7 (half 1), one thread per row, TMEM lanes
+//     32 (w % 4) .. of the half's 256 columns (S and P in 0-127, O in 128-):
+//     rotate and scale the query rows into shared memory; per tile read the
+//     row's 128 scores S from tensor memory, mask them, keep the running
+//     maximum m and normaliser l (log2 units; the maximum moves lazily, by
+//     more than 8, so the accumulator is rarely rescaled), and write
+//     P = 2^(S - m) as bf16 pairs back over S in tensor memory; at the end
+//     read O, divide by l, store bf16 (or the partial state of a split);
+//   * warps 8 and 9: TMA tensor copies of the K and of the V tiles (16-key
+//     page blocks, [16 rows][128 bytes] boxes, 128-byte swizzle) into a K ring
+//     and a V ring of 2 (d 128) or 3 (d 64) slots; a thread issues about one
+//     copy every 115 clocks, so each ring has its own issuer;
+//   * warp 10, one thread: issues the MMAs and commits them to mbarriers:
+//     S = Q K^T (M 128, N 128, K d; both operands in shared memory) and
+//     O += P V (M 128, N d, K 128; P from tensor memory, V in shared memory).
+// N of 128 keeps the tensor pipe at its rate with operands read from shared
+// memory (at N 64 the reads of A bound it), and P never passes through shared
+// memory.  Per half the steps are serial (S(i + 1) overwrites P(i) once the
+// P V products of tile i are done); the two halves interleave, so one half's
+// MMAs run while the other's softmax works.  Every wait is bounded
+// (KVATTN_DEV_TIMEOUT).
+#include <cuda_fp16.h>
+
 #include "prefill_common.cuh"
 
 namespace kvattn {
 
 namespace {
 
-constexpr int kTcRows = 4 * kTcTok;  // MMA M: 32 new tokens x 4 heads
-constexpr int kTcStages = 3;        // K/V tiles in flight
-constexpr int kTcThreads = 192;
-constexpr uint32_t kTmemCols = 256; // S[2][64] + O[d]
+constexpr int kTcHalf = kTcTok / 2;  // new tokens of a half
+constexpr int kTcRows = 4 * kTcHalf; // MMA M: 32 new tokens x 4 heads
+constexpr int kTcSoftWarps = 8;      // two halves of four warps
+// warps kTcSoftWarps, + 1: the K and the V producer (one thread issues a
+// tensor copy every ~115 clocks, so the two rings get an issuer each);
+// kTcSoftWarps + 2: the MMA issuer
+constexpr int kTcThreads = 32 * (kTcSoftWarps + 3);
+constexpr uint32_t kTmemCols = 512;  // per half: S / P in 128 columns, O in d
+constexpr uint32_t kHalfCols = 256;
+constexpr uint32_t kOCol = 128;      // O's first TMEM column in a half
 
 template <int D>
 struct TcCfg {
+  static constexpr int kStages = D == 128 ? 2 : 3;           // K/V tiles in flight
   static constexpr int kRegions = D / 64;                    // 128-byte column blocks of a row
   static constexpr int kQRegion = kTcRows * 128;             // [128 rows][128 B]
-  static constexpr int kKVRegion = kTcKeys * 128;            // [64 keys][128 B]
+  static constexpr int kQHalf = kRegions * kQRegion;         // a half's Q
+  static constexpr int kKVRegion = kTcKeys * 128;            // [128 keys][128 B]
   static constexpr int kTile = kRegions * kKVRegion;         // K or V tile
-  static constexpr int kStage = 2 * kTile;                   // K then V
-  static constexpr int kPBuf = kTcRows * 128;                // P [128 rows][64 keys] bf16
   static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQOff + kRegions * kQRegion;
-  static constexpr int kPOff = kStageOff + kTcStages * kStage;
-  static constexpr int kBarOff = kPOff + 2 * kPBuf;
-  // full[S], empty[S], s_full[2], s_free[2], p_full[2], o_done[2], q_ready, mma_done
-  static constexpr int kNumBars = 2 * kTcStages + 10;
+  static constexpr int kKOff = kQOff + 2 * kQHalf;            // K ring [kStages][kTile]
+  static constexpr int kVOff = kKOff + kStages * kTile;       // V ring [kStages][kTile]
+  static constexpr int kBarOff = kVOff + kStages * kTile;
+  // k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2],
+  // o_done[2], q_ready, mma_done
+  static constexpr int kNumBars = 4 * kStages + 8;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;    // tmem base, abort flag, counters
   static constexpr int kTurnsOff = kMiscOff + 64;            // float2[64]
   static constexpr int kSmem = kTurnsOff + 512 + 1024;       // + slack for 1024-byte alignment
-  static constexpr uint32_t kOCol = 128;                     // O's first TMEM column
   static_assert(kSmem <= 227 * 1024, "shared memory");
-  static_assert(kStageOff % 1024 == 0 && kStage % 1024 == 0 && kPOff % 1024 == 0,
-                "swizzle atoms need 1024-byte alignment");
+  static_assert(kKOff % 1024 == 0 && kTile % 1024 == 0, "swizzle atoms need 1024-byte alignment");
 };
 
 struct PfTcParams {
@@ -83,13 +98,24 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 // D (TMEM, fp32) = A B (+ D when acc): A and B bf16 in shared memory
+// (no memory clobber: the operands are ordered by the mbarrier waits and
+// fences around the issue loop, and the address arithmetic may be scheduled
+// ahead of the instruction)
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc)
-      : "memory");
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc));
+}
+// D (TMEM, fp32) = A B (+ D when acc): A bf16 in tensor memory (row r in lane
+// r, two consecutive K elements a 32-bit column), B bf16 in shared memory
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc));
 }
 // `bar` receives one arrival when every tcgen05 operation this thread issued
 // before has completed
@@ -135,28 +161,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Columns c .. c + 63 of this thread's TMEM lane (32x32b shape: thread i
-// of the warp reads lane 32 (warp % 4) + i), as fp32; the wait for the load is
-// in the same statement, so no use of r can be scheduled before it.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // Store columns c .. c + 31 of this thread's TMEM lane and wait for the
 // stores to complete.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -171,6 +175,55 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+
+// Columns c .. c + 127 of this thread's TMEM lane as fp32, the wait in the
+// same statement.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+        "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Store 64 raw 32-bit columns (bf16 pairs) of this thread's TMEM lane and
+// wait for the stores to complete.
+__device__ __forceinline__ void tmem_st64u(uint32_t taddr, const uint32_t (&v)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :
+      : "r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]),
+        "r"(v[32]), "r"(v[33]), "r"(v[34]), "r"(v[35]), "r"(v[36]), "r"(v[37]), "r"(v[38]), "r"(v[39]),
+        "r"(v[40]), "r"(v[41]), "r"(v[42]), "r"(v[43]), "r"(v[44]), "r"(v[45]), "r"(v[46]), "r"(v[47]),
+        "r"(v[48]), "r"(v[49]), "r"(v[50]), "r"(v[51]), "r"(v[52]), "r"(v[53]), "r"(v[54]), "r"(v[55]),
+        "r"(v[56]), "r"(v[57]), "r"(v[58]), "r"(v[59]), "r"(v[60]), "r"(v[61]), "r"(v[62]), "r"(v[63])
       : "memory");
 }
 
@@ -196,9 +249,36 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
   return false;
 }
 
+// 2^x0 and 2^x1 (x <= 8 or -inf) from one special-function operation on an
+// f16 pair: the arguments are rounded to f16 (11-bit significand; at |x| < 8
+// that moves 2^x by less than 0.14 %, and where |x| is larger the weight is
+// below 2^-8), the results carry about 10 bits, more than the bf16 the
+// weights are rounded to for the MMA
+__device__ __forceinline__ float2 ex2_pair(float x0, float x1) {
+  uint32_t h, e;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
+  const __half2 eh = *reinterpret_cast<const __half2 *>(&e);
+  return __half22float2(eh);
+}
+
+// Largest of N values, as a tree (no chain of N dependent operations)
+template <int N>
+__device__ __forceinline__ float tree_max(const float (&s)[N]) {
+  float t[N / 4];
+#pragma unroll
+  for (int k = 0; k < N / 4; ++k) t[k] = fmaxf(fmaxf(s[4 * k], s[4 * k + 1]), fmaxf(s[4 * k + 2], s[4 * k + 3]));
+#pragma unroll
+  for (int w = N / 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
+  return t[0];
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ PfTcParams tp) {
   using C = TcCfg<D>;
+  constexpr int S = C::kStages;
   const PrefillParams &p = tp.p;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -216,11 +296,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   // (every early exit below is the same for the whole CTA; each thread waits
   // for the append grid before it leaves)
   if (!seq_span(p, b, start, n_new, ctx)) {
-    if (qt == 0 && grp == 0 && tid == 0) report(p, KVATTN_DEV_BAD_LEN);
+    if (qt == 0 && grp == 0 && tid == 0 && blockIdx.z == 0) report(p, KVATTN_DEV_BAD_LEN);
     pdl_wait_primary();
     return;
   }
-  if (qt == 0 && grp == 0 && tid == 0 && n_new > tp.cover) report(p, KVATTN_DEV_BAD_LEN);
+  if (qt == 0 && grp == 0 && tid == 0 && blockIdx.z == 0 && n_new > tp.cover)
+    report(p, KVATTN_DEV_BAD_LEN);
   const int n_rows_tok = min(n_new, tp.cover);  // new tokens the launch attends
   const int t0 = qt * kTcTok;
   if (t0 >= n_rows_tok) {
@@ -239,35 +320,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   const int per = (all_tiles + nz - 1) / nz;
   const int kt0 = min(all_tiles, z * per);
   const int n_tiles = min(all_tiles, kt0 + per) - kt0;  // may be 0: an empty partial state
+  // The CTA visits its key tiles starting at a rotation of its own: the CTAs
+  // of one sequence and head group that run at once (the query tiles of one
+  // wave) would otherwise all copy tile 0, then tile 1, ... at the same time
+  // and queue on the same L2 lines.  (The online softmax takes the tiles in
+  // any order.)
+  const int rot = n_tiles > 1 ? (int)(((unsigned)qt * 5u + (unsigned)grp) % (unsigned)n_tiles) : 0;
+  const auto tile_at = [&](int i) { return kt0 + (i + rot < n_tiles ? i + rot : i + rot - n_tiles); };
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
-  uint64_t *full = bars, *empty = bars + kTcStages;
-  uint64_t *s_full = bars + 2 * kTcStages, *s_free = s_full + 2, *p_full = s_free + 2;
-  uint64_t *o_done = p_full + 2, *q_ready = o_done + 2, *mma_done = q_ready + 1;
+  uint64_t *k_full = bars, *v_full = bars + S, *k_empty = bars + 2 * S, *v_empty = bars + 3 * S;
+  uint64_t *s_full = bars + 4 * S;  // [half]
+  uint64_t *p_full = s_full + 2;    // [half]
+  uint64_t *o_done = p_full + 2;    // [half]
+  uint64_t *q_ready = o_done + 2, *mma_done = q_ready + 1;
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
   uint32_t *tmem_slot = misc;                                 // [0]
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
-  volatile int *issued_tiles = reinterpret_cast<volatile int *>(misc + 2);
+  volatile int *issued_k = reinterpret_cast<volatile int *>(misc + 2);
+  volatile int *issued_v = reinterpret_cast<volatile int *>(misc + 3);
   float2 *turns = reinterpret_cast<float2 *>(smem + C::kTurnsOff);
   uint8_t *qs = smem + C::kQOff;
-  uint8_t *stages = smem + C::kStageOff;
-  uint8_t *pbuf = smem + C::kPOff;
+  uint8_t *kring = smem + C::kKOff, *vring = smem + C::kVOff;
 
   if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kTcRows);
       mbar_init(&p_full[i], kTcRows);
       mbar_init(&o_done[i], 1);
     }
-    mbar_init(q_ready, kTcRows);
+    mbar_init(q_ready, 2 * kTcRows);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
-    *issued_tiles = 0;
+    *issued_k = 0;
+    *issued_v = 0;
     fence_barrier_init();
   }
   if (tid < 64) turns[tid] = p.turns[tid];
@@ -280,23 +372,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < kTcSoftWarps) {
     // ---- softmax warps: one thread per row ------------------------------------
-    const int row = tid;  // 32 warp + lane: head h0 + warp, token t0 + lane
-    const int h = h0 + warp, t = t0 + lane;
+    const int hf = warp >> 2, wq = warp & 3;
+    const int row = 32 * wq + lane;          // row of the half: head h0 + wq, token t
+    const int h = h0 + wq, t = t0 + kTcHalf * hf + lane;
     const bool live = t < n_rows_tok;
-    // the row's query, rotated in fp32 at position ctx + t, scaled by
-    // scale * log2(e), rounded to bf16, into the swizzled Q tile
+    // The row's query, rotated in fp32 at position ctx + t, scaled by
+    // scale * log2(e), rounded to bf16, into the half's swizzled Q tile.  The
+    // rotation angles depend on the token only: the four threads of a token
+    // (one per head) each form a quarter of its (cos, sin) pairs into a table
+    // in the last V slot (its first copy is issued after q_ready), then read
+    // all of them.
     {
+      uint4 lo4[D / 16], hi4[D / 16];  // the whole row, loaded at once
       const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)(start + (live ? t : 0)) * p.n_qh + h) * D);
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < D / 16; ++c) {
-        uint4 lo4 = make_uint4(0u, 0u, 0u, 0u), hi4 = lo4;
-        if (live) {
-          lo4 = src[c];
-          hi4 = src[c + D / 16];
+        lo4[c] = live ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        hi4[c] = live ? src[c + D / 16] : make_uint4(0u, 0u, 0u, 0u);
+      }
+      float2 *cs_tab = reinterpret_cast<float2 *>(vring + (S - 1) * C::kTile);  // [D / 2][64]
+      static_assert(kTcTok * (D / 2) * 8 <= C::kTile, "the angle table fits a V slot");
+      const int tok = kTcHalf * hf + lane;                   // token within the CTA
+      if (p.use_rope) {
+#pragma unroll 1
+        for (int i = wq; i < D / 2; i += 4) {
+          float sn, cs;
+          sincospif(2.f * frac_turns(ctx + t, turns[i]), &sn, &cs);
+          cs_tab[i * kTcTok + tok] = make_float2(cs, sn);
         }
-        const uint32_t lw[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hw[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+      }
+      named_barrier_sync(1, 32 * kTcSoftWarps);
+      uint8_t *qh = qs + hf * C::kQHalf;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const uint32_t lw[4] = {lo4[c].x, lo4[c].y, lo4[c].z, lo4[c].w};
+        const uint32_t hw[4] = {hi4[c].x, hi4[c].y, hi4[c].z, hi4[c].w};
         uint32_t ol[4], oh[4];
 #pragma unroll
         for (int e2 = 0; e2 < 4; ++e2) {
@@ -306,10 +418,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             const int i = 8 * c + 2 * e2 + k;
             float lo = __uint_as_float(k ? (lw[e2] & 0xffff0000u) : (lw[e2] << 16));
             float hi = __uint_as_float(k ? (hw[e2] & 0xffff0000u) : (hw[e2] << 16));
-            if (p.use_rope && live) {
-              float sn, cs;
-              sincospif(2.f * frac_turns(ctx + t, turns[i]), &sn, &cs);
-              const float x = lo * cs - hi * sn, y = hi * cs + lo * sn;
+            if (p.use_rope) {
+              const float2 r = cs_tab[i * kTcTok + tok];
+              const float x = lo * r.x - hi * r.y, y = hi * r.x + lo * r.y;
               lo = x;
               hi = y;
             }
@@ -320,115 +431,112 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           oh[e2] = pack_bf16(bb[0], bb[1]);
         }
         const int il = 8 * c, ih = 8 * c + D / 2;  // first element of each chunk
-        uint8_t *dl = qs + (il / 64) * C::kQRegion + row * 128 + ((((il % 64) / 8) ^ (row & 7)) << 4);
-        uint8_t *dh = qs + (ih / 64) * C::kQRegion + row * 128 + ((((ih % 64) / 8) ^ (row & 7)) << 4);
+        uint8_t *dl = qh + (il / 64) * C::kQRegion + row * 128 + ((((il % 64) / 8) ^ (row & 7)) << 4);
+        uint8_t *dh = qh + (ih / 64) * C::kQRegion + row * 128 + ((((ih % 64) / 8) ^ (row & 7)) << 4);
         *reinterpret_cast<uint4 *>(dl) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
         *reinterpret_cast<uint4 *>(dh) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
       }
     }
-    fence_proxy_async_smem();  // the MMAs read Q through the async proxy
+    // every read of the table is done (the producer waits for q_ready before
+    // its first copy lands there) and Q is visible to the MMAs' async proxy
+    fence_proxy_async_smem();
     mbar_arrive(q_ready);
     pdl_wait_primary();
 
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * wq) << 16) + kHalfCols * (uint32_t)hf;
     const int kmax = live ? ctx + t : -1;  // last key the row sees
     const float kFloor = -1e30f;
     float m_run = kFloor, l_run = 0.f;
     int i = 0;
     for (; i < n_tiles; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int buf = i & 1;
-      if (!__all_sync(0xffffffffu, tc_wait(&s_full[buf], (uint32_t)((i >> 1) & 1), abort_flag, p))) break;
+      // masks: causal (key <= ctx + t), and pages outside the pool (lanes 0-7
+      // look up the tile's eight 16-key blocks, before the scores are waited
+      // for); a tile every row of the warp sees whole, on valid pages, needs none
+      const int key0 = tile_at(i) * kTcKeys;
+      int pg = 0;
+      if (lane < kTcKeys / 16 && key0 + 16 * lane < n_keys)
+        pg = __ldg(p.block_table + (size_t)b * p.max_pages + ((key0 + 16 * lane) >> p.page_shift));
+      {
+        // one lane polls for the scores, the warp follows it
+        bool got = true;
+        if (lane == 0) got = tc_wait(&s_full[hf], (uint32_t)(i & 1), abort_flag, p);
+        if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      }
       tc_fence_after();
-      float s[kTcKeys];
-      tmem_ld64(lane_base + (uint32_t)(buf * kTcKeys), s);
-      tc_fence_before();
-      mbar_arrive(&s_free[buf]);
-      // masks: causal (key <= ctx + t), and pages outside the pool
-      const int key0 = (kt0 + i) * kTcKeys;
-      bool gv[kTcKeys / 16];
+      // the row's 128 scores in one load
+      float sc[kTcKeys];
+      tmem_ld128(lane_base, sc);
+      const unsigned vbits = __ballot_sync(0xffffffffu, pg >= 0 && pg < p.num_pages) & 0xFFu;
+      if (__any_sync(0xffffffffu, key0 + kTcKeys - 1 > kmax) || vbits != 0xFFu) {
 #pragma unroll
-      for (int q4 = 0; q4 < kTcKeys / 16; ++q4) {
-        const int key = key0 + 16 * q4;
-        bool ok = key <= kmax;
-        if (ok) {
-          const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + (key >> p.page_shift));
-          ok = pg >= 0 && pg < p.num_pages;
+        for (int c = 0; c < kTcKeys; ++c) {
+          const bool ok = ((vbits >> (c >> 4)) & 1u) && key0 + c <= kmax;
+          sc[c] = ok ? sc[c] : -INFINITY;
         }
-        gv[q4] = ok;
       }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kTcKeys; ++c) {
-        const bool ok = gv[c >> 4] && key0 + c <= kmax;
-        s[c] = ok ? s[c] : -INFINITY;
-        mx = fmaxf(mx, s[c]);
-      }
-      const float m_new = fmaxf(m_run, mx);
+      const float m_new = fmaxf(m_run, tree_max<kTcKeys>(sc));
       const bool need = m_new > m_run + 8.f;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.f;
-      if (i > 0 && __any_sync(0xffffffffu, need)) {
-        // rescale this warp's rows of O once the P V products of tile i - 1 are in
-        if (!__all_sync(0xffffffffu, tc_wait(&o_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), abort_flag, p)))
-          break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float o[32];
-          tmem_ld32(lane_base + C::kOCol + (uint32_t)c0, o);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] *= alpha;
-          tmem_st32(lane_base + C::kOCol + (uint32_t)c0, o);
-        }
-      }
       if (need) {
         m_run = m_new;
         l_run *= alpha;
       }
       // The last tile may end inside a 16-key block whose rows past the keys
-      // hold whatever the pool has there (possibly not a number): zero those V
-      // rows, so that their zero weights cannot meet a NaN in the MMA (the
-      // masked scores are selected away, so stale K rows do no harm).
-      if (kt0 + i == all_tiles - 1 && (n_keys & 15) != 0) {
-        const int s = i % kTcStages;
-        if (!__all_sync(0xffffffffu, tc_wait(&full[s], (uint32_t)((i / kTcStages) & 1), abort_flag, p)))
-          break;
+      // hold whatever the pool has there (possibly not a number): half 0 zeroes
+      // those V rows, so that their zero weights cannot meet a NaN in the MMA
+      // (the masked scores are selected away, so stale K rows do no harm).
+      // Both halves' products of the tile are issued after half 0's P.
+      if (hf == 0 && tile_at(i) == all_tiles - 1 && (n_keys & 15) != 0) {
+        const int st = i % S;
+        if (!__all_sync(0xffffffffu, tc_wait(&v_full[st], (uint32_t)((i / S) & 1), abort_flag, p))) break;
         const int r0 = n_keys - key0, r1 = (r0 + 15) & ~15;
-        uint8_t *vt = stages + s * C::kStage + C::kTile;
+        uint8_t *vt = vring + st * C::kTile;
         for (int e = tid; e < (r1 - r0) * C::kRegions * 8; e += kTcRows) {
-          const int r = r0 + e / (C::kRegions * 8), rest = e % (C::kRegions * 8);
-          *reinterpret_cast<uint4 *>(vt + (rest >> 3) * C::kKVRegion + r * 128 + (rest & 7) * 16) =
+          const int r = r0 + e / (C::kRegions * 8), rr = e % (C::kRegions * 8);
+          *reinterpret_cast<uint4 *>(vt + (rr >> 3) * C::kKVRegion + r * 128 + (rr & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();
       }
-      // P buffer buf is free once the P V products of tile i - 2 are in
-      if (i >= 2 &&
-          !__all_sync(0xffffffffu, tc_wait(&o_done[buf], (uint32_t)(((i >> 1) - 1) & 1), abort_flag, p)))
-        break;
-      uint8_t *prow = pbuf + buf * C::kPBuf + row * 128;
+      // P = 2^(S - m) as bf16 pairs over the first 64 columns of S (column c:
+      // keys 2c, 2c + 1), in one store; the weights come two by two from the
+      // f16 exponential (half the special-function operations of fp32 ones,
+      // which bound this loop); the normaliser sums them as computed, in
+      // eight partial sums
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      {
+        uint32_t pw[kTcKeys / 2];
 #pragma unroll
-      for (int c8 = 0; c8 < kTcKeys / 8; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2_approx(s[8 * c8 + 2 * e2] - m_run),
-                                                          ex2_approx(s[8 * c8 + 2 * e2 + 1] - m_run));
-          const float2 pf = __bfloat1622float2(pr);
-          l_run += pf.x + pf.y;  // the normaliser of the weights the MMA uses
-          w[e2] = *reinterpret_cast<const uint32_t *>(&pr);
+        for (int c = 0; c < kTcKeys / 2; ++c) {
+          const float2 e = ex2_pair(sc[2 * c] - m_run, sc[2 * c + 1] - m_run);
+          ls[c & 7] += e.x + e.y;
+          pw[c] = pack_bf16(e.x, e.y);
         }
-        *reinterpret_cast<uint4 *>(prow + ((c8 ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        tmem_st64u(lane_base, pw);
       }
-      fence_proxy_async_smem();
+      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      // O holds the products of tiles < i, all complete: the MMA thread issued
+      // S(i) only after them.  Rescale this warp's rows when a maximum moved.
+      if (i > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tmem_ld32(lane_base + kOCol + (uint32_t)c0, o);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] *= alpha;
+          tmem_st32(lane_base + kOCol + (uint32_t)c0, o);
+        }
+      }
       tc_fence_before();
-      mbar_arrive(&p_full[buf]);
+      mbar_arrive(&p_full[hf]);
     }
     // ---- the row's output: O / l rounded to bf16, or (several splits) the
     // partial state o (relative to 2^m), m, l for the merge kernel ------------
     if (i == n_tiles) {
       const int last = n_tiles - 1;
       const bool ok = n_tiles == 0 ||
-                      __all_sync(0xffffffffu, tc_wait(&o_done[last & 1], (uint32_t)((last >> 1) & 1), abort_flag, p));
+                      __all_sync(0xffffffffu, tc_wait(&o_done[hf], (uint32_t)(last & 1), abort_flag, p));
       if (ok) {
         if (n_tiles > 0) tc_fence_after();
         const float f = l_run > 0.f ? 1.f / l_run : 0.f;  // no visible key: a zero row
@@ -439,7 +547,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
           if (n_tiles > 0) {
-            tmem_ld32(lane_base + C::kOCol + (uint32_t)c0, o);
+            tmem_ld32(lane_base + kOCol + (uint32_t)c0, o);
           } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] = 0.f;
@@ -461,48 +569,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
     }
     tc_fence_before();
-  } else if (warp == 4) {
-    // ---- producer: K and V tiles by TMA ----------------------------------------------
+  } else if (warp <= kTcSoftWarps + 1) {
+    // ---- producers: the K tiles (warp 8) and the V tiles (warp 9) by TMA --------
+    // K(i) and V(i) have rings of their own: K(i) is released once both halves'
+    // scores of tile i are done, V(i) once their P V products are, so the
+    // next keys start loading well before the weighted sums end
+    const bool is_v = warp == kTcSoftWarps + 1;
     pdl_wait_primary();  // the appended rows are complete and visible
-    prefetch_tensormap(&tp.tmap_k);
-    prefetch_tensormap(&tp.tmap_v);
-    int i = 0;
-    for (; i < n_tiles; ++i) {
+    prefetch_tensormap(is_v ? &tp.tmap_v : &tp.tmap_k);
+    uint64_t *ring_full = is_v ? v_full : k_full, *ring_empty = is_v ? v_empty : k_empty;
+    uint8_t *ring = is_v ? vring : kring;
+    volatile int *issued = is_v ? issued_v : issued_k;
+    const CUtensorMap *map = is_v ? &tp.tmap_v : &tp.tmap_k;
+    auto wait_slot = [&](uint64_t *bar, uint32_t parity) -> bool {
+      bool ok = true;
+      if (lane == 0) ok = tc_wait(bar, parity, abort_flag, p);
+      return __shfl_sync(0xffffffffu, ok, 0);
+    };
+    for (int i = 0; i < n_tiles; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int s = i % kTcStages;
-      if (i >= kTcStages) {
-        bool ok = true;
-        if (lane == 0) ok = tc_wait(&empty[s], (uint32_t)(((i / kTcStages) - 1) & 1), abort_flag, p);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      }
-      // pool row of each 16-key block of the tile (lanes 0-3); rows past the
+      const int s = i % S;
+      // pool row of each 16-key block of the tile (lanes 0-7); rows past the
       // keys or on an out-of-range page are fetched from row -16, outside the
       // view, which the copy fills with zeros
       int prow = -16;
       if (lane < kTcKeys / 16) {
-        const int key = (kt0 + i) * kTcKeys + 16 * lane;
+        const int key = tile_at(i) * kTcKeys + 16 * lane;
         if (key < n_keys) {
           const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + (key >> p.page_shift));
           if (pg >= 0 && pg < p.num_pages)
             prow = (pg * p.n_kvh + j) * p.page_size + (key & (p.page_size - 1));
-          else
+          else if (!is_v)
             report(p, KVATTN_DEV_BAD_PAGE);
         }
       }
       int rows[kTcKeys / 16];
 #pragma unroll
-      for (int q4 = 0; q4 < kTcKeys / 16; ++q4) rows[q4] = __shfl_sync(0xffffffffu, prow, q4);
+      for (int q8 = 0; q8 < kTcKeys / 16; ++q8) rows[q8] = __shfl_sync(0xffffffffu, prow, q8);
+      // the last V slot holds the query rows' angle table until every Q row
+      // is written
+      if (is_v && i == S - 1 && !wait_slot(q_ready, 0)) break;
+      if (i >= S && !wait_slot(&ring_empty[s], (uint32_t)(((i / S) - 1) & 1))) break;
       if (lane == 0) {
-        uint8_t *kd = stages + s * C::kStage, *vd = kd + C::kTile;
-        mbar_arrive_expect_tx(&full[s], C::kStage);
+        uint8_t *dst = ring + s * C::kTile;
+        mbar_arrive_expect_tx(&ring_full[s], C::kTile);
 #pragma unroll
-        for (int q4 = 0; q4 < kTcKeys / 16; ++q4)
+        for (int q8 = 0; q8 < kTcKeys / 16; ++q8)
 #pragma unroll
-          for (int r = 0; r < C::kRegions; ++r) {
-            tma_load_2d_keep(kd + r * C::kKVRegion + q4 * 2048, &tp.tmap_k, 64 * r, rows[q4], &full[s]);
-            tma_load_2d_keep(vd + r * C::kKVRegion + q4 * 2048, &tp.tmap_v, 64 * r, rows[q4], &full[s]);
-          }
-        *issued_tiles = i + 1;
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_2d_keep(dst + r * C::kKVRegion + q8 * 2048, map, 64 * r, rows[q8], &ring_full[s]);
+        *issued = i + 1;
       }
       __syncwarp();
     }
@@ -511,52 +627,82 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     pdl_wait_primary();
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(kTcRows, kTcKeys, false);
-      constexpr uint32_t kIdPV = idesc_bf16(kTcRows, 64, true);
-      const uint32_t q0 = smem_addr(qs), st0 = smem_addr(stages), p0 = smem_addr(pbuf);
+      constexpr uint32_t kIdPV = idesc_bf16(kTcRows, D, true);
+      // Descriptors of the first operand blocks, formed once: every other
+      // block (k-step, stage, half) is a constant number of 16-byte units on,
+      // added to the start-address field (which never carries: shared
+      // addresses stay below 2^18)
+      const uint32_t q0 = smem_addr(qs);
+      const uint64_t dq = sw128_desc(q0, 16, 1024);               // Q, K-major
+      const uint64_t dk = sw128_desc(smem_addr(kring), 16, 1024);  // K tiles, K-major
+      // V tiles, MN-major: rows of 64 d (one 128-byte swizzle atom across),
+      // 8-key groups 1024 bytes apart, the next 64 d one region on
+      const uint64_t dv = sw128_desc(smem_addr(vring), C::kKVRegion, 1024);
       bool ok = tc_wait(q_ready, 0, abort_flag, p);
       tc_fence_after();
-      auto issue_s = [&](int i) -> bool {
-        const int s = i % kTcStages, buf = i & 1;
-        if (!tc_wait(&full[s], (uint32_t)((i / kTcStages) & 1), abort_flag, p)) return false;
-        if (i >= 2 && !tc_wait(&s_free[buf], (uint32_t)(((i >> 1) - 1) & 1), abort_flag, p)) return false;
-        tc_fence_after();
-        const uint32_t kb = st0 + (uint32_t)(s * C::kStage);
+      auto issue_s = [&](int i, int hf) {
+        const int s = i % S;
+        const uint64_t kst = dk + (uint64_t)((s * C::kTile) >> 4);
+        const uint64_t qh = dq + (uint64_t)((hf * C::kQHalf) >> 4);
+        const uint32_t d_s = tmem + kHalfCols * (uint32_t)hf;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (uint32_t)((ks & 3) * 32);  // 16 elements on, inside the atom
-          const uint64_t a = sw128_desc(q0 + (uint32_t)((ks >> 2) * C::kQRegion) + off, 16, 1024);
-          const uint64_t bd = sw128_desc(kb + (uint32_t)((ks >> 2) * C::kKVRegion) + off, 16, 1024);
-          tc_mma(tmem + (uint32_t)(buf * kTcKeys), a, bd, kIdS, ks > 0 ? 1u : 0u);
+          // k-step ks: 64-element column block ks / 4, 32 bytes per step inside it
+          const uint64_t oq = (uint64_t)(((ks >> 2) * C::kQRegion + (ks & 3) * 32) >> 4);
+          const uint64_t ok2 = (uint64_t)(((ks >> 2) * C::kKVRegion + (ks & 3) * 32) >> 4);
+          tc_mma(d_s, qh + oq, kst + ok2, kIdS, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[buf]);
-        return true;
+        tc_commit(&s_full[hf]);
       };
-      auto issue_pv = [&](int i) -> bool {
-        const int s = i % kTcStages, buf = i & 1;
-        if (!tc_wait(&p_full[buf], (uint32_t)((i >> 1) & 1), abort_flag, p)) return false;
-        tc_fence_after();
-        const uint32_t vb = st0 + (uint32_t)(s * C::kStage + C::kTile);
-        const uint32_t pa = p0 + (uint32_t)(buf * C::kPBuf);
+      auto issue_pv = [&](int i, int hf) {
+        const int s = i % S;
+        const uint64_t vst = dv + (uint64_t)((s * C::kTile) >> 4);
+        const uint32_t d_o = tmem + kHalfCols * (uint32_t)hf + kOCol;
+        const uint32_t a_p = tmem + kHalfCols * (uint32_t)hf;  // P: columns 0-63 of the half
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
-        for (int hf = 0; hf < C::kRegions; ++hf)
-#pragma unroll
-          for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-            const uint64_t a = sw128_desc(pa + (uint32_t)(ks * 32), 16, 1024);
-            // V: [keys][64 d] per half, rows of d contiguous (MN-major for B);
-            // 16 keys = two 8-row groups = 2048 bytes on
-            const uint64_t bd = sw128_desc(vb + (uint32_t)(hf * C::kKVRegion + ks * 2048), 1024, 1024);
-            tc_mma(tmem + C::kOCol + (uint32_t)(64 * hf), a, bd, kIdPV, (i > 0 || ks > 0) ? 1u : 0u);
-          }
-        tc_commit(&o_done[buf]);
-        tc_commit(&empty[s]);
-        return true;
+        for (int ks = 0; ks < kTcKeys / 16; ++ks)
+          // 16 keys: 8 columns of P; two 8-row groups = 2048 bytes of V on
+          tc_mma_ts(d_o, a_p + (uint32_t)(8 * ks), vst + (uint64_t)(ks * 128), kIdPV, ks > 0 ? 1u : acc0);
+        tc_commit(&o_done[hf]);
       };
-      if (ok && n_tiles > 0) ok = issue_s(0);
-      if (ok && n_tiles > 1) ok = issue_s(1);
+      // Per tile: both halves' P V(i) (each once its P(i) is written and V(i)
+      // has landed), then both halves' S(i + 1) (each once its P V(i) is done,
+      // since S(i + 1) overwrites P(i), and K(i + 1) has landed).  Half 0's
+      // softmax runs ahead of half 1's by about one S, so the tensor pipe
+      // takes half 1's products while half 0 computes its weights.
+      if (ok && n_tiles > 0) {
+        ok = tc_wait(&k_full[0], 0, abort_flag, p);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+          issue_s(0, 1);
+          tc_commit(&k_empty[0]);  // both halves' scores of tile 0 issued
+        }
+      }
       for (int i = 0; ok && i < n_tiles; ++i) {
         if (*abort_flag) break;
-        ok = issue_pv(i);
-        if (ok && i + 2 < n_tiles) ok = issue_s(i + 2);
+        const int s = i % S;
+        ok = tc_wait(&v_full[s], (uint32_t)((i / S) & 1), abort_flag, p);
+        for (int hf = 0; hf < 2 && ok; ++hf) {
+          ok = tc_wait(&p_full[hf], (uint32_t)(i & 1), abort_flag, p);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(i, hf);
+        }
+        if (!ok) break;
+        tc_commit(&v_empty[s]);  // both halves' P V(i) issued
+        if (i + 1 < n_tiles) {
+          const int s1 = (i + 1) % S;
+          ok = tc_wait(&k_full[s1], (uint32_t)(((i + 1) / S) & 1), abort_flag, p);
+          for (int hf = 0; hf < 2 && ok; ++hf) {
+            ok = tc_wait(&o_done[hf], (uint32_t)(i & 1), abort_flag, p);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(i + 1, hf);
+          }
+          if (ok) tc_commit(&k_empty[s1]);  // both halves' S(i + 1) issued
+        }
       }
       // every MMA issued has completed before the tensor memory is freed
       tc_commit(mma_done);
@@ -566,11 +712,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   }
 
   __syncthreads();
-  if (warp == 4 && lane == 0 && *abort_flag) {
-    // copies still in flight on a stage nobody waited for land before the CTA leaves
-    const int n = *issued_tiles;
-    for (int i = max(0, n - kTcStages); i < n; ++i)
-      (void)mbar_wait_bounded(&full[i % kTcStages], (uint32_t)((i / kTcStages) & 1));
+  if (warp == kTcSoftWarps && lane == 0 && *abort_flag) {
+    // copies still in flight on a slot nobody waited for land before the CTA leaves
+    const int nk = *issued_k, nv = *issued_v;
+    for (int i = max(0, nk - S); i < nk; ++i) (void)mbar_wait_bounded(&k_full[i % S], (uint32_t)((i / S) & 1));
+    for (int i = max(0, nv - S); i < nv; ++i) (void)mbar_wait_bounded(&v_full[i % S], (uint32_t)((i / S) & 1));
   }
   __syncthreads();
   tc_fence_after();
