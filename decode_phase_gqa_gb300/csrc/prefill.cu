@@ -140,8 +140,26 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
     const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + ((size_t)r * p.n_kvh + j) * D);
     chunk = lane < CH ? ks[lane] : vs[lane - CH];
   }
+  // the tcgen05 attention kernel's query rows (see below): the first four
+  // heads of the group are fetched now too, so their latency overlaps the rest
+  constexpr int QB = 4;                  // query heads fetched at once
+  const int g = p.n_qh / p.n_kvh;
+  __nv_bfloat16 qv[QB][2 * (D / 64)];    // element i = lane + 32 k and i + D / 2
+  auto fetch_q = [&](int h_first) {
+#pragma unroll
+    for (int hh = 0; hh < QB; ++hh) {
+      const bool in = live && h_first + hh < g;
+      const __nv_bfloat16 *qs = p.q + ((size_t)r * p.n_qh + j * g + (in ? h_first + hh : 0)) * D;
+#pragma unroll
+      for (int k = 0; k < D / 64; ++k) {
+        qv[hh][2 * k] = in ? qs[lane + 32 * k] : __float2bfloat16_rn(0.f);
+        qv[hh][2 * k + 1] = in ? qs[lane + 32 * k + D / 2] : __float2bfloat16_rn(0.f);
+      }
+    }
+  };
+  if (p.tc_tiles) fetch_q(0);
   // (every test below depends on the token only, so all warps of a token agree)
-  bool ok = false;
+  bool span_ok = false, ok = false;
   int lo = 0, slot = 0, page = 0;
   if (live) {
     lo = seq_of_row(p, r, lane);
@@ -152,6 +170,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
         r - start >= p.tiles_per_seq * p.tile_rows) {
       if (lane == 0 && j == 0) report(p, KVATTN_DEV_BAD_LEN);
     } else {
+      span_ok = true;
       slot = ctx + (r - start);  // also the RoPE position
       page = __ldg(p.block_table + (size_t)lo * p.max_pages + (slot >> p.page_shift));
       if (page < 0 || page >= p.num_pages) {
@@ -161,18 +180,54 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
       }
     }
   }
-  __syncthreads();  // the tables
-  // the token's first warp in this CTA forms its angles
+  __shared__ int tok_slot[kPfWarps];  // RoPE position of each warp's token (-1: none)
+  tok_slot[warp] = (span_ok && p.use_rope) ? slot : -1;
+  __syncthreads();  // the tables and the positions
+  // The angles of each token the CTA holds are formed once, into the slot of
+  // the token's first warp (`owner`), by all the CTA's threads together: the
+  // correctly rounded cos/sin of an fp64 angle is costly at this part's fp64
+  // rate, and one warp doing a token's D/2 pairs alone is the CTA's longest
+  // step.
   const int owner = (int)(max((long long)r * p.n_kvh, item0) - item0);
-  if (ok && p.use_rope && owner == warp) {
-#pragma unroll
-    for (int k = 0; k < D / 64; ++k) {
-      float c, sn;
-      store_angle(slot, inv_freq[lane + 32 * k], table, c, sn);
-      cs[warp][lane + 32 * k] = make_float2(c, sn);
-    }
+  for (int e = tid; e < kPfWarps * (D / 2); e += kPfThreads) {
+    const int w = e / (D / 2), i = e - w * (D / 2);
+    const long long it_w = item0 + w;
+    const int own_w = (int)(max((it_w / p.n_kvh) * p.n_kvh, item0) - item0);  // first warp of w's token
+    if (own_w != w || tok_slot[w] < 0) continue;
+    float c, sn;
+    store_angle(tok_slot[w], inv_freq[i], table, c, sn);
+    cs[w][i] = make_float2(c, sn);
   }
   __syncthreads();
+  if (p.tc_tiles && span_ok) {
+    // For the tcgen05 attention kernel the query rows of the KV head's group
+    // are formed here, with the token's angles: rotated in fp32, scaled by
+    // scale * log2(e), rounded to bf16, written to the output rows (which the
+    // attention kernel reads by TMA and then overwrites with its result).
+    // Four heads at a time, all loaded before any is stored.
+#pragma unroll 1
+    for (int h_first = 0; h_first < g; h_first += QB) {
+      if (h_first > 0) fetch_q(h_first);
+#pragma unroll
+      for (int hh = 0; hh < QB; ++hh) {
+        if (h_first + hh >= g) break;
+        __nv_bfloat16 *qd = p.out + ((size_t)r * p.n_qh + j * g + h_first + hh) * D;
+#pragma unroll
+        for (int k = 0; k < D / 64; ++k) {
+          const int i = lane + 32 * k;
+          float lo = __bfloat162float(qv[hh][2 * k]), hi = __bfloat162float(qv[hh][2 * k + 1]);
+          if (p.use_rope) {
+            const float2 a = cs[owner][i];
+            const float x = lo * a.x - hi * a.y, y = hi * a.x + lo * a.y;
+            lo = x;
+            hi = y;
+          }
+          qd[i] = __float2bfloat16_rn(lo * p.qscale);
+          qd[i + D / 2] = __float2bfloat16_rn(hi * p.qscale);
+        }
+      }
+    }
+  }
   if (!ok) return;
   uint8_t *buf = rowbuf[warp];
   if (lane < 2 * CH) reinterpret_cast<uint4 *>(buf)[lane] = chunk;
@@ -1041,7 +1096,7 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   // call without a workspace.
   // Long prompts over a bf16 cache take the tcgen05 kernel (64-token query
   // tiles, one CTA an SM): their splits aim at two CTAs an SM.
-  p.tc_tiles = (!int8 && !short_chunks && max_new_tokens > 64) ? 1 : 0;
+  p.tc_tiles = (!int8 && !short_chunks && max_new_tokens > 64 && pf_aligned(out, 16)) ? 1 : 0;
   {
     int S = 1;
     if (max_new_tokens <= 64) {

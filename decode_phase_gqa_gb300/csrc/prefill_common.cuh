@@ -41,8 +41,10 @@ struct PrefillParams {
   int n_splits;       // CTAs sharing one query tile's key tiles
   float *part;        // n_splits > 1: [n_splits][n_tok][n_qh][D + 2] partial
                       // states (o relative to 2^m, m, l; log2 units)
-  int tc_tiles;       // the attention kernel is the tcgen05 one: 32-token query
-                      // tiles of 64-key tiles (the merge recomputes its splits)
+  int tc_tiles;       // the attention kernel is the tcgen05 one (64-token query
+                      // tiles of 128-key tiles; the merge recomputes its splits);
+                      // the append kernel then writes the rotated, scaled bf16
+                      // query rows into out, where that kernel reads them
   int use_rope;
   float qscale;       // scale * log2(e)
   float2 turns[64];   // rope_theta^(-2i/d) / (2 pi) as fp32 head + remainder

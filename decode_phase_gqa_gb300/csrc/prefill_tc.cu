@@ -12,16 +12,18 @@
 // Eleven warps:
 //   * warps 0-3 (half 0) and 4-7 (half 1), one thread per row, TMEM lanes
 //     32 (w % 4) .. of the half's 256 columns (S and P in 0-127, O in 128-):
-//     rotate and scale the query rows into shared memory; per tile read the
-//     row's 128 scores S from tensor memory, mask them, keep the running
-//     maximum m and normaliser l (log2 units; the maximum moves lazily, by
-//     more than 8, so the accumulator is rarely rescaled), and write
+//     per tile read the row's 128 scores S from tensor memory, mask them,
+//     keep the running maximum m and normaliser l (log2 units; the maximum
+//     moves lazily, by more than 8, so the accumulator is rarely rescaled),
+//     and write
 //     P = 2^(S - m) as bf16 pairs back over S in tensor memory; at the end
 //     read O, divide by l, store bf16 (or the partial state of a split);
-//   * warps 8 and 9: TMA tensor copies of the K and of the V tiles (16-key
-//     page blocks, [16 rows][128 bytes] boxes, 128-byte swizzle) into a K ring
-//     and a V ring of 2 (d 128) or 3 (d 64) slots; a thread issues about one
-//     copy every 115 clocks, so each ring has its own issuer;
+//   * warps 8 and 9: TMA tensor copies of the query rows (which the append
+//     kernel rotated, scaled and left in the output rows) and the K tiles,
+//     and of the V tiles (16-key page blocks, [16 rows][128 bytes] boxes,
+//     128-byte swizzle) into a K ring and a V ring of 2 (d 128) or 3 (d 64)
+//     slots; a thread issues about one copy every 115 clocks, so each ring
+//     has its own issuer;
 //   * warp 10, one thread: issues the MMAs and commits them to mbarriers:
 //     S = Q K^T (M 128, N 128, K d; both operands in shared memory) and
 //     O += P V (M 128, N d, K 128; P from tensor memory, V in shared memory).
@@ -31,7 +33,10 @@
 // P V products of tile i are done); the two halves interleave, so one half's
 // MMAs run while the other's softmax works.  Every wait is bounded
 // (KVATTN_DEV_TIMEOUT).
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
+
+#include <mutex>
 
 #include "prefill_common.cuh"
 
@@ -66,14 +71,16 @@ struct TcCfg {
   // o_done[2], q_ready, mma_done
   static constexpr int kNumBars = 4 * kStages + 8;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;    // tmem base, abort flag, counters
-  static constexpr int kTurnsOff = kMiscOff + 64;            // float2[64]
-  static constexpr int kSmem = kTurnsOff + 512 + 1024;       // + slack for 1024-byte alignment
+  static constexpr int kSmem = kMiscOff + 64 + 1024;         // + slack for 1024-byte alignment
   static_assert(kSmem <= 227 * 1024, "shared memory");
   static_assert(kKOff % 1024 == 0 && kTile % 1024 == 0, "swizzle atoms need 1024-byte alignment");
 };
 
 struct PfTcParams {
   CUtensorMap tmap_k, tmap_v;  // [rows][D] bf16 pools, [16][64] boxes, 128-byte swizzle
+  // [n_tok][n_qh][D] bf16 view of out, where the append kernel left the
+  // rotated, scaled query rows: [32 tokens][1 head][64] boxes, 128-byte swizzle
+  CUtensorMap tmap_q;
   PrefillParams p;
   int n_qt;   // 32-token query tiles per sequence
   int cover;  // new tokens of a sequence the launch covers
@@ -239,6 +246,16 @@ __device__ __forceinline__ void tma_load_2d_keep(void *dst, const CUtensorMap *m
       : "memory");
 }
 
+// 3-D TMA tensor copy with the default L2 policy
+__device__ __forceinline__ void tma_load_3d_keep(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                                 uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // Bounded wait on an mbarrier phase by one thread; on a timeout the CTA's
 // abort flag is set and KVATTN_DEV_TIMEOUT reported.
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -339,7 +356,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
   volatile int *issued_k = reinterpret_cast<volatile int *>(misc + 2);
   volatile int *issued_v = reinterpret_cast<volatile int *>(misc + 3);
-  float2 *turns = reinterpret_cast<float2 *>(smem + C::kTurnsOff);
   uint8_t *qs = smem + C::kQOff;
   uint8_t *kring = smem + C::kKOff, *vring = smem + C::kVOff;
 
@@ -355,14 +371,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       mbar_init(&p_full[i], kTcRows);
       mbar_init(&o_done[i], 1);
     }
-    mbar_init(q_ready, 2 * kTcRows);
+    mbar_init(q_ready, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     *issued_k = 0;
     *issued_v = 0;
     fence_barrier_init();
   }
-  if (tid < 64) turns[tid] = p.turns[tid];
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -375,74 +390,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   if (warp < kTcSoftWarps) {
     // ---- softmax warps: one thread per row ------------------------------------
     const int hf = warp >> 2, wq = warp & 3;
-    const int row = 32 * wq + lane;          // row of the half: head h0 + wq, token t
     const int h = h0 + wq, t = t0 + kTcHalf * hf + lane;
     const bool live = t < n_rows_tok;
-    // The row's query, rotated in fp32 at position ctx + t, scaled by
-    // scale * log2(e), rounded to bf16, into the half's swizzled Q tile.  The
-    // rotation angles depend on the token only: the four threads of a token
-    // (one per head) each form a quarter of its (cos, sin) pairs into a table
-    // in the last V slot (its first copy is issued after q_ready), then read
-    // all of them.
-    {
-      uint4 lo4[D / 16], hi4[D / 16];  // the whole row, loaded at once
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)(start + (live ? t : 0)) * p.n_qh + h) * D);
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        lo4[c] = live ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        hi4[c] = live ? src[c + D / 16] : make_uint4(0u, 0u, 0u, 0u);
-      }
-      float2 *cs_tab = reinterpret_cast<float2 *>(vring + (S - 1) * C::kTile);  // [D / 2][64]
-      static_assert(kTcTok * (D / 2) * 8 <= C::kTile, "the angle table fits a V slot");
-      const int tok = kTcHalf * hf + lane;                   // token within the CTA
-      if (p.use_rope) {
-#pragma unroll 1
-        for (int i = wq; i < D / 2; i += 4) {
-          float sn, cs;
-          sincospif(2.f * frac_turns(ctx + t, turns[i]), &sn, &cs);
-          cs_tab[i * kTcTok + tok] = make_float2(cs, sn);
-        }
-      }
-      named_barrier_sync(1, 32 * kTcSoftWarps);
-      uint8_t *qh = qs + hf * C::kQHalf;
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        const uint32_t lw[4] = {lo4[c].x, lo4[c].y, lo4[c].z, lo4[c].w};
-        const uint32_t hw[4] = {hi4[c].x, hi4[c].y, hi4[c].z, hi4[c].w};
-        uint32_t ol[4], oh[4];
-#pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          float a[2], bb[2];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int i = 8 * c + 2 * e2 + k;
-            float lo = __uint_as_float(k ? (lw[e2] & 0xffff0000u) : (lw[e2] << 16));
-            float hi = __uint_as_float(k ? (hw[e2] & 0xffff0000u) : (hw[e2] << 16));
-            if (p.use_rope) {
-              const float2 r = cs_tab[i * kTcTok + tok];
-              const float x = lo * r.x - hi * r.y, y = hi * r.x + lo * r.y;
-              lo = x;
-              hi = y;
-            }
-            a[k] = lo * p.qscale;
-            bb[k] = hi * p.qscale;
-          }
-          ol[e2] = pack_bf16(a[0], a[1]);
-          oh[e2] = pack_bf16(bb[0], bb[1]);
-        }
-        const int il = 8 * c, ih = 8 * c + D / 2;  // first element of each chunk
-        uint8_t *dl = qh + (il / 64) * C::kQRegion + row * 128 + ((((il % 64) / 8) ^ (row & 7)) << 4);
-        uint8_t *dh = qh + (ih / 64) * C::kQRegion + row * 128 + ((((ih % 64) / 8) ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4 *>(dl) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-        *reinterpret_cast<uint4 *>(dh) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-      }
-    }
-    // every read of the table is done (the producer waits for q_ready before
-    // its first copy lands there) and Q is visible to the MMAs' async proxy
-    fence_proxy_async_smem();
-    mbar_arrive(q_ready);
-    pdl_wait_primary();
-
     const uint32_t lane_base = tmem + ((uint32_t)(32 * wq) << 16) + kHalfCols * (uint32_t)hf;
     const int kmax = live ? ctx + t : -1;  // last key the row sees
     const float kFloor = -1e30f;
@@ -575,8 +524,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     // scores of tile i are done, V(i) once their P V products are, so the
     // next keys start loading well before the weighted sums end
     const bool is_v = warp == kTcSoftWarps + 1;
-    pdl_wait_primary();  // the appended rows are complete and visible
+    pdl_wait_primary();  // the appended rows and the query rows are complete and visible
     prefetch_tensormap(is_v ? &tp.tmap_v : &tp.tmap_k);
+    if (!is_v && lane == 0) {
+      // both halves' query rows: a [32 tokens][64] box per head and 64-column
+      // block, rows 32 hh + tl of the half's tile (tokens past the new rows are
+      // another sequence's or, past n_tok, zeros: never stored)
+      mbar_arrive_expect_tx(q_ready, 2 * C::kQHalf);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_3d_keep(qs + hf * C::kQHalf + r * C::kQRegion + hh * (kTcHalf * 128), &tp.tmap_q, 64 * r,
+                             h0 + hh, start + t0 + kTcHalf * hf, q_ready);
+    }
     uint64_t *ring_full = is_v ? v_full : k_full, *ring_empty = is_v ? v_empty : k_empty;
     uint8_t *ring = is_v ? vring : kring;
     volatile int *issued = is_v ? issued_v : issued_k;
@@ -606,9 +569,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       int rows[kTcKeys / 16];
 #pragma unroll
       for (int q8 = 0; q8 < kTcKeys / 16; ++q8) rows[q8] = __shfl_sync(0xffffffffu, prow, q8);
-      // the last V slot holds the query rows' angle table until every Q row
-      // is written
-      if (is_v && i == S - 1 && !wait_slot(q_ready, 0)) break;
       if (i >= S && !wait_slot(&ring_empty[s], (uint32_t)(((i / S) - 1) & 1))) break;
       if (lane == 0) {
         uint8_t *dst = ring + s * C::kTile;
@@ -723,6 +683,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// 3-D view [n_tok][n_qh][head_dim] of the bf16 rows at `base` in [32 tokens]
+// [1 head][64 columns] boxes with 128-byte swizzle
+bool query_tensor_map(CUtensorMap *map, const void *base, int n_tok, int n_qh, int head_dim) {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_qh, (cuuint64_t)n_tok};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_qh * head_dim * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kTcHalf};
+  cuuint32_t estride[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_tc_t(const PfTcParams &tp, cudaStream_t stream) {
   using C = TcCfg<D>;
@@ -754,7 +737,8 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, int head_dim, int cover, c
   tp.n_qt = (cover + kTcTok - 1) / kTcTok;
   const long long rows = (long long)p.num_pages * p.n_kvh * p.page_size;
   if (!pool_tensor_map(&tp.tmap_k, p.k_pages, rows, head_dim, false) ||
-      !pool_tensor_map(&tp.tmap_v, p.v_pages, rows, head_dim, false))
+      !pool_tensor_map(&tp.tmap_v, p.v_pages, rows, head_dim, false) ||
+      !query_tensor_map(&tp.tmap_q, p.out, p.n_tok, p.n_qh, head_dim))
     return cudaErrorInvalidValue;
   return head_dim == 64 ? launch_tc_t<64>(tp, stream) : launch_tc_t<128>(tp, stream);
 }
