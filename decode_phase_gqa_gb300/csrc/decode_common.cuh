@@ -41,6 +41,17 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// Two int8 codes of `u` (bytes selected by `sel`, a prmt selector whose other
+// nibbles pick 0x64) as an f16 pair.  The codes arrive with their sign bit
+// flipped (x + 128, an unsigned byte b); 0x6400 | b is the f16 1024 + b, and
+// subtracting 1152 leaves x exactly (the magic-number integer conversion).
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u_flipped, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(u_flipped), "r"(0x64646464u), "r"(sel));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64806480u));
+  return r;
+}
+
 // a[i] for a lane-dependent i without dynamic register indexing
 template <int N>
 __device__ __forceinline__ float pick(const float (&a)[N], int i) {

@@ -36,11 +36,13 @@
 //   * score_t = (q . codes_t) * ks_t: the query columns are f16 head and
 //     remainder of q * 2^kq, kq a power-of-two range scale per stream, and the
 //     raw dot product is multiplied by ks_t * 2^-kq;
-//   * the value weights p_t vs_t are formed as 2^(s_t + log2 vs_t - mo) with
-//     their own running maximum mo, so the largest weight of the stream so far
-//     is 1 (no f16 overflow or underflow whatever the scales); the normaliser
-//     l keeps the plain softmax maximum m, and the accumulator is brought
-//     from 2^mo to 2^m when the stream's part ends.
+//   * the value weights p_t vs_t are formed as 2^(s_t - m + log2 vs_t - dmo)
+//     with their own running maximum m + dmo, so the largest weight of the
+//     stream so far is 1 (no f16 overflow or underflow whatever the scales);
+//     dmo is kept relative to m so that log2 vs_t is added to a number near
+//     zero (added to a score of 5e5 fp32 would keep it to 1/32 only); the
+//     normaliser l keeps the plain softmax maximum m, and the accumulator is
+//     brought from 2^(m + dmo) to 2^m when the stream's part ends.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -131,17 +133,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 __device__ __forceinline__ float f16_round(float x) { return __half2float(__float2half_rn(x)); }
 __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
-}
-
-// Two int8 codes of `u` (bytes selected by `sel`, a prmt selector whose other
-// nibbles pick 0x64) as an f16 pair.  The codes arrive with their sign bit
-// flipped (x + 128, an unsigned byte b); 0x6400 | b is the f16 1024 + b, and
-// subtracting 1152 leaves x exactly (the magic-number integer conversion).
-__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u_flipped, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(u_flipped), "r"(0x64646464u), "r"(sel));
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64806480u));
-  return r;
 }
 
 // Two int8 codes of `u` as the f16 pair 1152 + x (the conversion above without
@@ -604,12 +595,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     for (int dt = 0; dt < C::kKSteps; ++dt)
 #pragma unroll
       for (int k = 0; k < 4; ++k) o[dt][k] = 0.f;
-    // m, l: reference maximum and normaliser of the softmax of head hl; mo:
-    // reference maximum of its value weights (int8; the bf16 cache weighs the
-    // values by the softmax weights themselves).  The references start at a
-    // finite floor below every score, so no step needs a guard for an empty
-    // state.
-    float m = kFloor, l = 0.f, mo = kFloor;
+    // m, l: reference maximum and normaliser of the softmax of head hl; dmo:
+    // reference maximum of its value weights, less m (int8; the bf16 cache
+    // weighs the values by the softmax weights themselves).  The references
+    // start at a finite floor below every score, so no step needs a guard for
+    // an empty state.
+    float m = kFloor, l = 0.f, dmo = kFloor;
 
     for (int tt = t; tt < e; ++tt) {
       if (own_last && tt == tab_at && !helped) {
@@ -698,17 +689,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
         // full scores of head hl at tokens tokr, tokr + 8: head column plus
         // remainder column
         float sc[2] = {s[0] + s[1], s[2] + s[3]};
-        // value-weight exponents (int8): score + log2 vs
-        float xv[2];
-#pragma unroll
-        for (int t2 = 0; t2 < 2; ++t2) {
-          if constexpr (INT8) sc[t2] *= ksr[t2];
-          xv[t2] = sc[t2] + lv[t2];
+        if constexpr (INT8) {
+          sc[0] *= ksr[0];
+          sc[1] *= ksr[1];
         }
         if (nrows < kUnitRows) {  // a sequence's last unit: drop the rows past its end
 #pragma unroll
           for (int t2 = 0; t2 < 2; ++t2)
-            if (tokr + 8 * t2 >= nrows) sc[t2] = xv[t2] = kNegInf;
+            if (tokr + 8 * t2 >= nrows) sc[t2] = lv[t2] = kNegInf;  // (stale scales too)
         }
 
         // online softmax (log2 units) with lazy references: a reference moves
@@ -724,22 +712,26 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
           float a = 1.f;
           if (mx > m + kLazy) {
             a = ex2_approx(m - mx);
+            if constexpr (INT8) dmo -= mx - m;  // the same absolute reference
             m = mx;
           }
           const float pw0 = ex2_approx(sc[0] - m), pw1 = ex2_approx(sc[1] - m);
           l = l * a + pw0 + pw1;
           if constexpr (INT8) {
-            float xo = fmaxf(xv[0], xv[1]);
+            // value-weight exponents S - m + log2 vs: log2 vs is added to a
+            // number near zero, so fp32 keeps it whatever the scores' size
+            const float xv0 = (sc[0] - m) + lv[0], xv1 = (sc[1] - m) + lv[1];
+            float xo = fmaxf(xv0, xv1);
             xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 4));
             xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 8));
             xo = fmaxf(xo, __shfl_xor_sync(0xffffffffu, xo, 16));
             a = 1.f;
-            if (xo > mo + kLazy) {
-              a = ex2_approx(mo - xo);
-              mo = xo;
+            if (xo > dmo + kLazy) {
+              a = ex2_approx(dmo - xo);
+              dmo = xo;
             }
-            pv[0] = ex2_approx(xv[0] - mo);
-            pv[1] = ex2_approx(xv[1] - mo);
+            pv[0] = ex2_approx(xv0 - dmo);
+            pv[1] = ex2_approx(xv1 - dmo);
           } else {
             pv[0] = pw0;
             pv[1] = pw1;
@@ -804,8 +796,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     l += __shfl_xor_sync(0xffffffffu, l, 4);
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
-    // accumulator scale to 2^m (int8: from 2^mo)
-    const float to_m = INT8 ? ex2_approx(mo - m) : 1.f;
+    // accumulator scale to 2^m (int8: from 2^(m + dmo))
+    const float to_m = INT8 ? ex2_approx(dmo) : 1.f;
     // lanes with hl < GS hold head hl's output rows d = dA(dt) (of[dt][0])
     // and d = dB(dt) (of[dt][1])
     const bool writer = hl < GS;

@@ -447,6 +447,7 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[nd][k] = 0.f;
   float m[2] = {kFloor, kFloor}, l[2] = {0.f, 0.f};
+  float dmo[2] = {kFloor, kFloor};  // int8: the value weights' running maximum, less m
   // absolute positions of this lane's rows g and g + 8
   const int qpos[2] = {ctx + t0 + (lane >> 2), ctx + t0 + (lane >> 2) + 8};
 
@@ -466,14 +467,14 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
     const uint8_t *Ks = stages + (it & 1) * C::kStage, *Vs = Ks + C::kTile;
     const int *rv = rvalid + (it & 1) * kPfKeys;
     if constexpr (INT8) {
-      // the stage's codes times their row scales -> f16 tiles (rows not to be
-      // read: zero, whatever their scale slot holds)
+      // the stage's codes -> exact f16 tiles (rows not to be read: zero); the
+      // row scales enter the scores and the value weights below, so no f16
+      // product of a code and a scale can overflow or lose range
       const int8_t *raw = reinterpret_cast<const int8_t *>(raws + (it & 1) * C::kRaw);
-      const float *scl = reinterpret_cast<const float *>(raws + (it & 1) * C::kRaw + 2 * kPfKeys * D);
       for (int idx = tid; idx < 2 * kPfKeys * CH; idx += kPfThreads) {
         const int v = idx / (kPfKeys * CH), rest = idx - v * kPfKeys * CH;
         const int r = rest / CH, c = rest % CH;
-        const float sc = rv[r] ? scl[v * kPfKeys + r] : 0.f;
+        const float sc = rv[r] ? 1.f : 0.f;
         const uint2 w = *reinterpret_cast<const uint2 *>(raw + v * kPfKeys * D + r * D + c * 8);
         const int8_t *e = reinterpret_cast<const int8_t *>(&w);
         uint4 o4;
@@ -507,25 +508,58 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
     }
     // causal and page masks, running maxima of rows g and g + 8
     const int key0 = kt * kPfKeys;
+    // int8: the raw dot products times the key rows' scales; the value weights
+    // are 2^(S - m + log2 vs - dmo) with their own running maximum m + dmo, so
+    // P vs fits f16 whatever the scales, and log2 vs is added to a number near
+    // zero, which fp32 keeps whatever the scores' size (the decode kernel's
+    // scheme)
+    const float *scl = INT8 ? reinterpret_cast<const float *>(raws + (it & 1) * C::kRaw + 2 * kPfKeys * D)
+                            : nullptr;
     float mx[2] = {-INFINITY, -INFINITY};
+    float xv[kPfNT][4];  // int8: log2 vs, then the value-weight exponents
 #pragma unroll
     for (int nt = 0; nt < kPfNT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
         const bool ok = key0 + kr <= qpos[e >> 1] && rv[kr] != 0;
-        s[nt][e] = ok ? s[nt][e] : -INFINITY;
+        if constexpr (INT8) {
+          s[nt][e] = ok ? s[nt][e] * scl[kr] : -INFINITY;
+          xv[nt][e] = ok ? lg2_approx(scl[kPfKeys + kr]) : -INFINITY;
+        } else {
+          s[nt][e] = ok ? s[nt][e] : -INFINITY;
+        }
         mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
       }
-    float alpha[2];
+    float alpha[2], alpha_o[2];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
       mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
       const float mn = fmaxf(m[rr], mx[rr]);
       alpha[rr] = ex2_approx(m[rr] - mn);
+      if constexpr (INT8) dmo[rr] -= mn - m[rr];  // the same absolute reference
       m[rr] = mn;
       l[rr] *= alpha[rr];
+      alpha_o[rr] = alpha[rr];
+    }
+    if constexpr (INT8) {
+      float mxo[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < kPfNT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xv[nt][e] += s[nt][e] - m[e >> 1];
+          mxo[e >> 1] = fmaxf(mxo[e >> 1], xv[nt][e]);
+        }
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        mxo[rr] = fmaxf(mxo[rr], __shfl_xor_sync(0xffffffffu, mxo[rr], 1));
+        mxo[rr] = fmaxf(mxo[rr], __shfl_xor_sync(0xffffffffu, mxo[rr], 2));
+        const float don = fmaxf(dmo[rr], mxo[rr]);
+        alpha_o[rr] = ex2_approx(dmo[rr] - don);
+        dmo[rr] = don;
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < kPfNT; ++nt)
@@ -533,13 +567,14 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
       for (int e = 0; e < 4; ++e) {
         s[nt][e] = ex2_approx(s[nt][e] - m[e >> 1]);
         l[e >> 1] += s[nt][e];
+        if constexpr (INT8) s[nt][e] = ex2_approx(xv[nt][e] - dmo[e >> 1]);  // the value weight
       }
 #pragma unroll
     for (int nd = 0; nd < ND; ++nd) {
-      o[nd][0] *= alpha[0];
-      o[nd][1] *= alpha[0];
-      o[nd][2] *= alpha[1];
-      o[nd][3] *= alpha[1];
+      o[nd][0] *= alpha_o[0];
+      o[nd][1] *= alpha_o[0];
+      o[nd][2] *= alpha_o[1];
+      o[nd][3] *= alpha_o[1];
     }
     // O += P V: P's accumulator layout is the next MMA's A layout, keys
     // 16 kk .. 16 kk + 15 from n-tiles 2 kk, 2 kk + 1
@@ -567,6 +602,14 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
   for (int rr = 0; rr < 2; ++rr) {
     l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
     l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
+    if constexpr (INT8) {  // o is relative to 2^(m + dmo): bring it to 2^m
+      const float f = ex2_approx(dmo[rr]);
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        o[nd][2 * rr] *= f;
+        o[nd][2 * rr + 1] *= f;
+      }
+    }
   }
   if (p.n_splits > 1) {  // a partial state per row, merged by prefill_merge_kernel
 #pragma unroll
@@ -609,14 +652,27 @@ struct PsCfg {
   static constexpr int kRowB = 2 * D;
   static constexpr int kQBytes = 16 * kRowB;
   static constexpr int kPart = kPsWarpKeys * kRowB;  // a warp's K (or V) rows of a stage (16-bit)
-  // int8 cache: a stage is the codes (K, V) and row scales (K, V) as copied,
-  // dequantised into one f16 K/V tile pair after the ring
+  // int8 cache: a stage is the codes (K, V; 16-byte chunks of a row permuted
+  // as cidx8 gives) and the row scales (K, V) as copied; the codes become f16
+  // in registers
   static constexpr int kRaw = 2 * kPsWarpKeys * D + 2 * kPsWarpKeys * 4;
-  static constexpr int kRing = INT8 ? kPsStages * kRaw + 2 * kPart : kPsStages * 2 * kPart;  // a warp's
+  // stages of a warp's ring: the int8 slices are half the bytes, so twice as
+  // many fit the same shared memory (3 CTAs an SM either way)
+  static constexpr int kStages = INT8 ? 2 * kPsStages : kPsStages;
+  static constexpr int kRing = INT8 ? kStages * kRaw : kStages * 2 * kPart;  // a warp's
   static constexpr int kSmem = kQBytes + kPfWarps * kRing + 64 * 8;
   // the end-of-kernel merge borrows the rings: [4 warps][16 rows][D] + (m, l)
   static_assert(kPfWarps * 16 * (D + 2) * 4 <= kPfWarps * kRing, "merge buffer");
 };
+
+// Position of 16-byte chunk c of code row r in a staged int8 slice [16][D]:
+// XOR-permuted so that the 8 rows an ldmatrix reads at one chunk fall in 8
+// different bank groups (rows of 128 bytes: with r mod 8; of 64 bytes, two to
+// 128 bytes: with (r / 2) mod 4)
+template <int D>
+__device__ __forceinline__ int cidx8(int r, int c) {
+  return D == 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+}
 
 template <int N>
 __device__ __forceinline__ void cp_async_wait_n() {
@@ -693,8 +749,9 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         const int r = idx / CC, c = idx % CC;
         const bool ok = base >= 0 && key + r < n_keys;
         const size_t off = ok ? (size_t)(base + r) * D + c * 16 : 0;
-        cp_async_16_zfill(Kd + r * D + c * 16, static_cast<const uint8_t *>(p.k_pages) + off, ok ? 16 : 0);
-        cp_async_16_zfill(Vd + r * D + c * 16, static_cast<const uint8_t *>(p.v_pages) + off, ok ? 16 : 0);
+        const int dc = r * D + cidx8<D>(r, c) * 16;
+        cp_async_16_zfill(Kd + dc, static_cast<const uint8_t *>(p.k_pages) + off, ok ? 16 : 0);
+        cp_async_16_zfill(Vd + dc, static_cast<const uint8_t *>(p.v_pages) + off, ok ? 16 : 0);
       }
       if (lane < 8) {
         const float *src = lane < 4 ? p.k_scales : p.v_scales;
@@ -715,7 +772,7 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   };
   // the first stages go out before the queries are formed
 #pragma unroll
-  for (int i = 0; i < kPsStages - 1; ++i) {
+  for (int i = 0; i < C::kStages - 1; ++i) {
     if (kt_begin + i < kt_end) load_part(kt_begin + i, i);
     cp_async_commit();
   }
@@ -743,9 +800,26 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   }
   __syncthreads();
   uint32_t qf[KS][4];
+  if constexpr (INT8) {
+    // the k order of the key codes' fragments (below): MMA columns 2t, 2t + 1
+    // of k-step ks are dimensions 16 ks + 4t, + 1, columns 2t + 8, 2t + 9 are
+    // 16 ks + 4t + 2, + 3 (t = lane % 4): one 8-byte load per row
+    const int t4 = lane & 3, g8 = lane >> 2;
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks)
-    ldmatrix_x4(qf[ks], smem_addr(qs) + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)));
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint32_t off = (uint32_t)((t4 & 1) * 8);
+      const uint2 r0 = *reinterpret_cast<const uint2 *>(qs + sw<D>(g8, 2 * ks + (t4 >> 1)) + off);
+      const uint2 r1 = *reinterpret_cast<const uint2 *>(qs + sw<D>(g8 + 8, 2 * ks + (t4 >> 1)) + off);
+      qf[ks][0] = r0.x;
+      qf[ks][1] = r1.x;
+      qf[ks][2] = r0.y;
+      qf[ks][3] = r1.y;
+    }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+      ldmatrix_x4(qf[ks], smem_addr(qs) + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)));
+  }
 
   float o[ND][4];
 #pragma unroll
@@ -753,98 +827,172 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[nd][k] = 0.f;
   float m[2] = {kFloor, kFloor}, l[2] = {0.f, 0.f};
+  // int8: the running maximum of the value weights' exponents (score + log2
+  // of the value row's scale), less m, so the f16 weights never overflow
+  float dmo[2] = {kFloor, kFloor};
   // this lane's rows g and g + 8: tokens g / 4 and 2 + g / 4
   const int qpos[2] = {ctx + (lane >> 4), ctx + 2 + (lane >> 4)};
 
   for (int it = 0, kt = kt_begin; kt < kt_end; ++it, ++kt) {
-    if (kt + kPsStages - 1 < kt_end) load_part(kt + kPsStages - 1, (it + kPsStages - 1) % kPsStages);
+    if (kt + C::kStages - 1 < kt_end) load_part(kt + C::kStages - 1, (it + C::kStages - 1) % C::kStages);
     cp_async_commit();
-    cp_async_wait_n<kPsStages - 1>();
+    cp_async_wait_n<C::kStages - 1>();
     __syncwarp();  // the other lanes' copies of this stage
-    const int st = it % kPsStages;
+    const int st = it % C::kStages;
     uint32_t kb = smem_addr(ring + st * 2 * C::kPart), vb = kb + C::kPart;
     const bool pg_ok = !((bad >> st) & 1u);
     if constexpr (INT8) {
-      // the slice's codes times their row scales -> the warp's f16 tiles (rows
-      // past the keys: zero, whatever their scale slot holds)
-      const int8_t *raw = reinterpret_cast<const int8_t *>(ring + st * C::kRaw);
+      // Scores from the codes: S = (Q codes^T) * the key row's scale; value
+      // weights 2^(S - m + log2 vs - dmo) with their own running maximum
+      // m + dmo, so that P vs fits f16 whatever the scales and log2 vs is added
+      // to a number near zero (the decode kernel's scheme); the codes become
+      // exact f16 in registers, no dequantised tile.
+      const uint8_t *raw = ring + st * C::kRaw;
+      const uint32_t kc = smem_addr(raw), vc = kc + kPsWarpKeys * D;
       const float *scl = reinterpret_cast<const float *>(raw + 2 * kPsWarpKeys * D);
-      uint8_t *tile = ring + kPsStages * C::kRaw;
+      float s[2][4] = {};
+#pragma unroll
+      for (int c = 0; c < D / 16; c += 2) {
+        // matrices (keys 0-7, chunk c), (keys 0-7, c + 1), (keys 8-15, c),
+        // (keys 8-15, c + 1); lane (g, t) holds codes 4t .. 4t + 3 of its key's
+        // chunk: k-step c takes bytes 0, 1 as b0 and 2, 3 as b1
+        const int kr = (lane & 7) + ((lane >> 4) << 3), ch = c + ((lane >> 3) & 1);
+        uint32_t r[4];
+        ldmatrix_x4(r, kc + (uint32_t)(kr * D + cidx8<D>(kr, ch) * 16));
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t u0 = r[h2] ^ 0x80808080u, u1 = r[2 + h2] ^ 0x80808080u;
+          mma16<true>(s[0], qf[c + h2], codes_to_f16x2(u0, 0x5140u), codes_to_f16x2(u0, 0x5342u));
+          mma16<true>(s[1], qf[c + h2], codes_to_f16x2(u1, 0x5140u), codes_to_f16x2(u1, 0x5342u));
+        }
+      }
       const int key0 = kt * kPsKeys + wk;
-#pragma unroll 4
-      for (int idx = lane; idx < 2 * kPsWarpKeys * (D / 8); idx += 32) {
-        const int v = idx / (kPsWarpKeys * (D / 8)), rest = idx - v * kPsWarpKeys * (D / 8);
-        const int r = rest / (D / 8), c = rest % (D / 8);
-        const float sc = key0 + r < n_keys ? scl[v * kPsWarpKeys + r] : 0.f;
-        const uint2 w = *reinterpret_cast<const uint2 *>(raw + v * kPsWarpKeys * D + r * D + c * 8);
-        const int8_t *e = reinterpret_cast<const int8_t *>(&w);
-        uint4 o4;
-        o4.x = pack16<true>(e[0] * sc, e[1] * sc);
-        o4.y = pack16<true>(e[2] * sc, e[3] * sc);
-        o4.z = pack16<true>(e[4] * sc, e[5] * sc);
-        o4.w = pack16<true>(e[6] * sc, e[7] * sc);
-        *reinterpret_cast<uint4 *>(tile + v * C::kPart + sw<D>(r, c)) = o4;
+      float mx[2] = {-INFINITY, -INFINITY}, mxo[2] = {-INFINITY, -INFINITY};
+      float xv[2][4];  // log2 vs, then the value-weight exponents
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
+          const bool ok = key0 + kr <= qpos[e >> 1] && pg_ok;  // (keys past n_keys: past qpos)
+          s[nt][e] = ok ? s[nt][e] * scl[kr] : -INFINITY;
+          xv[nt][e] = ok ? lg2_approx(scl[kPsWarpKeys + kr]) : -INFINITY;
+          mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+        }
+      float alpha[2], alpha_o[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+        const float mn = fmaxf(m[rr], mx[rr]);
+        alpha[rr] = ex2_approx(m[rr] - mn);
+        dmo[rr] -= mn - m[rr];  // the same absolute reference
+        m[rr] = mn;
+        l[rr] *= alpha[rr];
       }
-      __syncwarp();
-      kb = smem_addr(tile);
-      vb = kb + C::kPart;
-    }
-
-    float s[2][4] = {};
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t kf[4];
-      const int mi = lane >> 3;
-      ldmatrix_x4(kf, kb + sw<D>((mi >> 1) * 8 + (lane & 7), 2 * ks + (mi & 1)));
-      mma16<INT8>(s[0], qf[ks], kf[0], kf[1]);
-      mma16<INT8>(s[1], qf[ks], kf[2], kf[3]);
-    }
-    const int key0 = kt * kPsKeys + wk;
-    float mx[2] = {-INFINITY, -INFINITY};
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+        for (int e = 0; e < 4; ++e) {
+          xv[nt][e] += s[nt][e] - m[e >> 1];
+          mxo[e >> 1] = fmaxf(mxo[e >> 1], xv[nt][e]);
+        }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
-        const bool ok = key0 + kr <= qpos[e >> 1] && pg_ok;  // (keys past n_keys: past qpos)
-        s[nt][e] = ok ? s[nt][e] : -INFINITY;
-        mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+      for (int rr = 0; rr < 2; ++rr) {
+        mxo[rr] = fmaxf(mxo[rr], __shfl_xor_sync(0xffffffffu, mxo[rr], 1));
+        mxo[rr] = fmaxf(mxo[rr], __shfl_xor_sync(0xffffffffu, mxo[rr], 2));
+        const float don = fmaxf(dmo[rr], mxo[rr]);
+        alpha_o[rr] = ex2_approx(dmo[rr] - don);
+        dmo[rr] = don;
       }
-    float alpha[2];
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-      const float mn = fmaxf(m[rr], mx[rr]);
-      alpha[rr] = ex2_approx(m[rr] - mn);
-      m[rr] = mn;
-      l[rr] *= alpha[rr];
-    }
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+        for (int e = 0; e < 4; ++e) {
+          l[e >> 1] += ex2_approx(s[nt][e] - m[e >> 1]);
+          xv[nt][e] = ex2_approx(xv[nt][e] - dmo[e >> 1]);
+        }
+      const uint32_t a[4] = {pack16<true>(xv[0][0], xv[0][1]), pack16<true>(xv[0][2], xv[0][3]),
+                             pack16<true>(xv[1][0], xv[1][1]), pack16<true>(xv[1][2], xv[1][3])};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s[nt][e] = ex2_approx(s[nt][e] - m[e >> 1]);
-        l[e >> 1] += s[nt][e];
+      for (int c = 0; c < D / 16; c += 2) {
+        // matrices (keys 0-7, chunk c), (keys 8-15, c), (keys 0-7, c + 1),
+        // (keys 8-15, c + 1), transposed: lane (g, t) holds keys 2t, 2t + 1 at
+        // dimensions 2g, 2g + 1 of the chunk; n-tile 2 c' takes the even
+        // dimension (bytes 0, 2), 2 c' + 1 the odd one (bytes 1, 3)
+        const int vr = (lane & 7) + ((lane >> 3) & 1) * 8, ch = c + (lane >> 4);
+        uint32_t r[4];
+        ldmatrix_x4_trans(r, vc + (uint32_t)(vr * D + cidx8<D>(vr, ch) * 16));
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int cc = c + h2;
+          const uint32_t u0 = r[2 * h2] ^ 0x80808080u, u1 = r[2 * h2 + 1] ^ 0x80808080u;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            o[2 * cc][k] *= alpha_o[k >> 1];
+            o[2 * cc + 1][k] *= alpha_o[k >> 1];
+          }
+          mma16<true>(o[2 * cc], a, codes_to_f16x2(u0, 0x5240u), codes_to_f16x2(u1, 0x5240u));
+          mma16<true>(o[2 * cc + 1], a, codes_to_f16x2(u0, 0x5341u), codes_to_f16x2(u1, 0x5341u));
+        }
       }
-    const uint32_t a[4] = {pack16<INT8>(s[0][0], s[0][1]), pack16<INT8>(s[0][2], s[0][3]),
-                           pack16<INT8>(s[1][0], s[1][1]), pack16<INT8>(s[1][2], s[1][3])};
-#pragma unroll
-    for (int nd = 0; nd < ND; nd += 2) {
-      o[nd][0] *= alpha[0];
-      o[nd][1] *= alpha[0];
-      o[nd][2] *= alpha[1];
-      o[nd][3] *= alpha[1];
-      o[nd + 1][0] *= alpha[0];
-      o[nd + 1][1] *= alpha[0];
-      o[nd + 1][2] *= alpha[1];
-      o[nd + 1][3] *= alpha[1];
-      uint32_t vf[4];
-      ldmatrix_x4_trans(vf, vb + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, nd + (lane >> 4)));
-      mma16<INT8>(o[nd], a, vf[0], vf[1]);
-      mma16<INT8>(o[nd + 1], a, vf[2], vf[3]);
+    } else {
+      float s[2][4] = {};
+  #pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t kf[4];
+        const int mi = lane >> 3;
+        ldmatrix_x4(kf, kb + sw<D>((mi >> 1) * 8 + (lane & 7), 2 * ks + (mi & 1)));
+        mma16<INT8>(s[0], qf[ks], kf[0], kf[1]);
+        mma16<INT8>(s[1], qf[ks], kf[2], kf[3]);
+      }
+      const int key0 = kt * kPsKeys + wk;
+      float mx[2] = {-INFINITY, -INFINITY};
+  #pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
+          const bool ok = key0 + kr <= qpos[e >> 1] && pg_ok;  // (keys past n_keys: past qpos)
+          s[nt][e] = ok ? s[nt][e] : -INFINITY;
+          mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+        }
+      float alpha[2];
+  #pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+        const float mn = fmaxf(m[rr], mx[rr]);
+        alpha[rr] = ex2_approx(m[rr] - mn);
+        m[rr] = mn;
+        l[rr] *= alpha[rr];
+      }
+  #pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s[nt][e] = ex2_approx(s[nt][e] - m[e >> 1]);
+          l[e >> 1] += s[nt][e];
+        }
+      const uint32_t a[4] = {pack16<INT8>(s[0][0], s[0][1]), pack16<INT8>(s[0][2], s[0][3]),
+                             pack16<INT8>(s[1][0], s[1][1]), pack16<INT8>(s[1][2], s[1][3])};
+  #pragma unroll
+      for (int nd = 0; nd < ND; nd += 2) {
+        o[nd][0] *= alpha[0];
+        o[nd][1] *= alpha[0];
+        o[nd][2] *= alpha[1];
+        o[nd][3] *= alpha[1];
+        o[nd + 1][0] *= alpha[0];
+        o[nd + 1][1] *= alpha[0];
+        o[nd + 1][2] *= alpha[1];
+        o[nd + 1][3] *= alpha[1];
+        uint32_t vf[4];
+        ldmatrix_x4_trans(vf, vb + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, nd + (lane >> 4)));
+        mma16<INT8>(o[nd], a, vf[0], vf[1]);
+        mma16<INT8>(o[nd + 1], a, vf[2], vf[3]);
+      }
     }
-    __syncwarp();  // the stage is rewritten kPsStages stages on
+    __syncwarp();  // the stage is rewritten C::kStages stages on
   }
   cp_async_wait_all();
   if (!appended) pdl_wait_primary();
@@ -862,10 +1010,22 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int r = (lane >> 2) + 8 * rr;
-    float *dst = ob + (warp * 16 + r) * D + 2 * (lane & 3);
+    if constexpr (INT8) {
+      // o is relative to 2^(m + dmo): bring it to 2^m; n-tiles 2 c and 2 c + 1
+      // hold the even and odd dimensions of chunk c, this lane's 16 c + 4t .. + 3
+      const float f = ex2_approx(dmo[rr]);
+      float *dst = ob + (warp * 16 + r) * D + 4 * (lane & 3);
 #pragma unroll
-    for (int nd = 0; nd < ND; ++nd)
-      *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][2 * rr], o[nd][2 * rr + 1]);
+      for (int c = 0; c < D / 16; ++c)
+        *reinterpret_cast<float4 *>(dst + 16 * c) =
+            make_float4(o[2 * c][2 * rr] * f, o[2 * c + 1][2 * rr] * f, o[2 * c][2 * rr + 1] * f,
+                        o[2 * c + 1][2 * rr + 1] * f);
+    } else {
+      float *dst = ob + (warp * 16 + r) * D + 2 * (lane & 3);
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd)
+        *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][2 * rr], o[nd][2 * rr + 1]);
+    }
     if ((lane & 3) == 0) ml[warp * 16 + r] = make_float2(m[rr], l[rr]);
   }
   __syncthreads();

@@ -124,6 +124,48 @@ def test_new_token_dominates_when_aligned():
     assert np.max(np.abs(out_f64(out)[0, 0] - R.bf16_bits_to_f64(h["v_new"][0, 0]))) < 1e-2
 
 
+@pytest.mark.parametrize("num_splits", [0, 7])
+@pytest.mark.parametrize("factor", [1e-7, 1e5])
+def test_int8_value_scales_far_from_one(factor, num_splits):
+    """Every value row, cached and the new token's, times 1e-7 (dequantised
+    values below f16's smallest subnormal) or 1e5 (past f16's largest finite
+    value): the outputs move with them.  Compared with the oracle relative to
+    each output row's size, whole streams and streams cut into parts."""
+    wl, h = custom(8, 2, [0, 15, 300, 2000], d=128, kv="int8", seed=71)
+    h["v_scales"] = h["v_scales"] * np.float32(factor)
+    h["v_new"] = R.f32_to_bf16_bits(R.bf16_bits_to_f64(h["v_new"]) * factor)
+    out, st, _ = run_gpu(wl, to_dev(h), num_splits=num_splits)
+    ref, ost, *_ = oracle_decode(wl, h)
+    assert st == ost == 0
+    got = out_f64(out)
+    assert np.all(np.isfinite(got))
+    size = np.abs(ref).max(axis=-1, keepdims=True)
+    assert size.min() > 0
+    assert np.all(np.abs(got - ref) <= 2e-2 * size)
+
+
+@pytest.mark.parametrize("num_splits", [0, 7])
+def test_int8_key_scales_far_from_one(num_splits):
+    """Cached key rows with 1e-7 times their scales (scores near zero), and one
+    row per sequence with 3e4 times its scale (dequantised values past f16's
+    range, scores near 3e5) that the query is aligned with (NoPE): that row
+    takes the whole softmax."""
+    wl, h = custom(8, 2, [40, 300, 2000], d=128, kv="int8", seed=73, theta=0.0)
+    P = wl.page_size
+    ks = h["k_scales"]
+    for b, L in enumerate(wl.seq_lens):
+        big = int(L) // 3
+        for t in range(0, int(L), 5):
+            if t != big:
+                ks[wl.block_table[b, t // P], :, t % P] *= np.float32(1e-7)
+        pg, off = wl.block_table[b, big // P], big % P
+        for hq in range(8):   # aligned with the row before it grows
+            h["q"][b, hq] = R.f32_to_bf16_bits(
+                h["k_pages"][pg, hq // 4, off].astype(np.float64) * ks[pg, hq // 4, off])
+        ks[pg, :, off] *= np.float32(3e4)
+    check_against_oracle(wl, h, num_splits=num_splits)
+
+
 def test_relative_position_invariance_through_appends():
     # fill two caches token by token through the library, positions t and t + s,
     # then decode at m and m + s: scores depend on m - t only

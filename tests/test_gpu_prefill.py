@@ -11,6 +11,7 @@ import torch
 
 from decode_phase_gqa_gb300 import kvattn as K
 from decode_phase_gqa_gb300 import workloads as W
+from tests import refmath as R
 from tests.gpu_helpers import assert_close, out_f64, pool_bits, run_gpu, to_dev
 from tests.helpers import bits, host_inputs, oracle_decode, oracle_prefill
 
@@ -396,4 +397,98 @@ def test_many_sequences_with_empty_chunks(max_new):
         n_new[::97] = 20
     ctx = rng.integers(0, 41, 1100)
     wl, h, starts, ctx = make_case(4, 1, ctx, n_new, d=64, seed=41 + max_new)
+    check(wl, h, starts, ctx)
+
+
+# ---- range: peaked scores, int8 row scales far from 1 -------------------------
+
+def _stored_key(h, wl, starts, ctx, b, kk, j):
+    """The key attention sees at index kk of sequence b, KV head j (NoPE): a
+    cached row (bf16 bits, or int8 codes x scale rounded to bf16), else the new
+    token's k_new row."""
+    P = wl.page_size
+    if kk < ctx[b]:
+        pg, off = h["block_table"][b, kk // P], kk % P
+        if wl.kv_dtype == "int8":
+            return R.f32_to_bf16_bits(h["k_pages"][pg, j, off].astype(np.float64) * h["k_scales"][pg, j, off])
+        return h["k_pages"][pg, j, off].copy()
+    return h["k_new"][starts[b] + kk - ctx[b], j].copy()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("kind", ["prompts", "chunks", "drafts"])
+def test_peaked_scores(kind, kv):
+    """Scale 30 and every query equal to one key it sees (NoPE): one score
+    exceeds the others by thousands, so the softmax is a single weight of 1.
+    Through every attention kernel: the tcgen05 one (prompts over a bf16
+    cache), the 16-token one (chunks, and int8 prompts) and the short one
+    (drafts)."""
+    ctx, n_new = {"prompts": ([0, 40], [130, 97]), "chunks": ([300, 17], [33, 50]),
+                  "drafts": ([900, 70], [4, 3])}[kind]
+    wl, h, starts, ctx = make_case(8, 2, ctx, n_new, d=128, seed=51, theta=0.0, kv=kv)
+    wl.scale = 30.0
+    g = 4
+    for b in range(len(ctx)):
+        for i in range(int(np.diff(starts)[b])):
+            kk = (int(ctx[b]) + i) // 2
+            for hq in range(8):
+                h["q"][starts[b] + i, hq] = _stored_key(h, wl, starts, ctx, b, kk, hq // g)
+    check(wl, h, starts, ctx)
+
+
+def _scaled_bf16(u16, factor):
+    return R.f32_to_bf16_bits(R.bf16_bits_to_f64(u16) * factor)
+
+
+_RANGE_CASES = {"prompts": ([200, 0], [100, 80]), "chunks": ([300, 170], [33, 20]),
+                "drafts": ([900, 170], [4, 3])}
+
+
+@pytest.mark.parametrize("factor", [1e-7, 1e5])
+@pytest.mark.parametrize("kind", ["prompts", "chunks", "drafts"])
+def test_int8_value_scales_far_from_one(kind, factor):
+    """Every value row, cached and new, multiplied by 1e-7 (dequantised values
+    below f16's smallest subnormal) or by 1e5 (beyond f16's largest finite
+    value): the outputs move with them, compared with the oracle relative to
+    each output row's size."""
+    ctx, n_new = _RANGE_CASES[kind]
+    wl, h, starts, ctx = make_case(8, 2, ctx, n_new, d=128, seed=53, kv="int8")
+    P = wl.page_size
+    for b in range(len(ctx)):
+        for t in range(int(ctx[b])):
+            pg, off = h["block_table"][b, t // P], t % P
+            h["v_scales"][pg, :, off] *= np.float32(factor)
+    h["v_new"] = _scaled_bf16(h["v_new"], factor)
+    out, st, d = run_prefill(wl, h, starts, ctx)
+    ref, ost, kp, vp = oracle_prefill(h, starts, ctx, wl.rope_theta, wl.scale)
+    assert st == 0 and ost == 0
+    got = out_f64(out)
+    assert np.all(np.isfinite(got))
+    size = np.abs(ref).max(axis=-1, keepdims=True)
+    assert size.min() > 0
+    assert np.all(np.abs(got - ref) <= 2e-2 * size)
+
+
+@pytest.mark.parametrize("kind", ["prompts", "chunks", "drafts"])
+def test_int8_key_scales_far_from_one(kind):
+    """Cached key rows with scales of 1e-7 of their own (scores near zero), and
+    one row per sequence with 3e4 times its scale (dequantised values past
+    f16's range) that every query of the sequence is aligned with (NoPE):
+    that row takes the whole softmax, the output is its value row."""
+    ctx, n_new = _RANGE_CASES[kind]
+    ctx = [max(c, 60) for c in ctx]
+    wl, h, starts, ctx = make_case(8, 2, ctx, n_new, d=128, seed=57, theta=0.0, kv="int8")
+    P = wl.page_size
+    ks = h["k_scales"]
+    for b in range(len(ctx)):
+        big = int(ctx[b]) // 3
+        for t in range(0, int(ctx[b]), 5):
+            if t != big:
+                pg, off = h["block_table"][b, t // P], t % P
+                ks[pg, :, off] *= np.float32(1e-7)
+        pg, off = h["block_table"][b, big // P], big % P
+        for i in range(int(np.diff(starts)[b])):   # aligned with the row before it grows
+            for hq in range(8):
+                h["q"][starts[b] + i, hq] = _stored_key(h, wl, starts, ctx, b, big, hq // 4)
+        ks[pg, :, off] *= np.float32(3e4)
     check(wl, h, starts, ctx)
