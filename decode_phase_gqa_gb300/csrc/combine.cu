@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   constexpr int RS = record_floats(GS, D);
   constexpr int NC = GS * D / 4;  // float4 columns of a record's accumulator
   static_assert(kCombineThreads % NC == 0, "columns must tile the CTA");
+  static_assert((NC & (NC - 1)) == 0, "chunk sizes and record lanes are powers of two");
   constexpr int kGroups = kCombineThreads / NC;  // concurrent short merges per CTA
   // A stream of at most kShort shares is merged by a group of NC threads,
   // one column each, kGroups at a time and without CTA barriers.  A longer
@@ -116,7 +117,8 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
   constexpr int kMinCols = 16 < NC ? 16 : NC;
   constexpr int kMaxChunks = NC / kMinCols;
   __shared__ ColState part[kCombineThreads];  // [record lane][column]
-  __shared__ int4 list[kCombineThreads];      // (stream, chunk, chunks, first share)
+  __shared__ int4 list[kCombineThreads];      // (first record slot, chunk, log2 chunks, v)
+  __shared__ int lh0[kCombineThreads];        // first query head
   __shared__ int lseg[kCombineThreads];
   __shared__ int n_list;
   __shared__ int scratch[32];
@@ -160,8 +162,9 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
         const int nch = nseg <= kShort ? 1 : max(1, min(kMaxChunks, NC * R / kCombineThreads));
         if (nseg > 1 && q < nch) {
           const int k = atomicAdd(&n_list, 1);
-          list[k] = make_int4(sid, q, nch, w0);
+          list[k] = make_int4(sid + w0, q, __ffs(nch) - 1, v);  // (nch: a power of two)
           lseg[k] = nseg;
+          lh0[k] = (si / p.n_sub) * GS * p.n_sub + (si % p.n_sub) * GS;
         }
       }
     }
@@ -176,10 +179,8 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
       for (int i = gi; i < n_list; i += kGroups) {
         const int4 w = list[i];
         if (lseg[i] > kShort) continue;
-        const int v = w.x / spu, si = w.x % spu;
-        const int h0 = (si / p.n_sub) * GS * p.n_sub + (si % p.n_sub) * GS;
-        const ColState st = merge_column<D, GS>(p.records + (size_t)(w.x + w.w) * RS, 0, 1, lseg[i], c);
-        store_column(p.out + ((size_t)v * p.n_qh + h0) * D + c * 4, st);
+        const ColState st = merge_column<D, GS>(p.records + (size_t)w.x * RS, 0, 1, lseg[i], c);
+        store_column(p.out + ((size_t)w.w * p.n_qh + lh0[i]) * D + c * 4, st);
       }
     }
     // long merges: the whole CTA, one item at a time
@@ -187,15 +188,14 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
       const int4 w = list[i];
       const int nseg = lseg[i];
       if (nseg <= kShort) continue;
-      const int sid = w.x, q = w.y, nch = w.z, w0 = w.w;
-      const int v = sid / spu, si = sid % spu;
-      const int h0 = (si / p.n_sub) * GS * p.n_sub + (si % p.n_sub) * GS;
+      const int q = w.y, lg = w.z, v = w.w, h0 = lh0[i];
       // thread (record lane rl, column cc of the chunk) merges records rl,
-      // rl + R, ... of column c online
-      const int ncq = NC / nch, R = kCombineThreads / ncq;
-      const int cc = tid % ncq, rl = tid / ncq;
+      // rl + R, ... of column c online (powers of two: shifts and masks only)
+      constexpr int kLogNC = __builtin_ctz(NC);
+      const int ncq = NC >> lg, R = (kCombineThreads / NC) << lg;
+      const int cc = tid & (ncq - 1), rl = tid >> (kLogNC - lg);
       const int c = q * ncq + cc;
-      ColState st = merge_column<D, GS>(p.records + (size_t)(sid + w0) * RS, rl, R, nseg, c);
+      ColState st = merge_column<D, GS>(p.records + (size_t)w.x * RS, rl, R, nseg, c);
       part[tid] = st;
       __syncthreads();
       if (rl == 0) {

@@ -10,14 +10,29 @@
 
 namespace kvattn {
 
+// floor(a / b) for 0 <= a < 2^31 and 1 <= b whose quotient is below 2^20:
+// a quotient estimate from the fp32 reciprocal of b (relative error under
+// 2^-21, so within one of the quotient) corrected on the remainder.  A few
+// dependent instructions instead of the general integer division, which
+// weighs on the latency-bound set-up of a small decode step.
+__device__ __forceinline__ int div_small(int a, int b) {
+  float rb;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rb) : "f"((float)b));
+  int q = (int)((float)a * rb);
+  const long long r = (long long)a - (long long)q * b;
+  q += (int)(r >= b) - (int)(r < 0);
+  return q;
+}
+
 // T units cut into n equal shares: share c covers [begin(c), begin(c + 1)),
 // begin(c) = floor(c T / n) = c q + floor(c r / n) with T = q n + r.  All in
-// 32-bit integers (the host keeps T below 2^31 and n <= 4096, so c r < 2^24):
-// a 64-bit division is a long software routine on this GPU.
+// 32-bit integers (the host keeps T below 2^31 and n <= 4096, so c r < 2^24
+// and its quotient by n is below 2^12): a 64-bit division is a long software
+// routine on this GPU.
 struct Split {
   int T, n, q, r;
   __device__ __forceinline__ Split(int T_, int n_) : T(T_), n(n_), q(T_ / n_), r(T_ - (T_ / n_) * n_) {}
-  __device__ __forceinline__ int begin(int c) const { return c * q + (c * r) / n; }
+  __device__ __forceinline__ int begin(int c) const { return c * q + div_small(c * r, n); }
   // share holding unit t (0 <= t < T): an fp32 estimate of t n / T, off by
   // at most one, corrected against the exact boundaries
   __device__ __forceinline__ int owner(int t) const {
@@ -150,7 +165,7 @@ struct WeightedSplit {
       *v = L * B - 1;
       return L * TL;
     }
-    const int l = (LAYERED && y >= XL) ? y / XL : 0;
+    const int l = (LAYERED && y >= XL) ? div_small(y, XL) : 0;  // (l < L <= 1024)
     y -= l * XL;
     int lo = 0, hi = B;  // seq_pos(lo) <= y; every sequence from hi on starts after y
     while (hi - lo > 1) {
@@ -163,7 +178,7 @@ struct WeightedSplit {
     const int u = pref[lo + 1] - pref[lo];
     const int ws = 4 * u + sc;  // > 0: y lies inside sequence lo's streams
     const int off = y - seq_pos(lo);
-    const int si = off / ws, rem = off - si * ws;
+    const int si = div_small(off, ws), rem = off - si * ws;  // (off < spu ws: si < spu)
     const int t = spu * pref[lo] + si * u + min(u, (rem + 3) >> 2);
     int bl = lo, bh = B;  // the last sequence whose first unit is at or before t
     while (bh - bl > 1) {
@@ -176,11 +191,42 @@ struct WeightedSplit {
     *v = l * B + bl;
     return l * TL + t;
   }
+  // first_unit for a batch of at most 32 sequences, by the whole warp at
+  // once: lane b holds pref[b] (pl; any value for b >= B), and the two
+  // searches are ballots over the sequences (seq_pos and pref are
+  // nondecreasing, so the sequences at or before a position are a prefix).
+  template <bool LAYERED>
+  __device__ __forceinline__ int first_unit_warp(int y, int *v, int lane, int pl) const {
+    if (y >= split.T) {
+      *v = L * B - 1;
+      return L * TL;
+    }
+    const int l = (LAYERED && y >= XL) ? div_small(y, XL) : 0;
+    y -= l * XL;
+    const bool in = lane < B;
+    const int lo = __popc(__ballot_sync(0xffffffffu, in && 4 * spu * pl + sc * spu * lane <= y)) - 1;
+    const int p0 = __shfl_sync(0xffffffffu, pl, lo);
+    const int u = pref[lo + 1] - p0;
+    const int ws = 4 * u + sc;
+    const int off = y - (4 * spu * p0 + sc * spu * lo);
+    const int si = div_small(off, ws), rem = off - si * ws;
+    const int t = spu * p0 + si * u + min(u, (rem + 3) >> 2);
+    const int bl = __popc(__ballot_sync(0xffffffffu, in && spu * pl <= t)) - 1;
+    *v = l * B + bl;
+    return l * TL + t;
+  }
   // Unit range [*t0, *t1) of share c and the virtual sequences of its ends,
-  // for the whole warp: even lanes search the start, odd lanes the end, at once.
+  // for the whole warp: up to 32 sequences by ballots (both ends in turn),
+  // else even lanes search the start and odd lanes the end, at once.
   template <bool LAYERED>
   __device__ __forceinline__ void share_bounds(int c, int lane, int *t0, int *b0, int *t1,
                                                int *b1) const {
+    if (B <= 32) {
+      const int pl = lane < B ? pref[lane] : 0;
+      *t0 = first_unit_warp<LAYERED>(split.begin(c), b0, lane, pl);
+      *t1 = first_unit_warp<LAYERED>(split.begin(c + 1), b1, lane, pl);
+      return;
+    }
     int b = 0;
     const int t = first_unit<LAYERED>(split.begin(c + (lane & 1)), &b);
     *t0 = __shfl_sync(0xffffffffu, t, 0);
@@ -219,7 +265,7 @@ __device__ __forceinline__ UnitPos locate_unit(int t, int &v, const int *pref, i
                                                int TL) {
   int l = 0, b = v;
   if (LAYERED && v >= B) {
-    l = v / B;
+    l = div_small(v, B);  // (l < L <= 1024)
     b = v - l * B;
   }
   while ((LAYERED ? l * TL : 0) + spu * pref[b + 1] <= t) {  // unit t lies past sequence (l, b)
@@ -236,7 +282,7 @@ __device__ __forceinline__ UnitPos locate_unit(int t, int &v, const int *pref, i
   r.b = b;
   r.units = pref[b + 1] - pref[b];
   const int off = t - ((LAYERED ? l * TL : 0) + spu * pref[b]);
-  r.si = off / r.units;
+  r.si = div_small(off, r.units);  // (the stream within the sequence: below spu)
   r.u = off - r.si * r.units;
   r.first = t - r.u;
   return r;

@@ -261,6 +261,20 @@ __device__ __forceinline__ void warp_query_fragments(const DecodeParams &p, cons
   }
 }
 
+// Lines per CTA of an L2 prefetch spread over the grid: an fp32 estimate of
+// lines / grid plus two.  A prefetch is only a hint (a line fetched twice
+// costs little, one left out only waits later), and the CTAs placed last run
+// this before their wait, on the step's critical path: no 64-bit division.
+__device__ __forceinline__ size_t prefetch_share(size_t lines) {
+  float rg;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rg) : "f"((float)gridDim.x));
+  return (size_t)((float)lines * rg) + 2;
+}
+
+// KV head of stream si of a sequence (n_sub query-head groups per KV head);
+// most models have one group per KV head, which skips the division
+__device__ __forceinline__ int sub_head(int si, int n_sub) { return n_sub == 1 ? si : si / n_sub; }
+
 template <int D, int GS, bool INT8, bool LAYERED>
 // at most 3 CTAs fit an SM's shared memory: let each thread have 1/384 of the
 // register file
@@ -324,14 +338,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     // every CTA pulls its slice of the queries into L2, so that the warps'
     // query rows do not queue behind the flood of K/V requests
     const size_t q_lines = ((size_t)p.n_layers * p.n_seq * p.n_qh * D * 2 + 127) / 128;
-    const size_t per = (q_lines + gridDim.x - 1) / gridDim.x;
+    const size_t per = prefetch_share(q_lines);
     const char *qc = reinterpret_cast<const char *>(p.q);
 #pragma unroll 1
     for (size_t l = blockIdx.x * per + tid; l < min(q_lines, (blockIdx.x + 1) * per); l += kDecodeThreads)
       asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(qc + l * 128));
     // and the new keys and values, which the warps appending them read
     const size_t kv_lines = ((size_t)p.n_layers * p.n_seq * p.n_kvh * D * 2 + 127) / 128;
-    const size_t kper = (kv_lines + gridDim.x - 1) / gridDim.x;
+    const size_t kper = prefetch_share(kv_lines);
     const char *kc = reinterpret_cast<const char *>(p.k_new);
     const char *vc = reinterpret_cast<const char *>(p.v_new);
 #pragma unroll 1
@@ -344,7 +358,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     // the planning below find it in L2 instead of waiting on DRAM again
     const size_t bt_lines = ((size_t)p.n_seq * p.max_pages * 4 + 127) / 128;
     if (bt_lines <= kTablePrefetchLines) {
-      const size_t bper = (bt_lines + gridDim.x - 1) / gridDim.x;
+      const size_t bper = prefetch_share(bt_lines);
       const char *bc = reinterpret_cast<const char *>(p.block_table);
 #pragma unroll 1
       for (size_t l = blockIdx.x * bper + tid; l < min(bt_lines, (blockIdx.x + 1) * bper); l += kDecodeThreads)
@@ -370,7 +384,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
   // alone takes microseconds for the correctly rounded cos/sin).  Otherwise
   // warp g of the grid takes share g.
   const bool spread = 2 * nwa <= n_warps;
-  const int A = spread ? (nwa + (int)gridDim.x - 1) / (int)gridDim.x : W;
+  // (spread: nwa <= grid W / 2, so A = ceil(nwa / grid) is 1 or 2)
+  static_assert(W == 4, "two spread shares per CTA at most");
+  const int A = spread ? (nwa > (int)gridDim.x ? 2 : 1) : W;
   const int g = spread ? warp * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.x * W + warp;
   uint64_t *row_ready = reinterpret_cast<uint64_t *>(smem + C::kMiscOff + 32);  // [W]
   if (g >= nwa) {
@@ -383,7 +399,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
       const UnitPos up = locate_unit<LAYERED>(wa0 < wa1 ? wa0 : 0, b, pref, spu, p.n_seq, TL);
       if (wa0 < wa1 && up.first + up.units <= wa1) {  // warp a appends its first stream's new token
         uint8_t *arow = smem + C::kNewOff + a * C::kNewBytes;
-        const size_t kv = ((size_t)up.v * p.n_kvh + up.si / p.n_sub) * D;
+        const size_t kv = ((size_t)up.v * p.n_kvh + sub_head(up.si, p.n_sub)) * D;
         const char *ks = reinterpret_cast<const char *>(p.k_new + kv);
         const char *vs = reinterpret_cast<const char *>(p.v_new + kv);
         for (int c = lane; c < 4 * D / 16; c += 32)
@@ -438,8 +454,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const UnitPos up = locate_unit<LAYERED>(wt0, v, pref, spu, p.n_seq, TL);
     cb_l = up.l;
     cb_b = up.b;
-    cb_j = up.si / p.n_sub;
-    cb_sub = up.si % p.n_sub;
+    cb_j = sub_head(up.si, p.n_sub);
+    cb_sub = up.si - cb_j * p.n_sub;
     cb_u = up.u;
     cb_units = up.units;
     prefetch_queries(up.v, cb_j * GS * p.n_sub + cb_sub * GS);
@@ -547,7 +563,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int F = sp.first, E = F + sp.units;
     const int e = min(wt1, E);
     const int L = lens[sp.b];
-    const int j = sp.si / p.n_sub, sub = sp.si % p.n_sub;
+    const int j = sub_head(sp.si, p.n_sub), sub = sp.si - j * p.n_sub;
     const int h0 = j * GS * p.n_sub + sub * GS;
     const int sid = sp.v * spu + sp.si;  // (all layers' streams)
 
@@ -585,7 +601,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     if (E < wt1) {  // the share continues: fetch the next stream's query rows
       int v = sp.v;
       const UnitPos nx = locate_unit<LAYERED>(E, v, pref, spu, p.n_seq, TL);
-      prefetch_queries(nx.v, (nx.si / p.n_sub) * GS * p.n_sub + (nx.si % p.n_sub) * GS);
+      const int nj = sub_head(nx.si, p.n_sub);
+      prefetch_queries(nx.v, nj * GS * p.n_sub + (nx.si - nj * p.n_sub) * GS);
     }
     // this stream's raw new rows (the first stream's came in the prologue),
     // after the query wait above so that it does not wait for them
