@@ -67,6 +67,17 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u_flipped, uint32_t 
   return r;
 }
 
+// Two int8 codes of `u` as the f16 pair 1152 + x: the conversion above
+// without its subtraction, for MMAs whose accumulators take the bias off
+// (1152 times the sum of the other operand, formed by an MMA with the
+// constant pair kF16x2_1152).
+__device__ __forceinline__ uint32_t codes_biased_f16x2(uint32_t u_flipped, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(u_flipped), "r"(0x64646464u), "r"(sel));
+  return r;
+}
+constexpr uint32_t kF16x2_1152 = 0x64806480u;  // the f16 pair (1152, 1152)
+
 // a[i] for a lane-dependent i without dynamic register indexing
 template <int N>
 __device__ __forceinline__ float pick(const float (&a)[N], int i) {

@@ -135,15 +135,6 @@ __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-// Two int8 codes of `u` as the f16 pair 1152 + x (the conversion above without
-// its subtraction); the key's dot products start from -1152 * sum(q), so the
-// bias cancels inside the MMA accumulation.
-__device__ __forceinline__ uint32_t codes_to_f16x2_biased(uint32_t u_flipped, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(u_flipped), "r"(0x64646464u), "r"(sel));
-  return r;
-}
-
 // D (16x8 fp32) += A (16x16 f16, row) * B (16x8 f16, col)
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                               uint32_t b1) {
@@ -693,10 +684,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               const uint32_t r0 = a[2 * c] ^ 0x80808080u, r1 = a[2 * c + 1] ^ 0x80808080u;
-              const uint32_t f[4] = {codes_to_f16x2_biased(r0, 0x5140u),
-                                     codes_to_f16x2_biased(r1, 0x5140u),
-                                     codes_to_f16x2_biased(r0, 0x5342u),
-                                     codes_to_f16x2_biased(r1, 0x5342u)};
+              const uint32_t f[4] = {codes_biased_f16x2(r0, 0x5140u),
+                                     codes_biased_f16x2(r1, 0x5140u),
+                                     codes_biased_f16x2(r0, 0x5342u),
+                                     codes_biased_f16x2(r1, 0x5342u)};
               mma_f16_16816(s, f, qb[2 * it + c][0], qb[2 * it + c][1]);
             }
           } else {

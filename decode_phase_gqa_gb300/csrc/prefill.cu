@@ -642,28 +642,51 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
 // The 16 MMA rows are the 4 new tokens x the 4 query heads of a group (row
 // 4 t + i: token t, head i), so no row is padding when the chunk is a
 // speculative step's drafts.  A 64-key stage is split among the 4 warps (16
-// keys each); each warp gathers and uses its own 16 keys of every stage (one
-// page lookup, two 256-byte rows a copy instruction) through a private
-// double-buffered cp.async ring, so warps stream independently with no CTA barrier
-// per stage.  Each warp keeps its own online-softmax state of all 16 rows; the
-// four states are merged in shared memory at the end.
+// keys each); each warp streams its own 16 keys of every stage (one page)
+// through a private ring of stages that TMA tensor copies fill ([16 rows]
+// boxes of the pool, 128- or 64-byte swizzle, the decode kernel's views),
+// each stage with its own barrier, so warps stream independently with no CTA
+// barrier per stage.  Each warp keeps its own online-softmax state of all 16
+// rows; the four states are merged in shared memory at the end.
 template <int D, bool INT8>
 struct PsCfg {
-  static constexpr int kRowB = 2 * D;
+  static constexpr int kRowB = 2 * D;                 // a query row (16-bit)
   static constexpr int kQBytes = 16 * kRowB;
-  static constexpr int kPart = kPsWarpKeys * kRowB;  // a warp's K (or V) rows of a stage (16-bit)
-  // int8 cache: a stage is the codes (K, V; 16-byte chunks of a row permuted
-  // as cidx8 gives) and the row scales (K, V) as copied; the codes become f16
-  // in registers
-  static constexpr int kRaw = 2 * kPsWarpKeys * D + 2 * kPsWarpKeys * 4;
+  static constexpr int kCacheRowB = INT8 ? D : 2 * D;  // a cached row
+  static constexpr int kBoxB = kCacheRowB < 128 ? kCacheRowB : 128;  // bytes of a box row
+  static constexpr int kRegions = kCacheRowB / kBoxB;  // boxes a 16-row tile
+  static constexpr int kBox = kPsWarpKeys * kBoxB;
+  static constexpr int kTile = kRegions * kBox;        // a warp's K (or V) rows of a stage
+  static constexpr int kStage = 2 * kTile;             // K then V
   // stages of a warp's ring: the int8 slices are half the bytes, so twice as
   // many fit the same shared memory (3 CTAs an SM either way)
   static constexpr int kStages = INT8 ? 2 * kPsStages : kPsStages;
-  static constexpr int kRing = INT8 ? kStages * kRaw : kStages * 2 * kPart;  // a warp's
-  static constexpr int kSmem = kQBytes + kPfWarps * kRing + 64 * 8;
+  static constexpr int kRing = kStages * kStage;       // a warp's
+  // after 1024 bytes of alignment slack: the rings, the query rows, the int8
+  // row scales [warp][stage][K 16, V 16], the stage barriers, the RoPE turns
+  static constexpr int kQOff = kPfWarps * kRing;
+  static constexpr int kScaleOff = kQOff + kQBytes;
+  static constexpr int kBarOff = kScaleOff + (INT8 ? kPfWarps * kStages * 2 * kPsWarpKeys * 4 : 0);
+  static constexpr int kTurnsOff = kBarOff + kPfWarps * kStages * 8;
+  static constexpr int kSmem = 1024 + kTurnsOff + 64 * 8;
+  static_assert(kBox % 1024 == 0 || (kBoxB == 64 && kBox % 512 == 0), "swizzled boxes need alignment");
   // the end-of-kernel merge borrows the rings: [4 warps][16 rows][D] + (m, l)
   static_assert(kPfWarps * 16 * (D + 2) * 4 <= kPfWarps * kRing, "merge buffer");
 };
+
+// The short kernel's parameters: the call's, and the pools' TMA views
+struct PsParams {
+  PrefillParams p;
+  CUtensorMap tmap_k, tmap_v;
+};
+
+// Byte offset of 16-byte chunk c of row r in a bf16 K or V tile as the TMA
+// writes it: boxes of [16 rows][128 bytes] one after another, the chunk index
+// XORed with the row's low three bits (128-byte swizzle)
+template <int D>
+__device__ __forceinline__ uint32_t tile_sw(int r, int c) {
+  return (uint32_t)((c >> 3) * (kPsWarpKeys * 128) + r * 128 + (((c ^ r) & 7) << 4));
+}
 
 // Position of 16-byte chunk c of code row r in a staged int8 slice [16][D]:
 // XOR-permuted so that the 8 rows an ldmatrix reads at one chunk fall in 8
@@ -680,16 +703,18 @@ __device__ __forceinline__ void cp_async_wait_n() {
 }
 
 template <int D, bool INT8>
-__global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __grid_constant__ PsParams sp) {
   using C = PsCfg<D, INT8>;
+  const PrefillParams &p = sp.p;
   constexpr int KS = D / 16;
   constexpr int ND = D / 8;
-  constexpr int RCH = 2 * D / 16;  // 16-byte chunks of a row
   const float kFloor = -1e30f;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *qs = smem;
-  uint8_t *rings = smem + C::kQBytes;
-  float2 *turns = reinterpret_cast<float2 *>(rings + kPfWarps * C::kRing);
+  const float kLazy = 8.f;  // log2 headroom of the lazy softmax references
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t *rings = smem;
+  uint8_t *qs = smem + C::kQOff;
+  float2 *turns = reinterpret_cast<float2 *>(smem + C::kTurnsOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.n_qh / kPfWarps;  // head quads
@@ -701,10 +726,13 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   // Launched as the append kernel's programmatic dependent: the cached keys
   // (slots below ctx) are read while the append runs; a warp waits for the
   // append grid before its first slice that holds new slots, and every
-  // thread waits before it leaves, so the grid ends after the append's.
+  // working thread waits before it leaves, so the grid ends after the
+  // append's.  CTAs with nothing to do leave at once (the first CTA waits
+  // all the same, so that the grid cannot end before the append's).
+  const bool first_cta = blockIdx.x == 0 && blockIdx.z == 0;
   if (!seq_span(p, b, start, n_new, ctx)) {
     if (grp == 0 && blockIdx.z == 0 && tid == 0) report(p, KVATTN_DEV_BAD_LEN);
-    pdl_wait_primary();
+    if (first_cta) pdl_wait_primary();
     return;
   }
   if (grp == 0 && blockIdx.z == 0 && tid == 0 && n_new > kPsTok) report(p, KVATTN_DEV_BAD_LEN);
@@ -712,70 +740,90 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   const int n_tiles = (n_keys + kPsKeys - 1) / kPsKeys;
   const int z = blockIdx.z, nz = short_splits(n_tiles, p.n_splits);
   if (n_new <= 0 || z >= nz) {
-    pdl_wait_primary();
+    if (first_cta) pdl_wait_primary();
     return;
   }
   const int per = (n_tiles + nz - 1) / nz;
   const int kt_begin = z * per, kt_end = min(n_tiles, kt_begin + per);
   if (tid < 64) turns[tid] = p.turns[tid];
-  __syncthreads();
 
   const int wk = warp * kPsWarpKeys;  // the warp's keys within a stage
   uint8_t *ring = rings + warp * C::kRing;
-  uint32_t bad = 0;  // bit s: stage s's keys lie in an out-of-range page
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff) + warp * C::kStages;
+  float *wscl = reinterpret_cast<float *>(smem + C::kScaleOff) + warp * C::kStages * 2 * kPsWarpKeys;
+  if (lane == 0) {
+    for (int s = 0; s < C::kStages; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+    prefetch_tensormap(&sp.tmap_k);
+    prefetch_tensormap(&sp.tmap_v);
+  }
+  __syncthreads();  // (the turns; the barriers are the warp's own)
+  const uint64_t pol = l2_evict_first_policy();
+  uint32_t bad = 0;  // bit s: stage s's keys lie in an out-of-range page (nothing copied)
   bool appended = false;  // the append grid is complete and its rows visible
-  // the warp's 16 keys of stage kt (in one page: pages hold 16 keys or more)
+  // Block-table entries of the warp's stages, 32 at a time: lane i holds the
+  // page of stage win_base + i, so a stage's copies never wait on a table
+  // load (the table is no output of the append grid)
+  const int *bt_row = p.block_table + (size_t)b * p.max_pages;
+  auto stage_page = [&](int kt) {
+    const int key = kt * kPsKeys + wk;
+    return (kt < kt_end && key < n_keys) ? __ldg(bt_row + (key >> p.page_shift)) : -1;
+  };
+  int win_base = kt_begin;
+  int win_page = stage_page(kt_begin + lane);
+  // The warp's 16 keys of stage kt (one page: pages hold 16 keys or more)
+  // into ring slot s: TMA boxes of K and V (the 16 rows of the page slots;
+  // rows past the keys come as the pool holds them and are masked, bf16 V
+  // rows zeroed), the int8 row scales by 16-byte copies the slot's barrier
+  // tracks.  Called for kt = kt_begin, kt_begin + 1, ... in order, by the
+  // whole warp.
   auto load_part = [&](int kt, int s) {
     const int key = kt * kPsKeys + wk;
+    if (kt - win_base >= 32) {
+      win_base += 32;
+      win_page = stage_page(win_base + lane);
+    }
+    const int page = __shfl_sync(0xffffffffu, win_page, kt - win_base);
     if (!appended && key + kPsWarpKeys > ctx) {
       pdl_wait_primary();
       appended = true;
     }
-    long long base = -1;
+    int row = -1;
     if (key < n_keys) {
-      const int page = __ldg(p.block_table + (size_t)b * p.max_pages + (key >> p.page_shift));
       if (page >= 0 && page < p.num_pages)
-        base = ((long long)page * p.n_kvh + j) * p.page_size + (key & (p.page_size - 1));
+        row = (page * p.n_kvh + j) * p.page_size + (key & (p.page_size - 1));
       else if (lane == 0)
         report(p, KVATTN_DEV_BAD_PAGE);
     }
-    bad = base >= 0 ? bad & ~(1u << s) : bad | (1u << s);
+    bad = row >= 0 ? bad & ~(1u << s) : bad | (1u << s);
     if constexpr (INT8) {
-      // codes row by row (plain layout), then the 16 K and 16 V scales
-      uint8_t *Kd = ring + s * C::kRaw, *Vd = Kd + kPsWarpKeys * D;
-      constexpr int CC = D / 16;  // 16-byte chunks of a code row
-#pragma unroll
-      for (int idx = lane; idx < kPsWarpKeys * CC; idx += 32) {
-        const int r = idx / CC, c = idx % CC;
-        const bool ok = base >= 0 && key + r < n_keys;
-        const size_t off = ok ? (size_t)(base + r) * D + c * 16 : 0;
-        const int dc = r * D + cidx8<D>(r, c) * 16;
-        cp_async_16_zfill(Kd + dc, static_cast<const uint8_t *>(p.k_pages) + off, ok ? 16 : 0);
-        cp_async_16_zfill(Vd + dc, static_cast<const uint8_t *>(p.v_pages) + off, ok ? 16 : 0);
+      if (row >= 0 && lane < 8) {
+        cp_async_16(wscl + s * 2 * kPsWarpKeys + 4 * lane,
+                    (lane < 4 ? p.k_scales : p.v_scales) + row + 4 * (lane & 3));
+        cp_async_mbar_arrive(&bars[s]);
       }
-      if (lane < 8) {
-        const float *src = lane < 4 ? p.k_scales : p.v_scales;
-        const size_t off = base >= 0 ? (size_t)base + 4 * (lane & 3) : 0;
-        cp_async_16_zfill(Vd + kPsWarpKeys * D + 16 * lane, src + off, base >= 0 ? 16 : 0);
-      }
-      return;
+      __syncwarp();
     }
-    uint8_t *Kd = ring + s * 2 * C::kPart, *Vd = Kd + C::kPart;
+    __syncwarp();  // every lane is done with the slot (and its bf16 zeroing)
+    if (lane == 0) {
+      if (row >= 0) {
+        fence_proxy_async_smem();  // those generic accesses before the copy's writes
+        uint8_t *dst = ring + s * C::kStage;
+        mbar_arrive_expect_tx(&bars[s], C::kStage);
 #pragma unroll
-    for (int idx = lane; idx < kPsWarpKeys * RCH; idx += 32) {
-      const int r = idx / RCH, c = idx % RCH;
-      const bool ok = base >= 0 && key + r < n_keys;
-      const size_t off = ok ? (size_t)(base + r) * (2 * D) + c * 16 : 0;
-      cp_async_16_zfill(Kd + sw<D>(r, c), static_cast<const uint8_t *>(p.k_pages) + off, ok ? 16 : 0);
-      cp_async_16_zfill(Vd + sw<D>(r, c), static_cast<const uint8_t *>(p.v_pages) + off, ok ? 16 : 0);
+        for (int r = 0; r < C::kRegions; ++r) {
+          const int x = r * C::kBoxB / (INT8 ? 1 : 2);  // element column of box r
+          tma_load_2d(dst + r * C::kBox, &sp.tmap_k, x, row, &bars[s], pol);
+          tma_load_2d(dst + C::kTile + r * C::kBox, &sp.tmap_v, x, row, &bars[s], pol);
+        }
+      } else {
+        mbar_arrive(&bars[s]);
+      }
     }
   };
   // the first stages go out before the queries are formed
-#pragma unroll
-  for (int i = 0; i < C::kStages - 1; ++i) {
-    if (kt_begin + i < kt_end) load_part(kt_begin + i, i);
-    cp_async_commit();
-  }
+  int issued = 0;
+  for (; issued < C::kStages - 1 && kt_begin + issued < kt_end; ++issued) load_part(kt_begin + issued, issued);
 
   // ---- the 16 query rows (token r / 4, head h0 + r % 4): rotated, scaled ----
   for (int e = tid; e < 16 * (D / 2); e += kPfThreads) {
@@ -830,27 +878,74 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   // int8: the running maximum of the value weights' exponents (score + log2
   // of the value row's scale), less m, so the f16 weights never overflow
   float dmo[2] = {kFloor, kFloor};
+  // int8: the accumulators' bias 1152 sum_k P of rows g, g + 8 (ob[0], ob[2])
+  // and the scores' starting value -1152 sum_d Q (same rows), formed by the
+  // MMA itself from the f16 query fragments
+  float ob[4] = {0.f, 0.f, 0.f, 0.f};
+  float kbias[2] = {0.f, 0.f};
+  if constexpr (INT8) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) mma16<true>(acc, qf[ks], kF16x2_1152, kF16x2_1152);
+    kbias[0] = -acc[0];
+    kbias[1] = -acc[2];
+  }
   // this lane's rows g and g + 8: tokens g / 4 and 2 + g / 4
   const int qpos[2] = {ctx + (lane >> 4), ctx + 2 + (lane >> 4)};
 
+  bool aborted = false;
+  int consumed = 0;
   for (int it = 0, kt = kt_begin; kt < kt_end; ++it, ++kt) {
-    if (kt + C::kStages - 1 < kt_end) load_part(kt + C::kStages - 1, (it + C::kStages - 1) % C::kStages);
-    cp_async_commit();
-    cp_async_wait_n<C::kStages - 1>();
-    __syncwarp();  // the other lanes' copies of this stage
+    if (kt + C::kStages - 1 < kt_end) {
+      load_part(kt + C::kStages - 1, (it + C::kStages - 1) % C::kStages);
+      ++issued;
+    }
     const int st = it % C::kStages;
-    uint32_t kb = smem_addr(ring + st * 2 * C::kPart), vb = kb + C::kPart;
-    const bool pg_ok = !((bad >> st) & 1u);
+    // (bounded: a copy that never lands leaves a status bit, not a hang)
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], (uint32_t)((it / C::kStages) & 1)))) {
+      aborted = true;
+      if (lane == 0) report(p, KVATTN_DEV_TIMEOUT);
+      break;
+    }
+    consumed = it + 1;
+    // a stage on an out-of-range page was not copied: nothing of it is used
+    if ((bad >> st) & 1u) continue;
+    const uint32_t kb = smem_addr(ring + st * C::kStage), vb = kb + C::kTile;
+    const int key0 = kt * kPsKeys + wk;
+    if constexpr (!INT8) {
+      // bf16 rows past the keys hold whatever the pool holds (NaN, maybe):
+      // zero them in V, so that their zero weights meet zeros
+      const int nv = n_keys - key0;
+      if (nv < kPsWarpKeys) {
+        uint8_t *Vt = ring + st * C::kStage + C::kTile;
+        const int n16 = (kPsWarpKeys - nv) * C::kRegions * 8;
+        for (int idx = lane; idx < n16; idx += 32) {
+          const int rr = nv + idx / (C::kRegions * 8), c = idx % (C::kRegions * 8);
+          *reinterpret_cast<uint4 *>(Vt + (c >> 3) * C::kBox + rr * 128 + (c & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
+    }
     if constexpr (INT8) {
-      // Scores from the codes: S = (Q codes^T) * the key row's scale; value
+      // Scores from the codes, which enter the MMAs as the f16 1152 + x (one
+      // prmt a pair, the subtraction left to the accumulators): S = (Q codes^T)
+      // * the key row's scale, starting from kbias = -1152 sum_d Q; value
       // weights 2^(S - m + log2 vs - dmo) with their own running maximum
       // m + dmo, so that P vs fits f16 whatever the scales and log2 vs is added
-      // to a number near zero (the decode kernel's scheme); the codes become
-      // exact f16 in registers, no dequantised tile.
-      const uint8_t *raw = ring + st * C::kRaw;
-      const uint32_t kc = smem_addr(raw), vc = kc + kPsWarpKeys * D;
-      const float *scl = reinterpret_cast<const float *>(raw + 2 * kPsWarpKeys * D);
-      float s[2][4] = {};
+      // to a number near zero (the decode kernel's scheme); O accumulates
+      // P (1152 + codes), whose bias 1152 sum_k P, formed by one more MMA with
+      // a constant operand, ob takes, to be taken off at the end.  Lazy
+      // references: m and dmo move only when a tile passes them by more than
+      // kLazy, so the weights stay below 2^kLazy and most tiles leave the
+      // accumulators as they are.
+      const uint32_t kc = kb, vc = vb;
+      const float *scl = wscl + st * 2 * kPsWarpKeys;
+      float s[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = kbias[e >> 1];
 #pragma unroll
       for (int c = 0; c < D / 16; c += 2) {
         // matrices (keys 0-7, chunk c), (keys 0-7, c + 1), (keys 8-15, c),
@@ -862,11 +957,10 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const uint32_t u0 = r[h2] ^ 0x80808080u, u1 = r[2 + h2] ^ 0x80808080u;
-          mma16<true>(s[0], qf[c + h2], codes_to_f16x2(u0, 0x5140u), codes_to_f16x2(u0, 0x5342u));
-          mma16<true>(s[1], qf[c + h2], codes_to_f16x2(u1, 0x5140u), codes_to_f16x2(u1, 0x5342u));
+          mma16<true>(s[0], qf[c + h2], codes_biased_f16x2(u0, 0x5140u), codes_biased_f16x2(u0, 0x5342u));
+          mma16<true>(s[1], qf[c + h2], codes_biased_f16x2(u1, 0x5140u), codes_biased_f16x2(u1, 0x5342u));
         }
       }
-      const int key0 = kt * kPsKeys + wk;
       float mx[2] = {-INFINITY, -INFINITY}, mxo[2] = {-INFINITY, -INFINITY};
       float xv[2][4];  // log2 vs, then the value-weight exponents
 #pragma unroll
@@ -874,21 +968,20 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
-          const bool ok = key0 + kr <= qpos[e >> 1] && pg_ok;  // (keys past n_keys: past qpos)
+          const bool ok = key0 + kr <= qpos[e >> 1];  // (keys past n_keys: past qpos)
           s[nt][e] = ok ? s[nt][e] * scl[kr] : -INFINITY;
           xv[nt][e] = ok ? lg2_approx(scl[kPsWarpKeys + kr]) : -INFINITY;
           mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
         }
-      float alpha[2], alpha_o[2];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
         mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-        const float mn = fmaxf(m[rr], mx[rr]);
-        alpha[rr] = ex2_approx(m[rr] - mn);
-        dmo[rr] -= mn - m[rr];  // the same absolute reference
-        m[rr] = mn;
-        l[rr] *= alpha[rr];
+        if (mx[rr] > m[rr] + kLazy) {
+          l[rr] *= ex2_approx(m[rr] - mx[rr]);
+          dmo[rr] -= mx[rr] - m[rr];  // the same absolute reference
+          m[rr] = mx[rr];
+        }
       }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -897,13 +990,15 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
           xv[nt][e] += s[nt][e] - m[e >> 1];
           mxo[e >> 1] = fmaxf(mxo[e >> 1], xv[nt][e]);
         }
+      float alpha_o[2] = {1.f, 1.f};
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         mxo[rr] = fmaxf(mxo[rr], __shfl_xor_sync(0xffffffffu, mxo[rr], 1));
         mxo[rr] = fmaxf(mxo[rr], __shfl_xor_sync(0xffffffffu, mxo[rr], 2));
-        const float don = fmaxf(dmo[rr], mxo[rr]);
-        alpha_o[rr] = ex2_approx(dmo[rr] - don);
-        dmo[rr] = don;
+        if (mxo[rr] > dmo[rr] + kLazy) {
+          alpha_o[rr] = ex2_approx(dmo[rr] - mxo[rr]);
+          dmo[rr] = mxo[rr];
+        }
       }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -914,6 +1009,15 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         }
       const uint32_t a[4] = {pack16<true>(xv[0][0], xv[0][1]), pack16<true>(xv[0][2], xv[0][3]),
                              pack16<true>(xv[1][0], xv[1][1]), pack16<true>(xv[1][2], xv[1][3])};
+      if (__any_sync(0xffffffffu, alpha_o[0] != 1.f || alpha_o[1] != 1.f)) {
+#pragma unroll
+        for (int nd = 0; nd < ND; ++nd)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[nd][k] *= alpha_o[k >> 1];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ob[k] *= alpha_o[k >> 1];
+      }
+      mma16<true>(ob, a, kF16x2_1152, kF16x2_1152);
 #pragma unroll
       for (int c = 0; c < D / 16; c += 2) {
         // matrices (keys 0-7, chunk c), (keys 8-15, c), (keys 0-7, c + 1),
@@ -927,13 +1031,8 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         for (int h2 = 0; h2 < 2; ++h2) {
           const int cc = c + h2;
           const uint32_t u0 = r[2 * h2] ^ 0x80808080u, u1 = r[2 * h2 + 1] ^ 0x80808080u;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            o[2 * cc][k] *= alpha_o[k >> 1];
-            o[2 * cc + 1][k] *= alpha_o[k >> 1];
-          }
-          mma16<true>(o[2 * cc], a, codes_to_f16x2(u0, 0x5240u), codes_to_f16x2(u1, 0x5240u));
-          mma16<true>(o[2 * cc + 1], a, codes_to_f16x2(u0, 0x5341u), codes_to_f16x2(u1, 0x5341u));
+          mma16<true>(o[2 * cc], a, codes_biased_f16x2(u0, 0x5240u), codes_biased_f16x2(u1, 0x5240u));
+          mma16<true>(o[2 * cc + 1], a, codes_biased_f16x2(u0, 0x5341u), codes_biased_f16x2(u1, 0x5341u));
         }
       }
     } else {
@@ -942,30 +1041,31 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t kf[4];
         const int mi = lane >> 3;
-        ldmatrix_x4(kf, kb + sw<D>((mi >> 1) * 8 + (lane & 7), 2 * ks + (mi & 1)));
+        ldmatrix_x4(kf, kb + tile_sw<D>((mi >> 1) * 8 + (lane & 7), 2 * ks + (mi & 1)));
         mma16<INT8>(s[0], qf[ks], kf[0], kf[1]);
         mma16<INT8>(s[1], qf[ks], kf[2], kf[3]);
       }
-      const int key0 = kt * kPsKeys + wk;
       float mx[2] = {-INFINITY, -INFINITY};
   #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
   #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
-          const bool ok = key0 + kr <= qpos[e >> 1] && pg_ok;  // (keys past n_keys: past qpos)
+          const bool ok = key0 + kr <= qpos[e >> 1];  // (keys past n_keys: past qpos)
           s[nt][e] = ok ? s[nt][e] : -INFINITY;
           mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
         }
-      float alpha[2];
+      // lazy reference: m moves only when a tile passes it by more than kLazy
+      float alpha[2] = {1.f, 1.f};
   #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
         mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-        const float mn = fmaxf(m[rr], mx[rr]);
-        alpha[rr] = ex2_approx(m[rr] - mn);
-        m[rr] = mn;
-        l[rr] *= alpha[rr];
+        if (mx[rr] > m[rr] + kLazy) {
+          alpha[rr] = ex2_approx(m[rr] - mx[rr]);
+          m[rr] = mx[rr];
+          l[rr] *= alpha[rr];
+        }
       }
   #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -976,23 +1076,27 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         }
       const uint32_t a[4] = {pack16<INT8>(s[0][0], s[0][1]), pack16<INT8>(s[0][2], s[0][3]),
                              pack16<INT8>(s[1][0], s[1][1]), pack16<INT8>(s[1][2], s[1][3])};
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+  #pragma unroll
+        for (int nd = 0; nd < ND; ++nd)
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) o[nd][k] *= alpha[k >> 1];
+      }
   #pragma unroll
       for (int nd = 0; nd < ND; nd += 2) {
-        o[nd][0] *= alpha[0];
-        o[nd][1] *= alpha[0];
-        o[nd][2] *= alpha[1];
-        o[nd][3] *= alpha[1];
-        o[nd + 1][0] *= alpha[0];
-        o[nd + 1][1] *= alpha[0];
-        o[nd + 1][2] *= alpha[1];
-        o[nd + 1][3] *= alpha[1];
         uint32_t vf[4];
-        ldmatrix_x4_trans(vf, vb + sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, nd + (lane >> 4)));
+        ldmatrix_x4_trans(vf, vb + tile_sw<D>((lane & 7) + ((lane >> 3) & 1) * 8, nd + (lane >> 4)));
         mma16<INT8>(o[nd], a, vf[0], vf[1]);
         mma16<INT8>(o[nd + 1], a, vf[2], vf[3]);
       }
     }
     __syncwarp();  // the stage is rewritten C::kStages stages on
+  }
+  if (aborted && lane == 0) {
+    // copies issued to slots no wait has looked at since are still in
+    // flight: let them land before the warp leaves
+    for (int i = consumed; i < issued; ++i)
+      (void)mbar_wait_bounded(&bars[i % C::kStages], (uint32_t)((i / C::kStages) & 1));
   }
   cp_async_wait_all();
   if (!appended) pdl_wait_primary();
@@ -1005,23 +1109,24 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
     l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
     l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
   }
-  float *ob = reinterpret_cast<float *>(rings);  // [warp][row][D]
-  float2 *ml = reinterpret_cast<float2 *>(ob + kPfWarps * 16 * D);  // [warp][row]
+  float *obuf = reinterpret_cast<float *>(rings);  // [warp][row][D]
+  float2 *ml = reinterpret_cast<float2 *>(obuf + kPfWarps * 16 * D);  // [warp][row]
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int r = (lane >> 2) + 8 * rr;
     if constexpr (INT8) {
-      // o is relative to 2^(m + dmo): bring it to 2^m; n-tiles 2 c and 2 c + 1
-      // hold the even and odd dimensions of chunk c, this lane's 16 c + 4t .. + 3
-      const float f = ex2_approx(dmo[rr]);
-      float *dst = ob + (warp * 16 + r) * D + 4 * (lane & 3);
+      // o, less its bias, is relative to 2^(m + dmo): bring it to 2^m; n-tiles
+      // 2 c and 2 c + 1 hold the even and odd dimensions of chunk c, this
+      // lane's 16 c + 4t .. + 3
+      const float f = ex2_approx(dmo[rr]), bias = ob[2 * rr];
+      float *dst = obuf + (warp * 16 + r) * D + 4 * (lane & 3);
 #pragma unroll
       for (int c = 0; c < D / 16; ++c)
         *reinterpret_cast<float4 *>(dst + 16 * c) =
-            make_float4(o[2 * c][2 * rr] * f, o[2 * c + 1][2 * rr] * f, o[2 * c][2 * rr + 1] * f,
-                        o[2 * c + 1][2 * rr + 1] * f);
+            make_float4((o[2 * c][2 * rr] - bias) * f, (o[2 * c + 1][2 * rr] - bias) * f,
+                        (o[2 * c][2 * rr + 1] - bias) * f, (o[2 * c + 1][2 * rr + 1] - bias) * f);
     } else {
-      float *dst = ob + (warp * 16 + r) * D + 2 * (lane & 3);
+      float *dst = obuf + (warp * 16 + r) * D + 2 * (lane & 3);
 #pragma unroll
       for (int nd = 0; nd < ND; ++nd)
         *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][2 * rr], o[nd][2 * rr + 1]);
@@ -1045,7 +1150,7 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
     for (int w = 0; w < kPfWarps; ++w) {
       const float2 st = ml[w * 16 + r];
       const float wt = ex2_approx(st.x - M);
-      const float2 ov = *reinterpret_cast<const float2 *>(ob + (w * 16 + r) * D + c);
+      const float2 ov = *reinterpret_cast<const float2 *>(obuf + (w * 16 + r) * D + c);
       L += wt * st.y;
       a0 += wt * ov.x;
       a1 += wt * ov.y;
@@ -1112,8 +1217,8 @@ __global__ void __launch_bounds__(kPfThreads) prefill_merge_kernel(const __grid_
 
 // a launch that may overlap the end of the stream's previous kernel (its
 // threads wait for that kernel with griddepcontrol.wait)
-template <typename K>
-cudaError_t launch_pdl(K kern, dim3 grid, int smem, cudaStream_t stream, const PrefillParams &p) {
+template <class K, class P>
+cudaError_t launch_pdl(K kern, dim3 grid, int smem, cudaStream_t stream, const P &p) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kPfThreads);
@@ -1145,7 +1250,13 @@ cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t stream) {
     err = cudaFuncSetAttribute(prefill_short_kernel<D, INT8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                S::kSmem);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(prefill_short_kernel<D, INT8>, grid, S::kSmem, stream, p);
+    PsParams sp;
+    sp.p = p;
+    const long long rows = (long long)p.num_pages * p.n_kvh * p.page_size;
+    if (!pool_tensor_map(&sp.tmap_k, p.k_pages, rows, D, INT8) ||
+        !pool_tensor_map(&sp.tmap_v, p.v_pages, rows, D, INT8))
+      return cudaErrorInvalidValue;  // the tensor map could not be encoded
+    err = launch_pdl(prefill_short_kernel<D, INT8>, grid, S::kSmem, stream, sp);
     if (err != cudaSuccess) return err;
   } else if (p.tc_tiles) {
     // long prompts over a bf16 cache: the tcgen05 kernel (prefill_tc.cu)
