@@ -179,12 +179,13 @@ def test_bad_page_and_overfull_sequence_are_reported():
     assert np.array_equal(pool_bits(d["v_pages"]), vp)
 
 
-@pytest.mark.parametrize("kind", ["prefill", "verify"])
+@pytest.mark.parametrize("kind", ["prefill", "verify", "verify_int8"])
 def test_benchmark_shapes_at_full_size(kind):
-    """The two shapes the benchmark times, drawn as it draws them (on the GPU,
+    """The shapes the benchmark times, drawn as it draws them (on the GPU,
     same seeds) and run with its workspace: 8 SmolLM3-shaped prompts of 2048
     tokens into empty caches, and 4 draft tokens over each of the Qwen3-shaped
-    batch's 64 caches.  Every pool bit for bit, every output row in tolerance."""
+    batch's 64 caches, bf16 and int8.  Every pool (and int8 scale) bit for bit,
+    every output row in tolerance."""
     import math
     if kind == "prefill":
         n_qh, n_kvh, d, theta = 16, 4, 128, 1e6
@@ -196,7 +197,8 @@ def test_benchmark_shapes_at_full_size(kind):
         ctx = q3.seq_lens.astype(np.int64)
         n_new = np.full(len(ctx), 4, np.int64)
     wl = W.make_workload("custom", seed=0, n_seq=len(ctx), n_qh=n_qh, n_kvh=n_kvh, head_dim=d,
-                         page_size=16, rope_theta=theta, kv_dtype="bf16",
+                         page_size=16, rope_theta=theta,
+                         kv_dtype="int8" if kind == "verify_int8" else "bf16",
                          lengths=[int(x) for x in ctx + n_new - 1], spare=0.05)
     dev = torch.device("cuda")
     t = W.make_tensors(wl, device=dev)
@@ -207,6 +209,8 @@ def test_benchmark_shapes_at_full_size(kind):
     vn = torch.randn((T, n_kvh, d), generator=g, device=dev).to(torch.bfloat16)
     h = {"q": bits(q), "k_new": bits(kn), "v_new": bits(vn), "k_pages": bits(t["k_pages"]),
          "v_pages": bits(t["v_pages"]), "block_table": wl.block_table.copy()}
+    if t.get("k_scales") is not None:
+        h["k_scales"], h["v_scales"] = bits(t["k_scales"]), bits(t["v_scales"])
     starts = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
     out = torch.full_like(q, float("nan"))
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -214,13 +218,18 @@ def test_benchmark_shapes_at_full_size(kind):
     K.kvattn_prefill(q, kn, vn, t["k_pages"], t["v_pages"], torch.from_numpy(wl.block_table).to(dev),
                      torch.from_numpy(starts).to(dev), torch.from_numpy(ctx.astype(np.int32)).to(dev),
                      out, rope_theta=theta, scale=1.0 / math.sqrt(d),
-                     max_new_tokens=int(n_new.max()), dev_status=st, workspace=ws)
+                     max_new_tokens=int(n_new.max()), k_scales=t.get("k_scales"),
+                     v_scales=t.get("v_scales"), dev_status=st, workspace=ws)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     ref, ost, kp, vp = oracle_prefill(h, starts, ctx, theta, 1.0 / math.sqrt(d))
     assert ost == 0
     assert np.array_equal(pool_bits(t["k_pages"]), kp)
     assert np.array_equal(pool_bits(t["v_pages"]), vp)
+    ks, vs = oracle_prefill.scales
+    if ks is not None:
+        assert np.array_equal(t["k_scales"].cpu().numpy().view(np.uint32), ks.view(np.uint32))
+        assert np.array_equal(t["v_scales"].cpu().numpy().view(np.uint32), vs.view(np.uint32))
     assert_close(out_f64(out), ref)
 
 
