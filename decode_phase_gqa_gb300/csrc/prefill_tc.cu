@@ -626,11 +626,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tc_mma_ts(d_o, a_p + (uint32_t)(8 * ks), vst + (uint64_t)(ks * 128), kIdPV, ks > 0 ? 1u : acc0);
         tc_commit(&o_done[hf]);
       };
-      // Per tile: both halves' P V(i) (each once its P(i) is written and V(i)
-      // has landed), then both halves' S(i + 1) (each once its P V(i) is done,
-      // since S(i + 1) overwrites P(i), and K(i + 1) has landed).  Half 0's
-      // softmax runs ahead of half 1's by about one S, so the tensor pipe
-      // takes half 1's products while half 0 computes its weights.
+      // Per tile, half by half: P V(i) of the half once its P(i) is written
+      // (and V(i) has landed), then its S(i + 1) once that P V(i) is done
+      // (S(i + 1) overwrites P(i)) and K(i + 1) has landed.  So a half's next
+      // scores never wait for the other half's weights: while one half's
+      // softmax works, the tensor pipe runs the other half's products
+      // (ping-pong).
       if (ok && n_tiles > 0) {
         ok = tc_wait(&k_full[0], 0, abort_flag, p);
         if (ok) {
@@ -642,26 +643,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       for (int i = 0; ok && i < n_tiles; ++i) {
         if (*abort_flag) break;
-        const int s = i % S;
+        const int s = i % S, s1 = (i + 1) % S;
+        const bool more = i + 1 < n_tiles;
         ok = tc_wait(&v_full[s], (uint32_t)((i / S) & 1), abort_flag, p);
         for (int hf = 0; hf < 2 && ok; ++hf) {
           ok = tc_wait(&p_full[hf], (uint32_t)(i & 1), abort_flag, p);
           if (!ok) break;
           tc_fence_after();
           issue_pv(i, hf);
-        }
-        if (!ok) break;
-        tc_commit(&v_empty[s]);  // both halves' P V(i) issued
-        if (i + 1 < n_tiles) {
-          const int s1 = (i + 1) % S;
-          ok = tc_wait(&k_full[s1], (uint32_t)(((i + 1) / S) & 1), abort_flag, p);
-          for (int hf = 0; hf < 2 && ok; ++hf) {
-            ok = tc_wait(&o_done[hf], (uint32_t)(i & 1), abort_flag, p);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(i + 1, hf);
-          }
-          if (ok) tc_commit(&k_empty[s1]);  // both halves' S(i + 1) issued
+          if (hf == 1) tc_commit(&v_empty[s]);  // both halves' P V(i) issued
+          if (!more) continue;
+          if (hf == 0) ok = tc_wait(&k_full[s1], (uint32_t)(((i + 1) / S) & 1), abort_flag, p);
+          if (ok) ok = tc_wait(&o_done[hf], (uint32_t)(i & 1), abort_flag, p);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(i + 1, hf);
+          if (hf == 1) tc_commit(&k_empty[s1]);  // both halves' S(i + 1) issued
         }
       }
       // every MMA issued has completed before the tensor memory is freed
