@@ -526,20 +526,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const bool is_v = warp == kTcSoftWarps + 1;
     pdl_wait_primary();  // the appended rows and the query rows are complete and visible
     prefetch_tensormap(is_v ? &tp.tmap_v : &tp.tmap_k);
-    if (!is_v && lane == 0) {
-      // both halves' query rows: a [32 tokens][64] box per head and 64-column
-      // block, rows 32 hh + tl of the half's tile (tokens past the new rows are
-      // another sequence's or, past n_tok, zeros: never stored)
-      mbar_arrive_expect_tx(q_ready, 2 * C::kQHalf);
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh)
-#pragma unroll
-          for (int r = 0; r < C::kRegions; ++r)
-            tma_load_3d_keep(qs + hf * C::kQHalf + r * C::kQRegion + hh * (kTcHalf * 128), &tp.tmap_q, 64 * r,
-                             h0 + hh, start + t0 + kTcHalf * hf, q_ready);
-    }
     uint64_t *ring_full = is_v ? v_full : k_full, *ring_empty = is_v ? v_empty : k_empty;
     uint8_t *ring = is_v ? vring : kring;
     volatile int *issued = is_v ? issued_v : issued_k;
@@ -598,6 +584,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       // V tiles, MN-major: rows of 64 d (one 128-byte swizzle atom across),
       // 8-key groups 1024 bytes apart, the next 64 d one region on
       const uint64_t dv = sw128_desc(smem_addr(vring), C::kKVRegion, 1024);
+      // both halves' query rows, issued here so that the K producer's first
+      // tile goes out at the same time: a [32 tokens][64] box per head and
+      // 64-column block, rows 32 hh + tl of the half's tile (tokens past the
+      // new rows are another sequence's or, past n_tok, zeros: never stored)
+      prefetch_tensormap(&tp.tmap_q);
+      mbar_arrive_expect_tx(q_ready, 2 * C::kQHalf);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_3d_keep(qs + hf * C::kQHalf + r * C::kQRegion + hh * (kTcHalf * 128), &tp.tmap_q, 64 * r,
+                             h0 + hh, start + t0 + kTcHalf * hf, q_ready);
       bool ok = tc_wait(q_ready, 0, abort_flag, p);
       tc_fence_after();
       auto issue_s = [&](int i, int hf) {

@@ -109,6 +109,20 @@ def test_long_prompts_without_splits(d):
     check(wl, h, starts, ctx, split=False)
 
 
+@pytest.mark.parametrize("split", [False, True])
+def test_more_prompt_tiles_than_sms(split):
+    """More 64-token query tiles than the GPU has SMs, so each CTA of the
+    persistent tensor-core kernel walks several of them (query rows reloaded,
+    tensor memory and rings reused, barrier phases carried on), with
+    prompts of 65..160 tokens over short cached prefixes and a page mix."""
+    rng = np.random.default_rng(29)
+    n = 180
+    ctx = [int(x) for x in rng.integers(0, 40, n)]
+    n_new = [int(x) for x in rng.integers(65, 161, n)]
+    wl, h, starts, ctx = make_case(4, 1, ctx, n_new, d=128, seed=29)
+    check(wl, h, starts, ctx, split=split)
+
+
 def test_long_prompt_eight_query_heads_per_kv_head():
     # a group of 8 query heads is two CTAs of 4 heads each
     wl, h, starts, ctx = make_case(16, 2, [0, 40], [400, 129], d=128, seed=17)
