@@ -378,14 +378,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     *issued_v = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+  __syncthreads();  // the barriers are initialised
+  // The tensor memory is allocated by warp 0 and its address shared with the
+  // softmax and MMA warps by a named barrier: the producers, which do not use
+  // it, start copying at once.
+  constexpr int kTmemUsers = 32 * (kTcSoftWarps + 1);
+  uint32_t tmem = 0;
+  if (warp < kTcSoftWarps || warp == kTcSoftWarps + 2) {
+    if (warp == 0) {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(kTmemUsers) : "memory");
+    tc_fence_after();
+    tmem = *tmem_slot;
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp < kTcSoftWarps) {
     // ---- softmax warps: one thread per row ------------------------------------
@@ -524,8 +532,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     // scores of tile i are done, V(i) once their P V products are, so the
     // next keys start loading well before the weighted sums end
     const bool is_v = warp == kTcSoftWarps + 1;
-    pdl_wait_primary();  // the appended rows and the query rows are complete and visible
     prefetch_tensormap(is_v ? &tp.tmap_v : &tp.tmap_k);
+    // pool row of each 16-key block of tile i (lanes 0-7); rows past the keys
+    // or on an out-of-range page are fetched from row -16, outside the view,
+    // which the copy fills with zeros (the block table is no output of the
+    // append grid: the first tile's rows are found before the wait on it)
+    auto pool_rows = [&](int i) {
+      int prow = -16;
+      if (lane < kTcKeys / 16) {
+        const int key = tile_at(i) * kTcKeys + 16 * lane;
+        if (key < n_keys) {
+          const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + (key >> p.page_shift));
+          if (pg >= 0 && pg < p.num_pages)
+            prow = (pg * p.n_kvh + j) * p.page_size + (key & (p.page_size - 1));
+          else if (!is_v)
+            report(p, KVATTN_DEV_BAD_PAGE);
+        }
+      }
+      return prow;
+    };
+    const int prow0 = n_tiles > 0 ? pool_rows(0) : -16;
+    pdl_wait_primary();  // the appended rows and the query rows are complete and visible
     uint64_t *ring_full = is_v ? v_full : k_full, *ring_empty = is_v ? v_empty : k_empty;
     uint8_t *ring = is_v ? vring : kring;
     volatile int *issued = is_v ? issued_v : issued_k;
@@ -538,20 +565,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     for (int i = 0; i < n_tiles; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int s = i % S;
-      // pool row of each 16-key block of the tile (lanes 0-7); rows past the
-      // keys or on an out-of-range page are fetched from row -16, outside the
-      // view, which the copy fills with zeros
-      int prow = -16;
-      if (lane < kTcKeys / 16) {
-        const int key = tile_at(i) * kTcKeys + 16 * lane;
-        if (key < n_keys) {
-          const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + (key >> p.page_shift));
-          if (pg >= 0 && pg < p.num_pages)
-            prow = (pg * p.n_kvh + j) * p.page_size + (key & (p.page_size - 1));
-          else if (!is_v)
-            report(p, KVATTN_DEV_BAD_PAGE);
-        }
-      }
+      const int prow = i == 0 ? prow0 : pool_rows(i);
       int rows[kTcKeys / 16];
 #pragma unroll
       for (int q8 = 0; q8 < kTcKeys / 16; ++q8) rows[q8] = __shfl_sync(0xffffffffu, prow, q8);
