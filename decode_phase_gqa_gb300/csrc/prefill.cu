@@ -941,11 +941,16 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
       // accumulators as they are.
       const uint32_t kc = kb, vc = vb;
       const float *scl = wscl + st * 2 * kPsWarpKeys;
-      float s[2][4];
+      // two accumulator chains per n-tile (k-steps c and c + 1), added at the
+      // end: half the dependent MMAs in a row
+      float s[2][4], s2[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s[nt][e] = kbias[e >> 1];
+        for (int e = 0; e < 4; ++e) {
+          s[nt][e] = kbias[e >> 1];
+          s2[nt][e] = 0.f;
+        }
 #pragma unroll
       for (int c = 0; c < D / 16; c += 2) {
         // matrices (keys 0-7, chunk c), (keys 0-7, c + 1), (keys 8-15, c),
@@ -954,13 +959,17 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         const int kr = (lane & 7) + ((lane >> 4) << 3), ch = c + ((lane >> 3) & 1);
         uint32_t r[4];
         ldmatrix_x4(r, kc + (uint32_t)(kr * D + cidx8<D>(kr, ch) * 16));
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t u0 = r[h2] ^ 0x80808080u, u1 = r[2 + h2] ^ 0x80808080u;
-          mma16<true>(s[0], qf[c + h2], codes_biased_f16x2(u0, 0x5140u), codes_biased_f16x2(u0, 0x5342u));
-          mma16<true>(s[1], qf[c + h2], codes_biased_f16x2(u1, 0x5140u), codes_biased_f16x2(u1, 0x5342u));
-        }
+        const uint32_t u00 = r[0] ^ 0x80808080u, u10 = r[2] ^ 0x80808080u;
+        const uint32_t u01 = r[1] ^ 0x80808080u, u11 = r[3] ^ 0x80808080u;
+        mma16<true>(s[0], qf[c], codes_biased_f16x2(u00, 0x5140u), codes_biased_f16x2(u00, 0x5342u));
+        mma16<true>(s[1], qf[c], codes_biased_f16x2(u10, 0x5140u), codes_biased_f16x2(u10, 0x5342u));
+        mma16<true>(s2[0], qf[c + 1], codes_biased_f16x2(u01, 0x5140u), codes_biased_f16x2(u01, 0x5342u));
+        mma16<true>(s2[1], qf[c + 1], codes_biased_f16x2(u11, 0x5140u), codes_biased_f16x2(u11, 0x5342u));
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
       float mx[2] = {-INFINITY, -INFINITY}, mxo[2] = {-INFINITY, -INFINITY};
       float xv[2][4];  // log2 vs, then the value-weight exponents
 #pragma unroll
