@@ -283,6 +283,21 @@ def test_appended_keys_over_many_positions(kv, d, theta):
     check_against_oracle(wl, h)
 
 
+@pytest.mark.parametrize("theta", [1e4, 1e6])
+def test_appended_keys_at_many_fast_path_positions(theta):
+    # 2048 sequences whose positions spread over [0, 2^18), where the stored
+    # key's angle is formed from the integer product pos * inv_freq and the
+    # float-float reduction: 131072 angles, every appended slot bit for bit
+    n = 2048
+    lens = list(np.random.default_rng(11).integers(0, 4, size=n))
+    wl, h = custom(4, 1, lens, d=128, seed=31, theta=theta)
+    pos = np.random.default_rng(13).integers(0, 1 << 18, size=n).astype(np.int32)
+    pos[:6] = [1, 2, 3, (1 << 18) - 1, 12345, 65536]
+    wl.positions = pos
+    h["positions"] = pos.copy()
+    check_against_oracle(wl, h)
+
+
 @pytest.mark.parametrize("kv", ["bf16", "int8"])
 def test_back_to_back_steps_see_the_previous_append(kv):
     # two decode steps queued on one stream with no other kernel between them:
