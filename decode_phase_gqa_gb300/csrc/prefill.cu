@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_append_kernel(const __grid
     const int own_w = (int)(max((it_w / p.n_kvh) * p.n_kvh, item0) - item0);  // first warp of w's token
     if (own_w != w || tok_slot[w] < 0) continue;
     float c, sn;
-    store_angle(tok_slot[w], inv_freq[i], table, c, sn);
+    store_angle_inl(tok_slot[w], inv_freq[i], table, c, sn);
     cs[w][i] = make_float2(c, sn);
   }
   __syncthreads();

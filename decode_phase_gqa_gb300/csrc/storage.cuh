@@ -127,8 +127,8 @@ static __device__ __noinline__ void angle_slow(double phi, float &c, float &s) {
 // of that double would round them.  `table` is a copy of kSinCosStep (in
 // shared memory: a lane-divergent read of global memory would queue behind
 // the SM's tile copies).
-static __device__ __noinline__ void store_angle(int pos, double inv_freq, const float4 *table, float &c,
-                                            float &s) {
+__device__ __forceinline__ void store_angle_inl(int pos, double inv_freq, const float4 *table, float &c,
+                                               float &s) {
   const double phi = (double)pos * inv_freq;
   // the quadrant from an fp32 estimate of phi (its error and that of the
   // product with 2/pi stay below 5 * 2^-24 phi): while phi < 2^18 the
@@ -189,6 +189,14 @@ static __device__ __noinline__ void store_angle(int pos, double inv_freq, const 
     }
   }
   if (slow) angle_slow(phi, c, s);
+}
+
+// The same out of line, so that the decode kernels carry one copy of it
+// (their latency-bound phases stalled on instruction fetch with more code);
+// the prefill append kernel, a short kernel run by many CTAs, inlines it.
+static __device__ __noinline__ void store_angle(int pos, double inv_freq, const float4 *table, float &c,
+                                            float &s) {
+  store_angle_inl(pos, inv_freq, table, c, s);
 }
 
 // Quantise one warp-held row of d fp32 values: int8 codes (lane's slots, in
