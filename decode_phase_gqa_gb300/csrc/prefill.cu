@@ -24,6 +24,7 @@
 #include <algorithm>
 #include <climits>
 #include <cmath>
+#include <type_traits>
 
 #include "prefill_common.cuh"
 #include "storage.cuh"
@@ -369,25 +370,43 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_attn_kernel(const __gri
   __syncthreads();
 
   // ---- the warp's 16 query rows: rotated in fp32, scaled, rounded to bf16 ----
+  // lane: row lane / 2, blocks of 8 dimension pairs (i, i + D / 2) from
+  // i0 = 8 (lane % 2 + 2 m), m < NB: all loads (16 bytes each) issued at once
   uint8_t *qw = qs + warp * kPfRows * C::kRowB;
-  for (int e = lane; e < kPfRows * (D / 2); e += 32) {
-    const int r = e / (D / 2), i = e % (D / 2);
-    float lo = 0.f, hi = 0.f;
-    if (t0 + r < n_new) {
-      const __nv_bfloat16 *qr = p.q + ((size_t)(start + t0 + r) * p.n_qh + h) * D;
-      lo = __bfloat162float(qr[i]);
-      hi = __bfloat162float(qr[i + D / 2]);
-      if (p.use_rope) {
-        float sn, cs;
-        sincospif(2.f * frac_turns(ctx + t0 + r, turns[i]), &sn, &cs);
-        const float a = lo * cs - hi * sn, bb = hi * cs + lo * sn;
-        lo = a;
-        hi = bb;
-      }
+  {
+    constexpr int NB = D / 32;
+    const int r = lane >> 1;
+    const bool has = t0 + r < n_new;
+    const __nv_bfloat16 *qr = p.q + ((size_t)(start + t0 + (has ? r : 0)) * p.n_qh + h) * D;
+    uint4 qlo[NB], qhi[NB];
+#pragma unroll
+    for (int m = 0; m < NB; ++m) {
+      const int i0 = 8 * ((lane & 1) + 2 * m);
+      qlo[m] = has ? __ldg(reinterpret_cast<const uint4 *>(qr + i0)) : make_uint4(0u, 0u, 0u, 0u);
+      qhi[m] = has ? __ldg(reinterpret_cast<const uint4 *>(qr + i0 + D / 2)) : make_uint4(0u, 0u, 0u, 0u);
     }
-    *reinterpret_cast<uint16_t *>(qw + sw<D>(r, i / 8) + (i % 8) * 2) = to16<INT8>(lo * p.qscale);
-    *reinterpret_cast<uint16_t *>(qw + sw<D>(r, (i + D / 2) / 8) + ((i + D / 2) % 8) * 2) =
-        to16<INT8>(hi * p.qscale);
+#pragma unroll
+    for (int m = 0; m < NB; ++m) {
+      const int i0 = 8 * ((lane & 1) + 2 * m);
+      const __nv_bfloat16 *lo16 = reinterpret_cast<const __nv_bfloat16 *>(&qlo[m]);
+      const __nv_bfloat16 *hi16 = reinterpret_cast<const __nv_bfloat16 *>(&qhi[m]);
+      uint16_t olo[8], ohi[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float lo = __bfloat162float(lo16[k]), hi = __bfloat162float(hi16[k]);
+        if (p.use_rope && has) {
+          float sn, cs;
+          sincospif(2.f * frac_turns(ctx + t0 + r, turns[i0 + k]), &sn, &cs);
+          const float a = lo * cs - hi * sn, bb = hi * cs + lo * sn;
+          lo = a;
+          hi = bb;
+        }
+        olo[k] = to16<INT8>(lo * p.qscale);
+        ohi[k] = to16<INT8>(hi * p.qscale);
+      }
+      *reinterpret_cast<uint4 *>(qw + sw<D>(r, i0 / 8)) = *reinterpret_cast<const uint4 *>(olo);
+      *reinterpret_cast<uint4 *>(qw + sw<D>(r, (i0 + D / 2) / 8)) = *reinterpret_cast<const uint4 *>(ohi);
+    }
   }
   __syncwarp();
   uint32_t qf[KS][4];  // A fragments: rows g, g + 8; k 2t.., 2t + 8..
@@ -821,30 +840,46 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
       }
     }
   };
+  // The 16 query rows (token r / 4, head h0 + r % 4), rotated and scaled: a
+  // thread takes row tid / 8 and the NP dimension pairs (i, i + D / 2) from
+  // i0 = NP (tid % 8): one vector load of each half, issued before the first
+  // stages' copies so that the loads overlap the block-table look-up (the
+  // latency of a row of dependent two-byte loads dominated the CTA's set-up).
+  constexpr int NP = D / 16;
+  static_assert(16 * (D / 2) == NP * kPfThreads, "a thread's pairs");
+  const int qr_r = tid >> 3, qr_i0 = (tid & 7) * NP, qr_t = qr_r >> 2;
+  using QVec = typename std::conditional<NP == 8, uint4, uint2>::type;
+  QVec qlo{}, qhi{};
+  if (qr_t < n_new) {
+    const __nv_bfloat16 *qr = p.q + ((size_t)(start + qr_t) * p.n_qh + h0 + (qr_r & 3)) * D + qr_i0;
+    qlo = __ldg(reinterpret_cast<const QVec *>(qr));
+    qhi = __ldg(reinterpret_cast<const QVec *>(qr + D / 2));
+  }
   // the first stages go out before the queries are formed
   int issued = 0;
   for (; issued < C::kStages - 1 && kt_begin + issued < kt_end; ++issued) load_part(kt_begin + issued, issued);
 
-  // ---- the 16 query rows (token r / 4, head h0 + r % 4): rotated, scaled ----
-  for (int e = tid; e < 16 * (D / 2); e += kPfThreads) {
-    const int r = e / (D / 2), i = e % (D / 2);
-    const int t = r >> 2;
-    float lo = 0.f, hi = 0.f;
-    if (t < n_new) {
-      const __nv_bfloat16 *qr = p.q + ((size_t)(start + t) * p.n_qh + h0 + (r & 3)) * D;
-      lo = __bfloat162float(qr[i]);
-      hi = __bfloat162float(qr[i + D / 2]);
-      if (p.use_rope) {
+  {
+    const __nv_bfloat16 *lo16 = reinterpret_cast<const __nv_bfloat16 *>(&qlo);
+    const __nv_bfloat16 *hi16 = reinterpret_cast<const __nv_bfloat16 *>(&qhi);
+    uint16_t olo[NP], ohi[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+      float lo = __bfloat162float(lo16[k]), hi = __bfloat162float(hi16[k]);
+      if (p.use_rope && qr_t < n_new) {
         float sn, cs;
-        sincospif(2.f * frac_turns(ctx + t, turns[i]), &sn, &cs);
+        sincospif(2.f * frac_turns(ctx + qr_t, turns[qr_i0 + k]), &sn, &cs);
         const float a = lo * cs - hi * sn, bb = hi * cs + lo * sn;
         lo = a;
         hi = bb;
       }
+      olo[k] = to16<INT8>(lo * p.qscale);
+      ohi[k] = to16<INT8>(hi * p.qscale);
     }
-    *reinterpret_cast<uint16_t *>(qs + sw<D>(r, i / 8) + (i % 8) * 2) = to16<INT8>(lo * p.qscale);
-    *reinterpret_cast<uint16_t *>(qs + sw<D>(r, (i + D / 2) / 8) + ((i + D / 2) % 8) * 2) =
-        to16<INT8>(hi * p.qscale);
+    // NP consecutive 16-bit values: a whole 16-byte chunk (d 128) or half of one
+    *reinterpret_cast<QVec *>(qs + sw<D>(qr_r, qr_i0 / 8) + (qr_i0 % 8) * 2) = *reinterpret_cast<const QVec *>(olo);
+    *reinterpret_cast<QVec *>(qs + sw<D>(qr_r, (qr_i0 + D / 2) / 8) + ((qr_i0 + D / 2) % 8) * 2) =
+        *reinterpret_cast<const QVec *>(ohi);
   }
   __syncthreads();
   uint32_t qf[KS][4];
