@@ -741,6 +741,9 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   const int g = p.n_qh / p.n_kvh;
   const int j = grp / (g / kPfWarps);
   const int h0 = j * g + (grp % (g / kPfWarps)) * kPfWarps;  // the quad's first head
+  // (the frequencies first: their load from the parameters overlaps the
+  // sequence's)
+  if (tid < 64) turns[tid] = p.turns[tid];
   int start, n_new, ctx;
   // Launched as the append kernel's programmatic dependent: the cached keys
   // (slots below ctx) are read while the append runs; a warp waits for the
@@ -764,7 +767,6 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   }
   const int per = (n_tiles + nz - 1) / nz;
   const int kt_begin = z * per, kt_end = min(n_tiles, kt_begin + per);
-  if (tid < 64) turns[tid] = p.turns[tid];
 
   const int wk = warp * kPsWarpKeys;  // the warp's keys within a stage
   uint8_t *ring = rings + warp * C::kRing;
@@ -840,45 +842,56 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
       }
     }
   };
-  // The 16 query rows (token r / 4, head h0 + r % 4), rotated and scaled: a
-  // thread takes row tid / 8 and the NP dimension pairs (i, i + D / 2) from
-  // i0 = NP (tid % 8): one vector load of each half, issued before the first
-  // stages' copies so that the loads overlap the block-table look-up (the
-  // latency of a row of dependent two-byte loads dominated the CTA's set-up).
-  constexpr int NP = D / 16;
-  static_assert(16 * (D / 2) == NP * kPfThreads, "a thread's pairs");
-  const int qr_r = tid >> 3, qr_i0 = (tid & 7) * NP, qr_t = qr_r >> 2;
-  using QVec = typename std::conditional<NP == 8, uint4, uint2>::type;
-  QVec qlo{}, qhi{};
-  if (qr_t < n_new) {
-    const __nv_bfloat16 *qr = p.q + ((size_t)(start + qr_t) * p.n_qh + h0 + (qr_r & 3)) * D + qr_i0;
-    qlo = __ldg(reinterpret_cast<const QVec *>(qr));
-    qhi = __ldg(reinterpret_cast<const QVec *>(qr + D / 2));
+  // The 16 query rows (token r / 4, head h0 + r % 4), rotated and scaled: warp
+  // t takes token t, a thread PP dimension pairs (i, i + D / 2) from
+  // i0 = PP lane for all four heads (one angle serves the four).  The loads
+  // go out before the first stages' copies and the angles are formed while
+  // they are in flight (the latency of a row of dependent two-byte loads
+  // dominated the CTA's set-up).
+  constexpr int PP = D / 64;
+  static_assert(16 * (D / 2) == 4 * PP * kPfThreads, "a thread's pairs");
+  using QVec = typename std::conditional<PP == 2, uint32_t, uint16_t>::type;
+  const int qt = warp, qi0 = lane * PP;
+  const bool qlive = qt < n_new;
+  QVec qlo[4], qhi[4];
+  {
+    const __nv_bfloat16 *qr = p.q + ((size_t)(start + (qlive ? qt : 0)) * p.n_qh + h0) * D + qi0;
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      qlo[hh] = qlive ? __ldg(reinterpret_cast<const QVec *>(qr + hh * D)) : QVec(0);
+      qhi[hh] = qlive ? __ldg(reinterpret_cast<const QVec *>(qr + hh * D + D / 2)) : QVec(0);
+    }
+  }
+  float qcs[PP], qsn[PP];
+#pragma unroll
+  for (int k = 0; k < PP; ++k) {
+    qcs[k] = 1.f;
+    qsn[k] = 0.f;
+    if (p.use_rope && qlive) sincospif(2.f * frac_turns(ctx + qt, turns[qi0 + k]), &qsn[k], &qcs[k]);
   }
   // the first stages go out before the queries are formed
   int issued = 0;
   for (; issued < C::kStages - 1 && kt_begin + issued < kt_end; ++issued) load_part(kt_begin + issued, issued);
 
-  {
-    const __nv_bfloat16 *lo16 = reinterpret_cast<const __nv_bfloat16 *>(&qlo);
-    const __nv_bfloat16 *hi16 = reinterpret_cast<const __nv_bfloat16 *>(&qhi);
-    uint16_t olo[NP], ohi[NP];
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
+  for (int hh = 0; hh < 4; ++hh) {
+    const __nv_bfloat16 *lo16 = reinterpret_cast<const __nv_bfloat16 *>(&qlo[hh]);
+    const __nv_bfloat16 *hi16 = reinterpret_cast<const __nv_bfloat16 *>(&qhi[hh]);
+    uint16_t olo[PP], ohi[PP];
+#pragma unroll
+    for (int k = 0; k < PP; ++k) {
       float lo = __bfloat162float(lo16[k]), hi = __bfloat162float(hi16[k]);
-      if (p.use_rope && qr_t < n_new) {
-        float sn, cs;
-        sincospif(2.f * frac_turns(ctx + qr_t, turns[qr_i0 + k]), &sn, &cs);
-        const float a = lo * cs - hi * sn, bb = hi * cs + lo * sn;
+      if (p.use_rope && qlive) {
+        const float a = lo * qcs[k] - hi * qsn[k], bb = hi * qcs[k] + lo * qsn[k];
         lo = a;
         hi = bb;
       }
       olo[k] = to16<INT8>(lo * p.qscale);
       ohi[k] = to16<INT8>(hi * p.qscale);
     }
-    // NP consecutive 16-bit values: a whole 16-byte chunk (d 128) or half of one
-    *reinterpret_cast<QVec *>(qs + sw<D>(qr_r, qr_i0 / 8) + (qr_i0 % 8) * 2) = *reinterpret_cast<const QVec *>(olo);
-    *reinterpret_cast<QVec *>(qs + sw<D>(qr_r, (qr_i0 + D / 2) / 8) + ((qr_i0 + D / 2) % 8) * 2) =
+    const int r = 4 * qt + hh;
+    *reinterpret_cast<QVec *>(qs + sw<D>(r, qi0 / 8) + (qi0 % 8) * 2) = *reinterpret_cast<const QVec *>(olo);
+    *reinterpret_cast<QVec *>(qs + sw<D>(r, (qi0 + D / 2) / 8) + ((qi0 + D / 2) % 8) * 2) =
         *reinterpret_cast<const QVec *>(ohi);
   }
   __syncthreads();
