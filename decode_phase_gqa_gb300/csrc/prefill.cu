@@ -1195,31 +1195,53 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   // prefill_merge_kernel (a warp per row there hides the loads' latency better
   // than the last split to finish merging, or a CTA per head quad)
   const bool direct = p.n_splits == 1;
-  for (int e = tid; e < 16 * (D / 2); e += kPfThreads) {
-    const int r = e / (D / 2), c = 2 * (e % (D / 2));
-    const int t = r >> 2, h = h0 + (r & 3);
-    if (t >= n_new || t >= kPsTok) continue;
+  // thread: row tid / 8 and columns cq + 32 k (cq = 4 (tid % 8)): the row's
+  // weights once, then every load of its columns at once
+  const int r = tid >> 3, cq = (tid & 7) * 4;
+  const int t = r >> 2, h = h0 + (r & 3);
+  if (t < n_new && t < kPsTok) {
+    float2 st[kPfWarps];
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kPfWarps; ++w) M = fmaxf(M, ml[w * 16 + r].x);
-    float L = 0.f, a0 = 0.f, a1 = 0.f;
+    for (int w = 0; w < kPfWarps; ++w) {
+      st[w] = ml[w * 16 + r];
+      M = fmaxf(M, st[w].x);
+    }
+    float wt[kPfWarps], L = 0.f;
 #pragma unroll
     for (int w = 0; w < kPfWarps; ++w) {
-      const float2 st = ml[w * 16 + r];
-      const float wt = ex2_approx(st.x - M);
-      const float2 ov = *reinterpret_cast<const float2 *>(obuf + (w * 16 + r) * D + c);
-      L += wt * st.y;
-      a0 += wt * ov.x;
-      a1 += wt * ov.y;
+      wt[w] = ex2_approx(st[w].x - M);
+      L += wt[w] * st[w].y;
     }
+    float4 acc[D / 32];
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kPfWarps; ++w)
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) {
+        const float4 ov = *reinterpret_cast<const float4 *>(obuf + (w * 16 + r) * D + cq + 32 * k);
+        acc[k].x += wt[w] * ov.x;
+        acc[k].y += wt[w] * ov.y;
+        acc[k].z += wt[w] * ov.z;
+        acc[k].w += wt[w] * ov.w;
+      }
     if (!direct) {
+      // (records are D + 2 floats: 8-byte aligned)
       float *rec = p.part + (((size_t)z * p.n_tok + start + t) * p.n_qh + h) * (D + 2);
-      *reinterpret_cast<float2 *>(rec + c) = make_float2(a0, a1);
-      if (c == 0) *reinterpret_cast<float2 *>(rec + D) = make_float2(M, L);
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) {
+        *reinterpret_cast<float2 *>(rec + cq + 32 * k) = make_float2(acc[k].x, acc[k].y);
+        *reinterpret_cast<float2 *>(rec + cq + 32 * k + 2) = make_float2(acc[k].z, acc[k].w);
+      }
+      if (cq == 0) *reinterpret_cast<float2 *>(rec + D) = make_float2(M, L);
     } else {
       const float f = L > 0.f ? 1.f / L : 0.f;
-      *reinterpret_cast<__nv_bfloat162 *>(p.out + ((size_t)(start + t) * p.n_qh + h) * D + c) =
-          __floats2bfloat162_rn(a0 * f, a1 * f);
+      __nv_bfloat16 *orow = p.out + ((size_t)(start + t) * p.n_qh + h) * D;
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k)
+        *reinterpret_cast<uint2 *>(orow + cq + 32 * k) =
+            make_uint2(pack_bf16(acc[k].x * f, acc[k].y * f), pack_bf16(acc[k].z * f, acc[k].w * f));
     }
   }
 }
