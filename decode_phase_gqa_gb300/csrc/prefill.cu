@@ -765,8 +765,21 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
     if (first_cta) pdl_wait_primary();
     return;
   }
-  const int per = (n_tiles + nz - 1) / nz;
-  const int kt_begin = z * per, kt_end = min(n_tiles, kt_begin + per);
+  // Split z takes stages [B(z), B(z + 1)), B(z) = n (1 - r^z) / (1 - r^nz)
+  // rounded, r = 3/4: each split a quarter shorter than the one before.  The
+  // grid is placed split by split, so the CTAs placed last, while the GPU
+  // drains, are the short ones (equal splits left a tail of whole splits
+  // started late).  A split may come out empty: it leaves an empty state.
+  const auto bound = [&](int zz) -> int {
+    if (zz >= nz) return n_tiles;
+    float pz = 1.f, pn = 1.f;
+    for (int k = 0; k < nz; ++k) {
+      if (k < zz) pz *= 0.75f;
+      pn *= 0.75f;
+    }
+    return (int)((float)n_tiles * ((1.f - pz) / (1.f - pn)) + 0.5f);
+  };
+  const int kt_begin = bound(z), kt_end = bound(z + 1);
 
   const int wk = warp * kPsWarpKeys;  // the warp's keys within a stage
   uint8_t *ring = rings + warp * C::kRing;
