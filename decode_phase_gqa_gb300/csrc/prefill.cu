@@ -1454,7 +1454,9 @@ extern "C" int kvattn_prefill(const void *q, const void *k_new, const void *v_ne
   p.tile_rows = short_chunks ? kPsTok : kPfRows;
   // Splits of a query tile's key tiles: short chunks over long contexts
   // (speculative verification, small decode-like chunks) share them among up
-  // to 16 CTAs, each with at least 16 tiles, so every context streams at once;
+  // to 16 CTAs (at least kPfMinTiles key tiles each; chunks of at most kPsTok
+  // tokens kPsMinTiles stages on average, in splits that shrink from one to
+  // the next), so every context streams at once;
   // long prompts, whose query tiles already fill the GPU, take one, as does a
   // call without a workspace.
   // Long prompts over a bf16 cache take the tcgen05 kernel (64-token query

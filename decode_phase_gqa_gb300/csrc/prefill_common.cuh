@@ -20,7 +20,7 @@ constexpr int kPsTok = 4;                    // new tokens a CTA (x 4 heads: the
 constexpr int kPsWarpKeys = 16;              // keys of a stage each warp takes
 constexpr int kPsKeys = kPfWarps * kPsWarpKeys;  // keys a stage holds
 constexpr int kPsStages = 2;
-constexpr int kPsMinTiles = 16;              // stages a split takes at least
+constexpr int kPsMinTiles = 20;              // stages a split takes, on average, at least
 
 // the tcgen05 attention kernel (prefill_tc.cu): 64 new tokens x 4 heads (two
 // halves of 128 MMA rows) a CTA, 128-key tiles, splits of at least 4 tiles
