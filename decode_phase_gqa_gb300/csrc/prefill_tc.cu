@@ -68,8 +68,8 @@ struct TcCfg {
   static constexpr int kVOff = kKOff + kStages * kTile;       // V ring [kStages][kTile]
   static constexpr int kBarOff = kVOff + kStages * kTile;
   // k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2],
-  // o_done[2], q_ready, mma_done
-  static constexpr int kNumBars = 4 * kStages + 8;
+  // o_done[2], q_ready, mma_done, out_bar[2]
+  static constexpr int kNumBars = 4 * kStages + 10;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;    // tmem base, abort flag, counters
   static constexpr int kSmem = kMiscOff + 64 + 1024;         // + slack for 1024-byte alignment
   static_assert(kSmem <= 227 * 1024, "shared memory");
@@ -246,6 +246,19 @@ __device__ __forceinline__ void tma_load_2d_keep(void *dst, const CUtensorMap *m
       : "memory");
 }
 
+// 3-D TMA tensor store of a box in shared memory (bulk group completion)
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's committed bulk stores have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // 3-D TMA tensor copy with the default L2 policy
 __device__ __forceinline__ void tma_load_3d_keep(void *dst, const CUtensorMap *map, int x, int y, int z,
                                                  uint64_t *bar) {
@@ -301,6 +314,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+  uint64_t *k_full = bars, *v_full = bars + S, *k_empty = bars + 2 * S, *v_empty = bars + 3 * S;
+  uint64_t *s_full = bars + 4 * S;  // [half]
+  uint64_t *p_full = s_full + 2;    // [half]
+  uint64_t *o_done = p_full + 2;    // [half]
+  uint64_t *q_ready = o_done + 2, *mma_done = q_ready + 1;
+  uint64_t *out_bar = mma_done + 1;  // [half]: its output rows are in shared memory
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+  uint32_t *tmem_slot = misc;                                 // [0]
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+  volatile int *issued_k = reinterpret_cast<volatile int *>(misc + 2);
+  volatile int *issued_v = reinterpret_cast<volatile int *>(misc + 3);
+  uint8_t *qs = smem + C::kQOff;
+  uint8_t *kring = smem + C::kKOff, *vring = smem + C::kVOff;
+
+  // (initialised first, while the sequence's lengths load; a CTA that leaves
+  // early never uses them)
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kTcRows);
+      mbar_init(&o_done[i], 1);
+      mbar_init(&out_bar[i], kTcRows);
+    }
+    mbar_init(q_ready, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    *issued_k = 0;
+    *issued_v = 0;
+    fence_barrier_init();
+  }
+
   // CTA x: head quad x % G, then sequence, then query tile from the last (the
   // tiles with the most keys start first)
   const int G = p.n_qh / kPfWarps;
@@ -345,39 +396,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   const int rot = n_tiles > 1 ? (int)(((unsigned)qt * 5u + (unsigned)grp) % (unsigned)n_tiles) : 0;
   const auto tile_at = [&](int i) { return kt0 + (i + rot < n_tiles ? i + rot : i + rot - n_tiles); };
 
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
-  uint64_t *k_full = bars, *v_full = bars + S, *k_empty = bars + 2 * S, *v_empty = bars + 3 * S;
-  uint64_t *s_full = bars + 4 * S;  // [half]
-  uint64_t *p_full = s_full + 2;    // [half]
-  uint64_t *o_done = p_full + 2;    // [half]
-  uint64_t *q_ready = o_done + 2, *mma_done = q_ready + 1;
-  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
-  uint32_t *tmem_slot = misc;                                 // [0]
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
-  volatile int *issued_k = reinterpret_cast<volatile int *>(misc + 2);
-  volatile int *issued_v = reinterpret_cast<volatile int *>(misc + 3);
-  uint8_t *qs = smem + C::kQOff;
-  uint8_t *kring = smem + C::kKOff, *vring = smem + C::kVOff;
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], kTcRows);
-      mbar_init(&o_done[i], 1);
-    }
-    mbar_init(q_ready, 1);
-    mbar_init(mma_done, 1);
-    *abort_flag = 0;
-    *issued_k = 0;
-    *issued_v = 0;
-    fence_barrier_init();
-  }
   __syncthreads();  // the barriers are initialised
   // The tensor memory is allocated by warp 0 and its address shared with the
   // softmax and MMA warps by a named barrier: the producers, which do not use
@@ -500,8 +518,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         __nv_bfloat16 *dst = p.out + ((size_t)(start + (live ? t : 0)) * p.n_qh + h) * D;
         float *rec = p.part + (((size_t)z * p.n_tok + start + (live ? t : 0)) * p.n_qh + h) * (D + 2);
         const bool split = p.n_splits > 1;
+        // A half whose 32 tokens are all this sequence's new rows (so a whole
+        // box is the CTA's own) leaves its bf16 rows in shared memory, where
+        // its query rows were (the last scores are complete), in the query
+        // copies' swizzled layout, and one thread writes them out with the
+        // same tensor map: whole lines instead of each thread's 16-byte pieces
+        // of rows 4 KB apart.
+        const bool boxed = !split && n_tiles > 0 && t0 + kTcHalf * (hf + 1) <= n_rows_tok;
+        if (boxed) {
+          uint8_t *qrow = qs + hf * C::kQHalf + wq * (kTcHalf * 128) + lane * 128;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float o[32];
+            tmem_ld32(lane_base + kOCol + (uint32_t)c0, o);
+#pragma unroll
+            for (int k = 0; k < 32; k += 8) {
+              const int c = (c0 + k) / 8;  // 16-byte chunk of the row: block c / 8, chunk c % 8 in it
+              const uint4 v = make_uint4(pack_bf16(o[k] * f, o[k + 1] * f), pack_bf16(o[k + 2] * f, o[k + 3] * f),
+                                         pack_bf16(o[k + 4] * f, o[k + 5] * f), pack_bf16(o[k + 6] * f, o[k + 7] * f));
+              *reinterpret_cast<uint4 *>(qrow + (c >> 3) * C::kQRegion + (((c & 7) ^ (lane & 7)) << 4)) = v;
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&out_bar[hf]);  // (release: the row is visible)
+          if (wq == 0 && lane == 0 && tc_wait(&out_bar[hf], 0, abort_flag, p)) {
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+              for (int r = 0; r < C::kRegions; ++r)
+                tma_store_3d(&tp.tmap_q, qs + hf * C::kQHalf + r * C::kQRegion + hh * (kTcHalf * 128), 64 * r,
+                             h0 + hh, start + t0 + kTcHalf * hf);
+            bulk_commit();
+            bulk_wait_read_all();  // the rows are read before the shared memory is given up
+          }
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < D && !boxed; c0 += 32) {
           float o[32];
           if (n_tiles > 0) {
             tmem_ld32(lane_base + kOCol + (uint32_t)c0, o);
