@@ -292,17 +292,46 @@ __device__ __forceinline__ float2 ex2_pair(float x0, float x1) {
   return __half22float2(eh);
 }
 
-// Largest of N values, as a tree (no chain of N dependent operations)
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// Largest of N values: a tree of three-input maxima (N / 2 instructions, no
+// long chain of dependent ones)
 template <int N>
-__device__ __forceinline__ float tree_max(const float (&s)[N]) {
-  float t[N / 4];
+__device__ __forceinline__ float max_of(const float (&s)[N]) {
+  float t[(N + 2) / 3];
+  constexpr int M = N / 3;
 #pragma unroll
-  for (int k = 0; k < N / 4; ++k) t[k] = fmaxf(fmaxf(s[4 * k], s[4 * k + 1]), fmaxf(s[4 * k + 2], s[4 * k + 3]));
-#pragma unroll
-  for (int w = N / 8; w >= 1; w >>= 1)
-#pragma unroll
-    for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
-  return t[0];
+  for (int k = 0; k < M; ++k) t[k] = max3f(s[3 * k], s[3 * k + 1], s[3 * k + 2]);
+  if constexpr (N % 3 == 1) t[M] = s[N - 1];
+  if constexpr (N % 3 == 2) t[M] = fmaxf(s[N - 2], s[N - 1]);
+  if constexpr ((N + 2) / 3 == 1) {
+    return t[0];
+  } else {
+    return max_of<(N + 2) / 3>(t);
+  }
+}
+
+// (x0 - m, x1 - m) and a + b by packed fp32 instructions, rounded as two
+// scalar ones
+__device__ __forceinline__ float2 sub_f32x2(float x0, float x1, float m) {
+  float2 o;
+  asm("{\n\t.reg .b64 x, y, r;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\t"
+      "sub.rn.f32x2 r, x, y;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(o.x), "=f"(o.y)
+      : "f"(x0), "f"(x1), "f"(m));
+  return o;
+}
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
+  float2 o;
+  asm("{\n\t.reg .b64 x, y, r;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "add.rn.f32x2 r, x, y;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(o.x), "=f"(o.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return o;
 }
 
 template <int D>
@@ -450,7 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           sc[c] = ok ? sc[c] : -INFINITY;
         }
       }
-      const float m_new = fmaxf(m_run, tree_max<kTcKeys>(sc));
+      const float m_new = fmaxf(m_run, max_of<kTcKeys>(sc));
       const bool need = m_new > m_run + 8.f;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.f;
       if (need) {
@@ -476,21 +505,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       // P = 2^(S - m) as bf16 pairs over the first 64 columns of S (column c:
       // keys 2c, 2c + 1), in one store; the weights come two by two from the
-      // f16 exponential (half the special-function operations of fp32 ones,
-      // which bound this loop); the normaliser sums them as computed, in
-      // eight partial sums
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // f16 exponential (half the special-function operations of fp32 ones),
+      // the differences and the normaliser's sums two by two from packed fp32
+      // arithmetic (one instruction a pair: the chain of this loop is what a
+      // tile waits for), the sums in four partial pairs
+      float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
       {
         uint32_t pw[kTcKeys / 2];
 #pragma unroll
         for (int c = 0; c < kTcKeys / 2; ++c) {
-          const float2 e = ex2_pair(sc[2 * c] - m_run, sc[2 * c + 1] - m_run);
-          ls[c & 7] += e.x + e.y;
+          const float2 d = sub_f32x2(sc[2 * c], sc[2 * c + 1], m_run);
+          const float2 e = ex2_pair(d.x, d.y);
+          ls[c & 3] = add_f32x2(ls[c & 3], e);
           pw[c] = pack_bf16(e.x, e.y);
         }
         tmem_st64u(lane_base, pw);
       }
-      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      l_run += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
       // O holds the products of tiles < i, all complete: the MMA thread issued
       // S(i) only after them.  Rescale this warp's rows when a maximum moved.
       if (i > 0 && __any_sync(0xffffffffu, need)) {
