@@ -1027,22 +1027,42 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         mma16<true>(s2[0], qf[c + 1], codes_biased_f16x2(u01, 0x5140u), codes_biased_f16x2(u01, 0x5342u));
         mma16<true>(s2[1], qf[c + 1], codes_biased_f16x2(u11, 0x5140u), codes_biased_f16x2(u11, 0x5342u));
       }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
-      float mx[2] = {-INFINITY, -INFINITY}, mxo[2] = {-INFINITY, -INFINITY};
+      // Lane (g, t) holds rows g, g + 8 (e / 2) at keys kr = 8 nt + 2t, + 1
+      // (e % 2): each pair of a row shares its keys' scales (one 8-byte load
+      // each), so the pair arithmetic is packed; a stage whose keys are all
+      // cached ones (every row sees them) skips the causal mask.
+      const bool whole = key0 + kPsWarpKeys - 1 <= ctx;
       float xv[2][4];  // log2 vs, then the value-weight exponents
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt) {
+        const int kr = nt * 8 + 2 * (lane & 3);
+        const float2 ks = *reinterpret_cast<const float2 *>(scl + kr);
+        const float2 vs = *reinterpret_cast<const float2 *>(scl + kPsWarpKeys + kr);
+        const float lv0 = lg2_approx(vs.x), lv1 = lg2_approx(vs.y);
+        // (the two accumulator chains added first)
+        const float2 a01 =
+            mul_f32x2(add_f32x2(make_float2(s[nt][0], s[nt][1]), make_float2(s2[nt][0], s2[nt][1])), ks);
+        const float2 a23 =
+            mul_f32x2(add_f32x2(make_float2(s[nt][2], s[nt][3]), make_float2(s2[nt][2], s2[nt][3])), ks);
+        s[nt][0] = a01.x;
+        s[nt][1] = a01.y;
+        s[nt][2] = a23.x;
+        s[nt][3] = a23.y;
+        xv[nt][0] = lv0;
+        xv[nt][1] = lv1;
+        xv[nt][2] = lv0;
+        xv[nt][3] = lv1;
+        if (!whole) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
-          const bool ok = key0 + kr <= qpos[e >> 1];  // (keys past n_keys: past qpos)
-          s[nt][e] = ok ? s[nt][e] * scl[kr] : -INFINITY;
-          xv[nt][e] = ok ? lg2_approx(scl[kPsWarpKeys + kr]) : -INFINITY;
-          mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+          for (int e = 0; e < 4; ++e)
+            if (key0 + kr + (e & 1) > qpos[e >> 1]) {  // (keys past n_keys: past qpos)
+              s[nt][e] = -INFINITY;
+              xv[nt][e] = -INFINITY;
+            }
         }
+      }
+      float mx[2] = {fmaxf(max3f(s[0][0], s[0][1], s[1][0]), s[1][1]),
+                     fmaxf(max3f(s[0][2], s[0][3], s[1][2]), s[1][3])};
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
@@ -1053,13 +1073,21 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
           m[rr] = mx[rr];
         }
       }
+      // d = S - m, pair by pair; the value-weight exponents log2 vs + d
+      float2 dd[2][2];  // [nt][row]
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          xv[nt][e] += s[nt][e] - m[e >> 1];
-          mxo[e >> 1] = fmaxf(mxo[e >> 1], xv[nt][e]);
-        }
+      for (int nt = 0; nt < 2; ++nt) {
+        dd[nt][0] = sub_f32x2(s[nt][0], s[nt][1], m[0]);
+        dd[nt][1] = sub_f32x2(s[nt][2], s[nt][3], m[1]);
+        const float2 x01 = add_f32x2(make_float2(xv[nt][0], xv[nt][1]), dd[nt][0]);
+        const float2 x23 = add_f32x2(make_float2(xv[nt][2], xv[nt][3]), dd[nt][1]);
+        xv[nt][0] = x01.x;
+        xv[nt][1] = x01.y;
+        xv[nt][2] = x23.x;
+        xv[nt][3] = x23.y;
+      }
+      float mxo[2] = {fmaxf(max3f(xv[0][0], xv[0][1], xv[1][0]), xv[1][1]),
+                      fmaxf(max3f(xv[0][2], xv[0][3], xv[1][2]), xv[1][3])};
       float alpha_o[2] = {1.f, 1.f};
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
@@ -1070,15 +1098,17 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
           dmo[rr] = mxo[rr];
         }
       }
+      // the normaliser from fp32 exponentials; the value weights as f16 pairs
+      // (the MMA's A fragment: rows g, g + 8 x keys 2t, 2t + 1 of each n-tile)
+      // straight from the f16 exponential, at most 2^kLazy
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          l[e >> 1] += ex2_approx(s[nt][e] - m[e >> 1]);
-          xv[nt][e] = ex2_approx(xv[nt][e] - dmo[e >> 1]);
-        }
-      const uint32_t a[4] = {pack16<true>(xv[0][0], xv[0][1]), pack16<true>(xv[0][2], xv[0][3]),
-                             pack16<true>(xv[1][0], xv[1][1]), pack16<true>(xv[1][2], xv[1][3])};
+      for (int rr = 0; rr < 2; ++rr)
+        l[rr] += (ex2_approx(dd[0][rr].x) + ex2_approx(dd[0][rr].y)) +
+                 (ex2_approx(dd[1][rr].x) + ex2_approx(dd[1][rr].y));
+      const uint32_t a[4] = {ex2_f16x2(xv[0][0] - dmo[0], xv[0][1] - dmo[0]),
+                             ex2_f16x2(xv[0][2] - dmo[1], xv[0][3] - dmo[1]),
+                             ex2_f16x2(xv[1][0] - dmo[0], xv[1][1] - dmo[0]),
+                             ex2_f16x2(xv[1][2] - dmo[1], xv[1][3] - dmo[1])};
       if (__any_sync(0xffffffffu, alpha_o[0] != 1.f || alpha_o[1] != 1.f)) {
 #pragma unroll
         for (int nd = 0; nd < ND; ++nd)

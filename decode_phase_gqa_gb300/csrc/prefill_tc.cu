@@ -292,12 +292,6 @@ __device__ __forceinline__ float2 ex2_pair(float x0, float x1) {
   return __half22float2(eh);
 }
 
-// max(a, b, c) in one instruction
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
 // Largest of N values: a tree of three-input maxima (N / 2 instructions, no
 // long chain of dependent ones)
 template <int N>
@@ -313,25 +307,6 @@ __device__ __forceinline__ float max_of(const float (&s)[N]) {
   } else {
     return max_of<(N + 2) / 3>(t);
   }
-}
-
-// (x0 - m, x1 - m) and a + b by packed fp32 instructions, rounded as two
-// scalar ones
-__device__ __forceinline__ float2 sub_f32x2(float x0, float x1, float m) {
-  float2 o;
-  asm("{\n\t.reg .b64 x, y, r;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\t"
-      "sub.rn.f32x2 r, x, y;\n\tmov.b64 {%0, %1}, r;\n\t}"
-      : "=f"(o.x), "=f"(o.y)
-      : "f"(x0), "f"(x1), "f"(m));
-  return o;
-}
-__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
-  float2 o;
-  asm("{\n\t.reg .b64 x, y, r;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-      "add.rn.f32x2 r, x, y;\n\tmov.b64 {%0, %1}, r;\n\t}"
-      : "=f"(o.x), "=f"(o.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return o;
 }
 
 template <int D>
