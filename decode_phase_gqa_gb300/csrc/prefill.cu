@@ -808,8 +808,8 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
   // The warp's 16 keys of stage kt (one page: pages hold 16 keys or more)
   // into ring slot s: TMA boxes of K and V (the 16 rows of the page slots;
   // rows past the keys come as the pool holds them and are masked, bf16 V
-  // rows zeroed), the int8 row scales by 16-byte copies the slot's barrier
-  // tracks.  Called for kt = kt_begin, kt_begin + 1, ... in order, by the
+  // rows zeroed), the int8 row scales by two bulk copies, all on the slot's
+  // barrier.  Called for kt = kt_begin, kt_begin + 1, ... in order, by the
   // whole warp.
   auto load_part = [&](int kt, int s) {
     const int key = kt * kPsKeys + wk;
@@ -830,20 +830,19 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         report(p, KVATTN_DEV_BAD_PAGE);
     }
     bad = row >= 0 ? bad & ~(1u << s) : bad | (1u << s);
-    if constexpr (INT8) {
-      if (row >= 0 && lane < 8) {
-        cp_async_16(wscl + s * 2 * kPsWarpKeys + 4 * lane,
-                    (lane < 4 ? p.k_scales : p.v_scales) + row + 4 * (lane & 3));
-        cp_async_mbar_arrive(&bars[s]);
-      }
-      __syncwarp();
-    }
     __syncwarp();  // every lane is done with the slot (and its bf16 zeroing)
     if (lane == 0) {
       if (row >= 0) {
         fence_proxy_async_smem();  // those generic accesses before the copy's writes
         uint8_t *dst = ring + s * C::kStage;
-        mbar_arrive_expect_tx(&bars[s], C::kStage);
+        mbar_arrive_expect_tx(&bars[s], C::kStage + (INT8 ? 2 * kPsWarpKeys * 4 : 0));
+        if constexpr (INT8) {
+          // the 16 rows' key and value scales: 64 bytes each, 64-byte aligned
+          // (the warp's 16 keys start a 16-row block of the page)
+          float *ws = wscl + s * 2 * kPsWarpKeys;
+          bulk_g2s(ws, p.k_scales + row, kPsWarpKeys * 4, &bars[s], pol);
+          bulk_g2s(ws + kPsWarpKeys, p.v_scales + row, kPsWarpKeys * 4, &bars[s], pol);
+        }
 #pragma unroll
         for (int r = 0; r < C::kRegions; ++r) {
           const int x = r * C::kBoxB / (INT8 ? 1 : 2);  // element column of box r
