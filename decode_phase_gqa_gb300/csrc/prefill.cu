@@ -1097,17 +1097,20 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
           dmo[rr] = mxo[rr];
         }
       }
-      // the normaliser from fp32 exponentials; the value weights as f16 pairs
-      // (the MMA's A fragment: rows g, g + 8 x keys 2t, 2t + 1 of each n-tile)
-      // straight from the f16 exponential, at most 2^kLazy
+      // the normaliser and the value weights from fp32 exponentials (an f16
+      // pair exponential measured no faster); the weights, at most 2^kLazy, as
+      // f16 pairs: the MMA's A fragment, rows g, g + 8 x keys 2t, 2t + 1 of
+      // each n-tile (q: n-tile q / 2, row q % 2)
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr)
         l[rr] += (ex2_approx(dd[0][rr].x) + ex2_approx(dd[0][rr].y)) +
                  (ex2_approx(dd[1][rr].x) + ex2_approx(dd[1][rr].y));
-      const uint32_t a[4] = {ex2_f16x2(xv[0][0] - dmo[0], xv[0][1] - dmo[0]),
-                             ex2_f16x2(xv[0][2] - dmo[1], xv[0][3] - dmo[1]),
-                             ex2_f16x2(xv[1][0] - dmo[0], xv[1][1] - dmo[0]),
-                             ex2_f16x2(xv[1][2] - dmo[1], xv[1][3] - dmo[1])};
+      uint32_t a[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 w = sub_f32x2(xv[q >> 1][2 * (q & 1)], xv[q >> 1][2 * (q & 1) + 1], dmo[q & 1]);
+        a[q] = pack16<true>(ex2_approx(w.x), ex2_approx(w.y));
+      }
       if (__any_sync(0xffffffffu, alpha_o[0] != 1.f || alpha_o[1] != 1.f)) {
 #pragma unroll
         for (int nd = 0; nd < ND; ++nd)

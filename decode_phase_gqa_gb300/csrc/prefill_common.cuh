@@ -51,7 +51,7 @@ struct PrefillParams {
   double inv_freq[64];
 };
 
-// ---- packed fp32 / f16 arithmetic (one instruction for a pair) ----------------
+// ---- packed fp32 arithmetic (one instruction for a pair) ----------------------
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
@@ -84,16 +84,6 @@ __device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return o;
 }
-// 2^x0, 2^x1 (x <= 15 or -inf) as an f16 pair (x0 in the low half) from one
-// special-function operation: the arguments are rounded to f16 first (at
-// |x| < 8 that moves 2^x by less than 0.14 %)
-__device__ __forceinline__ uint32_t ex2_f16x2(float x0, float x1) {
-  uint32_t h, e;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
-  return e;
-}
-
 __device__ __forceinline__ void report(const PrefillParams &p, uint32_t bits) {
   if (p.status) atomicOr(p.status, bits);
 }

@@ -279,19 +279,6 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
   return false;
 }
 
-// 2^x0 and 2^x1 (x <= 8 or -inf) from one special-function operation on an
-// f16 pair: the arguments are rounded to f16 (11-bit significand; at |x| < 8
-// that moves 2^x by less than 0.14 %, and where |x| is larger the weight is
-// below 2^-8), the results carry about 10 bits, more than the bf16 the
-// weights are rounded to for the MMA
-__device__ __forceinline__ float2 ex2_pair(float x0, float x1) {
-  uint32_t h, e;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
-  const __half2 eh = *reinterpret_cast<const __half2 *>(&e);
-  return __half22float2(eh);
-}
-
 // Largest of N values: a tree of three-input maxima (N / 2 instructions, no
 // long chain of dependent ones)
 template <int N>
@@ -479,18 +466,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         fence_proxy_async_smem();
       }
       // P = 2^(S - m) as bf16 pairs over the first 64 columns of S (column c:
-      // keys 2c, 2c + 1), in one store; the weights come two by two from the
-      // f16 exponential (half the special-function operations of fp32 ones),
-      // the differences and the normaliser's sums two by two from packed fp32
-      // arithmetic (one instruction a pair: the chain of this loop is what a
-      // tile waits for), the sums in four partial pairs
+      // keys 2c, 2c + 1), in one store; the differences and the normaliser's
+      // sums two by two from packed fp32 arithmetic (one instruction a pair:
+      // the chain of this loop is what a tile waits for), the sums in four
+      // partial pairs.  fp32 exponentials: the f16 pair exponential takes half
+      // the special-function operations but three conversions a pair more,
+      // which made the chain longer (0.214 against 0.207 ms a prompt batch).
       float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
       {
         uint32_t pw[kTcKeys / 2];
 #pragma unroll
         for (int c = 0; c < kTcKeys / 2; ++c) {
           const float2 d = sub_f32x2(sc[2 * c], sc[2 * c + 1], m_run);
-          const float2 e = ex2_pair(d.x, d.y);
+          const float2 e = make_float2(ex2_approx(d.x), ex2_approx(d.y));
           ls[c & 3] = add_f32x2(ls[c & 3], e);
           pw[c] = pack_bf16(e.x, e.y);
         }
