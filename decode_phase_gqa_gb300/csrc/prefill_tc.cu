@@ -68,8 +68,8 @@ struct TcCfg {
   static constexpr int kVOff = kKOff + kStages * kTile;       // V ring [kStages][kTile]
   static constexpr int kBarOff = kVOff + kStages * kTile;
   // k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2],
-  // o_done[2], q_ready, mma_done, out_bar[2]
-  static constexpr int kNumBars = 4 * kStages + 10;
+  // o_done[2], q_ready[2], mma_done, out_bar[2]
+  static constexpr int kNumBars = 4 * kStages + 11;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;    // tmem base, abort flag, counters
   static constexpr int kSmem = kMiscOff + 64 + 1024;         // + slack for 1024-byte alignment
   static_assert(kSmem <= 227 * 1024, "shared memory");
@@ -310,7 +310,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   uint64_t *s_full = bars + 4 * S;  // [half]
   uint64_t *p_full = s_full + 2;    // [half]
   uint64_t *o_done = p_full + 2;    // [half]
-  uint64_t *q_ready = o_done + 2, *mma_done = q_ready + 1;
+  uint64_t *q_ready = o_done + 2;  // [half]: its query rows have landed
+  uint64_t *mma_done = q_ready + 2;
   uint64_t *out_bar = mma_done + 1;  // [half]: its output rows are in shared memory
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
   uint32_t *tmem_slot = misc;                                 // [0]
@@ -335,7 +336,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       mbar_init(&o_done[i], 1);
       mbar_init(&out_bar[i], kTcRows);
     }
-    mbar_init(q_ready, 1);
+    mbar_init(&q_ready[0], 1);
+    mbar_init(&q_ready[1], 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     *issued_k = 0;
@@ -648,18 +650,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       // tile goes out at the same time: a [32 tokens][64] box per head and
       // 64-column block, rows 32 hh + tl of the half's tile (tokens past the
       // new rows are another sequence's or, past n_tok, zeros: never stored)
+      // (a barrier a half: half 0's first scores need only its own rows)
       prefetch_tensormap(&tp.tmap_q);
-      mbar_arrive_expect_tx(q_ready, 2 * C::kQHalf);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
+      for (int hf = 0; hf < 2; ++hf) {
+        mbar_arrive_expect_tx(&q_ready[hf], C::kQHalf);
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh)
 #pragma unroll
           for (int r = 0; r < C::kRegions; ++r)
             tma_load_3d_keep(qs + hf * C::kQHalf + r * C::kQRegion + hh * (kTcHalf * 128), &tp.tmap_q, 64 * r,
-                             h0 + hh, start + t0 + kTcHalf * hf, q_ready);
-      bool ok = tc_wait(q_ready, 0, abort_flag, p);
-      tc_fence_after();
+                             h0 + hh, start + t0 + kTcHalf * hf, &q_ready[hf]);
+      }
+      bool ok = true;
       auto issue_s = [&](int i, int hf) {
         const int s = i % S;
         const uint64_t kst = dk + (uint64_t)((s * C::kTile) >> 4);
@@ -692,14 +695,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       // scores never wait for the other half's weights: while one half's
       // softmax works, the tensor pipe runs the other half's products
       // (ping-pong).
-      if (ok && n_tiles > 0) {
-        ok = tc_wait(&k_full[0], 0, abort_flag, p);
+      if (n_tiles > 0) {
+        ok = tc_wait(&q_ready[0], 0, abort_flag, p) && tc_wait(&k_full[0], 0, abort_flag, p);
         if (ok) {
           tc_fence_after();
           issue_s(0, 0);
+          ok = tc_wait(&q_ready[1], 0, abort_flag, p);
+        }
+        if (ok) {
+          tc_fence_after();
           issue_s(0, 1);
           tc_commit(&k_empty[0]);  // both halves' scores of tile 0 issued
         }
+      } else {
+        // (no tiles: the query copies land before the CTA leaves)
+        ok = tc_wait(&q_ready[0], 0, abort_flag, p) && tc_wait(&q_ready[1], 0, abort_flag, p);
       }
       for (int i = 0; ok && i < n_tiles; ++i) {
         if (*abort_flag) break;
@@ -734,6 +744,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const int nk = *issued_k, nv = *issued_v;
     for (int i = max(0, nk - S); i < nk; ++i) (void)mbar_wait_bounded(&k_full[i % S], (uint32_t)((i / S) & 1));
     for (int i = max(0, nv - S); i < nv; ++i) (void)mbar_wait_bounded(&v_full[i % S], (uint32_t)((i / S) & 1));
+    (void)mbar_wait_bounded(&q_ready[0], 0);
+    (void)mbar_wait_bounded(&q_ready[1], 0);
   }
   __syncthreads();
   tc_fence_after();
