@@ -1147,16 +1147,17 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
         mma16<INT8>(s[0], qf[ks], kf[0], kf[1]);
         mma16<INT8>(s[1], qf[ks], kf[2], kf[3]);
       }
-      float mx[2] = {-INFINITY, -INFINITY};
+      // the causal mask, skipped on a stage whose keys are all cached ones
+      if (key0 + kPsWarpKeys - 1 > ctx) {
   #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
   #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int kr = nt * 8 + 2 * (lane & 3) + (e & 1);
-          const bool ok = key0 + kr <= qpos[e >> 1];  // (keys past n_keys: past qpos)
-          s[nt][e] = ok ? s[nt][e] : -INFINITY;
-          mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
-        }
+          for (int e = 0; e < 4; ++e)
+            if (key0 + nt * 8 + 2 * (lane & 3) + (e & 1) > qpos[e >> 1])  // (keys past n_keys: past qpos)
+              s[nt][e] = -INFINITY;
+      }
+      float mx[2] = {fmaxf(max3f(s[0][0], s[0][1], s[1][0]), s[1][1]),
+                     fmaxf(max3f(s[0][2], s[0][3], s[1][2]), s[1][3])};
       // lazy reference: m moves only when a tile passes it by more than kLazy
       float alpha[2] = {1.f, 1.f};
   #pragma unroll
@@ -1169,15 +1170,15 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_short_kernel(const __gr
           l[rr] *= alpha[rr];
         }
       }
+      // weights 2^(S - m), the differences a row's pair at a time
+      uint32_t a[4];
   #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-  #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          s[nt][e] = ex2_approx(s[nt][e] - m[e >> 1]);
-          l[e >> 1] += s[nt][e];
-        }
-      const uint32_t a[4] = {pack16<INT8>(s[0][0], s[0][1]), pack16<INT8>(s[0][2], s[0][3]),
-                             pack16<INT8>(s[1][0], s[1][1]), pack16<INT8>(s[1][2], s[1][3])};
+      for (int q = 0; q < 4; ++q) {  // n-tile q / 2, row q % 2
+        const float2 d = sub_f32x2(s[q >> 1][2 * (q & 1)], s[q >> 1][2 * (q & 1) + 1], m[q & 1]);
+        const float w0 = ex2_approx(d.x), w1 = ex2_approx(d.y);
+        l[q & 1] += w0 + w1;
+        a[q] = pack16<INT8>(w0, w1);
+      }
       if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
   #pragma unroll
         for (int nd = 0; nd < ND; ++nd)
