@@ -346,6 +346,16 @@ def test_short_chunks(d, n_qh, n_kvh):
 
 
 @pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_short_chunk_over_the_most_splits(kv):
+    """Drafts of 4 and 2 tokens over 24000 and 3 cached keys: the long one's
+    376 stages go to the most splits a query tile takes (16), each a quarter
+    shorter than the one before, the last ones a few stages long; every split's
+    partial state meets the others in the merge."""
+    wl, h, starts, ctx = make_case(8, 2, [24000, 3], [4, 2], kv=kv, seed=5)
+    check(wl, h, starts, ctx)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
 @pytest.mark.parametrize("page", [16, 64, 256])
 def test_short_chunks_page_sizes(page, kv):
     wl, h, starts, ctx = make_case(8, 2, [30, 600, 0, 4095], [4, 2, 1, 3], d=128, page=page,
